@@ -1,0 +1,396 @@
+#!/usr/bin/env python
+"""Benchmark of the gated delta rule hot path on GB300.
+
+One step = one chunked forward (prologue, UT transform, inter-chunk
+recurrence, final-state write) over the headline workload
+  B=4, H=16, L=2048, d_k=d_v=128, chunk 64, bf16 q/k/v, fp32 gates/state,
+with inputs resident in HBM.  The decode half of the metric (64 successive
+single-token steps on N=256, H=16, d=128, fp32 state) is measured in the same
+run and reported under "decode".
+
+Timing: W warm-up steps, then K timed steps, each bracketed by CUDA events on
+the launching stream; the L2 cache is flushed (a 512 MiB buffer is written)
+before every timed step, outside the events.  Under torchrun every rank runs
+its own replica of the workload (independent sequences: weak scaling, no
+collective on the data path); rank 0 prints the max over ranks.
+
+--impl reference times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of the same workload, and prints the same JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gated_delta_rule_12_gb300 import inputs  # noqa: E402
+
+METRIC = "tokens/s chunked fwd (H=16,d=128,L=2048) + decode steps/s; % roofline"
+PREFILL = "prefill_b4_h16_l2048_d128_bf16"
+DECODE = "decode_n256_h16_d128_bf16"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        d["source"] = "measured"
+        return d
+    return dict(PEAKS_FALLBACK)
+
+
+def prefill_algorithmic_bytes(w: inputs.Workload) -> int:
+    """q, k, v, out once (element size s), g and beta fp32, states in/out once per sequence."""
+    s = 2 if w.dtype == "bf16" else 4
+    th = w.B * w.L * w.H
+    per_th = (2 * w.dk + 2 * w.dv) * s + 8
+    nseq = w.num_seqs if w.kind == "varlen" else w.B
+    states = nseq * w.H * w.dv * w.dk * 4 * (2 if w.init_state else 1)
+    return th * per_th + states
+
+
+def prefill_algorithmic_flops(w: inputs.Workload) -> int:
+    C = w.chunk_size
+    return w.B * w.L * w.H * (2 * C * (3 * w.dk + 2 * w.dv) + 6 * w.dk * w.dv)
+
+
+def decode_algorithmic_bytes(w: inputs.Workload) -> int:
+    """Per step: the fp32 state read and written once, plus q, k, v, out, g, beta."""
+    s = 2 if w.dtype == "bf16" else 4
+    nh = w.num_seqs * w.H
+    return nh * (2 * w.dv * w.dk * 4 + (2 * w.dk + 2 * w.dv) * s + 8)
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_record(kernel: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel source is unchanged since."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        rec = json.load(open(p)).get(kernel)
+    except (ValueError, OSError):
+        return None
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if h != rec.get("source_sha256_16"):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def make_group(ws):
+    if ws <= 1:
+        return None
+    import torch.distributed as dist
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def bench_ours(args):
+    import gated_delta_rule_12_gb300 as gdn
+    ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = make_group(ws_n)
+    gdn.load_library()
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+
+    w = inputs.WORKLOADS[PREFILL]
+    host = inputs.make(w)
+    d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in host.items()}
+    out = torch.empty((w.B, w.L, w.H, w.dv), dtype=torch.bfloat16, device=dev)
+    sf = torch.empty((w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=dev)
+    wsz = gdn.chunk_fwd_workspace_size(w.B, w.L, w.H, w.dk, w.dv, 0, torch.bfloat16)
+    work = torch.empty(wsz, dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        gdn.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], init_state=d["init_state"], scale=w.scale,
+                      use_qk_l2norm=True, out=out, final_state=sf, workspace=work)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    barrier(dist)
+    ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    ms = max_over_ranks(dist, ms)
+    clocks = clk.summary()
+
+    tokens = w.B * w.L
+    value = tokens * ws_n / (ms * 1e-3)
+    algo_bytes = prefill_algorithmic_bytes(w)
+    achieved = algo_bytes / (ms * 1e-3) / 1e9
+    launches_per_step = 3
+
+    # end to end through the C ABI with host buffers: pinned H2D of the inputs,
+    # the call, D2H of the outputs, every step
+    pin = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in host.items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    sf_h = torch.empty(sf.shape, dtype=sf.dtype).pin_memory()
+    names = ["q", "k", "v", "g", "beta"]
+    h2d = sum(pin[n].numel() * pin[n].element_size() for n in names)
+    d2h = out_h.numel() * out_h.element_size() + sf_h.numel() * sf_h.element_size()
+
+    def e2e_step():
+        for n in names:
+            d[n].copy_(pin[n], non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        sf_h.copy_(sf, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / args.steps)
+
+    # decode half of the metric
+    wd = inputs.WORKLOADS[DECODE]
+    dh = inputs.make(wd)
+    dd = {k: v.to(dev) for k, v in dh.items()}
+    state = dd["state0"].clone()
+    dout = torch.empty((wd.num_seqs, wd.H, wd.dv), dtype=torch.bfloat16, device=dev)
+
+    def decode_all():
+        for t in range(wd.steps):
+            gdn.decode_step(state, dd["q"][t], dd["k"][t], dd["v"][t], dd["g"][t], dd["beta"][t],
+                            scale=wd.scale, use_qk_l2norm=True, out=dout)
+
+    for _ in range(max(1, args.warmup)):
+        decode_all()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        decode_all()
+    graph.replay()
+    torch.cuda.synchronize()
+    reps = max(3, args.steps // 4)
+    t_ms = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        t_ms.append(a.elapsed_time(b) / wd.steps)
+    dms = max_over_ranks(dist, statistics.median(t_ms))
+    dbytes = decode_algorithmic_bytes(wd)
+    d_ach = dbytes / (dms * 1e-3) / 1e9
+
+    if rank == 0:
+        cpu = cpu_baseline(w) if ws_n == 1 else None
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws_n, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": PREFILL, "B": w.B, "T": w.L, "H": w.H, "dk": w.dk, "dv": w.dv,
+                       "chunk": w.chunk_size, "tokens_per_step": tokens, "l2": "flushed (512 MiB write) before each timed step",
+                       "parallelism": f"replicas x{ws_n}"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_record("chunk_fwd"),
+                         "kernel": "chunk_fwd (prologue + UT + recurrence launches of one call)",
+                         "algorithmic_bytes": algo_bytes, "peak_source": peaks["source"]},
+            "e2e": {"value": tokens * ws_n / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "decode": {"workload": DECODE, "value": 1e3 / dms * ws_n, "unit": "steps/s",
+                       "tokens_per_s": wd.num_seqs * 1e3 / dms * ws_n, "ms_per_step": dms,
+                       "roofline": {"bound": "hbm", "achieved": d_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                    "frac": d_ach / peaks["hbm_gbs"], "traffic": traffic_record("decode"),
+                                    "algorithmic_bytes": dbytes},
+                       "timing": f"{wd.steps} steps in one CUDA graph, median of {reps}"},
+            "gpu_launches": args.steps * launches_per_step,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w: inputs.Workload, host=None, seqs=1, heads=None):
+    """A bounded sample of the workload: `seqs` sequences x `heads` heads, full length."""
+    host = host if host is not None else inputs.make(w)
+    hs = heads or w.H
+    sel = lambda t: t[:seqs, :, :hs].contiguous()
+    return {k: sel(host[k]) for k in ("q", "k", "v", "g", "beta")}, seqs * w.L * hs
+
+
+def cpu_baseline(w: inputs.Workload, host=None):
+    import oracle
+    s, token_heads = oracle_sample(w, host, seqs=1)
+    t0 = time.perf_counter()
+    oracle.recurrent_fwd(s["q"], s["k"], s["v"], s["g"], s["beta"], scale=w.scale, use_qk_l2norm=True)
+    dt = time.perf_counter() - t0
+    cores = min(oracle.num_threads(), w.H)
+    return {"value": token_heads / w.H / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"1 of {w.B} sequences ({w.L} tokens x {w.H} heads), fp64 recurrence, {dt:.2f} s"}
+
+
+def bench_reference(args):
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = inputs.WORKLOADS[PREFILL]
+    host = inputs.make(w)
+    s, token_heads = oracle_sample(w, host, seqs=1)
+    cores = min(oracle.num_threads(), w.H)
+
+    def step():
+        oracle.recurrent_fwd(s["q"], s["k"], s["v"], s["g"], s["beta"], scale=w.scale, use_qk_l2norm=True)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = token_heads / w.H / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws_n,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": PREFILL, "B": w.B, "T": w.L, "H": w.H, "dk": w.dk, "dv": w.dv, "chunk": w.chunk_size},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"per step: 1 of {w.B} sequences ({w.H} heads x {w.L} tokens) of the workload, fp64 recurrence"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

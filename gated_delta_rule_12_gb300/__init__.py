@@ -1,0 +1,179 @@
+"""GB300 (sm_103a) gated delta rule: Python binding of libgdn.so.
+
+This module only marshals arguments: it checks tensor placement, dtype and
+contiguity, allocates outputs/workspace with PyTorch when the caller does not
+pass them, and calls the C ABI declared in ``include/gdn.h`` through ctypes on
+the current PyTorch CUDA stream.  Every step of the computation runs in the
+library's CUDA kernels; there is no other code path.  If ``libgdn.so`` cannot
+be loaded the calls raise: there is no fallback.
+
+Entry points (same names as the C ABI, without the ``gdn_`` prefix):
+    chunk_fwd(q, k, v, g, beta, ...)      -> (out, final_state)
+    decode_step(state, q, k, v, g, beta)  -> out            (state updated in place)
+    chunk_fwd_workspace_size(...)         -> bytes
+    check_device_error(workspace)         -> None or raises
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libgdn.so")
+
+GDN_OK = 0
+STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_WORKSPACE",
+          4: "GDN_ERR_CUDA", 5: "GDN_ERR_DEVICE_TIMEOUT"}
+GDN_F32, GDN_BF16 = 0, 1
+CHUNK = 64
+
+EXPORTS = ["gdn_status_string", "gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd", "gdn_decode_step",
+           "gdn_check_device_error"]
+
+
+class GDNError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what} failed: {STATUS.get(code, code)}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_f32 = ctypes.c_float
+_sz = ctypes.c_size_t
+
+
+def load_library(path: str = LIB_PATH, build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libgdn.so (optionally building it first) and declare the ABI."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            if build_if_missing:
+                from . import build as _b
+                path = _b.build()
+            else:
+                raise RuntimeError(f"libgdn.so not found at {path}; run gated_delta_rule_12_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        lib.gdn_status_string.argtypes = [ctypes.c_int]
+        lib.gdn_status_string.restype = ctypes.c_char_p
+        lib.gdn_chunk_fwd_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_int]
+        lib.gdn_chunk_fwd_workspace_size.restype = _sz
+        lib.gdn_chunk_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
+                                      _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _f32, _i32, _i32,
+                                      _vp, _sz, _vp]
+        lib.gdn_chunk_fwd.restype = ctypes.c_int
+        lib.gdn_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                        _i32, _i32, _i32, _i32, ctypes.c_int, _f32, _i32, _vp]
+        lib.gdn_decode_step.restype = ctypes.c_int
+        lib.gdn_check_device_error.argtypes = [_vp, _vp]
+        lib.gdn_check_device_error.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return GDN_F32
+    if t.dtype == torch.bfloat16:
+        return GDN_BF16
+    raise TypeError(f"q/k/v must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors")
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def chunk_fwd_workspace_size(B, T, H, dk, dv, num_seqs=0, dtype=torch.bfloat16) -> int:
+    dt = GDN_BF16 if dtype == torch.bfloat16 else GDN_F32
+    return int(load_library().gdn_chunk_fwd_workspace_size(B, T, H, dk, dv, num_seqs, dt))
+
+
+def chunk_fwd(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale=None, use_qk_l2norm=True,
+              out=None, final_state=None, output_final_state=True, workspace=None, chunk_size=CHUNK,
+              stream=None):
+    """Chunked forward of the gated delta rule (see ``gdn_chunk_fwd`` in include/gdn.h).
+
+    q, k [B,T,H,dk], v [B,T,H,dv] (fp32 or bf16); g, beta [B,T,H] fp32;
+    init_state [N,H,dv,dk] fp32 or None; cu_seqlens int32 [N+1] (device) or None.
+    Returns ``(out, final_state)``; final_state is None if not requested.
+    """
+    lib = load_library()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else B
+    if scale is None:
+        scale = dk ** -0.5
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, dv, dk), dtype=torch.float32, device=q.device)
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    for t, dtp in ((g, torch.float32), (beta, torch.float32), (init_state, torch.float32),
+                   (final_state, torch.float32)):
+        if t is not None and t.dtype != dtp:
+            raise TypeError("g, beta and states must be float32")
+    _need_cuda(q, k, v, g, beta, init_state, cu_seqlens, out, final_state)
+    dt = _dt(q)
+    num_seqs = N if cu_seqlens is not None else 0
+    need = int(lib.gdn_chunk_fwd_workspace_size(B, T, H, dk, dv, num_seqs, dt))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    rc = lib.gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state),
+                           _ptr(cu_seqlens), num_seqs, _ptr(out), _ptr(final_state),
+                           B, T, H, dk, dv, dt, float(scale), int(bool(use_qk_l2norm)), int(chunk_size),
+                           _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    if rc != GDN_OK:
+        raise GDNError(rc, "gdn_chunk_fwd")
+    return out, final_state
+
+
+def decode_step(state, q, k, v, g, beta, scale=None, use_qk_l2norm=True, out=None, stream=None):
+    """One decode token per (sequence, head); ``state`` [N,H,dv,dk] fp32 is updated in place.
+
+    q, k [N,H,dk], v [N,H,dv] (fp32 or bf16); g, beta [N,H] fp32.  Returns out [N,H,dv].
+    """
+    lib = load_library()
+    N, H, dv, dk = state.shape
+    if scale is None:
+        scale = dk ** -0.5
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    if state.dtype != torch.float32 or g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("state, g and beta must be float32")
+    _need_cuda(state, q, k, v, g, beta, out)
+    rc = lib.gdn_decode_step(_ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(out),
+                             N, H, dk, dv, _dt(q), float(scale), int(bool(use_qk_l2norm)), _stream(stream))
+    if rc != GDN_OK:
+        raise GDNError(rc, "gdn_decode_step")
+    return out
+
+
+def check_device_error(workspace, stream=None):
+    rc = load_library().gdn_check_device_error(_ptr(workspace), _stream(stream))
+    if rc != GDN_OK:
+        raise GDNError(rc, "gdn_check_device_error")

@@ -1,0 +1,38 @@
+// kernels.h -- internal launcher interface between the C ABI (api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace gdn {
+
+struct ChunkArgs {
+    const void *q, *k, *v;
+    const float *g, *beta, *init_state;
+    void *out;
+    float *final_state;
+    Geometry gm;
+    int64_t slots;
+    int dt;          // 0 = fp32, 1 = bf16
+    float scale;
+    int l2;
+    void *workspace;
+};
+
+struct DecodeArgs {
+    float *state;
+    const void *q, *k, *v;
+    const float *g, *beta;
+    void *out;
+    int N, H, dk, dv, dt;
+    float scale;
+    int l2;
+};
+
+cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t st);
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
+
+}  // namespace gdn

@@ -1,0 +1,142 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) gated delta rule library (libgdn.so).
+ *
+ * The operator is the gated delta rule of "Gated Delta Networks: Improving
+ * Mamba2 with Delta Rule", §3.1 eq. 10:
+ *
+ *     S_t = S_{t-1} (alpha_t (I - beta_t k_t k_t^T)) + beta_t v_t k_t^T,
+ *     o_t = S_t q_t,          S_t in R^{dv x dk},
+ *
+ * evaluated in the chunkwise WY/UT form of the same page, §3.3 (with the
+ * decay mask Gamma in the intra-chunk output term, as derived on
+ * "【论文解读】Gated Delta Network", §二(一)2(3)-(4)), and as a single-token
+ * decode step (decay first, then correct the decayed prediction:
+ * "Gated DeltaNet：先忘一点，再按误差更新记忆", "为什么再加一个遗忘门？").
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library allocates nothing, keeps no global state, never synchronises
+ *     the device (except gdn_check_device_error) and enqueues all work on
+ *     `stream` (a cudaStream_t; NULL means the legacy default stream).
+ *   - Layouts are row-major and contiguous:
+ *         q, k        [B, T, H, dk]     token-major, dtype `dt`
+ *         v, out      [B, T, H, dv]     dtype `dt`
+ *         g, beta     [B, T, H]         fp32; g = log(alpha) (<= 0 for a decay)
+ *         states      [N, H, dv, dk]    fp32 (row j of S holds dk entries)
+ *         cu_seqlens  [N + 1]           int32, device
+ *   - Every pointer must be 16-byte aligned.
+ *   - q is multiplied by `scale` after the optional per-token-head L2
+ *     normalisation of q and k (use_qk_l2norm != 0: x / sqrt(sum x^2 + 1e-6)).
+ *   - Gate values are device data and are not validated; any finite values
+ *     are accepted (beta outside (0,1) included).
+ *   - Host-side validation is synchronous and returns a status before any
+ *     work is enqueued; a launch failure returns GDN_ERR_CUDA.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,     /* NULL/misaligned pointer, bad size or shape   */
+    GDN_ERR_UNSUPPORTED = 2,     /* valid but not implemented (e.g. head dims)  */
+    GDN_ERR_WORKSPACE = 3,       /* workspace missing or smaller than required  */
+    GDN_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed        */
+    GDN_ERR_DEVICE_TIMEOUT = 5   /* a kernel gave up waiting (see check below)  */
+} gdn_status;
+
+typedef enum {
+    GDN_F32 = 0,
+    GDN_BF16 = 1
+} gdn_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *gdn_status_string(gdn_status s);
+
+/*
+ * Bytes of device workspace gdn_chunk_fwd needs for this problem size.
+ * num_seqs is the number of packed sequences when cu_seqlens is used, else 0.
+ * Returns 0 for an invalid or unsupported size.
+ */
+size_t gdn_chunk_fwd_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv,
+                                    int32_t num_seqs, gdn_dtype dt);
+
+/*
+ * Chunked forward pass (prefill / training forward) of the gated delta rule.
+ * "Gated Delta Networks: Improving Mamba2 with Delta Rule", §3.3: per chunk
+ * of C = chunk_size tokens the UT transform
+ *     U~ = [I + strictLower(diag(beta)(Gamma o K K^T))]^{-1} diag(beta) V
+ * (and the matching W<-), then the inter-chunk recurrence
+ *     S_[t+1] = gamma^C S_[t] + (U~ - W<- S_[t]^T)^T K->,
+ *     O_[t]   = Q<- S_[t]^T + (Q K^T o Gamma)(U~ - W<- S_[t]^T).
+ *
+ *   q, k, v       inputs (layouts above), dtype dt.
+ *   g, beta       fp32 per token-head.
+ *   init_state    [N, H, dv, dk] fp32 initial state per sequence, or NULL for
+ *                 zeros ("state carry": pass a previous call's final_state).
+ *   cu_seqlens    NULL: N = B sequences of T tokens each.  Non-NULL: packed
+ *                 variable-length input, B must be 1, N = num_seqs, sequence n
+ *                 is tokens [cu[n], cu[n+1]) of the T axis; cu[0] = 0,
+ *                 cu[N] = T, non-decreasing (device data, not validated by
+ *                 the host).  The state resets at every boundary to
+ *                 init_state[n] (or 0).  Chunks never cross a boundary.
+ *   out           [B, T, H, dv] dtype dt, written for every token.
+ *   final_state   [N, H, dv, dk] fp32, or NULL to skip; may alias init_state.
+ *   B, T, H       batch, tokens per row, heads (T >= 0, B, H >= 1).
+ *   dk, dv        head dims: dk in {64, 128}; dv a multiple of 32 up to 256
+ *                 (others return GDN_ERR_UNSUPPORTED).
+ *   dt            GDN_F32 or GDN_BF16 (q, k, v and out); arithmetic is fp32.
+ *   scale         multiplier of q (commonly 1/sqrt(dk)).
+ *   chunk_size    must be 64.
+ *   workspace     device scratch of at least gdn_chunk_fwd_workspace_size()
+ *                 bytes, 256-byte aligned; its first 256 bytes hold the
+ *                 device error word read by gdn_check_device_error.
+ * Errors: GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE,
+ *         GDN_ERR_CUDA.  Nothing is enqueued when an error is returned
+ *         before the first launch.
+ */
+gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
+                         const float *g, const float *beta,
+                         const float *init_state,
+                         const int32_t *cu_seqlens, int32_t num_seqs,
+                         void *out, float *final_state,
+                         int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv,
+                         gdn_dtype dt, float scale, int32_t use_qk_l2norm, int32_t chunk_size,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * One decode step per (sequence, head), state updated in place.
+ * "Gated DeltaNet：先忘一点，再按误差更新记忆", "为什么再加一个遗忘门？" and
+ * "Decode 递归":  Sbar = alpha S;  S <- Sbar + beta (v - Sbar k) k^T;
+ * o = S q (with the updated S).
+ *   state   [N, H, dv, dk] fp32, read once and written once.
+ *   q, k    [N, H, dk] dtype dt;  v, out [N, H, dv] dtype dt.
+ *   g, beta [N, H] fp32.
+ *   dk in {64, 128, 256}, dv >= 1.
+ * Errors: GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA.
+ */
+gdn_status gdn_decode_step(float *state,
+                           const void *q, const void *k, const void *v,
+                           const float *g, const float *beta,
+                           void *out,
+                           int32_t N, int32_t H, int32_t dk, int32_t dv, gdn_dtype dt,
+                           float scale, int32_t use_qk_l2norm, void *stream);
+
+/*
+ * Reads and clears the device error word at the start of `workspace`
+ * (synchronises `stream`).  Returns GDN_OK, GDN_ERR_DEVICE_TIMEOUT when a
+ * kernel gave up on a bounded wait, or GDN_ERR_CUDA.
+ */
+gdn_status gdn_check_device_error(void *workspace, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

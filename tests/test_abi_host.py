@@ -1,0 +1,133 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must build for sm_103a, load, and export every function the
+public header declares.  Argument validation runs on the host before any
+CUDA call, so the error paths are exercised here with pointers that are
+never dereferenced.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_delta_rule_12_gb300 as gdn
+from gated_delta_rule_12_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h")]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gdn.load_library()
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(gdn_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(gdn.EXPORTS) <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"libgdn.so does not export {n}"
+    # and the symbol is a real dynamic export (not only resolvable by ctypes magic)
+    out = os.popen(f"nm -D --defined-only {gdn.LIB_PATH}").read()
+    for n in names:
+        assert re.search(rf"\bT {n}\b", out), f"{n} missing from the dynamic symbol table"
+
+
+def test_status_strings(lib):
+    for code, name in gdn.STATUS.items():
+        assert lib.gdn_status_string(code).decode() == name
+    assert lib.gdn_status_string(99).decode() == "GDN_UNKNOWN_STATUS"
+
+
+def test_workspace_size_rules(lib):
+    ws = lib.gdn_chunk_fwd_workspace_size
+    assert ws(4, 2048, 16, 128, 128, 0, gdn.GDN_BF16) > 0
+    assert ws(1, 32768, 16, 128, 128, 8, gdn.GDN_BF16) > 0
+    assert ws(1, 256, 2, 64, 64, 0, gdn.GDN_F32) > 0
+    assert ws(4, 100, 2, 128, 128, 8, gdn.GDN_BF16) == 0     # varlen needs B == 1
+    assert ws(1, 64, 1, 96, 64, 0, gdn.GDN_F32) == 0         # unsupported dk
+    assert ws(0, 64, 1, 64, 64, 0, gdn.GDN_F32) == 0
+    # grows with the problem
+    assert ws(1, 4096, 2, 64, 64, 0, 0) > ws(1, 2048, 2, 64, 64, 0, 0)
+    assert ws(1, 0, 2, 64, 64, 0, 0) >= 256
+
+
+def _call_chunk(lib, **over):
+    fake = 1 << 20  # 256-aligned, never dereferenced: validation fails first
+    args = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, s0=None, cu=None, nseq=0, out=fake, sf=None,
+                B=1, T=64, H=1, dk=64, dv=64, dt=gdn.GDN_F32, scale=0.125, l2=1, C=64,
+                ws=fake, wsb=1 << 30, stream=None)
+    args.update(over)
+    a = args
+    return lib.gdn_chunk_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["s0"], a["cu"], a["nseq"], a["out"],
+                             a["sf"], a["B"], a["T"], a["H"], a["dk"], a["dv"], a["dt"], a["scale"], a["l2"],
+                             a["C"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(C=32), 2),                       # chunk size other than 64
+    (dict(dk=96), 2),                      # unsupported head dim
+    (dict(dv=48), 2),
+    (dict(B=0), 1),
+    (dict(H=0), 1),
+    (dict(dt=7), 1),
+    (dict(q=None), 1),                     # NULL input with tokens present
+    (dict(out=None), 1),
+    (dict(k=(1 << 20) + 4), 1),            # misaligned
+    (dict(ws=None), 3),                    # no workspace
+    (dict(ws=(1 << 20) + 16), 3),          # workspace not 256-aligned
+    (dict(wsb=64), 3),                     # workspace too small
+    (dict(cu=1 << 20, nseq=0), 1),         # varlen without a sequence count
+    (dict(cu=1 << 20, nseq=2, B=2), 1),    # varlen needs B == 1
+    (dict(nseq=3), 1),                     # num_seqs inconsistent with B
+])
+def test_chunk_fwd_validation(lib, over, code):
+    assert _call_chunk(lib, **over) == code
+
+
+def test_decode_validation(lib):
+    fake = 1 << 20
+    d = lib.gdn_decode_step
+    assert d(fake, fake, fake, fake, fake, fake, fake, 4, 2, 96, 64, 0, 1.0, 1, None) == 2   # dk
+    assert d(fake, fake, fake, fake, fake, fake, fake, 4, 2, 128, 12, 0, 1.0, 1, None) == 2  # dv % 8
+    assert d(None, fake, fake, fake, fake, fake, fake, 4, 2, 128, 64, 0, 1.0, 1, None) == 1
+    assert d(fake + 8, fake, fake, fake, fake, fake, fake, 4, 2, 128, 64, 0, 1.0, 1, None) == 1
+    assert d(fake, fake, fake, fake, fake, fake, fake, 4, 0, 128, 64, 0, 1.0, 1, None) == 1
+    assert d(fake, fake, fake, fake, fake, fake, fake, 0, 2, 128, 64, 0, 1.0, 1, None) == 0  # nothing to do
+
+
+def test_check_device_error_validation(lib):
+    assert lib.gdn_check_device_error(None, None) == 1
+    assert lib.gdn_check_device_error((1 << 20) + 8, None) == 1
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    q = torch.zeros(1, 64, 1, 64)
+    with pytest.raises(ValueError):
+        gdn.chunk_fwd(q, q, q, torch.zeros(1, 64, 1), torch.zeros(1, 64, 1), out=q.clone(),
+                      final_state=torch.zeros(1, 1, 64, 64), workspace=torch.zeros(1 << 20, dtype=torch.uint8))
+
+
+def test_product_path_does_not_reference_the_oracle():
+    pkg = os.path.join(ROOT, "gated_delta_rule_12_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        if "_build" in dirpath:
+            continue
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "gdn_oracle" not in text and "liboracle" not in text, f

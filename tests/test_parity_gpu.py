@@ -1,0 +1,154 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Small cases span several chunks, ragged tails, varlen boundaries (including
+length-0 and length-1 sequences), d_v > d_k, state carry and both dtypes.
+Full-size workloads are checked on all units where the oracle is quick and on
+sampled (sequence, head) units otherwise (units are independent).
+"""
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_12_gb300 as gdn
+import oracle
+from gated_delta_rule_12_gb300 import inputs
+from gpu_helpers import assert_close, cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_delta_rule_12_gb300 import build
+    build.build()
+    gdn.load_library()
+
+
+def run_both(d, dk, scale=None, l2=True):
+    scale = dk ** -0.5 if scale is None else scale
+    dd = cuda(d)
+    out, sf = gdn.chunk_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], init_state=dd["init_state"],
+                            cu_seqlens=dd["cu_seqlens"], scale=scale, use_qk_l2norm=l2)
+    torch.cuda.synchronize()
+    ro, rs = oracle.recurrent_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], init_state=d["init_state"],
+                                  cu_seqlens=d["cu_seqlens"], scale=scale, use_qk_l2norm=l2)
+    return out, sf, ro, rs
+
+
+def test_headline_small_fp32_case_exact_config():
+    """B=1, H=2, L=256, d=64, fp32, zero initial state, seed 0."""
+    w = inputs.WORKLOADS["prefill_b1_h2_l256_d64_f32"]
+    d = inputs.make(w)
+    out, sf, ro, rs = run_both(d, w.dk)
+    assert out.shape == (1, 256, 2, 64) and sf.shape == (1, 2, 64, 64)
+    assert_close(out, ro, "f32", "out")
+    assert_close(sf, rs, "f32", "final_state")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 256), (128, 32)])
+def test_prefill_ragged_with_initial_state(dtype, dk, dv):
+    d = inputs.make_prefill(B=2, L=200, H=3, dk=dk, dv=dv, dtype=dtype, seed=11, decay=0.3, init_state=True)
+    out, sf, ro, rs = run_both(d, dk)
+    assert_close(out, ro, dtype, "out")
+    assert_close(sf, rs, dtype, "final_state")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_varlen_boundaries(dtype):
+    lens = [1, 63, 64, 65, 0, 130, 7, 128]
+    d = inputs.make_prefill(B=1, L=sum(lens), H=2, dk=128, dv=128, dtype=dtype, seed=12, decay=0.5,
+                            init_state=True, num_seqs=len(lens), lengths=lens)
+    out, sf, ro, rs = run_both(d, 128)
+    assert_close(out, ro, dtype, "out")
+    assert_close(sf, rs, dtype, "final_state")
+    # a length-0 sequence keeps its initial state
+    np.testing.assert_allclose(sf[4].cpu().numpy(), d["init_state"][4].numpy(), atol=0)
+
+
+def test_heavy_decay_no_overflow():
+    d = inputs.make_prefill(B=1, L=256, H=2, dk=128, dv=128, dtype="bf16", seed=13, decay=4.0)
+    out, sf, ro, rs = run_both(d, 128)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(sf).all()
+    assert_close(out, ro, "bf16", "out")
+    assert_close(sf, rs, "bf16", "final_state")
+
+
+def test_without_l2norm_on_prenormalised_inputs():
+    d = inputs.make_prefill(B=1, L=150, H=2, dk=64, dv=64, dtype="f32", seed=14)
+    d["q"] = d["q"] / d["q"].norm(dim=-1, keepdim=True)
+    d["k"] = d["k"] / d["k"].norm(dim=-1, keepdim=True)
+    out, sf, ro, rs = run_both(d, 64, l2=False)
+    assert_close(out, ro, "f32", "out")
+    assert_close(sf, rs, "f32", "final_state")
+
+
+def test_empty_sequence_axis():
+    d = inputs.make_prefill(B=2, L=0, H=2, dk=64, dv=64, dtype="f32", seed=15, init_state=True)
+    dd = cuda(d)
+    out, sf = gdn.chunk_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], init_state=dd["init_state"])
+    torch.cuda.synchronize()
+    assert out.numel() == 0
+    np.testing.assert_array_equal(sf.cpu().numpy(), d["init_state"].numpy())
+
+
+def test_state_carry_two_calls_equal_one():
+    d = inputs.make_prefill(B=2, L=300, H=2, dk=128, dv=128, dtype="bf16", seed=16, init_state=True)
+    dd = cuda(d)
+    o, s = gdn.chunk_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], init_state=dd["init_state"])
+    cut = 130
+    sl = lambda t, a, b: t[:, a:b].contiguous()
+    o1, s1 = gdn.chunk_fwd(*(sl(dd[n], 0, cut) for n in ("q", "k", "v", "g", "beta")), init_state=dd["init_state"])
+    o2, s2 = gdn.chunk_fwd(*(sl(dd[n], cut, 300) for n in ("q", "k", "v", "g", "beta")), init_state=s1)
+    torch.cuda.synchronize()
+    ro, rs = oracle.recurrent_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], init_state=d["init_state"],
+                                  scale=128 ** -0.5, use_qk_l2norm=True)
+    assert_close(torch.cat([o1, o2], 1), ro, "bf16", "split out")
+    assert_close(s2, rs, "bf16", "split state")
+
+
+def test_device_error_word_clear_after_call():
+    d = cuda(inputs.make_prefill(B=1, L=128, H=1, dk=64, dv=64, dtype="f32", seed=17))
+    ws = torch.full((gdn.chunk_fwd_workspace_size(1, 128, 1, 64, 64, 0, torch.float32),), 0xFF,
+                    dtype=torch.uint8, device="cuda")
+    gdn.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], workspace=ws)
+    gdn.check_device_error(ws)   # raises if the word is not clear
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads
+# ---------------------------------------------------------------------------
+
+def test_full_prefill_b4_h16_l2048_all_units():
+    w = inputs.WORKLOADS["prefill_b4_h16_l2048_d128_bf16"]
+    d = inputs.make(w)
+    out, sf, ro, rs = run_both(d, w.dk)
+    assert_close(out, ro, "bf16", "out")
+    assert_close(sf, rs, "bf16", "final_state")
+
+
+def test_full_varlen_t32768_all_units():
+    w = inputs.WORKLOADS["varlen_t32768_h16_d128_bf16"]
+    d = inputs.make(w)
+    out, sf, ro, rs = run_both(d, w.dk)
+    assert_close(out, ro, "bf16", "out")
+    assert_close(sf, rs, "bf16", "final_state")
+
+
+def test_full_large_heavy_decay_sampled_units():
+    w = inputs.WORKLOADS["prefill_b8_h32_l8192_dk128_dv256_bf16"]
+    d = inputs.make(w)
+    dd = cuda(d)
+    out, sf = gdn.chunk_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], scale=w.scale, use_qk_l2norm=True)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+    rng = np.random.default_rng(4)
+    picks = [(int(rng.integers(w.B)), int(rng.integers(w.H))) for _ in range(6)]
+    for b, h in picks:
+        sel = lambda t: t[b:b + 1, :, h:h + 1].contiguous()
+        ro, rs = oracle.recurrent_fwd(sel(d["q"]), sel(d["k"]), sel(d["v"]), sel(d["g"]), sel(d["beta"]),
+                                      scale=w.scale, use_qk_l2norm=True)
+        assert_close(out[b:b + 1, :, h:h + 1], ro, "bf16", f"out[{b},{h}]")
+        assert_close(sf[b:b + 1, h:h + 1], rs, "bf16", f"state[{b},{h}]")
