@@ -16,6 +16,7 @@ using namespace gdn;
 namespace {
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+bool aligned_to(const void *p, unsigned a) { return ((uintptr_t)p & (uintptr_t)(a - 1)) == 0; }
 
 bool chunk_dims_supported(int dk, int dv) { return (dk == 64 || dk == 128) && dv >= 32 && dv <= 256 && dv % 32 == 0; }
 
@@ -65,9 +66,12 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
     const int N = varlen ? num_seqs : B;
     const bool have_tokens = (int64_t)B * T > 0;
     if (have_tokens && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_INVALID_ARG;
-    const void *ptrs[] = {q, k, v, g, beta, init_state, cu_seqlens, out, final_state};
-    for (const void *p : ptrs)
+    const void *ptrs16[] = {q, k, v, init_state, out, final_state};
+    for (const void *p : ptrs16)
         if (p && !aligned16(p)) return GDN_ERR_INVALID_ARG;
+    const void *ptrs4[] = {g, beta, cu_seqlens};
+    for (const void *p : ptrs4)
+        if (p && !aligned_to(p, 4)) return GDN_ERR_INVALID_ARG;
     if (!workspace) return GDN_ERR_WORKSPACE;
     if (((uintptr_t)workspace & 255u) != 0) return GDN_ERR_WORKSPACE;
     const size_t need = gdn_chunk_fwd_workspace_size(B, T, H, dk, dv, varlen ? num_seqs : 0, dt);
@@ -101,7 +105,11 @@ gdn_status gdn_decode_step(float *state, const void *q, const void *k, const voi
     if (N == 0) return GDN_OK;
     const void *ptrs[] = {state, q, k, v, g, beta, out};
     for (const void *p : ptrs)
-        if (!p || !aligned16(p)) return GDN_ERR_INVALID_ARG;
+        if (!p) return GDN_ERR_INVALID_ARG;
+    const unsigned esz = (dt == GDN_BF16) ? 2u : 4u;
+    if (!aligned16(state) || !aligned_to(q, esz) || !aligned_to(k, esz) || !aligned_to(v, esz) ||
+        !aligned_to(out, esz) || !aligned_to(g, 4) || !aligned_to(beta, 4))
+        return GDN_ERR_INVALID_ARG;
     DecodeArgs a;
     a.state = state; a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = out;
     a.N = N; a.H = H; a.dk = dk; a.dv = dv; a.dt = (dt == GDN_BF16) ? 1 : 0;

@@ -24,7 +24,9 @@
  *         g, beta     [B, T, H]         fp32; g = log(alpha) (<= 0 for a decay)
  *         states      [N, H, dv, dk]    fp32 (row j of S holds dk entries)
  *         cu_seqlens  [N + 1]           int32, device
- *   - Every pointer must be 16-byte aligned.
+ *   - Alignment: q, k, v, out and states 16 bytes (gdn_chunk_fwd); state
+ *     16 bytes and q, k, v, out their element size (gdn_decode_step); g, beta
+ *     and cu_seqlens 4 bytes; the workspace 256 bytes.
  *   - q is multiplied by `scale` after the optional per-token-head L2
  *     normalisation of q and k (use_qk_l2norm != 0: x / sqrt(sum x^2 + 1e-6)).
  *   - Gate values are device data and are not validated; any finite values
@@ -118,7 +120,7 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
  *   state   [N, H, dv, dk] fp32, read once and written once.
  *   q, k    [N, H, dk] dtype dt;  v, out [N, H, dv] dtype dt.
  *   g, beta [N, H] fp32.
- *   dk in {64, 128, 256}, dv >= 1.
+ *   dk in {64, 128, 256}, dv a multiple of 8.
  * Errors: GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA.
  */
 gdn_status gdn_decode_step(float *state,

@@ -86,6 +86,7 @@ def _call_chunk(lib, **over):
     (dict(q=None), 1),                     # NULL input with tokens present
     (dict(out=None), 1),
     (dict(k=(1 << 20) + 4), 1),            # misaligned
+    (dict(g=(1 << 20) + 2), 1),
     (dict(ws=None), 3),                    # no workspace
     (dict(ws=(1 << 20) + 16), 3),          # workspace not 256-aligned
     (dict(wsb=64), 3),                     # workspace too small
@@ -103,7 +104,9 @@ def test_decode_validation(lib):
     assert d(fake, fake, fake, fake, fake, fake, fake, 4, 2, 96, 64, 0, 1.0, 1, None) == 2   # dk
     assert d(fake, fake, fake, fake, fake, fake, fake, 4, 2, 128, 12, 0, 1.0, 1, None) == 2  # dv % 8
     assert d(None, fake, fake, fake, fake, fake, fake, 4, 2, 128, 64, 0, 1.0, 1, None) == 1
-    assert d(fake + 8, fake, fake, fake, fake, fake, fake, 4, 2, 128, 64, 0, 1.0, 1, None) == 1
+    assert d(fake + 8, fake, fake, fake, fake, fake, fake, 4, 2, 128, 64, 0, 1.0, 1, None) == 1   # state
+    assert d(fake, fake + 2, fake, fake, fake, fake, fake, 4, 2, 128, 64, 0, 1.0, 1, None) == 1   # fp32 q
+    assert d(fake, fake, fake, fake, fake + 2, fake, fake, 4, 2, 128, 64, 0, 1.0, 1, None) == 1   # g
     assert d(fake, fake, fake, fake, fake, fake, fake, 4, 0, 128, 64, 0, 1.0, 1, None) == 1
     assert d(fake, fake, fake, fake, fake, fake, fake, 0, 2, 128, 64, 0, 1.0, 1, None) == 0  # nothing to do
 
