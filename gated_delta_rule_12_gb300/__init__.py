@@ -31,7 +31,8 @@ GDN_F32, GDN_BF16 = 0, 1
 CHUNK = 64
 
 EXPORTS = ["gdn_status_string", "gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd", "gdn_decode_step",
-           "gdn_check_device_error"]
+           "gdn_check_device_error", "gdn_chunk_fwd_noalloc"]
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class GDNError(RuntimeError):
@@ -75,6 +76,10 @@ def load_library(path: str = LIB_PATH, build_if_missing: bool = False) -> ctypes
         lib.gdn_decode_step.restype = ctypes.c_int
         lib.gdn_check_device_error.argtypes = [_vp, _vp]
         lib.gdn_check_device_error.restype = ctypes.c_int
+        lib.gdn_chunk_fwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
+                                              _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _f32, _i32, _i32,
+                                              _vp]
+        lib.gdn_chunk_fwd_noalloc.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -177,3 +182,29 @@ def check_device_error(workspace, stream=None):
     rc = load_library().gdn_check_device_error(_ptr(workspace), _stream(stream))
     if rc != GDN_OK:
         raise GDNError(rc, "gdn_check_device_error")
+
+
+def chunk_fwd_noalloc(q, k, v, g, beta, out, final_state=None, init_state=None, cu_seqlens=None, scale=None,
+                      use_qk_l2norm=True, chunk_size=CHUNK, stream=None):
+    """``gdn_chunk_fwd_noalloc``: the chunked forward with the library's fixed
+    device scratch array instead of a workspace, for callers that cannot
+    allocate.  The caller passes every output buffer; nothing is allocated.
+    Problems needing more than ``NOALLOC_SCRATCH_BYTES`` of scratch are
+    rejected (GDN_ERR_WORKSPACE).  Calls that overlap on the GPU race."""
+    lib = load_library()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if scale is None:
+        scale = dk ** -0.5
+    _need_cuda(q, k, v, g, beta, init_state, cu_seqlens, out, final_state)
+    num_seqs = (cu_seqlens.numel() - 1) if cu_seqlens is not None else 0
+    rc = lib.gdn_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state),
+                                   _ptr(cu_seqlens), num_seqs, _ptr(out), _ptr(final_state),
+                                   B, T, H, dk, dv, _dt(q), float(scale), int(bool(use_qk_l2norm)),
+                                   int(chunk_size), _stream(stream))
+    if rc != GDN_OK:
+        what = "gdn_chunk_fwd_noalloc"
+        if rc == 3:
+            what += f" (problem needs more than the {NOALLOC_SCRATCH_BYTES >> 20} MiB fixed scratch)"
+        raise GDNError(rc, what)
+    return out, final_state

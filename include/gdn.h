@@ -137,6 +137,43 @@ gdn_status gdn_decode_step(float *state,
  */
 gdn_status gdn_check_device_error(void *workspace, void *stream);
 
+/*
+ * gdn_chunk_fwd_noalloc -- gdn_chunk_fwd for callers that cannot allocate.
+ * The pages have no counterpart of this call: it exists for callers that may
+ * not call cudaMalloc or any allocating routine where they run the operator
+ * (plugin hosts and serving runtimes that plan all device memory up front,
+ * bindings without a device allocator) and so cannot pass a workspace.
+ *
+ * Same arguments, semantics and errors as gdn_chunk_fwd, minus the
+ * workspace.  The scratch is a fixed GDN_NOALLOC_SCRATCH_BYTES array inside
+ * the library's device image: every GPU that loads the library holds it
+ * until the process exits, and this call allocates and frees nothing.
+ *   - The call runs the CUDA-core kernels, whose scratch need is 256 B plus
+ *     64 * (12 + 4 * (dk + dv)) B per chunk slot and head, with B * ceil(T/64)
+ *     slots (floor(T/64) + N + 1 for packed input).  A problem needing more
+ *     than GDN_NOALLOC_SCRATCH_BYTES is rejected with GDN_ERR_WORKSPACE
+ *     before any work is enqueued (for example B=1, H=16, T=2048, dk=dv=128
+ *     fits; B=4 of those does not).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps the previous
+ *     call's contents (the call clears what must start at zero).  Calls that
+ *     overlap on the GPU race on it: order them (one stream, or events).
+ *   - The device error word lives in the array, so gdn_check_device_error
+ *     does not apply to this call.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+gdn_status gdn_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
+                                 const float *g, const float *beta,
+                                 const float *init_state,
+                                 const int32_t *cu_seqlens, int32_t num_seqs,
+                                 void *out, float *final_state,
+                                 int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv,
+                                 gdn_dtype dt, float scale, int32_t use_qk_l2norm, int32_t chunk_size,
+                                 void *stream);
+
 #ifdef __cplusplus
 }
 #endif
