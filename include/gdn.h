@@ -152,8 +152,8 @@ gdn_status gdn_check_device_error(void *workspace, void *stream);
  *     64 * (12 + 4 * (dk + dv)) B per chunk slot and head, with B * ceil(T/64)
  *     slots (floor(T/64) + N + 1 for packed input).  A problem needing more
  *     than GDN_NOALLOC_SCRATCH_BYTES is rejected with GDN_ERR_WORKSPACE
- *     before any work is enqueued (for example B=1, H=16, T=2048, dk=dv=128
- *     fits; B=4 of those does not).
+ *     before any work is enqueued (for example B=1, H=8, T=2048, dk=dv=128
+ *     needs 16.2 MiB and fits; H=16 needs 32.4 MiB and does not).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture.
