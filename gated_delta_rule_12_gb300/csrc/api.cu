@@ -45,6 +45,8 @@ size_t gdn_chunk_fwd_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk,
     if (!chunk_dims_supported(dk, dv)) return 0;
     const bool varlen = num_seqs > 0;
     if (varlen && B != 1) return 0;
+    // the tensor-core path needs only the 256-B header (device error word)
+    if (chunk_tc_supported(dt == GDN_BF16 ? 1 : 0, dk, dv, (int64_t)B * T)) return 256;
     const int64_t slots = num_slots(B, T, varlen ? num_seqs : B, varlen);
     return chunk_workspace_layout(slots, H, dk, dv).total;
 }
@@ -90,7 +92,8 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
     a.l2 = use_qk_l2norm ? 1 : 0;
     a.workspace = workspace;
     cudaStream_t st = (cudaStream_t)stream;
-    cudaError_t e = launch_chunk_simt(a, st);
+    cudaError_t e = chunk_tc_supported(a.dt, dk, dv, (int64_t)B * T) ? launch_chunk_tc(a, st)
+                                                                     : launch_chunk_simt(a, st);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

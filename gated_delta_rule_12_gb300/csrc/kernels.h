@@ -33,6 +33,8 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t st);
+bool chunk_tc_supported(int dt, int dk, int dv, int64_t tokens);
+cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
 
 }  // namespace gdn

@@ -45,8 +45,10 @@ def test_noalloc_rejects_problems_beyond_the_fixed_scratch():
     rc = lib.gdn_chunk_fwd_noalloc(fake, fake, fake, fake, fake, None, None, 0, fake, None,
                                    8, 8192, 32, 128, 256, gdn.GDN_BF16, ctypes.c_float(0.1), 1, 64, None)
     assert rc == 3   # GDN_ERR_WORKSPACE
-    need = lib.gdn_chunk_fwd_workspace_size(8, 8192, 32, 128, 256, 0, gdn.GDN_BF16)
-    assert need > gdn.NOALLOC_SCRATCH_BYTES
+    # the header's scratch formula: 256 B + 64 * (12 + 4 * (dk + dv)) B per chunk slot and head
+    need = lambda B, T, H, dk, dv: 256 + B * -(-T // 64) * H * 64 * (12 + 4 * (dk + dv))
+    assert need(8, 8192, 32, 128, 256) > gdn.NOALLOC_SCRATCH_BYTES
+    assert need(1, 2048, 8, 128, 128) < gdn.NOALLOC_SCRATCH_BYTES < need(1, 2048, 16, 128, 128)
 
 
 @pytest.mark.gpu
