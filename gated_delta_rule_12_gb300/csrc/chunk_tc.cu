@@ -47,7 +47,9 @@ using namespace umma;
 constexpr int kThreadsTc = 320;
 constexpr uint32_t kQKStage = 32768;   // [K kb0][Q kb0][K kb1][Q kb1], 8 KB each (64 rows x 128 B)
 constexpr uint32_t kVStage = 16384;    // [V cols 0-63][V cols 64-127]
-constexpr uint32_t LDL = 68;           // fp32 row pitch of the solve matrices
+constexpr uint32_t LDA = 65;           // fp32 row pitch of L (conflict-free row-per-thread writes)
+constexpr uint32_t LDL = 68;           // fp32 row pitch of T (16-B aligned rows for vector loads)
+constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr uint32_t OFF_QK = 0;
 constexpr uint32_t OFF_V = OFF_QK + 3 * kQKStage;
@@ -55,8 +57,8 @@ constexpr uint32_t OFF_TP = OFF_V + 2 * kVStage;      // T'   bf16 [64 r][64 i] 
 constexpr uint32_t OFF_TPP = OFF_TP + 8192;           // T''  bf16 [64 r][64 i] K-major
 constexpr uint32_t OFF_WT = OFF_TPP + 8192;           // W~^T bf16 [128 d][64 r] (MN-major B)
 constexpr uint32_t OFF_AQK = OFF_WT + 16384;          // Aqk  bf16 [64 r][64 i] x 2 buffers
-constexpr uint32_t OFF_LF = OFF_AQK + 16384;          // L    fp32 [64][LDL]
-constexpr uint32_t OFF_TF = OFF_LF + 64 * LDL * 4;    // T    fp32 [64][LDL]
+constexpr uint32_t OFF_LF = OFF_AQK + 16384;          // L    fp32 [64][LDA]
+constexpr uint32_t OFF_TF = OFF_LF + 64 * LDA * 4;    // T    fp32 [64][LDL]
 constexpr uint32_t OFF_MT = OFF_TF + 64 * LDL * 4;    // merge temp fp32 [32][33]
 constexpr uint32_t OFF_SC = OFF_MT + 32 * 33 * 4;     // per stage: b, beta, rk, rq, spare [5][64] fp32
 constexpr uint32_t OFF_BAR = OFF_SC + 3 * 5 * 64 * 4;
@@ -105,15 +107,29 @@ struct TcParams {
     Geometry gm;
     float scale;
     int l2;
+#ifdef GDN_KERNEL_TRACE
+    long long *trace;
+#endif
 };
+
+// Development-only phase timestamps (SM clock) of the first CTA; compiled out
+// of the library unless GDN_KERNEL_TRACE is defined.
+#ifdef GDN_KERNEL_TRACE
+#define GDN_TR(role, c, ev)                                                                          \
+    do {                                                                                             \
+        if (p.trace && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (c) < 16)            \
+            p.trace[((role) * 16 + (c)) * 16 + (ev)] = clock64();                                    \
+    } while (0)
+#else
+#define GDN_TR(role, c, ev) do { } while (0)
+#endif
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned *err)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             *abort_flag = 1;
@@ -154,13 +170,15 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t u)
     return __bfloat1622float2(v);
 }
 
-// Sum of squares of the 64 bf16 of one 128-B row segment.
-__device__ __forceinline__ float row_sumsq(const uint8_t *row)
+// Sum of squares of the 64 bf16 of one 128-B row segment (row index r, used
+// only to visit the 16-B chunks in an order that spreads consecutive rows
+// over all shared-memory banks).
+__device__ __forceinline__ float row_sumsq(const uint8_t *row, int r)
 {
     float ss = 0.f;
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(row + ch * 16);
+        const uint4 u = *reinterpret_cast<const uint4 *>(row + ((ch ^ r) & 7) * 16);
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -171,11 +189,12 @@ __device__ __forceinline__ float row_sumsq(const uint8_t *row)
     return ss;
 }
 
-// Multiply the 64 bf16 of one 128-B row segment by f, in place.
-__device__ __forceinline__ void row_scale(uint8_t *row, float f)
+// Multiply the 64 bf16 of one 128-B row segment by f, in place (chunk order as above).
+__device__ __forceinline__ void row_scale(uint8_t *row, int r, float f)
 {
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
+    for (int ch0 = 0; ch0 < 8; ++ch0) {
+        const int ch = (ch0 ^ r) & 7;
         uint4 u = *reinterpret_cast<uint4 *>(row + ch * 16);
         uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -187,7 +206,7 @@ __device__ __forceinline__ void row_scale(uint8_t *row, float f)
     }
 }
 
-// T = (I + L)^{-1} for a strictly lower 64x64 L (row pitch LDL), 128 threads.
+// T = (I + L)^{-1} for a strictly lower 64x64 L (row pitch LDA; T pitch LDL), 128 threads.
 // 16x16 diagonal blocks by forward substitution (one thread per column),
 // then the block rule [A 0; C B]^{-1} = [A^-1 0; -B^-1 C A^-1  B^-1] for the
 // 16->32 and 32->64 merges.
@@ -203,7 +222,7 @@ __device__ __forceinline__ void solve_unit_lower(const float *__restrict__ Lf, f
         for (int r = 0; r < 16; ++r) {
             float acc = 0.f;
 #pragma unroll
-            for (int i = 0; i < r; ++i) acc += Lf[(base + r) * LDL + base + i] * x[i];
+            for (int i = 0; i < r; ++i) acc += Lf[(base + r) * LDA + base + i] * x[i];
             x[r] = (r == cc) ? 1.f : ((r < cc) ? 0.f : -acc);
         }
 #pragma unroll
@@ -216,7 +235,7 @@ __device__ __forceinline__ void solve_unit_lower(const float *__restrict__ Lf, f
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const float l = Lf[(b0 + r) * LDL + a0 + i];
+            const float l = Lf[(b0 + r) * LDA + a0 + i];
 #pragma unroll
             for (int c = 0; c < 4; ++c) acc[c] += l * Tf[(a0 + i) * LDL + a0 + cg + c];
         }
@@ -241,7 +260,7 @@ __device__ __forceinline__ void solve_unit_lower(const float *__restrict__ Lf, f
         for (int c = 0; c < 8; ++c) acc[c] = 0.f;
 #pragma unroll 8
         for (int i = 0; i < 32; ++i) {
-            const float l = Lf[(32 + r) * LDL + i];
+            const float l = Lf[(32 + r) * LDA + i];
             const float4 t0 = *reinterpret_cast<const float4 *>(Tf + i * LDL + cg);
             const float4 t1 = *reinterpret_cast<const float4 *>(Tf + i * LDL + cg + 4);
             acc[0] += l * t0.x; acc[1] += l * t0.y; acc[2] += l * t0.z; acc[3] += l * t0.w;
@@ -312,6 +331,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 const int z = (int)(tok0 + (int64_t)c * kChunk);
                 if (c >= 3 && !wait_bar(bar(B_QKE + s), ((c / 3) - 1) & 1, abort_flag, p.err)) break;
                 const uint32_t st = sb + OFF_QK + s * kQKStage;
+                GDN_TR(3, c, 0);
                 mbar_expect_tx(bar(B_QKF + s), kQKStage);
                 tma_load_3d(st, &tmk, 0, h, z, bar(B_QKF + s));
                 tma_load_3d(st + 8192, &tmq, 0, h, z, bar(B_QKF + s));
@@ -368,6 +388,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             if (ok) { fence_after_sync(); issue_p2(0); }
             for (int c = 0; c < nch && ok; ++c) {
                 if (!wait_bar(bar(B_PREP), c & 1, abort_flag, p.err)) break;
+                GDN_TR(1, c, 0);
                 fence_after_sync();
                 if (c + 1 < nch) {
                     if (!wait_bar(bar(B_QKF + (c + 1) % 3), ((c + 1) / 3) & 1, abort_flag, p.err)) break;
@@ -375,6 +396,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 }
                 if (!wait_bar(bar(B_VF + (c & 1)), (c >> 1) & 1, abort_flag, p.err)) break;
                 if (c > 0 && !wait_bar(bar(B_X), (c - 1) & 1, abort_flag, p.err)) break;   // D1 drained
+                GDN_TR(1, c, 1);
                 fence_after_sync();
                 {   // a1: D1 = V^T T'^T
                     const uint32_t vt = sb + OFF_V + (uint32_t)(c & 1) * kVStage;
@@ -382,21 +404,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     for (int ks = 0; ks < 4; ++ks)
                         mma_ss(tb + TM_D1, smem_desc(vt + ks * 2048, 8192, 1024),
                                smem_desc(sb + OFF_TP + ks * 32, 16, 1024), id_a1, ks > 0);
-                    commit(bar(B_VE + (c & 1)));
                 }
                 if (!wait_bar(bar(B_S), c & 1, abort_flag, p.err)) break;
+                GDN_TR(1, c, 2);
                 fence_after_sync();
-                {   // a2: D1 -= S W~^T ;  b: D2 = S Q<-^T
-                    const uint32_t st = stage(c);
+                {   // a2: D1 -= S W~^T
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
                         mma_ts(tb + TM_D1, tb + TM_SBF + ks * 8, smem_desc(sb + OFF_WT + ks * 2048, 16384, 1024),
                                id_a2, 1);
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t off = 8192 + (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_ts(tb + TM_D2, tb + TM_SBF + ks * 8, smem_desc(st + off, 16, 1024), id_b, ks > 0);
-                    }
                     commit(bar(B_D1));
                     commit(bar(B_TWFREE));
                 }
@@ -404,10 +420,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 bool need_c = true, need_p2 = (c + 1 < nch);
                 const uint64_t t0 = globaltimer_ns();
                 while (need_c || need_p2) {
+                    bool idle = true;
                     if (need_c && mbar_try_wait(bar(B_X), c & 1)) {
+                        // (the chain epilogue drained D2 of the previous chunk before arriving here)
                         fence_after_sync();
                         const uint32_t st = stage(c);
                         const uint32_t aq = sb + OFF_AQK + (uint32_t)(c & 1) * 8192;
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {   // b: D2 = S Q<-^T
+                            const uint32_t off = 8192 + (ks >> 2) * 16384 + (ks & 3) * 32;
+                            mma_ts(tb + TM_D2, tb + TM_SBF + ks * 8, smem_desc(st + off, 16, 1024), id_b, ks > 0);
+                        }
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)   // c1: D2 += V_new^T Aqk^T
                             mma_ts(tb + TM_D2, tb + TM_X1 + ks * 8, smem_desc(aq + ks * 32, 16, 1024), id_c1, 1);
@@ -418,12 +441,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                         commit(bar(B_QKE + c % 3));
                         commit(bar(B_AQKF + (c & 1)));
                         need_c = false;
+                        idle = false;
+                        GDN_TR(1, c, 3);
                     }
                     if (need_p2 && mbar_try_wait(bar(B_TRDY), (c + 1) & 1)) {
                         fence_after_sync();
                         issue_p2(c + 1);
                         need_p2 = false;
+                        idle = false;
+                        GDN_TR(1, c, 4);
                     }
+                    if (idle) __nanosleep(32);
                     if (*abort_flag) { ok = false; break; }
                     if (globaltimer_ns() - t0 > kWaitLimitNs) {
                         *abort_flag = 1;
@@ -444,18 +472,30 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
         float *Lf = reinterpret_cast<float *>(sm + OFF_LF);
         float *Tf = reinterpret_cast<float *>(sm + OFF_TF);
         float *Mt = reinterpret_cast<float *>(sm + OFF_MT);
+        // rows 0-63 carry g, rows 64-127 carry beta; the next chunk's values
+        // are loaded one iteration ahead to hide the global-memory latency
+        auto load_gate = [&](int c) -> float {
+            const int r = prow & 63;
+            const int rows_c = min(kChunk, len - c * kChunk);
+            if (r >= rows_c) return 0.f;
+            const int64_t t = (tok0 + (int64_t)c * kChunk + r) * H + h;
+            return prow < 64 ? p.g[t] : p.beta[t];
+        };
+        float gnext = (nch > 0) ? load_gate(0) : 0.f;
         for (int c = 0; c < nch; ++c) {
+            const float gcur = gnext;
+            if (c + 1 < nch) gnext = load_gate(c + 1);
             const int s = c % 3;
             const int rows = min(kChunk, len - c * kChunk);
-            const int64_t z0 = tok0 + (int64_t)c * kChunk;
             float *sc = sc_all + s * 5 * 64;
             const float *bsum = sc, *bet = sc + 64, *rk = sc + 128, *rq = sc + 192;
             uint8_t *st = sm + OFF_QK + s * kQKStage;
+            if (prow == 0) GDN_TR(0, c, 0);
 
-            // (1) gates: chunk-local cumulative log-gate, beta
+            // (1) gates: chunk-local cumulative log-gate (base 2), beta
             float x = 0.f;
             if (prow < 64) {
-                x = (prow < rows) ? p.g[(z0 + prow) * H + h] : 0.f;
+                x = gcur * kLog2e;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const float y = __shfl_up_sync(0xffffffffu, x, o);
@@ -463,29 +503,32 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 }
                 if (lane == 31) Mt[prow >> 5] = x;
             } else {
-                const int r = prow - 64;
-                sc[64 + r] = (r < rows) ? p.beta[(z0 + r) * H + h] : 0.f;
+                sc[prow] = gcur;   // beta (0 on padded rows)
             }
             group_sync(1, 128);
             if (prow < 64) sc[prow] = x + ((prow >= 32) ? Mt[0] : 0.f);
             group_sync(1, 128);
             if (prow == 0) mbar_arrive(bar(B_GATE + s));
+            if (prow == 0) GDN_TR(0, c, 1);
 
             // (2) inverse norms from the landed tiles
             bool ok = wait_bar(bar(B_QKF + s), (c / 3) & 1, abort_flag, p.err);
+            if (prow == 0) GDN_TR(0, c, 2);
             {
                 const int r = prow & 63;
                 const bool isq = prow >= 64;
                 const uint8_t *row = st + (isq ? 8192 : 0) + r * 128;
-                const float ss = row_sumsq(row) + row_sumsq(row + 16384);
+                const float ss = row_sumsq(row, r) + row_sumsq(row + 16384, r);
                 float inv = p.l2 ? 1.f / sqrtf(ss + kL2Eps) : 1.f;
                 if (isq) inv *= p.scale;
                 sc[(isq ? 192 : 128) + r] = (r < rows) ? inv : 0.f;
             }
             if (group_sync_or(2 + 0, 128, !ok || *abort_flag)) break;
+            if (prow == 0) GDN_TR(0, c, 3);
 
             // (3) Gram masking: L (rows 0-63) and Aqk (rows 64-127)
             ok = wait_bar(bar(B_P1), c & 1, abort_flag, p.err);
+            if (prow == 0) GDN_TR(0, c, 4);
             fence_after_sync();
             {
                 float G[64];
@@ -500,9 +543,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 if (prow < 64) {
                     const int r = prow;
                     const float br = bsum[r], f = bet[r] * rk[r];
-                    float *Lr = Lf + r * LDL;
+                    float *Lr = Lf + r * LDA;
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) Lr[i] = (i < r) ? f * expf(br - bsum[i]) * rk[i] * G[i] : 0.f;
+                    for (int i = 0; i < 64; ++i) Lr[i] = (i < r) ? f * exp2f(br - bsum[i]) * rk[i] * G[i] : 0.f;
                 } else {
                     const int r = prow - 64;
                     if (c >= 2) ok = ok && wait_bar(bar(B_AQKF + (c & 1)), ((c - 2) >> 1) & 1, abort_flag, p.err);
@@ -514,8 +557,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int i0 = ch * 8 + 2 * e;
-                            const float a0 = (i0 <= r) ? f * expf(br - bsum[i0]) * rk[i0] * G[i0] : 0.f;
-                            const float a1 = (i0 + 1 <= r) ? f * expf(br - bsum[i0 + 1]) * rk[i0 + 1] * G[i0 + 1] : 0.f;
+                            const float a0 = (i0 <= r) ? f * exp2f(br - bsum[i0]) * rk[i0] * G[i0] : 0.f;
+                            const float a1 = (i0 + 1 <= r) ? f * exp2f(br - bsum[i0 + 1]) * rk[i0 + 1] * G[i0 + 1] : 0.f;
                             w[e] = pack_bf16(a0, a1);
                         }
                         *reinterpret_cast<uint4 *>(aq + sw128_offset(r, ch * 8)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -527,8 +570,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             if (group_sync_or(2, 128, !ok || *abort_flag)) break;
 
             // (4) T = (I + L)^{-1};  T' = T diag(beta),  T'' = T diag(beta e^b rk)
+            if (prow == 0) GDN_TR(0, c, 5);
             solve_unit_lower(Lf, Tf, Mt, prow);
+            if (prow == 0) GDN_TR(0, c, 6);
             if (c >= 1) ok = wait_bar(bar(B_TWFREE), (c - 1) & 1, abort_flag, p.err);
+            if (prow == 0) GDN_TR(0, c, 7);
             {
                 const int r = prow >> 1, i0 = (prow & 1) * 32;
 #pragma unroll
@@ -540,7 +586,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                         const float t0 = Tf[r * LDL + i], t1 = Tf[r * LDL + i + 1];
                         const float p0 = t0 * bet[i], p1 = t1 * bet[i + 1];
                         w1[e] = pack_bf16(p0, p1);
-                        w2[e] = pack_bf16(p0 * expf(bsum[i]) * rk[i], p1 * expf(bsum[i + 1]) * rk[i + 1]);
+                        w2[e] = pack_bf16(p0 * exp2f(bsum[i]) * rk[i], p1 * exp2f(bsum[i + 1]) * rk[i + 1]);
                     }
                     const uint32_t off = sw128_offset(r, i0 + ch * 8);
                     *reinterpret_cast<uint4 *>(sm + OFF_TP + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
@@ -550,9 +596,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             fence_proxy_async();
             if (group_sync_or(2, 128, !ok || *abort_flag)) break;
             if (prow == 0) mbar_arrive(bar(B_TRDY));
+            if (prow == 0) GDN_TR(0, c, 8);
 
             // (5) W~^T to shared memory; K -> K->, Q -> Q<- in place
             ok = wait_bar(bar(B_P2), c & 1, abort_flag, p.err);
+            if (prow == 0) GDN_TR(0, c, 9);
             fence_after_sync();
             {
                 uint32_t u[16];
@@ -572,15 +620,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 }
                 const int r = prow >> 1, kb = prow & 1;
                 const float bC = bsum[63];
-                const float fk = (r < rows) ? expf(bC - bsum[r]) * rk[r] : 0.f;
-                const float fq = (r < rows) ? expf(bsum[r]) * rq[r] : 0.f;
-                row_scale(st + kb * 16384 + r * 128, fk);
-                row_scale(st + 8192 + kb * 16384 + r * 128, fq);
+                const float fk = (r < rows) ? exp2f(bC - bsum[r]) * rk[r] : 0.f;
+                const float fq = (r < rows) ? exp2f(bsum[r]) * rq[r] : 0.f;
+                row_scale(st + kb * 16384 + r * 128, r, fk);
+                row_scale(st + 8192 + kb * 16384 + r * 128, r, fq);
             }
             fence_before_sync();
             fence_proxy_async();
             if (group_sync_or(2, 128, !ok || *abort_flag)) break;
             if (prow == 0) mbar_arrive(bar(B_PREP));
+            if (prow == 0) GDN_TR(0, c, 10);
         }
     } else {
         // ------------------------------------------------------------ chain epilogue
@@ -596,7 +645,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
         } else {
             bool ok = wait_bar(bar(B_GATE), 0, abort_flag, p.err);
             {
-                const float e0 = expf(sc_all[63]);
+                const float e0 = exp2f(sc_all[63]);
 #pragma unroll
                 for (int q2 = 0; q2 < 4; ++q2) {   // 32 state entries per pass
                     float v[32];
@@ -626,6 +675,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 const int64_t z0 = tok0 + (int64_t)c * kChunk;
                 // V_new^T -> bf16 A operand
                 ok = wait_bar(bar(B_D1), c & 1, abort_flag, p.err);
+                if (j == 0) GDN_TR(2, c, 0);
                 fence_after_sync();
 #pragma unroll
                 for (int q2 = 0; q2 < 2; ++q2) {
@@ -644,27 +694,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 fence_before_sync();
                 if (group_sync_or(3, 128, !ok || *abort_flag)) break;
                 if (j == 0) mbar_arrive(bar(B_X));
-                // outputs and the next state
+                if (j == 0) GDN_TR(2, c, 1);
+                // next state first (it gates the next chunk), then the outputs
                 ok = wait_bar(bar(B_D2), c & 1, abort_flag, p.err);
+                if (j == 0) GDN_TR(2, c, 2);
                 fence_after_sync();
-                {
-                    __nv_bfloat16 *orow = p.out + (size_t)z0 * H * dv + (size_t)h * dv + j0 + j;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t u[16];
-                        tmem_ld16(lane_base + TM_D2 + q * 16, u);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int r = q * 16 + e;
-                            if (ok && r < rows) orow[(size_t)r * H * dv] = __float2bfloat16_rn(__uint_as_float(u[e]));
-                        }
-                    }
-                }
                 if (c + 1 < nch) {
                     const int s1 = (c + 1) % 3;
                     ok = ok && wait_bar(bar(B_GATE + s1), ((c + 1) / 3) & 1, abort_flag, p.err);
-                    const float e1 = expf(sc_all[s1 * 5 * 64 + 63]);
+                    if (j == 0) GDN_TR(2, c, 3);
+                    const float e1 = exp2f(sc_all[s1 * 5 * 64 + 63]);
 #pragma unroll
                     for (int q2 = 0; q2 < 4; ++q2) {
                         uint32_t a[16], b[16], pk[16];
@@ -689,6 +728,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     fence_before_sync();
                     if (group_sync_or(3, 128, !ok || *abort_flag)) break;
                     if (j == 0) mbar_arrive(bar(B_S));
+                    if (j == 0) GDN_TR(2, c, 4);
                 } else if (p.final_state && ok) {
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
@@ -701,6 +741,34 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                                 make_float4(__uint_as_float(u[e]), __uint_as_float(u[e + 1]),
                                             __uint_as_float(u[e + 2]), __uint_as_float(u[e + 3]));
                     }
+                }
+                // O^T (row j = output column j0 + j) through a [64 r][128 j] bf16 staging
+                // tile in this chunk's V stage (a1 has long completed), then 16-B stores
+                {
+                    uint8_t *stg = sm + OFF_V + (uint32_t)(c & 1) * kVStage;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t u[16];
+                        tmem_ld16(lane_base + TM_D2 + q * 16, u);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            *reinterpret_cast<__nv_bfloat16 *>(stg + ((q * 16 + e) * 128 + j) * 2) =
+                                __float2bfloat16_rn(__uint_as_float(u[e]));
+                    }
+                    fence_before_sync();
+                    if (group_sync_or(3, 128, !ok || *abort_flag)) break;
+                    __nv_bfloat16 *obase = p.out + (size_t)z0 * H * dv + (size_t)h * dv + j0;
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int idx = it * 128 + j, r = idx >> 4, ch = idx & 15;
+                        if (r < rows)
+                            *reinterpret_cast<uint4 *>(obase + (size_t)r * H * dv + ch * 8) =
+                                *reinterpret_cast<const uint4 *>(stg + r * 256 + ch * 16);
+                    }
+                    if (group_sync_or(3, 128, !ok || *abort_flag)) break;
+                    if (j == 0) mbar_arrive(bar(B_VE + (c & 1)));   // the V stage may be refilled
+                    if (j == 0) GDN_TR(2, c, 5);
                 }
             }
         }
@@ -745,7 +813,15 @@ bool make_tmap(CUtensorMap *m, const void *base, int d, int H, int64_t rows)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+#ifdef GDN_KERNEL_TRACE
+long long *g_trace_buffer = nullptr;
+#endif
+
 }  // namespace
+
+#ifdef GDN_KERNEL_TRACE
+extern "C" void gdn_debug_set_trace(long long *buf) { g_trace_buffer = buf; }
+#endif
 
 bool chunk_tc_supported(int dt, int dk, int dv, int64_t tokens)
 {
@@ -769,6 +845,9 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st)
     p.gm = a.gm;
     p.scale = a.scale;
     p.l2 = a.l2;
+#ifdef GDN_KERNEL_TRACE
+    p.trace = g_trace_buffer;
+#endif
     cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTc);
     if (e != cudaSuccess) return e;
     dim3 grid(a.gm.N, a.gm.H, a.gm.dv / 128);
