@@ -45,9 +45,9 @@ size_t gdn_chunk_fwd_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk,
     if (!chunk_dims_supported(dk, dv)) return 0;
     const bool varlen = num_seqs > 0;
     if (varlen && B != 1) return 0;
-    // the tensor-core path needs only the 256-B header (device error word)
-    if (chunk_tc_supported(dt == GDN_BF16 ? 1 : 0, dk, dv, (int64_t)B * T)) return 256;
     const int64_t slots = num_slots(B, T, varlen ? num_seqs : B, varlen);
+    if (chunk_tc_supported(dt == GDN_BF16 ? 1 : 0, dk, dv, (int64_t)B * T))
+        return chunk_tc_workspace_bytes(slots, H);
     return chunk_workspace_layout(slots, H, dk, dv).total;
 }
 

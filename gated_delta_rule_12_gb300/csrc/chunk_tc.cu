@@ -1,37 +1,38 @@
-// chunk_tc.cu -- fused chunked forward of the gated delta rule on the tensor
-// cores (tcgen05 + tensor memory + TMA), bf16 inputs, dk = 128, dv % 128 == 0.
+// chunk_tc.cu -- chunked forward of the gated delta rule on the tensor cores
+// (tcgen05 + tensor memory + TMA), bf16 inputs, dk = 128, dv % 128 == 0.
 //
-// One CTA per (sequence, head, 128-row slice of S) runs every step of
-// "Gated Delta Networks: Improving Mamba2 with Delta Rule", §3.3 for its
-// sequence, chunk after chunk, with the fp32 state S resident in tensor
-// memory for the whole sequence.  Per chunk of C = 64 tokens (row-stacked):
+// "Gated Delta Networks: Improving Mamba2 with Delta Rule", §3.3, split into the
+// two kernels its structure suggests:
 //
-//   prologue   b_r = sum_{i<=r} g_i; rk_r = 1/||k_r||, rq_r = scale/||q_r||
-//   P1 (MMA)   G = [K; Q] K^T                              (128 x 64, fp32)
-//   Gram mask  L_ri  = beta_r e^{b_r-b_i} rk_r rk_i G_ri,   i < r   (system)
-//              Aqk_ri = e^{b_r-b_i} rq_r rk_i G_(64+r)i,    i <= r  (Q K^T o Gamma)
-//   solve      T = (I + L)^{-1}  (blocked: 16x16 diagonal blocks by forward
-//              substitution, then two levels of block merges)
-//              T'  = T diag(beta),  T'' = T diag(beta e^b rk)
-//   P2 (MMA)   W~^T = K^T T''^T     (W~ = W<- of the pages, normalised keys)
-//   a1, a2     V_new^T = V^T T'^T - S W~^T                 (U~ - W<- S^T)^T
-//   b, c1      O^T = S Q<-^T + V_new^T Aqk^T,   Q<- = diag(e^b rq) Q
-//   c2         S  <- e^{b_C} S + V_new^T K->,   K-> = diag(e^{b_C-b} rk) K
+// ut_tc_kernel -- one CTA per (chunk, head), all chunks in parallel (the
+//   chunk-local UT transform, with the prologue folded in).  Per chunk of
+//   C = 64 row-stacked tokens:
+//     prologue   b_r = sum_{i<=r} g_i (chunk-local, base 2 internally);
+//                rk_r = 1/||k_r||, rq_r = scale/||q_r||
+//     P1 (MMA)   G = [K; Q] K^T                               (128 x 64, fp32)
+//     masks      L_ri   = beta_r e^{b_r-b_i} rk_r rk_i G_ri,   i <  r   (the system)
+//                Aqk_ri = e^{b_r-b_i} rq_r rk_i G_(64+r)i,     i <= r   (Q K^T o Gamma)
+//     solve      T = (I + L)^{-1} (16x16 diagonal blocks by forward substitution,
+//                then the block rule for the 16->32 and 32->64 merges)
+//                T' = T diag(beta),  T'' = T diag(beta e^b rk)
+//     P2 (MMA)   W~^T = K^T T''^T   (W<- of the pages for the normalised keys)
+//   and writes T', W~^T, Aqk (bf16, already in the 128-B-swizzled tile layout
+//   the recurrence kernel's MMAs read) plus the per-row factors
+//   fq_r = e^{b_r} rq_r, fk_r = e^{b_C - b_r} rk_r and e^{b_C} to the workspace.
+//
+// recur_tc_kernel -- one CTA per (sequence, head, 128-row slice of S), the
+//   sequential inter-chunk recurrence with the fp32 state resident in tensor
+//   memory for the whole sequence:
+//     a1, a2     V_new^T = V^T T'^T - S W~^T                  ((U~ - W<- S^T)^T)
+//     c2         S <- e^{b_C} S + (V_new^T diag(fk)) K         (K-> folded into V_new)
+//     b, c1      O^T = diag-scaled (S Q^T) + V_new^T Aqk^T     (O = Q<- S^T + Aqk V_new)
 //
 // All gate ratios are exp(b_r - b_i) with i <= r (never 1/gamma), so heavy
 // decay cannot overflow.  The output mask is the decay mask Gamma
-// ("【论文解读】Gated Delta Network", §二(一)2(3)).
-//
-// Warp roles (320 threads):
-//   warp 0      TMA producer (q/k/v tiles, 128-B swizzle) and TMEM allocator
-//   warp 1      single-thread tcgen05.mma issuer
-//   warps 2-5   "prep": prologue, Gram masking, solve, operand preparation for
-//               chunk c+1 while the chain runs chunk c
-//   warps 6-9   "chain": tensor-memory epilogues of the recurrence (row j of
-//               S per thread), output stores, final state
-// Every wait is bounded (globaltimer); a timeout records GDN device error
-// kDevErrTimeout in the workspace header, raises a CTA-wide abort flag, and
-// all roles unwind to the common exit, where tensor memory is released.
+// ("【论文解读】Gated Delta Network", §二(一)2(3)).  Every wait is bounded
+// (globaltimer); a timeout records kDevErrTimeout in the workspace header,
+// raises a CTA-wide abort flag, and all roles unwind to the common exit, where
+// tensor memory is released.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -44,84 +45,67 @@ namespace {
 
 using namespace umma;
 
-constexpr int kThreadsTc = 320;
-constexpr uint32_t kQKStage = 32768;   // [K kb0][Q kb0][K kb1][Q kb1], 8 KB each (64 rows x 128 B)
-constexpr uint32_t kVStage = 16384;    // [V cols 0-63][V cols 64-127]
 constexpr uint32_t LDA = 65;           // fp32 row pitch of L (conflict-free row-per-thread writes)
 constexpr uint32_t LDL = 68;           // fp32 row pitch of T (16-B aligned rows for vector loads)
 constexpr float kLog2e = 1.4426950408889634f;
-
-constexpr uint32_t OFF_QK = 0;
-constexpr uint32_t OFF_V = OFF_QK + 3 * kQKStage;
-constexpr uint32_t OFF_TP = OFF_V + 2 * kVStage;      // T'   bf16 [64 r][64 i] K-major
-constexpr uint32_t OFF_TPP = OFF_TP + 8192;           // T''  bf16 [64 r][64 i] K-major
-constexpr uint32_t OFF_WT = OFF_TPP + 8192;           // W~^T bf16 [128 d][64 r] (MN-major B)
-constexpr uint32_t OFF_AQK = OFF_WT + 16384;          // Aqk  bf16 [64 r][64 i] x 2 buffers
-constexpr uint32_t OFF_LF = OFF_AQK + 16384;          // L    fp32 [64][LDA]
-constexpr uint32_t OFF_TF = OFF_LF + 64 * LDA * 4;    // T    fp32 [64][LDL]
-constexpr uint32_t OFF_MT = OFF_TF + 64 * LDL * 4;    // merge temp fp32 [32][33]
-constexpr uint32_t OFF_SC = OFF_MT + 32 * 33 * 4;     // per stage: b, beta, rk, rq, spare [5][64] fp32
-constexpr uint32_t OFF_BAR = OFF_SC + 3 * 5 * 64 * 4;
-constexpr int kNumBars = 32;
-constexpr uint32_t OFF_MISC = OFF_BAR + kNumBars * 8;
-constexpr uint32_t kSmemTc = OFF_MISC + 64 + 1024;    // + slack for 1024-B alignment
-static_assert(kSmemTc <= 232448, "shared memory budget exceeded");
-static_assert(OFF_LF % 16 == 0 && OFF_TF % 16 == 0 && OFF_MT % 16 == 0 && OFF_SC % 16 == 0, "alignment");
-
-// tensor-memory columns (512 allocated)
-constexpr uint32_t TM_S = 0;      // fp32 state, 128 columns
-constexpr uint32_t TM_SBF = 128;  // bf16 state (A operand), 64 columns
-constexpr uint32_t TM_D1 = 192;   // V_new^T accumulator, 64
-constexpr uint32_t TM_D2 = 256;   // O^T accumulator, 64
-constexpr uint32_t TM_X1 = 320;   // V_new^T bf16 (A operand), 32
-constexpr uint32_t TM_P1 = 384;   // [K;Q] K^T accumulator, 64
-constexpr uint32_t TM_P2 = 448;   // W~^T accumulator, 64
-
-// mbarriers
-enum : int {
-    B_QKF = 0,      // [3] q/k tile landed
-    B_QKE = 3,      // [3] q/k stage free (chain done with K-> and Q<-)
-    B_VF = 6,       // [2] v tile landed
-    B_VE = 8,       // [2] v stage free
-    B_P1 = 10,      // P1 accumulator ready
-    B_P2 = 11,      // P2 accumulator ready
-    B_TRDY = 12,    // T', T'' written
-    B_PREP = 13,    // all chain operands of the chunk ready
-    B_TWFREE = 14,  // T' and W~^T of the previous chunk consumed
-    B_AQKF = 15,    // [2] Aqk buffer consumed
-    B_D1 = 17,      // V_new^T accumulated
-    B_D2 = 18,      // O^T and the state update accumulated
-    B_X = 19,       // V_new^T bf16 written to tensor memory (and D1 drained)
-    B_S = 20,       // bf16 state written, fp32 state pre-decayed (and D2 drained)
-    B_GATE = 21,    // [3] cumulative gates of a stage written
-    B_FIN = 24      // final drain of the MMA pipe
-};
-
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s: legitimate waits are microseconds
 
-struct TcParams {
-    const float *g, *beta, *init_state;
-    __nv_bfloat16 *out;
-    float *final_state;
-    unsigned *err;
-    Geometry gm;
-    float scale;
-    int l2;
-#ifdef GDN_KERNEL_TRACE
-    long long *trace;
-#endif
-};
+// Per (chunk, head) block of the workspace written by ut_tc_kernel.
+constexpr uint32_t PB_TP = 0;          // T'   bf16 [64 r][64 i]   (K-major, swizzled)
+constexpr uint32_t PB_WT = 8192;       // W~^T bf16 [128 d][64 r]  (MN-major, swizzled)
+constexpr uint32_t PB_AQK = 24576;     // Aqk  bf16 [64 r][64 i]   (K-major, swizzled)
+constexpr uint32_t PB_SC = 32768;      // fq[64], fk[64], e^{b_C}  (fp32)
+constexpr uint32_t kPrepBlock = 33792;
+constexpr uint32_t kWsHeader = 1024;   // device error word + padding
+
+// ---- ut_tc_kernel shared memory
+constexpr int kThreadsUt = 160;        // warp 0: TMA, MMA, TMEM; warps 1-4: 128 "prep" threads
+constexpr uint32_t U_QK = 0;           // [K kb0][Q kb0][K kb1][Q kb1], 8 KB each
+constexpr uint32_t U_TPP = 32768;      // T'' 8 KB
+constexpr uint32_t U_LF = 40960;       // L fp32 [64][LDA]
+constexpr uint32_t U_TF = U_LF + 64 * LDA * 4;
+constexpr uint32_t U_MT = U_TF + 64 * LDL * 4;
+constexpr uint32_t U_SC = U_MT + 32 * 33 * 4;     // b, beta, rk, rq [4][64] fp32
+constexpr uint32_t U_BAR = U_SC + 4 * 64 * 4;
+constexpr uint32_t U_MISC = U_BAR + 8 * 8;
+constexpr uint32_t kSmemUt = U_MISC + 64 + 1024;
+static_assert(U_TF % 16 == 0 && U_MT % 16 == 0 && U_SC % 16 == 0, "alignment");
+static_assert(2 * kSmemUt <= 232448, "two prep CTAs per SM");
+
+// ---- recur_tc_kernel shared memory: two stages of [prep block | Q,K tile | V tile]
+constexpr int kThreadsRc = 192;        // warp 0: TMA, TMEM; warp 1: MMA; warps 2-5: epilogue
+constexpr uint32_t R_QK = 34816;       // within a stage (1024-aligned)
+constexpr uint32_t R_V = R_QK + 32768;
+constexpr uint32_t R_STAGE = R_V + 16384;
+constexpr uint32_t R_BAR = 2 * R_STAGE;
+constexpr uint32_t R_MISC = R_BAR + 16 * 8;
+constexpr uint32_t kSmemRc = R_MISC + 64 + 1024;
+static_assert(R_STAGE % 1024 == 0 && kSmemRc <= 232448, "recurrence smem");
+constexpr uint32_t kStageTx = kPrepBlock + 32768 + 16384;
+
+// recurrence tensor-memory columns (512)
+constexpr uint32_t TM_S = 0;      // fp32 state, 128
+constexpr uint32_t TM_SBF = 128;  // bf16 state x 2 buffers (by chunk parity), 64 each
+constexpr uint32_t TM_D1 = 256;   // V_new^T accumulator, 64
+constexpr uint32_t TM_D2A = 320;  // S Q^T accumulator, 64
+constexpr uint32_t TM_D2B = 384;  // V_new^T Aqk^T accumulator, 64
+constexpr uint32_t TM_X1 = 448;   // V_new^T bf16, 32
+constexpr uint32_t TM_X1K = 480;  // V_new^T diag(fk) bf16, 32
+
+enum : int { RB_FULL = 0, RB_EMPTY = 2, RB_D1 = 4, RB_X = 5, RB_S = 6, RB_D2S = 7, RB_D2O = 8, RB_FIN = 9 };
+enum : int { UB_QK = 0, UB_P1 = 1, UB_TRDY = 2, UB_P2 = 3, UB_FIN = 4 };
 
 // Development-only phase timestamps (SM clock) of the first CTA; compiled out
 // of the library unless GDN_KERNEL_TRACE is defined.
 #ifdef GDN_KERNEL_TRACE
-#define GDN_TR(role, c, ev)                                                                          \
+long long *g_trace_buffer = nullptr;
+#define GDN_TR(trace, role, c, ev)                                                                   \
     do {                                                                                             \
-        if (p.trace && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (c) < 16)            \
-            p.trace[((role) * 16 + (c)) * 16 + (ev)] = clock64();                                    \
+        if ((trace) && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (c) < 16)            \
+            (trace)[((role) * 16 + (c)) * 16 + (ev)] = clock64();                                    \
     } while (0)
 #else
-#define GDN_TR(role, c, ev) do { } while (0)
+#define GDN_TR(trace, role, c, ev) do { } while (0)
 #endif
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned *err)
@@ -187,23 +171,6 @@ __device__ __forceinline__ float row_sumsq(const uint8_t *row, int r)
         }
     }
     return ss;
-}
-
-// Multiply the 64 bf16 of one 128-B row segment by f, in place (chunk order as above).
-__device__ __forceinline__ void row_scale(uint8_t *row, int r, float f)
-{
-#pragma unroll
-    for (int ch0 = 0; ch0 < 8; ++ch0) {
-        const int ch = (ch0 ^ r) & 7;
-        uint4 u = *reinterpret_cast<uint4 *>(row + ch * 16);
-        uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 x = unpack_bf16(w[e]);
-            w[e] = pack_bf16(x.x * f, x.y * f);
-        }
-        *reinterpret_cast<uint4 *>(row + ch * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
 }
 
 // T = (I + L)^{-1} for a strictly lower 64x64 L (row pitch LDA; T pitch LDL), 128 threads.
@@ -284,236 +251,117 @@ __device__ __forceinline__ void solve_unit_lower(const float *__restrict__ Lf, f
     group_sync(1, 128);
 }
 
-__global__ void __launch_bounds__(kThreadsTc, 1)
-chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                const __grid_constant__ CUtensorMap tmv, const TcParams p)
+
+// ===========================================================================
+// chunk-local UT transform
+// ===========================================================================
+struct UtParams {
+    const float *g, *beta;
+    uint8_t *blocks;
+    unsigned *err;
+    Geometry gm;
+    float scale;
+    int l2;
+    long long *trace;
+};
+
+__global__ void __launch_bounds__(kThreadsUt, 2)
+ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk, const UtParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sb = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n = blockIdx.x, h = blockIdx.y, j0 = blockIdx.z * 128;
+    // the first CTA clears the call's device error word (a timeout anywhere
+    // is at least kWaitLimitNs later)
+    if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) *p.err = kDevErrNone;
+    const int64_t slot = blockIdx.x;
+    const int h = blockIdx.y;
     const Geometry gm = p.gm;
-    const int H = gm.H, dv = gm.dv;
-    int64_t tok0;
-    int len;
-    seq_span(gm, n, tok0, len);
-    const int nch = ceil_div(len, kChunk);
-    uint32_t *tmem_sh = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_MISC + 4);
-    float *sc_all = reinterpret_cast<float *>(sm + OFF_SC);
-    auto bar = [&](int i) -> uint32_t { return sb + OFF_BAR + 8u * (uint32_t)i; };
+    int n, c, rows;
+    int64_t tok0c;
+    if (!slot_to_chunk(gm, slot, n, c, tok0c, rows)) return;
+    const int H = gm.H;
+    uint32_t *tmem_sh = reinterpret_cast<uint32_t *>(sm + U_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + U_MISC + 4);
+    auto bar = [&](int i) -> uint32_t { return sb + U_BAR + 8u * (uint32_t)i; };
+    uint8_t *blk = p.blocks + ((size_t)slot * H + h) * kPrepBlock;
 
-    // the first CTA clears the call's device error word; any timeout is at
-    // least kWaitLimitNs later, long after this store
-    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && tid == 0) *p.err = kDevErrNone;
     if (tid == 0) {
-        for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
+        for (int i = 0; i < 5; ++i) mbar_init(bar(i), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0) tmem_alloc(tmem_sh, 512);
+    if (warp == 0) tmem_alloc(tmem_sh, 128);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tb = *tmem_sh;
-    const uint32_t lane_base = tb + ((uint32_t)(32 * (warp & 3)) << 16);
+    const uint32_t TP1 = 0, TP2 = 64;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0 && nch > 0) {
-            prefetch_tmap(&tmq);
-            prefetch_tmap(&tmk);
-            prefetch_tmap(&tmv);
-            int last_qk = -1, last_v = -1;
-            for (int c = 0; c < nch; ++c) {
-                const int s = c % 3, sv = c & 1;
-                const int z = (int)(tok0 + (int64_t)c * kChunk);
-                if (c >= 3 && !wait_bar(bar(B_QKE + s), ((c / 3) - 1) & 1, abort_flag, p.err)) break;
-                const uint32_t st = sb + OFF_QK + s * kQKStage;
-                GDN_TR(3, c, 0);
-                mbar_expect_tx(bar(B_QKF + s), kQKStage);
-                tma_load_3d(st, &tmk, 0, h, z, bar(B_QKF + s));
-                tma_load_3d(st + 8192, &tmq, 0, h, z, bar(B_QKF + s));
-                tma_load_3d(st + 16384, &tmk, 64, h, z, bar(B_QKF + s));
-                tma_load_3d(st + 24576, &tmq, 64, h, z, bar(B_QKF + s));
-                last_qk = c;
-                if (c >= 2 && !wait_bar(bar(B_VE + sv), ((c >> 1) - 1) & 1, abort_flag, p.err)) break;
-                const uint32_t vt = sb + OFF_V + sv * kVStage;
-                mbar_expect_tx(bar(B_VF + sv), kVStage);
-                tma_load_3d(vt, &tmv, j0, h, z, bar(B_VF + sv));
-                tma_load_3d(vt + 8192, &tmv, j0 + 64, h, z, bar(B_VF + sv));
-                last_v = c;
-            }
-            if (*abort_flag) {
-                // let the copies still in flight land before the CTA exits
-                for (int c = (last_qk > 1 ? last_qk - 2 : 0); c <= last_qk; ++c)
-                    mbar_wait(bar(B_QKF + c % 3), (c / 3) & 1, 10000000ull);
-                for (int c = (last_v > 0 ? last_v - 1 : 0); c <= last_v; ++c)
-                    mbar_wait(bar(B_VF + (c & 1)), (c >> 1) & 1, 10000000ull);
-            }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && nch > 0) {
-            const uint32_t id_p1 = idesc_bf16(128, 64, false, false);
-            const uint32_t id_p2 = idesc_bf16(128, 64, true, false);
-            const uint32_t id_a1 = idesc_bf16(128, 64, true, false);
-            const uint32_t id_a2 = idesc_bf16(128, 64, false, true, true);   // negated B: -S W~^T
-            const uint32_t id_b = idesc_bf16(128, 64, false, false);
-            const uint32_t id_c1 = idesc_bf16(128, 64, false, false);
-            const uint32_t id_c2 = idesc_bf16(128, 128, false, true);
-            auto stage = [&](int c) -> uint32_t { return sb + OFF_QK + (uint32_t)(c % 3) * kQKStage; };
-            auto issue_p1 = [&](int c) {       // G = [K; Q] K^T
-                const uint32_t st = stage(c);
+        if (lane == 0) {
+            const int z = (int)tok0c;
+            mbar_expect_tx(bar(UB_QK), 32768);
+            tma_load_3d(sb + U_QK, &tmk, 0, h, z, bar(UB_QK));
+            tma_load_3d(sb + U_QK + 8192, &tmq, 0, h, z, bar(UB_QK));
+            tma_load_3d(sb + U_QK + 16384, &tmk, 64, h, z, bar(UB_QK));
+            tma_load_3d(sb + U_QK + 24576, &tmq, 64, h, z, bar(UB_QK));
+            if (wait_bar(bar(UB_QK), 0, abort_flag, p.err)) {
+                const uint32_t id_p1 = idesc_bf16(128, 64, false, false);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
+                for (int ks = 0; ks < 8; ++ks) {   // G = [K; Q] K^T
                     const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_ss(tb + TM_P1, smem_desc(st + off, 16, 1024), smem_desc(st + off, 16, 1024), id_p1, ks > 0);
+                    mma_ss(tb + TP1, smem_desc(sb + U_QK + off, 16, 1024), smem_desc(sb + U_QK + off, 16, 1024),
+                           id_p1, ks > 0);
                 }
-                commit(bar(B_P1));
-            };
-            auto issue_p2 = [&](int c) {       // W~^T = K^T T''^T
-                const uint32_t st = stage(c);
+                commit(bar(UB_P1));
+                if (wait_bar(bar(UB_TRDY), 0, abort_flag, p.err)) {
+                    fence_after_sync();
+                    const uint32_t id_p2 = idesc_bf16(128, 64, true, false);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_ss(tb + TM_P2, smem_desc(st + ks * 2048, 16384, 1024),
-                           smem_desc(sb + OFF_TPP + ks * 32, 16, 1024), id_p2, ks > 0);
-                commit(bar(B_P2));
-            };
-            bool ok = wait_bar(bar(B_QKF), 0, abort_flag, p.err);
-            if (ok) issue_p1(0);
-            ok = ok && wait_bar(bar(B_TRDY), 0, abort_flag, p.err);
-            if (ok) { fence_after_sync(); issue_p2(0); }
-            for (int c = 0; c < nch && ok; ++c) {
-                if (!wait_bar(bar(B_PREP), c & 1, abort_flag, p.err)) break;
-                GDN_TR(1, c, 0);
-                fence_after_sync();
-                if (c + 1 < nch) {
-                    if (!wait_bar(bar(B_QKF + (c + 1) % 3), ((c + 1) / 3) & 1, abort_flag, p.err)) break;
-                    issue_p1(c + 1);
-                }
-                if (!wait_bar(bar(B_VF + (c & 1)), (c >> 1) & 1, abort_flag, p.err)) break;
-                if (c > 0 && !wait_bar(bar(B_X), (c - 1) & 1, abort_flag, p.err)) break;   // D1 drained
-                GDN_TR(1, c, 1);
-                fence_after_sync();
-                {   // a1: D1 = V^T T'^T
-                    const uint32_t vt = sb + OFF_V + (uint32_t)(c & 1) * kVStage;
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_ss(tb + TM_D1, smem_desc(vt + ks * 2048, 8192, 1024),
-                               smem_desc(sb + OFF_TP + ks * 32, 16, 1024), id_a1, ks > 0);
-                }
-                if (!wait_bar(bar(B_S), c & 1, abort_flag, p.err)) break;
-                GDN_TR(1, c, 2);
-                fence_after_sync();
-                {   // a2: D1 -= S W~^T
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_ts(tb + TM_D1, tb + TM_SBF + ks * 8, smem_desc(sb + OFF_WT + ks * 2048, 16384, 1024),
-                               id_a2, 1);
-                    commit(bar(B_D1));
-                    commit(bar(B_TWFREE));
-                }
-                // the chain's second half and the next chunk's P2, whichever is ready first
-                bool need_c = true, need_p2 = (c + 1 < nch);
-                const uint64_t t0 = globaltimer_ns();
-                while (need_c || need_p2) {
-                    bool idle = true;
-                    if (need_c && mbar_try_wait(bar(B_X), c & 1)) {
-                        // (the chain epilogue drained D2 of the previous chunk before arriving here)
-                        fence_after_sync();
-                        const uint32_t st = stage(c);
-                        const uint32_t aq = sb + OFF_AQK + (uint32_t)(c & 1) * 8192;
-#pragma unroll
-                        for (int ks = 0; ks < 8; ++ks) {   // b: D2 = S Q<-^T
-                            const uint32_t off = 8192 + (ks >> 2) * 16384 + (ks & 3) * 32;
-                            mma_ts(tb + TM_D2, tb + TM_SBF + ks * 8, smem_desc(st + off, 16, 1024), id_b, ks > 0);
-                        }
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)   // c1: D2 += V_new^T Aqk^T
-                            mma_ts(tb + TM_D2, tb + TM_X1 + ks * 8, smem_desc(aq + ks * 32, 16, 1024), id_c1, 1);
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)   // c2: S += V_new^T K->
-                            mma_ts(tb + TM_S, tb + TM_X1 + ks * 8, smem_desc(st + ks * 2048, 16384, 1024), id_c2, 1);
-                        commit(bar(B_D2));
-                        commit(bar(B_QKE + c % 3));
-                        commit(bar(B_AQKF + (c & 1)));
-                        need_c = false;
-                        idle = false;
-                        GDN_TR(1, c, 3);
-                    }
-                    if (need_p2 && mbar_try_wait(bar(B_TRDY), (c + 1) & 1)) {
-                        fence_after_sync();
-                        issue_p2(c + 1);
-                        need_p2 = false;
-                        idle = false;
-                        GDN_TR(1, c, 4);
-                    }
-                    if (idle) __nanosleep(32);
-                    if (*abort_flag) { ok = false; break; }
-                    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                        *abort_flag = 1;
-                        atomicExch(p.err, kDevErrTimeout);
-                        ok = false;
-                        break;
-                    }
+                    for (int ks = 0; ks < 4; ++ks)   // W~^T = K^T T''^T
+                        mma_ss(tb + TP2, smem_desc(sb + U_QK + ks * 2048, 16384, 1024),
+                               smem_desc(sb + U_TPP + ks * 32, 16, 1024), id_p2, ks > 0);
+                    commit(bar(UB_P2));
                 }
             }
-            // every MMA issued above must complete before tensor memory is released
-            commit(bar(B_FIN));
-            mbar_wait(bar(B_FIN), 0, kWaitLimitNs);
+            if (*abort_flag) mbar_wait(bar(UB_QK), 0, 10000000ull);   // the tile copy must land before exit
+            commit(bar(UB_FIN));
+            mbar_wait(bar(UB_FIN), 0, kWaitLimitNs);
         }
         __syncwarp();
-    } else if (warp < 6) {
-        // ------------------------------------------------------------ prep group
+    } else {
         const int prow = 32 * (warp & 3) + lane;   // tensor-memory lane of this thread
-        float *Lf = reinterpret_cast<float *>(sm + OFF_LF);
-        float *Tf = reinterpret_cast<float *>(sm + OFF_TF);
-        float *Mt = reinterpret_cast<float *>(sm + OFF_MT);
-        // rows 0-63 carry g, rows 64-127 carry beta; the next chunk's values
-        // are loaded one iteration ahead to hide the global-memory latency
-        auto load_gate = [&](int c) -> float {
-            const int r = prow & 63;
-            const int rows_c = min(kChunk, len - c * kChunk);
-            if (r >= rows_c) return 0.f;
-            const int64_t t = (tok0 + (int64_t)c * kChunk + r) * H + h;
-            return prow < 64 ? p.g[t] : p.beta[t];
-        };
-        float gnext = (nch > 0) ? load_gate(0) : 0.f;
-        for (int c = 0; c < nch; ++c) {
-            const float gcur = gnext;
-            if (c + 1 < nch) gnext = load_gate(c + 1);
-            const int s = c % 3;
-            const int rows = min(kChunk, len - c * kChunk);
-            float *sc = sc_all + s * 5 * 64;
-            const float *bsum = sc, *bet = sc + 64, *rk = sc + 128, *rq = sc + 192;
-            uint8_t *st = sm + OFF_QK + s * kQKStage;
-            if (prow == 0) GDN_TR(0, c, 0);
-
-            // (1) gates: chunk-local cumulative log-gate (base 2), beta
-            float x = 0.f;
-            if (prow < 64) {
-                x = gcur * kLog2e;
+        float *Lf = reinterpret_cast<float *>(sm + U_LF);
+        float *Tf = reinterpret_cast<float *>(sm + U_TF);
+        float *Mt = reinterpret_cast<float *>(sm + U_MT);
+        float *sc = reinterpret_cast<float *>(sm + U_SC);
+        float *bsum = sc, *bet = sc + 64, *rk = sc + 128, *rq = sc + 192;
+        const uint32_t lane_base = tb + ((uint32_t)(32 * (warp & 3)) << 16);
+        uint8_t *st = sm + U_QK;
+        do {
+            // (1) gates: chunk-local cumulative log-gate in base 2, beta
+            {
+                const int r = prow & 63;
+                const int64_t t = (tok0c + r) * H + h;
+                float x = 0.f;
+                if (prow < 64) {
+                    x = (r < rows) ? p.g[t] * kLog2e : 0.f;
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, x, o);
-                    if (lane >= o) x += y;
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float y = __shfl_up_sync(0xffffffffu, x, o);
+                        if (lane >= o) x += y;
+                    }
+                    if (lane == 31) Mt[prow >> 5] = x;
+                } else {
+                    bet[r] = (r < rows) ? p.beta[t] : 0.f;
                 }
-                if (lane == 31) Mt[prow >> 5] = x;
-            } else {
-                sc[prow] = gcur;   // beta (0 on padded rows)
+                group_sync(1, 128);
+                if (prow < 64) bsum[prow] = x + ((prow >= 32) ? Mt[0] : 0.f);
             }
-            group_sync(1, 128);
-            if (prow < 64) sc[prow] = x + ((prow >= 32) ? Mt[0] : 0.f);
-            group_sync(1, 128);
-            if (prow == 0) mbar_arrive(bar(B_GATE + s));
-            if (prow == 0) GDN_TR(0, c, 1);
-
             // (2) inverse norms from the landed tiles
-            bool ok = wait_bar(bar(B_QKF + s), (c / 3) & 1, abort_flag, p.err);
-            if (prow == 0) GDN_TR(0, c, 2);
+            bool ok = wait_bar(bar(UB_QK), 0, abort_flag, p.err);
             {
                 const int r = prow & 63;
                 const bool isq = prow >= 64;
@@ -521,21 +369,19 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 const float ss = row_sumsq(row, r) + row_sumsq(row + 16384, r);
                 float inv = p.l2 ? 1.f / sqrtf(ss + kL2Eps) : 1.f;
                 if (isq) inv *= p.scale;
-                sc[(isq ? 192 : 128) + r] = (r < rows) ? inv : 0.f;
+                (isq ? rq : rk)[r] = (r < rows) ? inv : 0.f;
             }
-            if (group_sync_or(2 + 0, 128, !ok || *abort_flag)) break;
-            if (prow == 0) GDN_TR(0, c, 3);
+            if (group_sync_or(2, 128, !ok || *abort_flag)) break;
 
-            // (3) Gram masking: L (rows 0-63) and Aqk (rows 64-127)
-            ok = wait_bar(bar(B_P1), c & 1, abort_flag, p.err);
-            if (prow == 0) GDN_TR(0, c, 4);
+            // (3) masks: L (rows 0-63, to shared memory), Aqk (rows 64-127, to the workspace)
+            ok = wait_bar(bar(UB_P1), 0, abort_flag, p.err);
             fence_after_sync();
             {
                 float G[64];
                 uint32_t u[16];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    tmem_ld16(lane_base + TM_P1 + q * 16, u);
+                    tmem_ld16(lane_base + TP1 + q * 16, u);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 16; ++e) G[q * 16 + e] = __uint_as_float(u[e]);
@@ -548,8 +394,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     for (int i = 0; i < 64; ++i) Lr[i] = (i < r) ? f * exp2f(br - bsum[i]) * rk[i] * G[i] : 0.f;
                 } else {
                     const int r = prow - 64;
-                    if (c >= 2) ok = ok && wait_bar(bar(B_AQKF + (c & 1)), ((c - 2) >> 1) & 1, abort_flag, p.err);
-                    uint8_t *aq = sm + OFF_AQK + (c & 1) * 8192;
                     const float br = bsum[r], f = rq[r];
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch) {
@@ -561,20 +405,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                             const float a1 = (i0 + 1 <= r) ? f * exp2f(br - bsum[i0 + 1]) * rk[i0 + 1] * G[i0 + 1] : 0.f;
                             w[e] = pack_bf16(a0, a1);
                         }
-                        *reinterpret_cast<uint4 *>(aq + sw128_offset(r, ch * 8)) = make_uint4(w[0], w[1], w[2], w[3]);
+                        *reinterpret_cast<uint4 *>(blk + PB_AQK + sw128_offset(r, ch * 8)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
             }
             fence_before_sync();
-            fence_proxy_async();
             if (group_sync_or(2, 128, !ok || *abort_flag)) break;
 
-            // (4) T = (I + L)^{-1};  T' = T diag(beta),  T'' = T diag(beta e^b rk)
-            if (prow == 0) GDN_TR(0, c, 5);
+            // (4) T = (I + L)^{-1};  T' -> workspace,  T'' -> shared memory
             solve_unit_lower(Lf, Tf, Mt, prow);
-            if (prow == 0) GDN_TR(0, c, 6);
-            if (c >= 1) ok = wait_bar(bar(B_TWFREE), (c - 1) & 1, abort_flag, p.err);
-            if (prow == 0) GDN_TR(0, c, 7);
             {
                 const int r = prow >> 1, i0 = (prow & 1) * 32;
 #pragma unroll
@@ -589,24 +429,32 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                         w2[e] = pack_bf16(p0 * exp2f(bsum[i]) * rk[i], p1 * exp2f(bsum[i + 1]) * rk[i + 1]);
                     }
                     const uint32_t off = sw128_offset(r, i0 + ch * 8);
-                    *reinterpret_cast<uint4 *>(sm + OFF_TP + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-                    *reinterpret_cast<uint4 *>(sm + OFF_TPP + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+                    *reinterpret_cast<uint4 *>(blk + PB_TP + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+                    *reinterpret_cast<uint4 *>(sm + U_TPP + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
                 }
             }
             fence_proxy_async();
             if (group_sync_or(2, 128, !ok || *abort_flag)) break;
-            if (prow == 0) mbar_arrive(bar(B_TRDY));
-            if (prow == 0) GDN_TR(0, c, 8);
+            if (prow == 0) mbar_arrive(bar(UB_TRDY));
 
-            // (5) W~^T to shared memory; K -> K->, Q -> Q<- in place
-            ok = wait_bar(bar(B_P2), c & 1, abort_flag, p.err);
-            if (prow == 0) GDN_TR(0, c, 9);
+            // (5) W~^T and the per-row factors to the workspace
+            {
+                const int r = prow & 63;
+                const float bC = bsum[63];
+                if (prow < 64) {
+                    reinterpret_cast<float *>(blk + PB_SC)[r] = (r < rows) ? exp2f(bsum[r]) * rq[r] : 0.f;
+                } else {
+                    reinterpret_cast<float *>(blk + PB_SC)[64 + r] = (r < rows) ? exp2f(bC - bsum[r]) * rk[r] : 0.f;
+                    if (r == 0) reinterpret_cast<float *>(blk + PB_SC)[128] = exp2f(bC);
+                }
+            }
+            ok = wait_bar(bar(UB_P2), 0, abort_flag, p.err);
             fence_after_sync();
             {
                 uint32_t u[16];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    tmem_ld16(lane_base + TM_P2 + q * 16, u);
+                    tmem_ld16(lane_base + TP2 + q * 16, u);
                     tmem_wait_ld();
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
@@ -614,25 +462,145 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             w[e] = pack_bf16(__uint_as_float(u[hh * 8 + 2 * e]), __uint_as_float(u[hh * 8 + 2 * e + 1]));
-                        *reinterpret_cast<uint4 *>(sm + OFF_WT + sw128_offset(prow, q * 16 + hh * 8)) =
+                        *reinterpret_cast<uint4 *>(blk + PB_WT + sw128_offset(prow, q * 16 + hh * 8)) =
                             make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
-                const int r = prow >> 1, kb = prow & 1;
-                const float bC = bsum[63];
-                const float fk = (r < rows) ? exp2f(bC - bsum[r]) * rk[r] : 0.f;
-                const float fq = (r < rows) ? exp2f(bsum[r]) * rq[r] : 0.f;
-                row_scale(st + kb * 16384 + r * 128, r, fk);
-                row_scale(st + 8192 + kb * 16384 + r * 128, r, fq);
             }
             fence_before_sync();
-            fence_proxy_async();
-            if (group_sync_or(2, 128, !ok || *abort_flag)) break;
-            if (prow == 0) mbar_arrive(bar(B_PREP));
-            if (prow == 0) GDN_TR(0, c, 10);
+        } while (false);
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        fence_after_sync();
+        tmem_dealloc(tb, 128);
+    }
+}
+
+// ===========================================================================
+// inter-chunk recurrence
+// ===========================================================================
+struct RcParams {
+    const float *init_state;
+    const uint8_t *blocks;
+    __nv_bfloat16 *out;
+    float *final_state;
+    unsigned *err;
+    Geometry gm;
+    long long *trace;
+};
+
+__global__ void __launch_bounds__(kThreadsRc, 1)
+recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                const __grid_constant__ CUtensorMap tmv, const RcParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sb = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n = blockIdx.x, h = blockIdx.y, j0 = blockIdx.z * 128;
+    const Geometry gm = p.gm;
+    const int H = gm.H, dv = gm.dv;
+    int64_t tok0;
+    int len;
+    seq_span(gm, n, tok0, len);
+    const int nch = ceil_div(len, kChunk);
+    const int64_t slot0 = slot_base(gm, n);
+    uint32_t *tmem_sh = reinterpret_cast<uint32_t *>(sm + R_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + R_MISC + 4);
+    auto bar = [&](int i) -> uint32_t { return sb + R_BAR + 8u * (uint32_t)i; };
+    auto stage = [&](int c) -> uint32_t { return (uint32_t)(c & 1) * R_STAGE; };
+
+    if (tid == 0) {
+        for (int i = 0; i < 10; ++i) mbar_init(bar(i), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(tmem_sh, 512);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tb = *tmem_sh;
+    const uint32_t lane_base = tb + ((uint32_t)(32 * (warp & 3)) << 16);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ loads
+        if (lane == 0 && nch > 0) {
+            prefetch_tmap(&tmq);
+            prefetch_tmap(&tmk);
+            prefetch_tmap(&tmv);
+            int last = -1;
+            for (int c = 0; c < nch; ++c) {
+                const int s = c & 1;
+                if (c >= 2 && !wait_bar(bar(RB_EMPTY + s), ((c >> 1) - 1) & 1, abort_flag, p.err)) break;
+                GDN_TR(p.trace, 3, c, 0);
+                const uint32_t base = sb + stage(c);
+                const int z = (int)(tok0 + (int64_t)c * kChunk);
+                const uint8_t *src = p.blocks + ((size_t)(slot0 + c) * H + h) * kPrepBlock;
+                mbar_expect_tx(bar(RB_FULL + s), kStageTx);
+                bulk_load(base, src, kPrepBlock, bar(RB_FULL + s));
+                tma_load_3d(base + R_QK, &tmk, 0, h, z, bar(RB_FULL + s));
+                tma_load_3d(base + R_QK + 8192, &tmq, 0, h, z, bar(RB_FULL + s));
+                tma_load_3d(base + R_QK + 16384, &tmk, 64, h, z, bar(RB_FULL + s));
+                tma_load_3d(base + R_QK + 24576, &tmq, 64, h, z, bar(RB_FULL + s));
+                tma_load_3d(base + R_V, &tmv, j0, h, z, bar(RB_FULL + s));
+                tma_load_3d(base + R_V + 8192, &tmv, j0 + 64, h, z, bar(RB_FULL + s));
+                last = c;
+            }
+            if (*abort_flag)   // let the copies in flight land before the CTA exits
+                for (int c = (last > 0 ? last - 1 : 0); c <= last; ++c)
+                    mbar_wait(bar(RB_FULL + (c & 1)), (c >> 1) & 1, 10000000ull);
         }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0 && nch > 0) {
+            const uint32_t id_a1 = idesc_bf16(128, 64, true, false);
+            const uint32_t id_a2 = idesc_bf16(128, 64, false, true, true);   // negated B: -S W~^T
+            const uint32_t id_b = idesc_bf16(128, 64, false, false);
+            const uint32_t id_c1 = idesc_bf16(128, 64, false, false);
+            const uint32_t id_c2 = idesc_bf16(128, 128, false, true);
+            for (int c = 0; c < nch; ++c) {
+                const uint32_t base = sb + stage(c);
+                const uint32_t sbf = tb + TM_SBF + (uint32_t)(c & 1) * 64;
+                if (!wait_bar(bar(RB_FULL + (c & 1)), (c >> 1) & 1, abort_flag, p.err)) break;
+                if (c > 0 && !wait_bar(bar(RB_X), (c - 1) & 1, abort_flag, p.err)) break;   // D1 drained
+                fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)   // a1: D1 = V^T T'^T
+                    mma_ss(tb + TM_D1, smem_desc(base + R_V + ks * 2048, 8192, 1024),
+                           smem_desc(base + PB_TP + ks * 32, 16, 1024), id_a1, ks > 0);
+                if (!wait_bar(bar(RB_S), c & 1, abort_flag, p.err)) break;
+                GDN_TR(p.trace, 1, c, 0);
+                fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)   // a2: D1 -= S W~^T
+                    mma_ts(tb + TM_D1, sbf + ks * 8, smem_desc(base + PB_WT + ks * 2048, 16384, 1024), id_a2, 1);
+                commit(bar(RB_D1));
+                if (!wait_bar(bar(RB_X), c & 1, abort_flag, p.err)) break;
+                GDN_TR(p.trace, 1, c, 1);
+                fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)   // c2: S += (V_new^T diag(fk)) K
+                    mma_ts(tb + TM_S, tb + TM_X1K + ks * 8, smem_desc(base + R_QK + ks * 2048, 16384, 1024), id_c2, 1);
+                commit(bar(RB_D2S));
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {   // b: D2A = S Q^T
+                    const uint32_t off = R_QK + 8192 + (ks >> 2) * 16384 + (ks & 3) * 32;
+                    mma_ts(tb + TM_D2A, sbf + ks * 8, smem_desc(base + off, 16, 1024), id_b, ks > 0);
+                }
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)   // c1: D2B = V_new^T Aqk^T
+                    mma_ts(tb + TM_D2B, tb + TM_X1 + ks * 8, smem_desc(base + PB_AQK + ks * 32, 16, 1024), id_c1, ks > 0);
+                commit(bar(RB_D2O));
+            }
+            commit(bar(RB_FIN));   // every MMA must complete before tensor memory is released
+            mbar_wait(bar(RB_FIN), 0, kWaitLimitNs);
+        }
+        __syncwarp();
     } else {
-        // ------------------------------------------------------------ chain epilogue
+        // ------------------------------------------------------------ epilogue
         const int j = 32 * (warp & 3) + lane;   // row of S within the slice
         const size_t srow = (((size_t)n * H + h) * (size_t)dv + (size_t)(j0 + j)) * 128;
         if (nch == 0) {
@@ -643,9 +611,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     *reinterpret_cast<float4 *>(p.final_state + srow + d) = v4;
                 }
         } else {
-            bool ok = wait_bar(bar(B_GATE), 0, abort_flag, p.err);
+            bool ok = wait_bar(bar(RB_FULL), 0, abort_flag, p.err);
             {
-                const float e0 = exp2f(sc_all[63]);
+                const float e0 = reinterpret_cast<const float *>(sm + PB_SC)[128];
 #pragma unroll
                 for (int q2 = 0; q2 < 4; ++q2) {   // 32 state entries per pass
                     float v[32];
@@ -655,55 +623,62 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
                         v[e] = v4.x; v[e + 1] = v4.y; v[e + 2] = v4.z; v[e + 3] = v4.w;
                     }
-                    uint32_t pk[16], sc0[16], sc1[16];
+                    uint32_t pk[16], s0[16], s1[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         pk[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
-                        sc0[e] = __float_as_uint(e0 * v[e]);
-                        sc1[e] = __float_as_uint(e0 * v[16 + e]);
+                        s0[e] = __float_as_uint(e0 * v[e]);
+                        s1[e] = __float_as_uint(e0 * v[16 + e]);
                     }
                     tmem_st16(lane_base + TM_SBF + q2 * 16, pk);
-                    tmem_st16(lane_base + TM_S + q2 * 32, sc0);
-                    tmem_st16(lane_base + TM_S + q2 * 32 + 16, sc1);
+                    tmem_st16(lane_base + TM_S + q2 * 32, s0);
+                    tmem_st16(lane_base + TM_S + q2 * 32 + 16, s1);
                 }
                 tmem_wait_st();
             }
             fence_before_sync();
-            if (!group_sync_or(3, 128, !ok || *abort_flag) && j == 0) mbar_arrive(bar(B_S));
+            if (!group_sync_or(1, 128, !ok || *abort_flag) && j == 0) mbar_arrive(bar(RB_S));
             for (int c = 0; c < nch; ++c) {
                 const int rows = min(kChunk, len - c * kChunk);
                 const int64_t z0 = tok0 + (int64_t)c * kChunk;
-                // V_new^T -> bf16 A operand
-                ok = wait_bar(bar(B_D1), c & 1, abort_flag, p.err);
-                if (j == 0) GDN_TR(2, c, 0);
+                uint8_t *sbase = sm + stage(c);
+                const float *fq = reinterpret_cast<const float *>(sbase + PB_SC);
+                const float *fk = fq + 64;
+                // V_new^T -> bf16 A operands (plain, and with the K-> factors folded in)
+                ok = wait_bar(bar(RB_D1), c & 1, abort_flag, p.err);
+                if (j == 0) GDN_TR(p.trace, 2, c, 0);
                 fence_after_sync();
 #pragma unroll
                 for (int q2 = 0; q2 < 2; ++q2) {
-                    uint32_t a[16], b[16], pk[16];
+                    uint32_t a[16], b[16], pk[16], pkk[16];
                     tmem_ld16(lane_base + TM_D1 + q2 * 32, a);
                     tmem_ld16(lane_base + TM_D1 + q2 * 32 + 16, b);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        pk[e] = pack_bf16(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
-                        pk[8 + e] = pack_bf16(__uint_as_float(b[2 * e]), __uint_as_float(b[2 * e + 1]));
+                        const int r0 = q2 * 32 + 2 * e, r1 = q2 * 32 + 16 + 2 * e;
+                        const float x0 = __uint_as_float(a[2 * e]), x1 = __uint_as_float(a[2 * e + 1]);
+                        const float y0 = __uint_as_float(b[2 * e]), y1 = __uint_as_float(b[2 * e + 1]);
+                        pk[e] = pack_bf16(x0, x1);
+                        pk[8 + e] = pack_bf16(y0, y1);
+                        pkk[e] = pack_bf16(x0 * fk[r0], x1 * fk[r0 + 1]);
+                        pkk[8 + e] = pack_bf16(y0 * fk[r1], y1 * fk[r1 + 1]);
                     }
                     tmem_st16(lane_base + TM_X1 + q2 * 16, pk);
+                    tmem_st16(lane_base + TM_X1K + q2 * 16, pkk);
                 }
                 tmem_wait_st();
                 fence_before_sync();
-                if (group_sync_or(3, 128, !ok || *abort_flag)) break;
-                if (j == 0) mbar_arrive(bar(B_X));
-                if (j == 0) GDN_TR(2, c, 1);
-                // next state first (it gates the next chunk), then the outputs
-                ok = wait_bar(bar(B_D2), c & 1, abort_flag, p.err);
-                if (j == 0) GDN_TR(2, c, 2);
+                if (group_sync_or(1, 128, !ok || *abort_flag)) break;
+                if (j == 0) mbar_arrive(bar(RB_X));
+                // the next state (it gates the next chunk), then the outputs
+                ok = wait_bar(bar(RB_D2S), c & 1, abort_flag, p.err);
+                if (j == 0) GDN_TR(p.trace, 2, c, 1);
                 fence_after_sync();
                 if (c + 1 < nch) {
-                    const int s1 = (c + 1) % 3;
-                    ok = ok && wait_bar(bar(B_GATE + s1), ((c + 1) / 3) & 1, abort_flag, p.err);
-                    if (j == 0) GDN_TR(2, c, 3);
-                    const float e1 = exp2f(sc_all[s1 * 5 * 64 + 63]);
+                    ok = ok && wait_bar(bar(RB_FULL + ((c + 1) & 1)), ((c + 1) >> 1) & 1, abort_flag, p.err);
+                    const float e1 = reinterpret_cast<const float *>(sm + stage(c + 1) + PB_SC)[128];
+                    const uint32_t sbf = lane_base + TM_SBF + (uint32_t)((c + 1) & 1) * 64;
 #pragma unroll
                     for (int q2 = 0; q2 < 4; ++q2) {
                         uint32_t a[16], b[16], pk[16];
@@ -720,15 +695,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                             a[e] = __float_as_uint(e1 * __uint_as_float(a[e]));
                             b[e] = __float_as_uint(e1 * __uint_as_float(b[e]));
                         }
-                        tmem_st16(lane_base + TM_SBF + q2 * 16, pk);
+                        tmem_st16(sbf + q2 * 16, pk);
                         tmem_st16(lane_base + TM_S + q2 * 32, a);
                         tmem_st16(lane_base + TM_S + q2 * 32 + 16, b);
                     }
                     tmem_wait_st();
                     fence_before_sync();
-                    if (group_sync_or(3, 128, !ok || *abort_flag)) break;
-                    if (j == 0) mbar_arrive(bar(B_S));
-                    if (j == 0) GDN_TR(2, c, 4);
+                    if (group_sync_or(1, 128, !ok || *abort_flag)) break;
+                    if (j == 0) mbar_arrive(bar(RB_S));
+                    if (j == 0) GDN_TR(p.trace, 2, c, 2);
                 } else if (p.final_state && ok) {
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
@@ -742,22 +717,27 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                                             __uint_as_float(u[e + 2]), __uint_as_float(u[e + 3]));
                     }
                 }
-                // O^T (row j = output column j0 + j) through a [64 r][128 j] bf16 staging
-                // tile in this chunk's V stage (a1 has long completed), then 16-B stores
+                // O = fq . (Q S^T) + Aqk V_new through a [64 r][128 j] bf16 staging tile
+                // in this chunk's V buffer (its last reader, a1, has completed)
+                ok = ok && wait_bar(bar(RB_D2O), c & 1, abort_flag, p.err);
+                fence_after_sync();
                 {
-                    uint8_t *stg = sm + OFF_V + (uint32_t)(c & 1) * kVStage;
+                    uint8_t *stg = sbase + R_V;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        uint32_t u[16];
-                        tmem_ld16(lane_base + TM_D2 + q * 16, u);
+                        uint32_t a[16], b[16];
+                        tmem_ld16(lane_base + TM_D2A + q * 16, a);
+                        tmem_ld16(lane_base + TM_D2B + q * 16, b);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            *reinterpret_cast<__nv_bfloat16 *>(stg + ((q * 16 + e) * 128 + j) * 2) =
-                                __float2bfloat16_rn(__uint_as_float(u[e]));
+                        for (int e = 0; e < 16; ++e) {
+                            const int r = q * 16 + e;
+                            *reinterpret_cast<__nv_bfloat16 *>(stg + (r * 128 + j) * 2) =
+                                __float2bfloat16_rn(fq[r] * __uint_as_float(a[e]) + __uint_as_float(b[e]));
+                        }
                     }
                     fence_before_sync();
-                    if (group_sync_or(3, 128, !ok || *abort_flag)) break;
+                    if (group_sync_or(1, 128, !ok || *abort_flag)) break;
                     __nv_bfloat16 *obase = p.out + (size_t)z0 * H * dv + (size_t)h * dv + j0;
 #pragma unroll
                     for (int it = 0; it < 8; ++it) {
@@ -766,9 +746,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                             *reinterpret_cast<uint4 *>(obase + (size_t)r * H * dv + ch * 8) =
                                 *reinterpret_cast<const uint4 *>(stg + r * 256 + ch * 16);
                     }
-                    if (group_sync_or(3, 128, !ok || *abort_flag)) break;
-                    if (j == 0) mbar_arrive(bar(B_VE + (c & 1)));   // the V stage may be refilled
-                    if (j == 0) GDN_TR(2, c, 5);
+                    if (group_sync_or(1, 128, !ok || *abort_flag)) break;
+                    if (j == 0) mbar_arrive(bar(RB_EMPTY + (c & 1)));   // the stage may be refilled
+                    if (j == 0) GDN_TR(p.trace, 2, c, 3);
                 }
             }
         }
@@ -813,10 +793,6 @@ bool make_tmap(CUtensorMap *m, const void *base, int d, int H, int64_t rows)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-#ifdef GDN_KERNEL_TRACE
-long long *g_trace_buffer = nullptr;
-#endif
-
 }  // namespace
 
 #ifdef GDN_KERNEL_TRACE
@@ -828,6 +804,11 @@ bool chunk_tc_supported(int dt, int dk, int dv, int64_t tokens)
     return dt == 1 && dk == 128 && dv % 128 == 0 && tokens > 0 && tokens < ((int64_t)1 << 31);
 }
 
+size_t chunk_tc_workspace_bytes(int64_t slots, int H)
+{
+    return kWsHeader + (size_t)slots * H * kPrepBlock;
+}
+
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st)
 {
     const int64_t rows = (int64_t)a.gm.B * a.gm.T;
@@ -835,23 +816,26 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st)
     if (!make_tmap(&tq, a.q, a.gm.dk, a.gm.H, rows) || !make_tmap(&tk, a.k, a.gm.dk, a.gm.H, rows) ||
         !make_tmap(&tv, a.v, a.gm.dv, a.gm.H, rows))
         return cudaErrorInvalidValue;
-    TcParams p;
-    p.g = a.g;
-    p.beta = a.beta;
-    p.init_state = a.init_state;
-    p.out = reinterpret_cast<__nv_bfloat16 *>(a.out);
-    p.final_state = a.final_state;
-    p.err = reinterpret_cast<unsigned *>(a.workspace);
-    p.gm = a.gm;
-    p.scale = a.scale;
-    p.l2 = a.l2;
+    long long *trace = nullptr;
 #ifdef GDN_KERNEL_TRACE
-    p.trace = g_trace_buffer;
+    trace = g_trace_buffer;
 #endif
-    cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTc);
+    uint8_t *blocks = reinterpret_cast<uint8_t *>(a.workspace) + kWsHeader;
+    unsigned *err = reinterpret_cast<unsigned *>(a.workspace);
+
+    UtParams up;
+    up.g = a.g; up.beta = a.beta; up.blocks = blocks; up.err = err; up.gm = a.gm;
+    up.scale = a.scale; up.l2 = a.l2; up.trace = trace;
+    cudaError_t e = cudaFuncSetAttribute(ut_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemUt);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.gm.N, a.gm.H, a.gm.dv / 128);
-    chunk_tc_kernel<<<grid, kThreadsTc, kSmemTc, st>>>(tq, tk, tv, p);
+    ut_tc_kernel<<<dim3((unsigned)a.slots, a.gm.H), kThreadsUt, kSmemUt, st>>>(tq, tk, up);
+
+    RcParams rp;
+    rp.init_state = a.init_state; rp.blocks = blocks; rp.out = reinterpret_cast<__nv_bfloat16 *>(a.out);
+    rp.final_state = a.final_state; rp.err = err; rp.gm = a.gm; rp.trace = trace;
+    e = cudaFuncSetAttribute(recur_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemRc);
+    if (e != cudaSuccess) return e;
+    recur_tc_kernel<<<dim3(a.gm.N, a.gm.H, a.gm.dv / 128), kThreadsRc, kSmemRc, st>>>(tq, tk, tv, rp);
     return cudaGetLastError();
 }
 

@@ -34,6 +34,7 @@ struct DecodeArgs {
 
 cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t st);
 bool chunk_tc_supported(int dt, int dk, int dv, int64_t tokens);
+size_t chunk_tc_workspace_bytes(int64_t slots, int H);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
 

@@ -213,6 +213,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int 
         :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar) : "memory");
 }
 
+// Plain (non-tensor) bulk copy global -> shared, completion counted on `bar`.
+// Both addresses 16-B aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");
