@@ -45,7 +45,6 @@ namespace {
 
 using namespace umma;
 
-constexpr uint32_t LDA = 65;           // fp32 row pitch of L (conflict-free row-per-thread writes)
 constexpr uint32_t LDL = 68;           // fp32 row pitch of T (16-B aligned rows for vector loads)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s: legitimate waits are microseconds
@@ -61,16 +60,14 @@ constexpr uint32_t kWsHeader = 1024;   // device error word + padding
 // ---- ut_tc_kernel shared memory
 constexpr int kThreadsUt = 160;        // warp 0: TMA, MMA, TMEM; warps 1-4: 128 "prep" threads
 constexpr uint32_t U_QK = 0;           // [K kb0][Q kb0][K kb1][Q kb1], 8 KB each
-constexpr uint32_t U_TPP = 32768;      // T'' 8 KB
-constexpr uint32_t U_LF = 40960;       // L fp32 [64][LDA]
-constexpr uint32_t U_TF = U_LF + 64 * LDA * 4;
-constexpr uint32_t U_MT = U_TF + 64 * LDL * 4;
-constexpr uint32_t U_SC = U_MT + 32 * 33 * 4;     // b, beta, rk, rq [4][64] fp32
-constexpr uint32_t U_BAR = U_SC + 4 * 64 * 4;
+constexpr uint32_t U_TPP = 32768;      // T'' 8 KB (scratch of the solve before that)
+constexpr uint32_t U_A = 40960;        // L, then T, in place: fp32 [64][LDL]
+constexpr uint32_t U_SC = U_A + 64 * LDL * 4;     // b, beta, rk, rq, cw, ecol [6][64] fp32
+constexpr uint32_t U_BAR = U_SC + 6 * 64 * 4;
 constexpr uint32_t U_MISC = U_BAR + 8 * 8;
 constexpr uint32_t kSmemUt = U_MISC + 64 + 1024;
-static_assert(U_TF % 16 == 0 && U_MT % 16 == 0 && U_SC % 16 == 0, "alignment");
-static_assert(2 * kSmemUt <= 232448, "two prep CTAs per SM");
+static_assert(U_A % 16 == 0 && U_SC % 16 == 0, "alignment");
+static_assert(3 * (kSmemUt + 1024) <= 233472, "three UT CTAs per SM");
 
 // ---- recur_tc_kernel shared memory: two stages of [prep block | Q,K tile | V tile]
 constexpr int kThreadsRc = 192;        // warp 0: TMA, TMEM; warp 1: MMA; warps 2-5: epilogue
@@ -114,6 +111,24 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicExch(err, kDevErrTimeout);
+            return false;
+        }
+    }
+}
+
+// Spinning variant for the latency-critical hand-offs of the recurrence: a
+// sleeping try_wait can wake up late, which adds directly to the serial chain.
+__device__ __forceinline__ bool wait_spin(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned *err)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        for (int i = 0; i < 256; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             *abort_flag = 1;
@@ -173,84 +188,127 @@ __device__ __forceinline__ float row_sumsq(const uint8_t *row, int r)
     return ss;
 }
 
-// T = (I + L)^{-1} for a strictly lower 64x64 L (row pitch LDA; T pitch LDL), 128 threads.
-// 16x16 diagonal blocks by forward substitution (one thread per column),
-// then the block rule [A 0; C B]^{-1} = [A^-1 0; -B^-1 C A^-1  B^-1] for the
-// 16->32 and 32->64 merges.
-__device__ __forceinline__ void solve_unit_lower(const float *__restrict__ Lf, float *__restrict__ Tf,
-                                                 float *__restrict__ Mt, int pid)
+__device__ __forceinline__ uint32_t to_tf32(float x)
 {
-    for (int e = pid; e < 64 * (int)LDL; e += 128) Tf[e] = 0.f;
-    group_sync(1, 128);
-    if (pid < 64) {
-        const int base = (pid >> 4) * 16, cc = pid & 15;
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float acc = 0.f;
-#pragma unroll
-            for (int i = 0; i < r; ++i) acc += Lf[(base + r) * LDA + base + i] * x[i];
-            x[r] = (r == cc) ? 1.f : ((r < cc) ? 0.f : -acc);
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) Tf[(base + r) * LDL + base + cc] = x[r];
-    }
-    group_sync(1, 128);
-    {   // 16 -> 32 merges: blocks (a0 = 0, b0 = 16) and (a0 = 32, b0 = 48)
-        const int m = pid >> 6, q = pid & 63, r = q >> 2, cg = (q & 3) * 4;
-        const int a0 = m * 32, b0 = a0 + 16;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float l = Lf[(b0 + r) * LDA + a0 + i];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[c] += l * Tf[(a0 + i) * LDL + a0 + cg + c];
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) Mt[m * 272 + r * 17 + cg + c] = acc[c];
-        group_sync(1, 128);
-        float o[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float t = Tf[(b0 + r) * LDL + b0 + i];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) o[c] += t * Mt[m * 272 + i * 17 + cg + c];
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) Tf[(b0 + r) * LDL + a0 + cg + c] = -o[c];
-    }
-    group_sync(1, 128);
-    {   // 32 -> 64 merge
-        const int r = pid >> 2, cg = (pid & 3) * 8;
-        float acc[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) acc[c] = 0.f;
-#pragma unroll 8
-        for (int i = 0; i < 32; ++i) {
-            const float l = Lf[(32 + r) * LDA + i];
-            const float4 t0 = *reinterpret_cast<const float4 *>(Tf + i * LDL + cg);
-            const float4 t1 = *reinterpret_cast<const float4 *>(Tf + i * LDL + cg + 4);
-            acc[0] += l * t0.x; acc[1] += l * t0.y; acc[2] += l * t0.z; acc[3] += l * t0.w;
-            acc[4] += l * t1.x; acc[5] += l * t1.y; acc[6] += l * t1.z; acc[7] += l * t1.w;
-        }
-#pragma unroll
-        for (int c = 0; c < 8; ++c) Mt[r * 33 + cg + c] = acc[c];
-        group_sync(1, 128);
-        float o[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) o[c] = 0.f;
-#pragma unroll 8
-        for (int i = 0; i < 32; ++i) {
-            const float t = Tf[(32 + r) * LDL + 32 + i];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) o[c] += t * Mt[i * 33 + cg + c];
-        }
-#pragma unroll
-        for (int c = 0; c < 8; ++c) Tf[(32 + r) * LDL + cg + c] = -o[c];
-    }
-    group_sync(1, 128);
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
 }
 
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 "
+                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// One warp: D (16 x 16) = X (16 x K) * Y (K x 16) on the tensor cores (tf32),
+// X(r, k) = X0[r * xp + k], Y(k, c) = Y0[k * yp + c]; written as -D (negate)
+// or D to Z0[r * zp + c].
+template <int K>
+__device__ __forceinline__ void warp_gemm16(const float *X0, int xp, const float *Y0, int yp, float *Z0, int zp,
+                                            bool negate, int lane)
+{
+    const int g = lane >> 2, t = lane & 3;
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        uint32_t a[4];
+        a[0] = to_tf32(X0[g * xp + k0 + t]);
+        a[1] = to_tf32(X0[(g + 8) * xp + k0 + t]);
+        a[2] = to_tf32(X0[g * xp + k0 + t + 4]);
+        a[3] = to_tf32(X0[(g + 8) * xp + k0 + t + 4]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const uint32_t b0 = to_tf32(Y0[(k0 + t) * yp + nt * 8 + g]);
+            const uint32_t b1 = to_tf32(Y0[(k0 + t + 4) * yp + nt * 8 + g]);
+            mma_tf32(acc[nt], a, b0, b1);
+        }
+    }
+    const float sg = negate ? -1.f : 1.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        Z0[g * zp + nt * 8 + 2 * t] = sg * acc[nt][0];
+        Z0[g * zp + nt * 8 + 2 * t + 1] = sg * acc[nt][1];
+        Z0[(g + 8) * zp + nt * 8 + 2 * t] = sg * acc[nt][2];
+        Z0[(g + 8) * zp + nt * 8 + 2 * t + 1] = sg * acc[nt][3];
+    }
+}
+
+// In place: A (64 x 64, pitch LDL) holds the strictly lower L on entry (zeros
+// elsewhere) and T = (I + L)^{-1} on exit; 128 threads (4 warps), Mt >= 32 x 36
+// floats of scratch.  Diagonal 4x4 blocks by forward substitution, then the
+// block rule [A 0; C B]^{-1} = [A^-1 0; -B^-1 C A^-1  B^-1] for the 4->8 and
+// 8->16 merges (CUDA cores) and the 16->32 and 32->64 merges (tensor cores, tf32).
+__device__ __forceinline__ void solve_in_place(float *__restrict__ A, float *__restrict__ Mt, int tid, int warp,
+                                               int lane)
+{
+    // level 0: 16 diagonal 4x4 blocks, one thread per column
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+    const int base0 = (tid >> 2) * 4, c0 = tid & 3;
+    if (tid < 64) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < r; ++i) acc += A[(base0 + r) * LDL + base0 + i] * x[i];
+            x[r] = (r == c0) ? 1.f : ((r < c0) ? 0.f : -acc);
+        }
+    }
+    group_sync(1, 128);
+    if (tid < 64) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) A[(base0 + r) * LDL + base0 + c0] = x[r];
+    }
+    group_sync(1, 128);
+    // levels 1, 2: merges of size s = 4 and 8 on the CUDA cores
+#pragma unroll
+    for (int s = 4; s <= 8; s *= 2) {
+        const int epp = s / 4;   // entries per thread: 32*s entries over 128 threads
+        float m[2];
+#pragma unroll
+        for (int k = 0; k < epp; ++k) {
+            const int idx = tid * epp + k, c = idx % s, r = (idx / s) % s, a0 = (idx / (s * s)) * 2 * s, b0 = a0 + s;
+            float acc = 0.f;
+            for (int i = c; i < s; ++i) acc += A[(b0 + r) * LDL + a0 + i] * A[(a0 + i) * LDL + a0 + c];
+            m[k] = acc;
+        }
+#pragma unroll
+        for (int k = 0; k < epp; ++k) Mt[tid * epp + k] = m[k];
+        group_sync(1, 128);
+#pragma unroll
+        for (int k = 0; k < epp; ++k) {
+            const int idx = tid * epp + k, c = idx % s, r = (idx / s) % s, mm = idx / (s * s);
+            const int a0 = mm * 2 * s, b0 = a0 + s;
+            float acc = 0.f;
+            for (int i = 0; i <= r; ++i) acc += A[(b0 + r) * LDL + b0 + i] * Mt[mm * s * s + i * s + c];
+            A[(b0 + r) * LDL + a0 + c] = -acc;
+        }
+        group_sync(1, 128);
+    }
+    // level 3: the two 16 -> 32 merges; warp w: merge w >> 1, 8-column half... (16 x 16 per merge)
+    {
+        const int mm = warp >> 1;          // merge index (rows/cols 32*mm ...)
+        const int a0 = mm * 32, b0 = a0 + 16;
+        if ((warp & 1) == 0)   // M = L_ba T_aa   (16 x 16 x 16)
+            warp_gemm16<16>(A + b0 * LDL + a0, LDL, A + a0 * LDL + a0, LDL, Mt + mm * 16 * 20, 20, false, lane);
+        group_sync(1, 128);
+        if ((warp & 1) == 0)   // T_ba = -T_bb M
+            warp_gemm16<16>(A + b0 * LDL + b0, LDL, Mt + mm * 16 * 20, 20, A + b0 * LDL + a0, LDL, true, lane);
+        group_sync(1, 128);
+    }
+    // level 4: the 32 -> 64 merge; warp w computes the 16 x 16 quadrant (w & 1, w >> 1)
+    {
+        const int r0 = (warp & 1) * 16, q0 = (warp >> 1) * 16;
+        // M2 = L_BA T_AA  (32 x 32 x 32)
+        warp_gemm16<32>(A + (32 + r0) * LDL, LDL, A + q0, LDL, Mt + r0 * 36 + q0, 36, false, lane);
+        group_sync(1, 128);
+        // T_BA = -T_BB M2
+        warp_gemm16<32>(A + (32 + r0) * LDL + 32, LDL, Mt + q0, 36, A + (32 + r0) * LDL + q0, LDL, true, lane);
+        group_sync(1, 128);
+    }
+}
 
 // ===========================================================================
 // chunk-local UT transform
@@ -265,7 +323,7 @@ struct UtParams {
     long long *trace;
 };
 
-__global__ void __launch_bounds__(kThreadsUt, 2)
+__global__ void __launch_bounds__(kThreadsUt, 3)
 ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk, const UtParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -333,11 +391,10 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         __syncwarp();
     } else {
         const int prow = 32 * (warp & 3) + lane;   // tensor-memory lane of this thread
-        float *Lf = reinterpret_cast<float *>(sm + U_LF);
-        float *Tf = reinterpret_cast<float *>(sm + U_TF);
-        float *Mt = reinterpret_cast<float *>(sm + U_MT);
+        float *Am = reinterpret_cast<float *>(sm + U_A);
+        float *Mt = reinterpret_cast<float *>(sm + U_TPP);
         float *sc = reinterpret_cast<float *>(sm + U_SC);
-        float *bsum = sc, *bet = sc + 64, *rk = sc + 128, *rq = sc + 192;
+        float *bsum = sc, *bet = sc + 64, *rk = sc + 128, *rq = sc + 192, *cw = sc + 256, *ecol = sc + 320;
         const uint32_t lane_base = tb + ((uint32_t)(32 * (warp & 3)) << 16);
         uint8_t *st = sm + U_QK;
         do {
@@ -372,63 +429,82 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 (isq ? rq : rk)[r] = (r < rows) ? inv : 0.f;
             }
             if (group_sync_or(2, 128, !ok || *abort_flag)) break;
+            // column factors: decay of column i to the end of its 16-block (for the
+            // off-diagonal blocks, where e^{b_r - b_i} = e^{b_r - b_p} e^{b_p - b_i}
+            // with both factors <= 1), and e^{b_i} rk_i (for T'')
+            if (prow < 64) {
+                const int i = prow;
+                cw[i] = exp2f(bsum[i | 15] - bsum[i]) * rk[i];
+                ecol[i] = exp2f(bsum[i]) * rk[i];
+            }
+            group_sync(1, 128);
 
-            // (3) masks: L (rows 0-63, to shared memory), Aqk (rows 64-127, to the workspace)
+            // (3) masks: L (rows 0-63, into A), Aqk (rows 64-127, to the workspace)
             ok = wait_bar(bar(UB_P1), 0, abort_flag, p.err);
             fence_after_sync();
             {
-                float G[64];
-                uint32_t u[16];
+                const int r = prow & 63, R = r >> 4;
+                const bool isq = prow >= 64;
+                const float br = bsum[r];
+                const float f = isq ? rq[r] : bet[r] * rk[r];
+                const int lim = isq ? r + 1 : r;   // columns i < lim
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    tmem_ld16(lane_base + TP1 + q * 16, u);
+                    uint32_t u[16];
+                    tmem_ld16(lane_base + q * 16, u);
                     tmem_wait_ld();
+                    float v[16];
+                    if (q < R) {
+                        const float fu = f * exp2f(br - bsum[q * 16 + 15]);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) G[q * 16 + e] = __uint_as_float(u[e]);
-                }
-                if (prow < 64) {
-                    const int r = prow;
-                    const float br = bsum[r], f = bet[r] * rk[r];
-                    float *Lr = Lf + r * LDA;
+                        for (int e = 0; e < 16; ++e) v[e] = fu * cw[q * 16 + e] * __uint_as_float(u[e]);
+                    } else if (q == R) {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) Lr[i] = (i < r) ? f * exp2f(br - bsum[i]) * rk[i] * G[i] : 0.f;
-                } else {
-                    const int r = prow - 64;
-                    const float br = bsum[r], f = rq[r];
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int i0 = ch * 8 + 2 * e;
-                            const float a0 = (i0 <= r) ? f * exp2f(br - bsum[i0]) * rk[i0] * G[i0] : 0.f;
-                            const float a1 = (i0 + 1 <= r) ? f * exp2f(br - bsum[i0 + 1]) * rk[i0 + 1] * G[i0 + 1] : 0.f;
-                            w[e] = pack_bf16(a0, a1);
+                        for (int e = 0; e < 16; ++e) {
+                            const int i = q * 16 + e;
+                            v[e] = (i < lim) ? f * exp2f(br - bsum[i]) * rk[i] * __uint_as_float(u[e]) : 0.f;
                         }
-                        *reinterpret_cast<uint4 *>(blk + PB_AQK + sw128_offset(r, ch * 8)) =
-                            make_uint4(w[0], w[1], w[2], w[3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) v[e] = 0.f;
+                    }
+                    if (!isq) {
+                        float4 *dst = reinterpret_cast<float4 *>(Am + r * LDL + q * 16);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                    } else {
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) w[e] = pack_bf16(v[hh * 8 + 2 * e], v[hh * 8 + 2 * e + 1]);
+                            *reinterpret_cast<uint4 *>(blk + PB_AQK + sw128_offset(r, q * 16 + hh * 8)) =
+                                make_uint4(w[0], w[1], w[2], w[3]);
+                        }
                     }
                 }
             }
             fence_before_sync();
             if (group_sync_or(2, 128, !ok || *abort_flag)) break;
 
-            // (4) T = (I + L)^{-1};  T' -> workspace,  T'' -> shared memory
-            solve_unit_lower(Lf, Tf, Mt, prow);
+            // (4) T = (I + L)^{-1} in place;  T' -> workspace,  T'' -> shared memory
+            solve_in_place(Am, Mt, prow, warp - 1, lane);
             {
                 const int r = prow >> 1, i0 = (prow & 1) * 32;
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
+                    const int ib = i0 + ch * 8;
+                    const float4 t0 = *reinterpret_cast<const float4 *>(Am + r * LDL + ib);
+                    const float4 t1 = *reinterpret_cast<const float4 *>(Am + r * LDL + ib + 4);
+                    const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
                     uint32_t w1[4], w2[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int i = i0 + ch * 8 + 2 * e;
-                        const float t0 = Tf[r * LDL + i], t1 = Tf[r * LDL + i + 1];
-                        const float p0 = t0 * bet[i], p1 = t1 * bet[i + 1];
+                        const float p0 = tv[2 * e] * bet[ib + 2 * e], p1 = tv[2 * e + 1] * bet[ib + 2 * e + 1];
                         w1[e] = pack_bf16(p0, p1);
-                        w2[e] = pack_bf16(p0 * exp2f(bsum[i]) * rk[i], p1 * exp2f(bsum[i + 1]) * rk[i + 1]);
+                        w2[e] = pack_bf16(p0 * ecol[ib + 2 * e], p1 * ecol[ib + 2 * e + 1]);
                     }
-                    const uint32_t off = sw128_offset(r, i0 + ch * 8);
+                    const uint32_t off = sw128_offset(r, ib);
                     *reinterpret_cast<uint4 *>(blk + PB_TP + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
                     *reinterpret_cast<uint4 *>(sm + U_TPP + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
                 }
@@ -564,21 +640,21 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             for (int c = 0; c < nch; ++c) {
                 const uint32_t base = sb + stage(c);
                 const uint32_t sbf = tb + TM_SBF + (uint32_t)(c & 1) * 64;
-                if (!wait_bar(bar(RB_FULL + (c & 1)), (c >> 1) & 1, abort_flag, p.err)) break;
-                if (c > 0 && !wait_bar(bar(RB_X), (c - 1) & 1, abort_flag, p.err)) break;   // D1 drained
+                if (!wait_spin(bar(RB_FULL + (c & 1)), (c >> 1) & 1, abort_flag, p.err)) break;
+                if (c > 0 && !wait_spin(bar(RB_X), (c - 1) & 1, abort_flag, p.err)) break;   // D1 drained
                 fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)   // a1: D1 = V^T T'^T
                     mma_ss(tb + TM_D1, smem_desc(base + R_V + ks * 2048, 8192, 1024),
                            smem_desc(base + PB_TP + ks * 32, 16, 1024), id_a1, ks > 0);
-                if (!wait_bar(bar(RB_S), c & 1, abort_flag, p.err)) break;
+                if (!wait_spin(bar(RB_S), c & 1, abort_flag, p.err)) break;
                 GDN_TR(p.trace, 1, c, 0);
                 fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)   // a2: D1 -= S W~^T
                     mma_ts(tb + TM_D1, sbf + ks * 8, smem_desc(base + PB_WT + ks * 2048, 16384, 1024), id_a2, 1);
                 commit(bar(RB_D1));
-                if (!wait_bar(bar(RB_X), c & 1, abort_flag, p.err)) break;
+                if (!wait_spin(bar(RB_X), c & 1, abort_flag, p.err)) break;
                 GDN_TR(p.trace, 1, c, 1);
                 fence_after_sync();
 #pragma unroll
@@ -611,7 +687,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     *reinterpret_cast<float4 *>(p.final_state + srow + d) = v4;
                 }
         } else {
-            bool ok = wait_bar(bar(RB_FULL), 0, abort_flag, p.err);
+            bool ok = wait_spin(bar(RB_FULL), 0, abort_flag, p.err);
             {
                 const float e0 = reinterpret_cast<const float *>(sm + PB_SC)[128];
 #pragma unroll
@@ -645,7 +721,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 const float *fq = reinterpret_cast<const float *>(sbase + PB_SC);
                 const float *fk = fq + 64;
                 // V_new^T -> bf16 A operands (plain, and with the K-> factors folded in)
-                ok = wait_bar(bar(RB_D1), c & 1, abort_flag, p.err);
+                ok = wait_spin(bar(RB_D1), c & 1, abort_flag, p.err);
                 if (j == 0) GDN_TR(p.trace, 2, c, 0);
                 fence_after_sync();
 #pragma unroll
@@ -672,11 +748,11 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 if (group_sync_or(1, 128, !ok || *abort_flag)) break;
                 if (j == 0) mbar_arrive(bar(RB_X));
                 // the next state (it gates the next chunk), then the outputs
-                ok = wait_bar(bar(RB_D2S), c & 1, abort_flag, p.err);
+                ok = wait_spin(bar(RB_D2S), c & 1, abort_flag, p.err);
                 if (j == 0) GDN_TR(p.trace, 2, c, 1);
                 fence_after_sync();
                 if (c + 1 < nch) {
-                    ok = ok && wait_bar(bar(RB_FULL + ((c + 1) & 1)), ((c + 1) >> 1) & 1, abort_flag, p.err);
+                    ok = ok && wait_spin(bar(RB_FULL + ((c + 1) & 1)), ((c + 1) >> 1) & 1, abort_flag, p.err);
                     const float e1 = reinterpret_cast<const float *>(sm + stage(c + 1) + PB_SC)[128];
                     const uint32_t sbf = lane_base + TM_SBF + (uint32_t)((c + 1) & 1) * 64;
 #pragma unroll
@@ -719,7 +795,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 }
                 // O = fq . (Q S^T) + Aqk V_new through a [64 r][128 j] bf16 staging tile
                 // in this chunk's V buffer (its last reader, a1, has completed)
-                ok = ok && wait_bar(bar(RB_D2O), c & 1, abort_flag, p.err);
+                ok = ok && wait_spin(bar(RB_D2O), c & 1, abort_flag, p.err);
                 fence_after_sync();
                 {
                     uint8_t *stg = sbase + R_V;
