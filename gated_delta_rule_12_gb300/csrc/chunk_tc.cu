@@ -70,7 +70,7 @@ static_assert(U_A % 16 == 0 && U_SC % 16 == 0, "alignment");
 static_assert(3 * (kSmemUt + 1024) <= 233472, "three UT CTAs per SM");
 
 // ---- recur_tc_kernel shared memory: two stages of [prep block | Q,K tile | V tile]
-constexpr int kThreadsRc = 192;        // warp 0: TMA, TMEM; warp 1: MMA; warps 2-5: epilogue
+constexpr int kThreadsRc = 320;        // warp 0: TMA, TMEM; warp 1: MMA; warps 2-5: state; 6-9: outputs
 constexpr uint32_t R_QK = 34816;       // within a stage (1024-aligned)
 constexpr uint32_t R_V = R_QK + 32768;
 constexpr uint32_t R_STAGE = R_V + 16384;
@@ -89,7 +89,8 @@ constexpr uint32_t TM_D2B = 384;  // V_new^T Aqk^T accumulator, 64
 constexpr uint32_t TM_X1 = 448;   // V_new^T bf16, 32
 constexpr uint32_t TM_X1K = 480;  // V_new^T diag(fk) bf16, 32
 
-enum : int { RB_FULL = 0, RB_EMPTY = 2, RB_D1 = 4, RB_X = 5, RB_S = 6, RB_D2S = 7, RB_D2O = 8, RB_FIN = 9 };
+enum : int { RB_FULL = 0, RB_EMPTY = 2, RB_D1 = 4, RB_X = 5, RB_S = 6, RB_D2S = 7, RB_D2O = 8, RB_FIN = 9,
+             RB_OFREE = 10 };
 enum : int { UB_QK = 0, UB_P1 = 1, UB_TRDY = 2, UB_P2 = 3, UB_FIN = 4 };
 
 // Development-only phase timestamps (SM clock) of the first CTA; compiled out
@@ -589,7 +590,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     auto stage = [&](int c) -> uint32_t { return (uint32_t)(c & 1) * R_STAGE; };
 
     if (tid == 0) {
-        for (int i = 0; i < 10; ++i) mbar_init(bar(i), 1);
+        for (int i = 0; i < 11; ++i) mbar_init(bar(i), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -661,6 +662,8 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 for (int ks = 0; ks < 4; ++ks)   // c2: S += (V_new^T diag(fk)) K
                     mma_ts(tb + TM_S, tb + TM_X1K + ks * 8, smem_desc(base + R_QK + ks * 2048, 16384, 1024), id_c2, 1);
                 commit(bar(RB_D2S));
+                if (c > 0 && !wait_spin(bar(RB_OFREE), (c - 1) & 1, abort_flag, p.err)) break;   // D2 drained
+                fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {   // b: D2A = S Q^T
                     const uint32_t off = R_QK + 8192 + (ks >> 2) * 16384 + (ks & 3) * 32;
@@ -675,8 +678,8 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             mbar_wait(bar(RB_FIN), 0, kWaitLimitNs);
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------------------ epilogue
+    } else if (warp < 6) {
+        // ------------------------------------------------------------ state epilogue (the serial chain)
         const int j = 32 * (warp & 3) + lane;   // row of S within the slice
         const size_t srow = (((size_t)n * H + h) * (size_t)dv + (size_t)(j0 + j)) * 128;
         if (nch == 0) {
@@ -715,39 +718,35 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             fence_before_sync();
             if (!group_sync_or(1, 128, !ok || *abort_flag) && j == 0) mbar_arrive(bar(RB_S));
             for (int c = 0; c < nch; ++c) {
-                const int rows = min(kChunk, len - c * kChunk);
-                const int64_t z0 = tok0 + (int64_t)c * kChunk;
-                uint8_t *sbase = sm + stage(c);
-                const float *fq = reinterpret_cast<const float *>(sbase + PB_SC);
-                const float *fk = fq + 64;
+                const float *fk = reinterpret_cast<const float *>(sm + stage(c) + PB_SC) + 64;
                 // V_new^T -> bf16 A operands (plain, and with the K-> factors folded in)
                 ok = wait_spin(bar(RB_D1), c & 1, abort_flag, p.err);
                 if (j == 0) GDN_TR(p.trace, 2, c, 0);
                 fence_after_sync();
+                {
+                    uint32_t a[64];
 #pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) {
-                    uint32_t a[16], b[16], pk[16], pkk[16];
-                    tmem_ld16(lane_base + TM_D1 + q2 * 32, a);
-                    tmem_ld16(lane_base + TM_D1 + q2 * 32 + 16, b);
+                    for (int q = 0; q < 4; ++q) tmem_ld16(lane_base + TM_D1 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(a + q * 16));
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int r0 = q2 * 32 + 2 * e, r1 = q2 * 32 + 16 + 2 * e;
-                        const float x0 = __uint_as_float(a[2 * e]), x1 = __uint_as_float(a[2 * e + 1]);
-                        const float y0 = __uint_as_float(b[2 * e]), y1 = __uint_as_float(b[2 * e + 1]);
-                        pk[e] = pack_bf16(x0, x1);
-                        pk[8 + e] = pack_bf16(y0, y1);
-                        pkk[e] = pack_bf16(x0 * fk[r0], x1 * fk[r0 + 1]);
-                        pkk[8 + e] = pack_bf16(y0 * fk[r1], y1 * fk[r1 + 1]);
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        uint32_t pk[16], pkk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int r = q2 * 32 + 2 * e;
+                            const float x0 = __uint_as_float(a[r]), x1 = __uint_as_float(a[r + 1]);
+                            pk[e] = pack_bf16(x0, x1);
+                            pkk[e] = pack_bf16(x0 * fk[r], x1 * fk[r + 1]);
+                        }
+                        tmem_st16(lane_base + TM_X1K + q2 * 16, pkk);
+                        tmem_st16(lane_base + TM_X1 + q2 * 16, pk);
                     }
-                    tmem_st16(lane_base + TM_X1 + q2 * 16, pk);
-                    tmem_st16(lane_base + TM_X1K + q2 * 16, pkk);
                 }
                 tmem_wait_st();
                 fence_before_sync();
                 if (group_sync_or(1, 128, !ok || *abort_flag)) break;
                 if (j == 0) mbar_arrive(bar(RB_X));
-                // the next state (it gates the next chunk), then the outputs
+                // the next state
                 ok = wait_spin(bar(RB_D2S), c & 1, abort_flag, p.err);
                 if (j == 0) GDN_TR(p.trace, 2, c, 1);
                 fence_after_sync();
@@ -755,26 +754,22 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     ok = ok && wait_spin(bar(RB_FULL + ((c + 1) & 1)), ((c + 1) >> 1) & 1, abort_flag, p.err);
                     const float e1 = reinterpret_cast<const float *>(sm + stage(c + 1) + PB_SC)[128];
                     const uint32_t sbf = lane_base + TM_SBF + (uint32_t)((c + 1) & 1) * 64;
+                    uint32_t a[128];
 #pragma unroll
-                    for (int q2 = 0; q2 < 4; ++q2) {
-                        uint32_t a[16], b[16], pk[16];
-                        tmem_ld16(lane_base + TM_S + q2 * 32, a);
-                        tmem_ld16(lane_base + TM_S + q2 * 32 + 16, b);
-                        tmem_wait_ld();
+                    for (int q = 0; q < 8; ++q) tmem_ld16(lane_base + TM_S + q * 16, *reinterpret_cast<uint32_t(*)[16]>(a + q * 16));
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            pk[e] = pack_bf16(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
-                            pk[8 + e] = pack_bf16(__uint_as_float(b[2 * e]), __uint_as_float(b[2 * e + 1]));
-                        }
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t pk[16];
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            a[e] = __float_as_uint(e1 * __uint_as_float(a[e]));
-                            b[e] = __float_as_uint(e1 * __uint_as_float(b[e]));
-                        }
-                        tmem_st16(sbf + q2 * 16, pk);
-                        tmem_st16(lane_base + TM_S + q2 * 32, a);
-                        tmem_st16(lane_base + TM_S + q2 * 32 + 16, b);
+                        for (int e = 0; e < 16; ++e)
+                            pk[e] = pack_bf16(__uint_as_float(a[q * 32 + 2 * e]), __uint_as_float(a[q * 32 + 2 * e + 1]));
+                        tmem_st16(sbf + q * 16, pk);
                     }
+#pragma unroll
+                    for (int e = 0; e < 128; ++e) a[e] = __float_as_uint(e1 * __uint_as_float(a[e]));
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) tmem_st16(lane_base + TM_S + q * 16, *reinterpret_cast<uint32_t(*)[16]>(a + q * 16));
                     tmem_wait_st();
                     fence_before_sync();
                     if (group_sync_or(1, 128, !ok || *abort_flag)) break;
@@ -793,40 +788,47 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                                             __uint_as_float(u[e + 2]), __uint_as_float(u[e + 3]));
                     }
                 }
-                // O = fq . (Q S^T) + Aqk V_new through a [64 r][128 j] bf16 staging tile
-                // in this chunk's V buffer (its last reader, a1, has completed)
-                ok = ok && wait_spin(bar(RB_D2O), c & 1, abort_flag, p.err);
-                fence_after_sync();
-                {
-                    uint8_t *stg = sbase + R_V;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t a[16], b[16];
-                        tmem_ld16(lane_base + TM_D2A + q * 16, a);
-                        tmem_ld16(lane_base + TM_D2B + q * 16, b);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int r = q * 16 + e;
-                            *reinterpret_cast<__nv_bfloat16 *>(stg + (r * 128 + j) * 2) =
-                                __float2bfloat16_rn(fq[r] * __uint_as_float(a[e]) + __uint_as_float(b[e]));
-                        }
-                    }
-                    fence_before_sync();
-                    if (group_sync_or(1, 128, !ok || *abort_flag)) break;
-                    __nv_bfloat16 *obase = p.out + (size_t)z0 * H * dv + (size_t)h * dv + j0;
-#pragma unroll
-                    for (int it = 0; it < 8; ++it) {
-                        const int idx = it * 128 + j, r = idx >> 4, ch = idx & 15;
-                        if (r < rows)
-                            *reinterpret_cast<uint4 *>(obase + (size_t)r * H * dv + ch * 8) =
-                                *reinterpret_cast<const uint4 *>(stg + r * 256 + ch * 16);
-                    }
-                    if (group_sync_or(1, 128, !ok || *abort_flag)) break;
-                    if (j == 0) mbar_arrive(bar(RB_EMPTY + (c & 1)));   // the stage may be refilled
-                    if (j == 0) GDN_TR(p.trace, 2, c, 3);
-                }
             }
+        }
+    } else {
+        // ------------------------------------------------------------ output epilogue
+        // O = fq . (Q S^T) + Aqk V_new through a [64 r][128 j] bf16 staging tile in
+        // the chunk's V buffer (its only reader, a1, has completed), then 16-B stores
+        const int j = 32 * (warp & 3) + lane;   // output column j0 + j
+        for (int c = 0; c < nch; ++c) {
+            const int rows = min(kChunk, len - c * kChunk);
+            const int64_t z0 = tok0 + (int64_t)c * kChunk;
+            uint8_t *sbase = sm + stage(c);
+            const float *fq = reinterpret_cast<const float *>(sbase + PB_SC);
+            bool ok = wait_bar(bar(RB_D2O), c & 1, abort_flag, p.err);
+            fence_after_sync();
+            uint32_t a[64], b[64];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                tmem_ld16(lane_base + TM_D2A + q * 16, *reinterpret_cast<uint32_t(*)[16]>(a + q * 16));
+                tmem_ld16(lane_base + TM_D2B + q * 16, *reinterpret_cast<uint32_t(*)[16]>(b + q * 16));
+            }
+            tmem_wait_ld();
+            fence_before_sync();
+            if (group_sync_or(2, 128, !ok || *abort_flag)) break;
+            if (j == 0) mbar_arrive(bar(RB_OFREE));   // D2 may be overwritten
+            uint8_t *stg = sbase + R_V;
+#pragma unroll
+            for (int r = 0; r < 64; ++r)
+                *reinterpret_cast<__nv_bfloat16 *>(stg + (r * 128 + j) * 2) =
+                    __float2bfloat16_rn(fq[r] * __uint_as_float(a[r]) + __uint_as_float(b[r]));
+            if (group_sync_or(2, 128, *abort_flag)) break;
+            __nv_bfloat16 *obase = p.out + (size_t)z0 * H * dv + (size_t)h * dv + j0;
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int idx = it * 128 + j, r = idx >> 4, ch = idx & 15;
+                if (r < rows)
+                    *reinterpret_cast<uint4 *>(obase + (size_t)r * H * dv + ch * 8) =
+                        *reinterpret_cast<const uint4 *>(stg + r * 256 + ch * 16);
+            }
+            if (group_sync_or(2, 128, *abort_flag)) break;
+            if (j == 0) mbar_arrive(bar(RB_EMPTY + (c & 1)));   // the stage may be refilled
+            if (j == 0) GDN_TR(p.trace, 2, c, 3);
         }
     }
 
