@@ -69,16 +69,21 @@ constexpr uint32_t kSmemUt = U_MISC + 64 + 1024;
 static_assert(U_A % 16 == 0 && U_SC % 16 == 0, "alignment");
 static_assert(3 * (kSmemUt + 1024) <= 233472, "three UT CTAs per SM");
 
-// ---- recur_tc_kernel shared memory: two stages of [prep block | Q,K tile | V tile]
-constexpr int kThreadsRc = 320;        // warp 0: TMA, TMEM; warp 1: MMA; warps 2-5: state; 6-9: outputs
-constexpr uint32_t R_QK = 34816;       // within a stage (1024-aligned)
+// ---- recur_tc_kernel shared memory: two stages of [T', W~^T, Aqk | Q,K tile | V tile],
+// a ring of the per-chunk factors (fetched further ahead), and an output staging tile
+constexpr int kThreadsRc = 320;        // warp 0: loads, TMEM; warp 1: MMA; warps 2-5: state; 6-9: outputs
+constexpr uint32_t R_QK = 32768;       // within a stage (1024-aligned)
 constexpr uint32_t R_V = R_QK + 32768;
 constexpr uint32_t R_STAGE = R_V + 16384;
-constexpr uint32_t R_BAR = 2 * R_STAGE;
-constexpr uint32_t R_MISC = R_BAR + 16 * 8;
+constexpr uint32_t R_OUT = 2 * R_STAGE;            // [64 r][128 j] bf16 output staging
+constexpr uint32_t R_SCR = R_OUT + 16384;          // factor ring: kScSlots x 1 KB
+constexpr int kScSlots = 4;
+constexpr uint32_t kScBytes = 528;                 // fq[64], fk[64], e^{b_C} (+ pad)
+constexpr uint32_t R_BAR = R_SCR + kScSlots * 1024;
+constexpr uint32_t R_MISC = R_BAR + 24 * 8;
 constexpr uint32_t kSmemRc = R_MISC + 64 + 1024;
 static_assert(R_STAGE % 1024 == 0 && kSmemRc <= 232448, "recurrence smem");
-constexpr uint32_t kStageTx = kPrepBlock + 32768 + 16384;
+constexpr uint32_t kStageTx = PB_SC + 32768 + 16384;   // prep tiles (no factors) + q/k + v
 
 // recurrence tensor-memory columns (512)
 constexpr uint32_t TM_S = 0;      // fp32 state, 128
@@ -90,7 +95,7 @@ constexpr uint32_t TM_X1 = 448;   // V_new^T bf16, 32
 constexpr uint32_t TM_X1K = 480;  // V_new^T diag(fk) bf16, 32
 
 enum : int { RB_FULL = 0, RB_EMPTY = 2, RB_D1 = 4, RB_X = 5, RB_S = 6, RB_D2S = 7, RB_D2O = 8, RB_FIN = 9,
-             RB_OFREE = 10 };
+             RB_OFREE = 10, RB_SP = 11, RB_SCF = 12, RB_SCE = 16 };   // RB_SCF/RB_SCE: [kScSlots]
 enum : int { UB_QK = 0, UB_P1 = 1, UB_TRDY = 2, UB_P2 = 3, UB_FIN = 4 };
 
 // Development-only phase timestamps (SM clock) of the first CTA; compiled out
@@ -590,7 +595,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     auto stage = [&](int c) -> uint32_t { return (uint32_t)(c & 1) * R_STAGE; };
 
     if (tid == 0) {
-        for (int i = 0; i < 11; ++i) mbar_init(bar(i), 1);
+        for (int i = 0; i < RB_SCE + kScSlots; ++i) mbar_init(bar(i), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -616,7 +621,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 const int z = (int)(tok0 + (int64_t)c * kChunk);
                 const uint8_t *src = p.blocks + ((size_t)(slot0 + c) * H + h) * kPrepBlock;
                 mbar_expect_tx(bar(RB_FULL + s), kStageTx);
-                bulk_load(base, src, kPrepBlock, bar(RB_FULL + s));
+                bulk_load(base, src, PB_SC, bar(RB_FULL + s));
                 tma_load_3d(base + R_QK, &tmk, 0, h, z, bar(RB_FULL + s));
                 tma_load_3d(base + R_QK + 8192, &tmq, 0, h, z, bar(RB_FULL + s));
                 tma_load_3d(base + R_QK + 16384, &tmk, 64, h, z, bar(RB_FULL + s));
@@ -628,6 +633,19 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             if (*abort_flag)   // let the copies in flight land before the CTA exits
                 for (int c = (last > 0 ? last - 1 : 0); c <= last; ++c)
                     mbar_wait(bar(RB_FULL + (c & 1)), (c >> 1) & 1, 10000000ull);
+        } else if (lane == 1 && nch > 0) {
+            int last = -1;
+            for (int c = 0; c < nch; ++c) {
+                const int s = c % kScSlots;
+                if (c >= kScSlots && !wait_bar(bar(RB_SCE + s), ((c / kScSlots) - 1) & 1, abort_flag, p.err)) break;
+                const uint8_t *src = p.blocks + ((size_t)(slot0 + c) * H + h) * kPrepBlock + PB_SC;
+                mbar_expect_tx(bar(RB_SCF + s), kScBytes);
+                bulk_load(sb + R_SCR + s * 1024, src, kScBytes, bar(RB_SCF + s));
+                last = c;
+            }
+            if (*abort_flag)
+                for (int c = (last >= kScSlots ? last - kScSlots + 1 : 0); c <= last; ++c)
+                    mbar_wait(bar(RB_SCF + c % kScSlots), (c / kScSlots) & 1, 10000000ull);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -658,6 +676,8 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 if (!wait_spin(bar(RB_X), c & 1, abort_flag, p.err)) break;
                 GDN_TR(p.trace, 1, c, 1);
                 fence_after_sync();
+                if (!wait_spin(bar(RB_SP), c & 1, abort_flag, p.err)) break;   // state pre-decayed
+                fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)   // c2: S += (V_new^T diag(fk)) K
                     mma_ts(tb + TM_S, tb + TM_X1K + ks * 8, smem_desc(base + R_QK + ks * 2048, 16384, 1024), id_c2, 1);
@@ -673,6 +693,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 for (int ks = 0; ks < 4; ++ks)   // c1: D2B = V_new^T Aqk^T
                     mma_ts(tb + TM_D2B, tb + TM_X1 + ks * 8, smem_desc(base + PB_AQK + ks * 32, 16, 1024), id_c1, ks > 0);
                 commit(bar(RB_D2O));
+                commit(bar(RB_EMPTY + (c & 1)));   // every read of this stage is done
             }
             commit(bar(RB_FIN));   // every MMA must complete before tensor memory is released
             mbar_wait(bar(RB_FIN), 0, kWaitLimitNs);
@@ -690,9 +711,9 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     *reinterpret_cast<float4 *>(p.final_state + srow + d) = v4;
                 }
         } else {
-            bool ok = wait_spin(bar(RB_FULL), 0, abort_flag, p.err);
+            bool ok = wait_spin(bar(RB_SCF), 0, abort_flag, p.err);
             {
-                const float e0 = reinterpret_cast<const float *>(sm + PB_SC)[128];
+                const float e0 = reinterpret_cast<const float *>(sm + R_SCR)[128];
 #pragma unroll
                 for (int q2 = 0; q2 < 4; ++q2) {   // 32 state entries per pass
                     float v[32];
@@ -716,9 +737,12 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 tmem_wait_st();
             }
             fence_before_sync();
-            if (!group_sync_or(1, 128, !ok || *abort_flag) && j == 0) mbar_arrive(bar(RB_S));
+            if (!group_sync_or(1, 128, !ok || *abort_flag) && j == 0) {
+                mbar_arrive(bar(RB_S));
+                mbar_arrive(bar(RB_SP));
+            }
             for (int c = 0; c < nch; ++c) {
-                const float *fk = reinterpret_cast<const float *>(sm + stage(c) + PB_SC) + 64;
+                const float *fk = reinterpret_cast<const float *>(sm + R_SCR + (c % kScSlots) * 1024) + 64;
                 // V_new^T -> bf16 A operands (plain, and with the K-> factors folded in)
                 ok = wait_spin(bar(RB_D1), c & 1, abort_flag, p.err);
                 if (j == 0) GDN_TR(p.trace, 2, c, 0);
@@ -751,8 +775,9 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 if (j == 0) GDN_TR(p.trace, 2, c, 1);
                 fence_after_sync();
                 if (c + 1 < nch) {
-                    ok = ok && wait_spin(bar(RB_FULL + ((c + 1) & 1)), ((c + 1) >> 1) & 1, abort_flag, p.err);
-                    const float e1 = reinterpret_cast<const float *>(sm + stage(c + 1) + PB_SC)[128];
+                    const int s1 = (c + 1) % kScSlots;
+                    ok = ok && wait_spin(bar(RB_SCF + s1), ((c + 1) / kScSlots) & 1, abort_flag, p.err);
+                    const float e1 = reinterpret_cast<const float *>(sm + R_SCR + s1 * 1024)[128];
                     const uint32_t sbf = lane_base + TM_SBF + (uint32_t)((c + 1) & 1) * 64;
                     uint32_t a[128];
 #pragma unroll
@@ -766,15 +791,19 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                             pk[e] = pack_bf16(__uint_as_float(a[q * 32 + 2 * e]), __uint_as_float(a[q * 32 + 2 * e + 1]));
                         tmem_st16(sbf + q * 16, pk);
                     }
+                    tmem_wait_st();
+                    fence_before_sync();
+                    if (group_sync_or(1, 128, !ok || *abort_flag)) break;
+                    if (j == 0) mbar_arrive(bar(RB_S));   // the bf16 state is ready: the next V_new may start
+                    if (j == 0) GDN_TR(p.trace, 2, c, 2);
 #pragma unroll
                     for (int e = 0; e < 128; ++e) a[e] = __float_as_uint(e1 * __uint_as_float(a[e]));
 #pragma unroll
                     for (int q = 0; q < 8; ++q) tmem_st16(lane_base + TM_S + q * 16, *reinterpret_cast<uint32_t(*)[16]>(a + q * 16));
                     tmem_wait_st();
                     fence_before_sync();
-                    if (group_sync_or(1, 128, !ok || *abort_flag)) break;
-                    if (j == 0) mbar_arrive(bar(RB_S));
-                    if (j == 0) GDN_TR(p.trace, 2, c, 2);
+                    if (group_sync_or(1, 128, *abort_flag)) break;
+                    if (j == 0) mbar_arrive(bar(RB_SP));  // the fp32 state is pre-decayed for the next update
                 } else if (p.final_state && ok) {
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
@@ -792,15 +821,15 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
         }
     } else {
         // ------------------------------------------------------------ output epilogue
-        // O = fq . (Q S^T) + Aqk V_new through a [64 r][128 j] bf16 staging tile in
-        // the chunk's V buffer (its only reader, a1, has completed), then 16-B stores
+        // O = fq . (Q S^T) + Aqk V_new through a [64 r][128 j] bf16 staging tile,
+        // then coalesced 16-B stores
         const int j = 32 * (warp & 3) + lane;   // output column j0 + j
         for (int c = 0; c < nch; ++c) {
             const int rows = min(kChunk, len - c * kChunk);
             const int64_t z0 = tok0 + (int64_t)c * kChunk;
-            uint8_t *sbase = sm + stage(c);
-            const float *fq = reinterpret_cast<const float *>(sbase + PB_SC);
-            bool ok = wait_bar(bar(RB_D2O), c & 1, abort_flag, p.err);
+            const float *fq = reinterpret_cast<const float *>(sm + R_SCR + (c % kScSlots) * 1024);
+            bool ok = wait_bar(bar(RB_SCF + c % kScSlots), (c / kScSlots) & 1, abort_flag, p.err);
+            ok = ok && wait_bar(bar(RB_D2O), c & 1, abort_flag, p.err);
             fence_after_sync();
             uint32_t a[64], b[64];
 #pragma unroll
@@ -812,7 +841,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             fence_before_sync();
             if (group_sync_or(2, 128, !ok || *abort_flag)) break;
             if (j == 0) mbar_arrive(bar(RB_OFREE));   // D2 may be overwritten
-            uint8_t *stg = sbase + R_V;
+            uint8_t *stg = sm + R_OUT;
 #pragma unroll
             for (int r = 0; r < 64; ++r)
                 *reinterpret_cast<__nv_bfloat16 *>(stg + (r * 128 + j) * 2) =
@@ -827,7 +856,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                         *reinterpret_cast<const uint4 *>(stg + r * 256 + ch * 16);
             }
             if (group_sync_or(2, 128, *abort_flag)) break;
-            if (j == 0) mbar_arrive(bar(RB_EMPTY + (c & 1)));   // the stage may be refilled
+            if (j == 0) mbar_arrive(bar(RB_SCE + c % kScSlots));   // the factor slot may be refilled
             if (j == 0) GDN_TR(p.trace, 2, c, 3);
         }
     }
