@@ -69,21 +69,25 @@ constexpr uint32_t kSmemUt = U_MISC + 64 + 1024;
 static_assert(U_A % 16 == 0 && U_SC % 16 == 0, "alignment");
 static_assert(3 * (kSmemUt + 1024) <= 233472, "three UT CTAs per SM");
 
-// ---- recur_tc_kernel shared memory: two stages of [T', W~^T, Aqk | Q,K tile | V tile],
-// a ring of the per-chunk factors (fetched further ahead), and an output staging tile
+// ---- recur_tc_kernel shared memory.  Operands are staged by lifetime:
+//   "early" stages (3): T', W~^T (read by a1, a2) and V (a1)
+//   "late"  stages (2): Aqk (c1) and the K|Q tile (c2, b)
+// plus a ring of the per-chunk factors (fetched further ahead) and an output staging tile.
 constexpr int kThreadsRc = 320;        // warp 0: loads, TMEM; warp 1: MMA; warps 2-5: state; 6-9: outputs
-constexpr uint32_t R_QK = 32768;       // within a stage (1024-aligned)
-constexpr uint32_t R_V = R_QK + 32768;
-constexpr uint32_t R_STAGE = R_V + 16384;
-constexpr uint32_t R_OUT = 2 * R_STAGE;            // [64 r][128 j] bf16 output staging
-constexpr uint32_t R_SCR = R_OUT + 16384;          // factor ring: kScSlots x 1 KB
-constexpr int kScSlots = 4;
-constexpr uint32_t kScBytes = 528;                 // fq[64], fk[64], e^{b_C} (+ pad)
+constexpr int kEarly = 3, kLate = 2, kScSlots = 4;
+constexpr uint32_t E_TP = 0, E_WT = 8192, E_V = 24576, kEarlyBytes = 40960;
+constexpr uint32_t L_AQK = 0, L_QK = 8192, kLateBytes = 40960;
+constexpr uint32_t R_EARLY = 0;
+constexpr uint32_t R_LATE = R_EARLY + kEarly * kEarlyBytes;
+constexpr uint32_t R_OUT = R_LATE + kLate * kLateBytes;   // [64 r][128 j] bf16 output staging
+constexpr uint32_t R_SCR = R_OUT + 16384;                 // factor ring: kScSlots x 1 KB
+constexpr uint32_t kScBytes = 528;                        // fq[64], fk[64], e^{b_C} (+ pad)
 constexpr uint32_t R_BAR = R_SCR + kScSlots * 1024;
-constexpr uint32_t R_MISC = R_BAR + 24 * 8;
+constexpr uint32_t R_MISC = R_BAR + 32 * 8;
 constexpr uint32_t kSmemRc = R_MISC + 64 + 1024;
-static_assert(R_STAGE % 1024 == 0 && kSmemRc <= 232448, "recurrence smem");
-constexpr uint32_t kStageTx = PB_SC + 32768 + 16384;   // prep tiles (no factors) + q/k + v
+static_assert(kEarlyBytes % 1024 == 0 && kLateBytes % 1024 == 0 && kSmemRc <= 232448, "recurrence smem");
+constexpr uint32_t kEarlyTx = PB_AQK + 16384;           // T', W~^T (contiguous) + V
+constexpr uint32_t kLateTx = 8192 + 32768;              // Aqk + K|Q
 
 // recurrence tensor-memory columns (512)
 constexpr uint32_t TM_S = 0;      // fp32 state, 128
@@ -94,8 +98,9 @@ constexpr uint32_t TM_D2B = 384;  // V_new^T Aqk^T accumulator, 64
 constexpr uint32_t TM_X1 = 448;   // V_new^T bf16, 32
 constexpr uint32_t TM_X1K = 480;  // V_new^T diag(fk) bf16, 32
 
-enum : int { RB_FULL = 0, RB_EMPTY = 2, RB_D1 = 4, RB_X = 5, RB_S = 6, RB_D2S = 7, RB_D2O = 8, RB_FIN = 9,
-             RB_OFREE = 10, RB_SP = 11, RB_SCF = 12, RB_SCE = 16 };   // RB_SCF/RB_SCE: [kScSlots]
+enum : int { RB_EF = 0, RB_EE = 3, RB_LF = 6, RB_LE = 8, RB_SCF = 10, RB_SCE = 14,   // rings
+             RB_D1 = 18, RB_X = 19, RB_X1 = 20, RB_S = 21, RB_SP = 22, RB_D2S = 23, RB_D2O = 24,
+             RB_OFREE = 25, RB_FIN = 26, RB_COUNT = 27 };
 enum : int { UB_QK = 0, UB_P1 = 1, UB_TRDY = 2, UB_P2 = 3, UB_FIN = 4 };
 
 // Development-only phase timestamps (SM clock) of the first CTA; compiled out
@@ -144,6 +149,12 @@ __device__ __forceinline__ bool wait_spin(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Group-wide wait with a single spinning thread: the leader polls the mbarrier
+// and a named barrier releases the other threads, so 128 pollers do not
+// contend for the barrier word.  Returns false (for the whole group) on abort.
+__device__ __forceinline__ bool group_wait(uint32_t bar, uint32_t parity, bool leader, int id, volatile int *abort_flag,
+                                           unsigned *err);
+
 // Named barrier over `count` threads that also ORs a predicate across them,
 // so a whole group leaves a loop at the same point.
 __device__ __forceinline__ bool group_sync_or(int id, int count, bool pred)
@@ -161,6 +172,14 @@ __device__ __forceinline__ bool group_sync_or(int id, int count, bool pred)
 __device__ __forceinline__ void group_sync(int id, int count)
 {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool group_wait(uint32_t bar, uint32_t parity, bool leader, int id, volatile int *abort_flag,
+                                           unsigned *err)
+{
+    bool ok = true;
+    if (leader) ok = wait_spin(bar, parity, abort_flag, err);
+    return !group_sync_or(id, 128, !ok);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b)
@@ -592,10 +611,11 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     uint32_t *tmem_sh = reinterpret_cast<uint32_t *>(sm + R_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + R_MISC + 4);
     auto bar = [&](int i) -> uint32_t { return sb + R_BAR + 8u * (uint32_t)i; };
-    auto stage = [&](int c) -> uint32_t { return (uint32_t)(c & 1) * R_STAGE; };
+    auto early = [&](int c) -> uint32_t { return R_EARLY + (uint32_t)(c % kEarly) * kEarlyBytes; };
+    auto late = [&](int c) -> uint32_t { return R_LATE + (uint32_t)(c % kLate) * kLateBytes; };
 
     if (tid == 0) {
-        for (int i = 0; i < RB_SCE + kScSlots; ++i) mbar_init(bar(i), 1);
+        for (int i = 0; i < RB_COUNT; ++i) mbar_init(bar(i), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -608,92 +628,107 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
 
     if (warp == 0) {
         // ------------------------------------------------------------ loads
-        if (lane == 0 && nch > 0) {
-            prefetch_tmap(&tmq);
-            prefetch_tmap(&tmk);
-            prefetch_tmap(&tmv);
+        // lane 0: early ring (T', W~^T, V); lane 1: factor ring; lane 2: late ring (Aqk, K|Q)
+        if (lane < 3 && nch > 0) {
+            if (lane == 0) { prefetch_tmap(&tmv); }
+            if (lane == 2) { prefetch_tmap(&tmq); prefetch_tmap(&tmk); }
+            const int slots = lane == 0 ? kEarly : (lane == 1 ? kScSlots : kLate);
+            const int fbar = lane == 0 ? RB_EF : (lane == 1 ? RB_SCF : RB_LF);
+            const int ebar = lane == 0 ? RB_EE : (lane == 1 ? RB_SCE : RB_LE);
             int last = -1;
             for (int c = 0; c < nch; ++c) {
-                const int s = c & 1;
-                if (c >= 2 && !wait_bar(bar(RB_EMPTY + s), ((c >> 1) - 1) & 1, abort_flag, p.err)) break;
-                GDN_TR(p.trace, 3, c, 0);
-                const uint32_t base = sb + stage(c);
+                const int s = c % slots;
+                if (c >= slots && !wait_bar(bar(ebar + s), ((c / slots) - 1) & 1, abort_flag, p.err)) break;
                 const int z = (int)(tok0 + (int64_t)c * kChunk);
-                const uint8_t *src = p.blocks + ((size_t)(slot0 + c) * H + h) * kPrepBlock;
-                mbar_expect_tx(bar(RB_FULL + s), kStageTx);
-                bulk_load(base, src, PB_SC, bar(RB_FULL + s));
-                tma_load_3d(base + R_QK, &tmk, 0, h, z, bar(RB_FULL + s));
-                tma_load_3d(base + R_QK + 8192, &tmq, 0, h, z, bar(RB_FULL + s));
-                tma_load_3d(base + R_QK + 16384, &tmk, 64, h, z, bar(RB_FULL + s));
-                tma_load_3d(base + R_QK + 24576, &tmq, 64, h, z, bar(RB_FULL + s));
-                tma_load_3d(base + R_V, &tmv, j0, h, z, bar(RB_FULL + s));
-                tma_load_3d(base + R_V + 8192, &tmv, j0 + 64, h, z, bar(RB_FULL + s));
+                const uint8_t *blk = p.blocks + ((size_t)(slot0 + c) * H + h) * kPrepBlock;
+                const uint32_t fb = bar(fbar + s);
+                if (lane == 0) {
+                    const uint32_t base = sb + early(c);
+                    mbar_expect_tx(fb, kEarlyTx);
+                    bulk_load(base + E_TP, blk + PB_TP, PB_AQK, fb);   // T' and W~^T
+                    tma_load_3d(base + E_V, &tmv, j0, h, z, fb);
+                    tma_load_3d(base + E_V + 8192, &tmv, j0 + 64, h, z, fb);
+                } else if (lane == 1) {
+                    mbar_expect_tx(fb, kScBytes);
+                    bulk_load(sb + R_SCR + s * 1024, blk + PB_SC, kScBytes, fb);
+                } else {
+                    const uint32_t base = sb + late(c);
+                    mbar_expect_tx(fb, kLateTx);
+                    bulk_load(base + L_AQK, blk + PB_AQK, 8192, fb);
+                    tma_load_3d(base + L_QK, &tmk, 0, h, z, fb);
+                    tma_load_3d(base + L_QK + 8192, &tmq, 0, h, z, fb);
+                    tma_load_3d(base + L_QK + 16384, &tmk, 64, h, z, fb);
+                    tma_load_3d(base + L_QK + 24576, &tmq, 64, h, z, fb);
+                }
                 last = c;
             }
             if (*abort_flag)   // let the copies in flight land before the CTA exits
-                for (int c = (last > 0 ? last - 1 : 0); c <= last; ++c)
-                    mbar_wait(bar(RB_FULL + (c & 1)), (c >> 1) & 1, 10000000ull);
-        } else if (lane == 1 && nch > 0) {
-            int last = -1;
-            for (int c = 0; c < nch; ++c) {
-                const int s = c % kScSlots;
-                if (c >= kScSlots && !wait_bar(bar(RB_SCE + s), ((c / kScSlots) - 1) & 1, abort_flag, p.err)) break;
-                const uint8_t *src = p.blocks + ((size_t)(slot0 + c) * H + h) * kPrepBlock + PB_SC;
-                mbar_expect_tx(bar(RB_SCF + s), kScBytes);
-                bulk_load(sb + R_SCR + s * 1024, src, kScBytes, bar(RB_SCF + s));
-                last = c;
-            }
-            if (*abort_flag)
-                for (int c = (last >= kScSlots ? last - kScSlots + 1 : 0); c <= last; ++c)
-                    mbar_wait(bar(RB_SCF + c % kScSlots), (c / kScSlots) & 1, 10000000ull);
+                for (int c = (last >= slots ? last - slots + 1 : 0); c <= last; ++c)
+                    mbar_wait(bar(fbar + c % slots), (c / slots) & 1, 10000000ull);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
+        // Software-pipelined so the serial chain (a2, c2) never queues behind the
+        // output products (b, c1) of the previous chunk on the tensor pipe.
         if (lane == 0 && nch > 0) {
             const uint32_t id_a1 = idesc_bf16(128, 64, true, false);
             const uint32_t id_a2 = idesc_bf16(128, 64, false, true, true);   // negated B: -S W~^T
             const uint32_t id_b = idesc_bf16(128, 64, false, false);
             const uint32_t id_c1 = idesc_bf16(128, 64, false, false);
             const uint32_t id_c2 = idesc_bf16(128, 128, false, true);
-            for (int c = 0; c < nch; ++c) {
-                const uint32_t base = sb + stage(c);
-                const uint32_t sbf = tb + TM_SBF + (uint32_t)(c & 1) * 64;
-                if (!wait_spin(bar(RB_FULL + (c & 1)), (c >> 1) & 1, abort_flag, p.err)) break;
-                if (c > 0 && !wait_spin(bar(RB_X), (c - 1) & 1, abort_flag, p.err)) break;   // D1 drained
+            auto issue_a = [&](int c) -> bool {   // V_new^T = V^T T'^T - S W~^T
+                const uint32_t eb = sb + early(c);
+                if (!wait_spin(bar(RB_EF + c % kEarly), (c / kEarly) & 1, abort_flag, p.err)) return false;
                 fence_after_sync();
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)   // a1: D1 = V^T T'^T
-                    mma_ss(tb + TM_D1, smem_desc(base + R_V + ks * 2048, 8192, 1024),
-                           smem_desc(base + PB_TP + ks * 32, 16, 1024), id_a1, ks > 0);
-                if (!wait_spin(bar(RB_S), c & 1, abort_flag, p.err)) break;
+                for (int ks = 0; ks < 4; ++ks)   // a1
+                    mma_ss(tb + TM_D1, smem_desc(eb + E_V + ks * 2048, 8192, 1024),
+                           smem_desc(eb + E_TP + ks * 32, 16, 1024), id_a1, ks > 0);
+                if (!wait_spin(bar(RB_S), c & 1, abort_flag, p.err)) return false;
                 GDN_TR(p.trace, 1, c, 0);
                 fence_after_sync();
+                const uint32_t sbf = tb + TM_SBF + (uint32_t)(c & 1) * 64;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)   // a2: D1 -= S W~^T
-                    mma_ts(tb + TM_D1, sbf + ks * 8, smem_desc(base + PB_WT + ks * 2048, 16384, 1024), id_a2, 1);
+                for (int ks = 0; ks < 8; ++ks)   // a2
+                    mma_ts(tb + TM_D1, sbf + ks * 8, smem_desc(eb + E_WT + ks * 2048, 16384, 1024), id_a2, 1);
                 commit(bar(RB_D1));
+                commit(bar(RB_EE + c % kEarly));
+                GDN_TR(p.trace, 1, c, 4);
+                return true;
+            };
+            bool ok = issue_a(0);
+            for (int c = 0; c < nch && ok; ++c) {
+                const uint32_t lb = sb + late(c);
+                if (!wait_spin(bar(RB_LF + c % kLate), (c / kLate) & 1, abort_flag, p.err)) break;
+                GDN_TR(p.trace, 1, c, 2);
                 if (!wait_spin(bar(RB_X), c & 1, abort_flag, p.err)) break;
-                GDN_TR(p.trace, 1, c, 1);
-                fence_after_sync();
+                GDN_TR(p.trace, 1, c, 3);
                 if (!wait_spin(bar(RB_SP), c & 1, abort_flag, p.err)) break;   // state pre-decayed
+                GDN_TR(p.trace, 1, c, 1);
                 fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)   // c2: S += (V_new^T diag(fk)) K
-                    mma_ts(tb + TM_S, tb + TM_X1K + ks * 8, smem_desc(base + R_QK + ks * 2048, 16384, 1024), id_c2, 1);
+                    mma_ts(tb + TM_S, tb + TM_X1K + ks * 8, smem_desc(lb + L_QK + ks * 2048, 16384, 1024), id_c2, 1);
                 commit(bar(RB_D2S));
+                // X1(c) is written right after X(c), long before the next state is ready,
+                // so waiting for it here costs nothing and keeps every barrier at most one
+                // phase ahead of its waiter
+                if (!wait_spin(bar(RB_X1), c & 1, abort_flag, p.err)) break;
+                if (c + 1 < nch && !(ok = issue_a(c + 1))) break;
                 if (c > 0 && !wait_spin(bar(RB_OFREE), (c - 1) & 1, abort_flag, p.err)) break;   // D2 drained
                 fence_after_sync();
+                const uint32_t sbf = tb + TM_SBF + (uint32_t)(c & 1) * 64;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {   // b: D2A = S Q^T
-                    const uint32_t off = R_QK + 8192 + (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_ts(tb + TM_D2A, sbf + ks * 8, smem_desc(base + off, 16, 1024), id_b, ks > 0);
+                    const uint32_t off = L_QK + 8192 + (ks >> 2) * 16384 + (ks & 3) * 32;
+                    mma_ts(tb + TM_D2A, sbf + ks * 8, smem_desc(lb + off, 16, 1024), id_b, ks > 0);
                 }
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)   // c1: D2B = V_new^T Aqk^T
-                    mma_ts(tb + TM_D2B, tb + TM_X1 + ks * 8, smem_desc(base + PB_AQK + ks * 32, 16, 1024), id_c1, ks > 0);
+                    mma_ts(tb + TM_D2B, tb + TM_X1 + ks * 8, smem_desc(lb + L_AQK + ks * 32, 16, 1024), id_c1, ks > 0);
                 commit(bar(RB_D2O));
-                commit(bar(RB_EMPTY + (c & 1)));   // every read of this stage is done
+                commit(bar(RB_LE + c % kLate));
             }
             commit(bar(RB_FIN));   // every MMA must complete before tensor memory is released
             mbar_wait(bar(RB_FIN), 0, kWaitLimitNs);
@@ -743,8 +778,9 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             }
             for (int c = 0; c < nch; ++c) {
                 const float *fk = reinterpret_cast<const float *>(sm + R_SCR + (c % kScSlots) * 1024) + 64;
-                // V_new^T -> bf16 A operands (plain, and with the K-> factors folded in)
-                ok = wait_spin(bar(RB_D1), c & 1, abort_flag, p.err);
+                // V_new^T -> bf16 A operands: first with the K-> factors folded in (the
+                // state update waits for it), then plain (for the output product)
+                ok = group_wait(bar(RB_D1), c & 1, j == 0, 1, abort_flag, p.err);
                 if (j == 0) GDN_TR(p.trace, 2, c, 0);
                 fence_after_sync();
                 {
@@ -754,24 +790,38 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     tmem_wait_ld();
 #pragma unroll
                     for (int q2 = 0; q2 < 2; ++q2) {
-                        uint32_t pk[16], pkk[16];
+                        uint32_t pkk[16];
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             const int r = q2 * 32 + 2 * e;
-                            const float x0 = __uint_as_float(a[r]), x1 = __uint_as_float(a[r + 1]);
-                            pk[e] = pack_bf16(x0, x1);
-                            pkk[e] = pack_bf16(x0 * fk[r], x1 * fk[r + 1]);
+                            pkk[e] = pack_bf16(__uint_as_float(a[r]) * fk[r], __uint_as_float(a[r + 1]) * fk[r + 1]);
                         }
                         tmem_st16(lane_base + TM_X1K + q2 * 16, pkk);
+                    }
+                    tmem_wait_st();
+                    fence_before_sync();
+                    if (group_sync_or(1, 128, !ok || *abort_flag)) break;
+                    if (j == 0) mbar_arrive(bar(RB_X));
+                    if (j == 0) GDN_TR(p.trace, 2, c, 4);
+                    // the plain copy is still read by the previous chunk's output product (c1),
+                    // which the MMA issues after this chunk's V_new: wait for it to complete
+                    if (c > 0) ok = wait_spin(bar(RB_D2O), (c - 1) & 1, abort_flag, p.err);
+                    fence_after_sync();
+#pragma unroll
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            pk[e] = pack_bf16(__uint_as_float(a[q2 * 32 + 2 * e]), __uint_as_float(a[q2 * 32 + 2 * e + 1]));
                         tmem_st16(lane_base + TM_X1 + q2 * 16, pk);
                     }
+                    tmem_wait_st();
+                    fence_before_sync();
+                    if (group_sync_or(1, 128, !ok || *abort_flag)) break;
+                    if (j == 0) mbar_arrive(bar(RB_X1));
                 }
-                tmem_wait_st();
-                fence_before_sync();
-                if (group_sync_or(1, 128, !ok || *abort_flag)) break;
-                if (j == 0) mbar_arrive(bar(RB_X));
                 // the next state
-                ok = wait_spin(bar(RB_D2S), c & 1, abort_flag, p.err);
+                ok = group_wait(bar(RB_D2S), c & 1, j == 0, 1, abort_flag, p.err);
                 if (j == 0) GDN_TR(p.trace, 2, c, 1);
                 fence_after_sync();
                 if (c + 1 < nch) {
@@ -804,6 +854,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     fence_before_sync();
                     if (group_sync_or(1, 128, *abort_flag)) break;
                     if (j == 0) mbar_arrive(bar(RB_SP));  // the fp32 state is pre-decayed for the next update
+                    if (j == 0) GDN_TR(p.trace, 2, c, 5);
                 } else if (p.final_state && ok) {
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
