@@ -73,7 +73,7 @@ static_assert(3 * (kSmemUt + 1024) <= 233472, "three UT CTAs per SM");
 //   "early" stages (3): T', W~^T (read by a1, a2) and V (a1)
 //   "late"  stages (2): Aqk (c1) and the K|Q tile (c2, b)
 // plus a ring of the per-chunk factors (fetched further ahead) and an output staging tile.
-constexpr int kThreadsRc = 320;        // warp 0: loads, TMEM; warp 1: MMA; warps 2-5: state; 6-9: outputs
+constexpr int kThreadsRc = 448;        // warp 0: loads, TMEM; warp 1: MMA; warps 2-9: state; 10-13: outputs
 constexpr int kEarly = 3, kLate = 2, kScSlots = 4;
 constexpr uint32_t E_TP = 0, E_WT = 8192, E_V = 24576, kEarlyBytes = 40960;
 constexpr uint32_t L_AQK = 0, L_QK = 8192, kLateBytes = 40960;
@@ -149,12 +149,6 @@ __device__ __forceinline__ bool wait_spin(uint32_t bar, uint32_t parity, volatil
     }
 }
 
-// Group-wide wait with a single spinning thread: the leader polls the mbarrier
-// and a named barrier releases the other threads, so 128 pollers do not
-// contend for the barrier word.  Returns false (for the whole group) on abort.
-__device__ __forceinline__ bool group_wait(uint32_t bar, uint32_t parity, bool leader, int id, volatile int *abort_flag,
-                                           unsigned *err);
-
 // Named barrier over `count` threads that also ORs a predicate across them,
 // so a whole group leaves a loop at the same point.
 __device__ __forceinline__ bool group_sync_or(int id, int count, bool pred)
@@ -172,14 +166,6 @@ __device__ __forceinline__ bool group_sync_or(int id, int count, bool pred)
 __device__ __forceinline__ void group_sync(int id, int count)
 {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool group_wait(uint32_t bar, uint32_t parity, bool leader, int id, volatile int *abort_flag,
-                                           unsigned *err)
-{
-    bool ok = true;
-    if (leader) ok = wait_spin(bar, parity, abort_flag, err);
-    return !group_sync_or(id, 128, !ok);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b)
@@ -734,27 +720,40 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             mbar_wait(bar(RB_FIN), 0, kWaitLimitNs);
         }
         __syncwarp();
-    } else if (warp < 6) {
-        // ------------------------------------------------------------ state epilogue (the serial chain)
-        const int j = 32 * (warp & 3) + lane;   // row of S within the slice
+    } else if (warp < 10) {
+        // ------------------------------------------------------------ state epilogue (warps 2-9)
+        // Each tensor-memory lane (row j of S) is served by two threads: half 0 owns
+        // the first half of every row's columns, half 1 the second.  Per chunk:
+        //   X   : V_new^T -> bf16 with the K-> factors (gates c2), then plain (for c1)
+        //   S   : S -> bf16 (gates the next a2), then S <- e^{b_C} S (gates the next c2)
+        const int j = 32 * (warp & 3) + lane;
+        const int hf = warp >= 6 ? 1 : 0;
+        const bool leader = (warp == 2 && lane == 0);
         const size_t srow = (((size_t)n * H + h) * (size_t)dv + (size_t)(j0 + j)) * 128;
+        auto gsync = [&](bool bad) -> bool { return group_sync_or(1, 256, bad); };
+        auto gwait = [&](int b, uint32_t parity) -> bool {
+            bool ok = true;
+            if (leader) ok = wait_spin(bar(b), parity, abort_flag, p.err);
+            return !gsync(!ok);
+        };
         if (nch == 0) {
             if (p.final_state)
-                for (int d = 0; d < 128; d += 4) {
+                for (int d = hf * 64; d < hf * 64 + 64; d += 4) {
                     float4 v4 = p.init_state ? *reinterpret_cast<const float4 *>(p.init_state + srow + d)
                                              : make_float4(0.f, 0.f, 0.f, 0.f);
                     *reinterpret_cast<float4 *>(p.final_state + srow + d) = v4;
                 }
-        } else {
+        } else do {
             bool ok = wait_spin(bar(RB_SCF), 0, abort_flag, p.err);
-            {
+            {   // initial state: this thread's 64 entries of row j
                 const float e0 = reinterpret_cast<const float *>(sm + R_SCR)[128];
 #pragma unroll
-                for (int q2 = 0; q2 < 4; ++q2) {   // 32 state entries per pass
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    const int d0 = hf * 64 + q2 * 32;
                     float v[32];
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
-                        float4 v4 = p.init_state ? *reinterpret_cast<const float4 *>(p.init_state + srow + q2 * 32 + e)
+                        float4 v4 = p.init_state ? *reinterpret_cast<const float4 *>(p.init_state + srow + d0 + e)
                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
                         v[e] = v4.x; v[e + 1] = v4.y; v[e + 2] = v4.z; v[e + 3] = v4.w;
                     }
@@ -765,122 +764,119 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                         s0[e] = __float_as_uint(e0 * v[e]);
                         s1[e] = __float_as_uint(e0 * v[16 + e]);
                     }
-                    tmem_st16(lane_base + TM_SBF + q2 * 16, pk);
-                    tmem_st16(lane_base + TM_S + q2 * 32, s0);
-                    tmem_st16(lane_base + TM_S + q2 * 32 + 16, s1);
+                    tmem_st16(lane_base + TM_SBF + d0 / 2, pk);
+                    tmem_st16(lane_base + TM_S + d0, s0);
+                    tmem_st16(lane_base + TM_S + d0 + 16, s1);
                 }
                 tmem_wait_st();
             }
             fence_before_sync();
-            if (!group_sync_or(1, 128, !ok || *abort_flag) && j == 0) {
-                mbar_arrive(bar(RB_S));
-                mbar_arrive(bar(RB_SP));
-            }
+            if (gsync(!ok || *abort_flag)) break;
+            if (leader) { mbar_arrive(bar(RB_S)); mbar_arrive(bar(RB_SP)); }
             for (int c = 0; c < nch; ++c) {
                 const float *fk = reinterpret_cast<const float *>(sm + R_SCR + (c % kScSlots) * 1024) + 64;
-                // V_new^T -> bf16 A operands: first with the K-> factors folded in (the
-                // state update waits for it), then plain (for the output product)
-                ok = group_wait(bar(RB_D1), c & 1, j == 0, 1, abort_flag, p.err);
-                if (j == 0) GDN_TR(p.trace, 2, c, 0);
+                // ---- X: this thread's 32 tokens of V_new^T row j
+                if (!gwait(RB_D1, c & 1)) { ok = false; break; }
+                if (leader) GDN_TR(p.trace, 2, c, 0);
+                fence_after_sync();
+                uint32_t a[32];
+                tmem_ld16(lane_base + TM_D1 + hf * 32, *reinterpret_cast<uint32_t(*)[16]>(a));
+                tmem_ld16(lane_base + TM_D1 + hf * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(a + 16));
+                tmem_wait_ld();
+                {
+                    uint32_t pkk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int r = hf * 32 + 2 * e;
+                        pkk[e] = pack_bf16(__uint_as_float(a[2 * e]) * fk[r], __uint_as_float(a[2 * e + 1]) * fk[r + 1]);
+                    }
+                    tmem_st16(lane_base + TM_X1K + hf * 16, pkk);
+                }
+                tmem_wait_st();
+                fence_before_sync();
+                if (gsync(*abort_flag)) { ok = false; break; }
+                if (leader) mbar_arrive(bar(RB_X));
+                if (leader) GDN_TR(p.trace, 2, c, 4);
+                // the plain copy is still read by the previous chunk's c1 until it completes
+                if (c > 0 && !gwait(RB_D2O, (c - 1) & 1)) { ok = false; break; }
                 fence_after_sync();
                 {
-                    uint32_t a[64];
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) tmem_ld16(lane_base + TM_D1 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(a + q * 16));
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int q2 = 0; q2 < 2; ++q2) {
-                        uint32_t pkk[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int r = q2 * 32 + 2 * e;
-                            pkk[e] = pack_bf16(__uint_as_float(a[r]) * fk[r], __uint_as_float(a[r + 1]) * fk[r + 1]);
-                        }
-                        tmem_st16(lane_base + TM_X1K + q2 * 16, pkk);
-                    }
-                    tmem_wait_st();
-                    fence_before_sync();
-                    if (group_sync_or(1, 128, !ok || *abort_flag)) break;
-                    if (j == 0) mbar_arrive(bar(RB_X));
-                    if (j == 0) GDN_TR(p.trace, 2, c, 4);
-                    // the plain copy is still read by the previous chunk's output product (c1),
-                    // which the MMA issues after this chunk's V_new: wait for it to complete
-                    if (c > 0) ok = wait_spin(bar(RB_D2O), (c - 1) & 1, abort_flag, p.err);
-                    fence_after_sync();
-#pragma unroll
-                    for (int q2 = 0; q2 < 2; ++q2) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            pk[e] = pack_bf16(__uint_as_float(a[q2 * 32 + 2 * e]), __uint_as_float(a[q2 * 32 + 2 * e + 1]));
-                        tmem_st16(lane_base + TM_X1 + q2 * 16, pk);
-                    }
-                    tmem_wait_st();
-                    fence_before_sync();
-                    if (group_sync_or(1, 128, !ok || *abort_flag)) break;
-                    if (j == 0) mbar_arrive(bar(RB_X1));
+                    for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
+                    tmem_st16(lane_base + TM_X1 + hf * 16, pk);
                 }
-                // the next state
-                ok = group_wait(bar(RB_D2S), c & 1, j == 0, 1, abort_flag, p.err);
-                if (j == 0) GDN_TR(p.trace, 2, c, 1);
+                tmem_wait_st();
+                fence_before_sync();
+                if (gsync(*abort_flag)) { ok = false; break; }
+                if (leader) mbar_arrive(bar(RB_X1));
+                // ---- S: this thread's 64 entries of row j
+                if (!gwait(RB_D2S, c & 1)) { ok = false; break; }
+                if (leader) GDN_TR(p.trace, 2, c, 1);
                 fence_after_sync();
                 if (c + 1 < nch) {
                     const int s1 = (c + 1) % kScSlots;
-                    ok = ok && wait_spin(bar(RB_SCF + s1), ((c + 1) / kScSlots) & 1, abort_flag, p.err);
+                    if (!gwait(RB_SCF + s1, ((c + 1) / kScSlots) & 1)) { ok = false; break; }
                     const float e1 = reinterpret_cast<const float *>(sm + R_SCR + s1 * 1024)[128];
-                    const uint32_t sbf = lane_base + TM_SBF + (uint32_t)((c + 1) & 1) * 64;
-                    uint32_t a[128];
+                    const uint32_t sbf = lane_base + TM_SBF + (uint32_t)((c + 1) & 1) * 64 + hf * 32;
+                    uint32_t sv[64];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) tmem_ld16(lane_base + TM_S + q * 16, *reinterpret_cast<uint32_t(*)[16]>(a + q * 16));
+                    for (int q = 0; q < 4; ++q)
+                        tmem_ld16(lane_base + TM_S + hf * 64 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(sv + q * 16));
                     tmem_wait_ld();
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < 2; ++q) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
-                            pk[e] = pack_bf16(__uint_as_float(a[q * 32 + 2 * e]), __uint_as_float(a[q * 32 + 2 * e + 1]));
+                            pk[e] = pack_bf16(__uint_as_float(sv[q * 32 + 2 * e]), __uint_as_float(sv[q * 32 + 2 * e + 1]));
                         tmem_st16(sbf + q * 16, pk);
                     }
                     tmem_wait_st();
                     fence_before_sync();
-                    if (group_sync_or(1, 128, !ok || *abort_flag)) break;
-                    if (j == 0) mbar_arrive(bar(RB_S));   // the bf16 state is ready: the next V_new may start
-                    if (j == 0) GDN_TR(p.trace, 2, c, 2);
+                    if (gsync(*abort_flag)) { ok = false; break; }
+                    if (leader) mbar_arrive(bar(RB_S));   // the bf16 state is ready: the next V_new may start
+                    if (leader) GDN_TR(p.trace, 2, c, 2);
 #pragma unroll
-                    for (int e = 0; e < 128; ++e) a[e] = __float_as_uint(e1 * __uint_as_float(a[e]));
+                    for (int e = 0; e < 64; ++e) sv[e] = __float_as_uint(e1 * __uint_as_float(sv[e]));
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) tmem_st16(lane_base + TM_S + q * 16, *reinterpret_cast<uint32_t(*)[16]>(a + q * 16));
+                    for (int q = 0; q < 4; ++q)
+                        tmem_st16(lane_base + TM_S + hf * 64 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(sv + q * 16));
                     tmem_wait_st();
                     fence_before_sync();
-                    if (group_sync_or(1, 128, *abort_flag)) break;
-                    if (j == 0) mbar_arrive(bar(RB_SP));  // the fp32 state is pre-decayed for the next update
-                    if (j == 0) GDN_TR(p.trace, 2, c, 5);
-                } else if (p.final_state && ok) {
+                    if (gsync(*abort_flag)) { ok = false; break; }
+                    if (leader) mbar_arrive(bar(RB_SP));  // the fp32 state is pre-decayed for the next update
+                    if (leader) GDN_TR(p.trace, 2, c, 5);
+                } else if (p.final_state) {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
+                    for (int q = 0; q < 4; ++q) {
                         uint32_t u[16];
-                        tmem_ld16(lane_base + TM_S + q * 16, u);
+                        tmem_ld16(lane_base + TM_S + hf * 64 + q * 16, u);
                         tmem_wait_ld();
 #pragma unroll
                         for (int e = 0; e < 16; e += 4)
-                            *reinterpret_cast<float4 *>(p.final_state + srow + q * 16 + e) =
+                            *reinterpret_cast<float4 *>(p.final_state + srow + hf * 64 + q * 16 + e) =
                                 make_float4(__uint_as_float(u[e]), __uint_as_float(u[e + 1]),
                                             __uint_as_float(u[e + 2]), __uint_as_float(u[e + 3]));
                     }
                 }
             }
-        }
+        } while (false);
     } else {
-        // ------------------------------------------------------------ output epilogue
+        // ------------------------------------------------------------ output epilogue (warps 10-13)
         // O = fq . (Q S^T) + Aqk V_new through a [64 r][128 j] bf16 staging tile,
         // then coalesced 16-B stores
         const int j = 32 * (warp & 3) + lane;   // output column j0 + j
+        const bool leader = (warp == 10 && lane == 0);
+        auto osync = [&](bool bad) -> bool { return group_sync_or(2, 128, bad); };
         for (int c = 0; c < nch; ++c) {
-            const int rows = min(kChunk, len - c * kChunk);
-            const int64_t z0 = tok0 + (int64_t)c * kChunk;
             const float *fq = reinterpret_cast<const float *>(sm + R_SCR + (c % kScSlots) * 1024);
-            bool ok = wait_bar(bar(RB_SCF + c % kScSlots), (c / kScSlots) & 1, abort_flag, p.err);
-            ok = ok && wait_bar(bar(RB_D2O), c & 1, abort_flag, p.err);
+            bool ok = true;
+            if (leader) {
+                ok = wait_spin(bar(RB_SCF + c % kScSlots), (c / kScSlots) & 1, abort_flag, p.err);
+                ok = ok && wait_spin(bar(RB_D2O), c & 1, abort_flag, p.err);
+            }
+            if (osync(!ok)) break;
             fence_after_sync();
             uint32_t a[64], b[64];
 #pragma unroll
@@ -890,15 +886,16 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             }
             tmem_wait_ld();
             fence_before_sync();
-            if (group_sync_or(2, 128, !ok || *abort_flag)) break;
-            if (j == 0) mbar_arrive(bar(RB_OFREE));   // D2 may be overwritten
+            if (osync(*abort_flag)) break;
+            if (leader) mbar_arrive(bar(RB_OFREE));   // D2 may be overwritten
             uint8_t *stg = sm + R_OUT;
 #pragma unroll
             for (int r = 0; r < 64; ++r)
                 *reinterpret_cast<__nv_bfloat16 *>(stg + (r * 128 + j) * 2) =
                     __float2bfloat16_rn(fq[r] * __uint_as_float(a[r]) + __uint_as_float(b[r]));
-            if (group_sync_or(2, 128, *abort_flag)) break;
-            __nv_bfloat16 *obase = p.out + (size_t)z0 * H * dv + (size_t)h * dv + j0;
+            if (osync(*abort_flag)) break;
+            const int rows = min(kChunk, len - c * kChunk);
+            __nv_bfloat16 *obase = p.out + (size_t)(tok0 + (int64_t)c * kChunk) * H * dv + (size_t)h * dv + j0;
 #pragma unroll
             for (int it = 0; it < 8; ++it) {
                 const int idx = it * 128 + j, r = idx >> 4, ch = idx & 15;
@@ -906,9 +903,9 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     *reinterpret_cast<uint4 *>(obase + (size_t)r * H * dv + ch * 8) =
                         *reinterpret_cast<const uint4 *>(stg + r * 256 + ch * 16);
             }
-            if (group_sync_or(2, 128, *abort_flag)) break;
-            if (j == 0) mbar_arrive(bar(RB_SCE + c % kScSlots));   // the factor slot may be refilled
-            if (j == 0) GDN_TR(p.trace, 2, c, 3);
+            if (osync(*abort_flag)) break;
+            if (leader) mbar_arrive(bar(RB_SCE + c % kScSlots));   // the factor slot may be refilled
+            if (leader) GDN_TR(p.trace, 2, c, 3);
         }
     }
 
