@@ -50,18 +50,21 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s: legitimate waits are microseconds
 
 // Per (chunk, head) block of the workspace written by ut_tc_kernel.
-constexpr uint32_t PB_TP = 0;          // T'   bf16 [64 r][64 i]   (K-major, swizzled)
-constexpr uint32_t PB_WT = 8192;       // W~^T bf16 [128 d][64 r]  (MN-major, swizzled)
-constexpr uint32_t PB_AQK = 24576;     // Aqk  bf16 [64 r][64 i]   (K-major, swizzled)
-constexpr uint32_t PB_SC = 32768;      // fq[64], fk[64], e^{b_C}  (fp32)
-constexpr uint32_t kPrepBlock = 33792;
+// All tiles are 128-B-swizzled rows of 64 bf16 (8 KB per 64 rows).
+constexpr uint32_t PB_TP = 0;          // T'    [64 r][64 i]                  (K-major B of a1)
+constexpr uint32_t PB_W = 8192;        // W~    [d-block][64 r][64 d]  x 2    (K-major B of a2)
+constexpr uint32_t PB_AQT = 24576;     // Aqk^T [64 i][64 r]                  (MN-major B of c)
+constexpr uint32_t PB_KT = 32768;      // K->   [d-block][64 r][64 d]  x 2    (MN-major B of c)
+constexpr uint32_t PB_SC = 49152;      // fq[64], fk[64], e^{b_C}  (fp32)
+constexpr uint32_t kPrepBlock = 50176;
 constexpr uint32_t kWsHeader = 1024;   // device error word + padding
 
 // ---- ut_tc_kernel shared memory
 constexpr int kThreadsUt = 160;        // warp 0: TMA, MMA, TMEM; warps 1-4: 128 "prep" threads
 constexpr uint32_t U_QK = 0;           // [K kb0][Q kb0][K kb1][Q kb1], 8 KB each
-constexpr uint32_t U_TPP = 32768;      // T'' 8 KB (scratch of the solve before that)
-constexpr uint32_t U_A = 40960;        // L, then T, in place: fp32 [64][LDL]
+constexpr uint32_t U_TPP = 32768;      // Aqk^T staging, then solve scratch, then T'' (8 KB)
+constexpr uint32_t U_ZERO = 40960;     // 8 KB of zeros: rows 64-127 of the padded A = [T''; 0]
+constexpr uint32_t U_A = 49152;        // L, then T, in place: fp32 [64][LDL]
 constexpr uint32_t U_SC = U_A + 64 * LDL * 4;     // b, beta, rk, rq, cw, ecol [6][64] fp32
 constexpr uint32_t U_BAR = U_SC + 6 * 64 * 4;
 constexpr uint32_t U_MISC = U_BAR + 8 * 8;
@@ -70,37 +73,35 @@ static_assert(U_A % 16 == 0 && U_SC % 16 == 0, "alignment");
 static_assert(3 * (kSmemUt + 1024) <= 233472, "three UT CTAs per SM");
 
 // ---- recur_tc_kernel shared memory.  Operands are staged by lifetime:
-//   "early" stages (3): T', W~^T (read by a1, a2) and V (a1)
-//   "late"  stages (2): Aqk (c1) and the K|Q tile (c2, b)
-// plus a ring of the per-chunk factors (fetched further ahead) and an output staging tile.
+//   "early" stages (3): T' and V (a1), [W~ | Q] interleaved (the merged a2 product)
+//   "late"  stages (2): [Aqk^T | K->] (the merged c product); then the output staging tile
+// plus a ring of the per-chunk factors, fetched further ahead.
 constexpr int kThreadsRc = 448;        // warp 0: loads, TMEM; warp 1: MMA; warps 2-9: state; 10-13: outputs
 constexpr int kEarly = 3, kLate = 2, kScSlots = 4;
-constexpr uint32_t E_TP = 0, E_WT = 8192, E_V = 24576, kEarlyBytes = 40960;
-constexpr uint32_t L_AQK = 0, L_QK = 8192, kLateBytes = 40960;
+constexpr uint32_t E_TP = 0, E_V = 8192, E_WQ = 24576, kEarlyBytes = 57344;
+constexpr uint32_t kLateBytes = 24576;
 constexpr uint32_t R_EARLY = 0;
 constexpr uint32_t R_LATE = R_EARLY + kEarly * kEarlyBytes;
-constexpr uint32_t R_OUT = R_LATE + kLate * kLateBytes;   // [64 r][128 j] bf16 output staging
-constexpr uint32_t R_SCR = R_OUT + 16384;                 // factor ring: kScSlots x 1 KB
+constexpr uint32_t R_SCR = R_LATE + kLate * kLateBytes;   // factor ring: kScSlots x 1 KB
 constexpr uint32_t kScBytes = 528;                        // fq[64], fk[64], e^{b_C} (+ pad)
 constexpr uint32_t R_BAR = R_SCR + kScSlots * 1024;
 constexpr uint32_t R_MISC = R_BAR + 32 * 8;
 constexpr uint32_t kSmemRc = R_MISC + 64 + 1024;
 static_assert(kEarlyBytes % 1024 == 0 && kLateBytes % 1024 == 0 && kSmemRc <= 232448, "recurrence smem");
-constexpr uint32_t kEarlyTx = PB_AQK + 16384;           // T', W~^T (contiguous) + V
-constexpr uint32_t kLateTx = 8192 + 32768;              // Aqk + K|Q
+constexpr uint32_t kEarlyTx = 8192 + 16384 + 32768;     // T', V, W~ and Q
+constexpr uint32_t kLateTx = 24576;                     // Aqk^T and K->
 
 // recurrence tensor-memory columns (512)
-constexpr uint32_t TM_S = 0;      // fp32 state, 128
-constexpr uint32_t TM_SBF = 128;  // bf16 state x 2 buffers (by chunk parity), 64 each
-constexpr uint32_t TM_D1 = 256;   // V_new^T accumulator, 64
-constexpr uint32_t TM_D2A = 320;  // S Q^T accumulator, 64
-constexpr uint32_t TM_D2B = 384;  // V_new^T Aqk^T accumulator, 64
-constexpr uint32_t TM_X1 = 448;   // V_new^T bf16, 32
-constexpr uint32_t TM_X1K = 480;  // V_new^T diag(fk) bf16, 32
+constexpr uint32_t TM_D1 = 0;     // V_new^T accumulator, 64      } the merged a2 product
+constexpr uint32_t TM_D2A = 64;   // -S Q^T accumulator, 64       } writes D1 | D2A
+constexpr uint32_t TM_D2B = 128;  // V_new^T Aqk^T accumulator, 64   } the merged c product
+constexpr uint32_t TM_S = 192;    // fp32 state, 128                 } writes D2B | S
+constexpr uint32_t TM_X = 320;    // V_new^T bf16 (A operand), 32
+constexpr uint32_t TM_SBF = 384;  // bf16 state (A operand), 64
 
 enum : int { RB_EF = 0, RB_EE = 3, RB_LF = 6, RB_LE = 8, RB_SCF = 10, RB_SCE = 14,   // rings
-             RB_D1 = 18, RB_X = 19, RB_X1 = 20, RB_S = 21, RB_SP = 22, RB_D2S = 23, RB_D2O = 24,
-             RB_OFREE = 25, RB_FIN = 26, RB_COUNT = 27 };
+             RB_D1 = 18, RB_X = 19, RB_S = 20, RB_SP = 21, RB_D2 = 22, RB_OFREE = 23, RB_FIN = 24,
+             RB_COUNT = 25 };
 enum : int { UB_QK = 0, UB_P1 = 1, UB_TRDY = 2, UB_P2 = 3, UB_FIN = 4 };
 
 // Development-only phase timestamps (SM clock) of the first CTA; compiled out
@@ -361,12 +362,15 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         *abort_flag = 0;
         fence_mbar_init();
     }
+    for (int i = tid; i < 8192 / 16; i += kThreadsUt)
+        reinterpret_cast<uint4 *>(sm + U_ZERO)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async();
     if (warp == 0) tmem_alloc(tmem_sh, 128);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tb = *tmem_sh;
-    const uint32_t TP1 = 0, TP2 = 64;
+    const uint32_t TP1 = 0, TP2 = 0;   // P2 reuses P1's columns once the masks are read
 
     if (warp == 0) {
         if (lane == 0) {
@@ -387,11 +391,11 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 commit(bar(UB_P1));
                 if (wait_bar(bar(UB_TRDY), 0, abort_flag, p.err)) {
                     fence_after_sync();
-                    const uint32_t id_p2 = idesc_bf16(128, 64, true, false);
+                    const uint32_t id_p2 = idesc_bf16(128, 128, false, true);
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)   // W~^T = K^T T''^T
-                        mma_ss(tb + TP2, smem_desc(sb + U_QK + ks * 2048, 16384, 1024),
-                               smem_desc(sb + U_TPP + ks * 32, 16, 1024), id_p2, ks > 0);
+                    for (int ks = 0; ks < 4; ++ks)   // [W~; 0] = [T''; 0] K   (rows 0-63 are W~)
+                        mma_ss(tb + TP2, smem_desc(sb + U_TPP + ks * 32, 16, 1024),
+                               smem_desc(sb + U_QK + ks * 2048, 16384, 1024), id_p2, ks > 0);
                     commit(bar(UB_P2));
                 }
             }
@@ -484,19 +488,22 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
 #pragma unroll
                         for (int e = 0; e < 4; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
                     } else {
+                        // row r of Q K^T o Gamma is column r of the transposed tile
 #pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            uint32_t w[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) w[e] = pack_bf16(v[hh * 8 + 2 * e], v[hh * 8 + 2 * e + 1]);
-                            *reinterpret_cast<uint4 *>(blk + PB_AQK + sw128_offset(r, q * 16 + hh * 8)) =
-                                make_uint4(w[0], w[1], w[2], w[3]);
-                        }
+                        for (int e = 0; e < 16; ++e)
+                            *reinterpret_cast<__nv_bfloat16 *>(sm + U_TPP + sw128_offset(q * 16 + e, r)) =
+                                __float2bfloat16_rn(v[e]);
                     }
                 }
             }
             fence_before_sync();
             if (group_sync_or(2, 128, !ok || *abort_flag)) break;
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {   // Aqk^T tile -> workspace
+                const int idx = it * 128 + prow;
+                reinterpret_cast<uint4 *>(blk + PB_AQT)[idx] = reinterpret_cast<const uint4 *>(sm + U_TPP)[idx];
+            }
+            group_sync(1, 128);   // the staging area becomes the solve's scratch
 
             // (4) T = (I + L)^{-1} in place;  T' -> workspace,  T'' -> shared memory
             solve_in_place(Am, Mt, prow, warp - 1, lane);
@@ -535,12 +542,33 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                     if (r == 0) reinterpret_cast<float *>(blk + PB_SC)[128] = exp2f(bC);
                 }
             }
+            if (prow >= 64) {   // K-> = diag(fk) K, written in the K tile's own layout
+                const int r = prow - 64;
+                const float fk = (r < rows) ? exp2f(bsum[63] - bsum[r]) * rk[r] : 0.f;
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+                    const uint8_t *src = st + kb * 16384 + r * 128;
+                    uint8_t *dst = blk + PB_KT + kb * 8192 + r * 128;
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const uint4 u = *reinterpret_cast<const uint4 *>(src + ch * 16);
+                        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                        uint32_t o[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 x = unpack_bf16(w[e]);
+                            o[e] = pack_bf16(x.x * fk, x.y * fk);
+                        }
+                        *reinterpret_cast<uint4 *>(dst + ch * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                }
+            }
             ok = wait_bar(bar(UB_P2), 0, abort_flag, p.err);
             fence_after_sync();
-            {
-                uint32_t u[16];
+            if (prow < 64) {   // row r of W~ (128 d), K-major tiles of 64 d
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 8; ++q) {
+                    uint32_t u[16];
                     tmem_ld16(lane_base + TP2 + q * 16, u);
                     tmem_wait_ld();
 #pragma unroll
@@ -549,7 +577,8 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             w[e] = pack_bf16(__uint_as_float(u[hh * 8 + 2 * e]), __uint_as_float(u[hh * 8 + 2 * e + 1]));
-                        *reinterpret_cast<uint4 *>(blk + PB_WT + sw128_offset(prow, q * 16 + hh * 8)) =
+                        const int d = q * 16 + hh * 8;
+                        *reinterpret_cast<uint4 *>(blk + PB_W + (d >> 6) * 8192 + sw128_offset(prow, d & 63)) =
                             make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
@@ -579,8 +608,7 @@ struct RcParams {
 };
 
 __global__ void __launch_bounds__(kThreadsRc, 1)
-recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                const __grid_constant__ CUtensorMap tmv, const RcParams p)
+recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmv, const RcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -614,10 +642,9 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
 
     if (warp == 0) {
         // ------------------------------------------------------------ loads
-        // lane 0: early ring (T', W~^T, V); lane 1: factor ring; lane 2: late ring (Aqk, K|Q)
+        // lane 0: early ring (T', V, W~ | Q); lane 1: factor ring; lane 2: late ring (Aqk^T | K->)
         if (lane < 3 && nch > 0) {
-            if (lane == 0) { prefetch_tmap(&tmv); }
-            if (lane == 2) { prefetch_tmap(&tmq); prefetch_tmap(&tmk); }
+            if (lane == 0) { prefetch_tmap(&tmq); prefetch_tmap(&tmv); }
             const int slots = lane == 0 ? kEarly : (lane == 1 ? kScSlots : kLate);
             const int fbar = lane == 0 ? RB_EF : (lane == 1 ? RB_SCF : RB_LF);
             const int ebar = lane == 0 ? RB_EE : (lane == 1 ? RB_SCE : RB_LE);
@@ -631,20 +658,19 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 if (lane == 0) {
                     const uint32_t base = sb + early(c);
                     mbar_expect_tx(fb, kEarlyTx);
-                    bulk_load(base + E_TP, blk + PB_TP, PB_AQK, fb);   // T' and W~^T
+                    bulk_load(base + E_TP, blk + PB_TP, 8192, fb);
                     tma_load_3d(base + E_V, &tmv, j0, h, z, fb);
                     tma_load_3d(base + E_V + 8192, &tmv, j0 + 64, h, z, fb);
+                    bulk_load(base + E_WQ, blk + PB_W, 8192, fb);                 // W~ d 0-63   -> rows 0-63
+                    tma_load_3d(base + E_WQ + 8192, &tmq, 0, h, z, fb);           // Q  d 0-63   -> rows 64-127
+                    bulk_load(base + E_WQ + 16384, blk + PB_W + 8192, 8192, fb);  // W~ d 64-127
+                    tma_load_3d(base + E_WQ + 24576, &tmq, 64, h, z, fb);         // Q  d 64-127
                 } else if (lane == 1) {
                     mbar_expect_tx(fb, kScBytes);
                     bulk_load(sb + R_SCR + s * 1024, blk + PB_SC, kScBytes, fb);
                 } else {
-                    const uint32_t base = sb + late(c);
                     mbar_expect_tx(fb, kLateTx);
-                    bulk_load(base + L_AQK, blk + PB_AQK, 8192, fb);
-                    tma_load_3d(base + L_QK, &tmk, 0, h, z, fb);
-                    tma_load_3d(base + L_QK + 8192, &tmq, 0, h, z, fb);
-                    tma_load_3d(base + L_QK + 16384, &tmk, 64, h, z, fb);
-                    tma_load_3d(base + L_QK + 24576, &tmq, 64, h, z, fb);
+                    bulk_load(sb + late(c), blk + PB_AQT, kLateTx, fb);
                 }
                 last = c;
             }
@@ -655,35 +681,41 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
-        // Software-pipelined so the serial chain (a2, c2) never queues behind the
-        // output products (b, c1) of the previous chunk on the tensor pipe.
+        // Per chunk three products (16 instructions):
+        //   a1 : D1        = V^T T'^T                      (N = 64,  K = 64)
+        //   a2 : [D1|D2A] -= S [W~ ; Q]^T                  (N = 128, K = 128)  V_new^T and -S Q^T
+        //   c  : [D2B|S]  += V_new^T [Aqk^T | K->]          (N = 192, K = 64)   outputs and state
+        // D2A and D2B are re-zeroed by the output warps once they have read them.
         if (lane == 0 && nch > 0) {
             const uint32_t id_a1 = idesc_bf16(128, 64, true, false);
-            const uint32_t id_a2 = idesc_bf16(128, 64, false, true, true);   // negated B: -S W~^T
-            const uint32_t id_b = idesc_bf16(128, 64, false, false);
-            const uint32_t id_c1 = idesc_bf16(128, 64, false, false);
-            const uint32_t id_c2 = idesc_bf16(128, 128, false, true);
-            auto issue_a = [&](int c) -> bool {   // V_new^T = V^T T'^T - S W~^T
+            const uint32_t id_a2 = idesc_bf16(128, 128, false, false, true);   // negated B
+            const uint32_t id_c = idesc_bf16(128, 192, false, true);
+            auto issue_a1 = [&](int c) -> bool {
                 const uint32_t eb = sb + early(c);
                 if (!wait_spin(bar(RB_EF + c % kEarly), (c / kEarly) & 1, abort_flag, p.err)) return false;
                 fence_after_sync();
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)   // a1
+                for (int ks = 0; ks < 4; ++ks)
                     mma_ss(tb + TM_D1, smem_desc(eb + E_V + ks * 2048, 8192, 1024),
                            smem_desc(eb + E_TP + ks * 32, 16, 1024), id_a1, ks > 0);
+                return true;
+            };
+            auto issue_a2 = [&](int c) -> bool {
+                const uint32_t eb = sb + early(c);
                 if (!wait_spin(bar(RB_S), c & 1, abort_flag, p.err)) return false;
+                if (!wait_spin(bar(RB_OFREE), c & 1, abort_flag, p.err)) return false;   // D2A, D2B zero
                 GDN_TR(p.trace, 1, c, 0);
                 fence_after_sync();
-                const uint32_t sbf = tb + TM_SBF + (uint32_t)(c & 1) * 64;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)   // a2
-                    mma_ts(tb + TM_D1, sbf + ks * 8, smem_desc(eb + E_WT + ks * 2048, 16384, 1024), id_a2, 1);
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_ts(tb + TM_D1, tb + TM_SBF + ks * 8,
+                           smem_desc(eb + E_WQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id_a2, 1);
                 commit(bar(RB_D1));
                 commit(bar(RB_EE + c % kEarly));
                 GDN_TR(p.trace, 1, c, 4);
                 return true;
             };
-            bool ok = issue_a(0);
+            bool ok = issue_a1(0) && issue_a2(0);
             for (int c = 0; c < nch && ok; ++c) {
                 const uint32_t lb = sb + late(c);
                 if (!wait_spin(bar(RB_LF + c % kLate), (c / kLate) & 1, abort_flag, p.err)) break;
@@ -694,27 +726,10 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 GDN_TR(p.trace, 1, c, 1);
                 fence_after_sync();
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)   // c2: S += (V_new^T diag(fk)) K
-                    mma_ts(tb + TM_S, tb + TM_X1K + ks * 8, smem_desc(lb + L_QK + ks * 2048, 16384, 1024), id_c2, 1);
-                commit(bar(RB_D2S));
-                // X1(c) is written right after X(c), long before the next state is ready,
-                // so waiting for it here costs nothing and keeps every barrier at most one
-                // phase ahead of its waiter
-                if (!wait_spin(bar(RB_X1), c & 1, abort_flag, p.err)) break;
-                if (c + 1 < nch && !(ok = issue_a(c + 1))) break;
-                if (c > 0 && !wait_spin(bar(RB_OFREE), (c - 1) & 1, abort_flag, p.err)) break;   // D2 drained
-                fence_after_sync();
-                const uint32_t sbf = tb + TM_SBF + (uint32_t)(c & 1) * 64;
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {   // b: D2A = S Q^T
-                    const uint32_t off = L_QK + 8192 + (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_ts(tb + TM_D2A, sbf + ks * 8, smem_desc(lb + off, 16, 1024), id_b, ks > 0);
-                }
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)   // c1: D2B = V_new^T Aqk^T
-                    mma_ts(tb + TM_D2B, tb + TM_X1 + ks * 8, smem_desc(lb + L_AQK + ks * 32, 16, 1024), id_c1, ks > 0);
-                commit(bar(RB_D2O));
-                commit(bar(RB_LE + c % kLate));
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_ts(tb + TM_D2B, tb + TM_X + ks * 8, smem_desc(lb + ks * 2048, 8192, 1024), id_c, 1);
+                commit(bar(RB_D2));
+                if (c + 1 < nch && !(ok = issue_a1(c + 1) && issue_a2(c + 1))) break;
             }
             commit(bar(RB_FIN));   // every MMA must complete before tensor memory is released
             mbar_wait(bar(RB_FIN), 0, kWaitLimitNs);
@@ -724,8 +739,8 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
         // ------------------------------------------------------------ state epilogue (warps 2-9)
         // Each tensor-memory lane (row j of S) is served by two threads: half 0 owns
         // the first half of every row's columns, half 1 the second.  Per chunk:
-        //   X   : V_new^T -> bf16 with the K-> factors (gates c2), then plain (for c1)
-        //   S   : S -> bf16 (gates the next a2), then S <- e^{b_C} S (gates the next c2)
+        //   X : V_new^T -> bf16 (gates the merged c product)
+        //   S : S -> bf16 (gates the next a2), then S <- e^{b_C} S (gates the next c)
         const int j = 32 * (warp & 3) + lane;
         const int hf = warp >= 6 ? 1 : 0;
         const bool leader = (warp == 2 && lane == 0);
@@ -774,51 +789,32 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             if (gsync(!ok || *abort_flag)) break;
             if (leader) { mbar_arrive(bar(RB_S)); mbar_arrive(bar(RB_SP)); }
             for (int c = 0; c < nch; ++c) {
-                const float *fk = reinterpret_cast<const float *>(sm + R_SCR + (c % kScSlots) * 1024) + 64;
                 // ---- X: this thread's 32 tokens of V_new^T row j
-                if (!gwait(RB_D1, c & 1)) { ok = false; break; }
+                if (!gwait(RB_D1, c & 1)) break;
                 if (leader) GDN_TR(p.trace, 2, c, 0);
                 fence_after_sync();
-                uint32_t a[32];
-                tmem_ld16(lane_base + TM_D1 + hf * 32, *reinterpret_cast<uint32_t(*)[16]>(a));
-                tmem_ld16(lane_base + TM_D1 + hf * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(a + 16));
-                tmem_wait_ld();
                 {
-                    uint32_t pkk[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int r = hf * 32 + 2 * e;
-                        pkk[e] = pack_bf16(__uint_as_float(a[2 * e]) * fk[r], __uint_as_float(a[2 * e + 1]) * fk[r + 1]);
-                    }
-                    tmem_st16(lane_base + TM_X1K + hf * 16, pkk);
-                }
-                tmem_wait_st();
-                fence_before_sync();
-                if (gsync(*abort_flag)) { ok = false; break; }
-                if (leader) mbar_arrive(bar(RB_X));
-                if (leader) GDN_TR(p.trace, 2, c, 4);
-                // the plain copy is still read by the previous chunk's c1 until it completes
-                if (c > 0 && !gwait(RB_D2O, (c - 1) & 1)) { ok = false; break; }
-                fence_after_sync();
-                {
-                    uint32_t pk[16];
+                    uint32_t a[32], pk[16];
+                    tmem_ld16(lane_base + TM_D1 + hf * 32, *reinterpret_cast<uint32_t(*)[16]>(a));
+                    tmem_ld16(lane_base + TM_D1 + hf * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(a + 16));
+                    tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
-                    tmem_st16(lane_base + TM_X1 + hf * 16, pk);
+                    tmem_st16(lane_base + TM_X + hf * 16, pk);
                 }
                 tmem_wait_st();
                 fence_before_sync();
-                if (gsync(*abort_flag)) { ok = false; break; }
-                if (leader) mbar_arrive(bar(RB_X1));
+                if (gsync(*abort_flag)) break;
+                if (leader) mbar_arrive(bar(RB_X));
+                if (leader) GDN_TR(p.trace, 2, c, 4);
                 // ---- S: this thread's 64 entries of row j
-                if (!gwait(RB_D2S, c & 1)) { ok = false; break; }
+                if (!gwait(RB_D2, c & 1)) break;
                 if (leader) GDN_TR(p.trace, 2, c, 1);
                 fence_after_sync();
                 if (c + 1 < nch) {
                     const int s1 = (c + 1) % kScSlots;
-                    if (!gwait(RB_SCF + s1, ((c + 1) / kScSlots) & 1)) { ok = false; break; }
+                    if (!gwait(RB_SCF + s1, ((c + 1) / kScSlots) & 1)) break;
                     const float e1 = reinterpret_cast<const float *>(sm + R_SCR + s1 * 1024)[128];
-                    const uint32_t sbf = lane_base + TM_SBF + (uint32_t)((c + 1) & 1) * 64 + hf * 32;
                     uint32_t sv[64];
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
@@ -830,12 +826,12 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
                             pk[e] = pack_bf16(__uint_as_float(sv[q * 32 + 2 * e]), __uint_as_float(sv[q * 32 + 2 * e + 1]));
-                        tmem_st16(sbf + q * 16, pk);
+                        tmem_st16(lane_base + TM_SBF + hf * 32 + q * 16, pk);
                     }
                     tmem_wait_st();
                     fence_before_sync();
-                    if (gsync(*abort_flag)) { ok = false; break; }
-                    if (leader) mbar_arrive(bar(RB_S));   // the bf16 state is ready: the next V_new may start
+                    if (gsync(*abort_flag)) break;
+                    if (leader) mbar_arrive(bar(RB_S));   // the bf16 state is ready: the next a2 may start
                     if (leader) GDN_TR(p.trace, 2, c, 2);
 #pragma unroll
                     for (int e = 0; e < 64; ++e) sv[e] = __float_as_uint(e1 * __uint_as_float(sv[e]));
@@ -844,8 +840,8 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                         tmem_st16(lane_base + TM_S + hf * 64 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(sv + q * 16));
                     tmem_wait_st();
                     fence_before_sync();
-                    if (gsync(*abort_flag)) { ok = false; break; }
-                    if (leader) mbar_arrive(bar(RB_SP));  // the fp32 state is pre-decayed for the next update
+                    if (gsync(*abort_flag)) break;
+                    if (leader) mbar_arrive(bar(RB_SP));  // the fp32 state is pre-decayed for the next c
                     if (leader) GDN_TR(p.trace, 2, c, 5);
                 } else if (p.final_state) {
 #pragma unroll
@@ -864,19 +860,33 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
         } while (false);
     } else {
         // ------------------------------------------------------------ output epilogue (warps 10-13)
-        // O = fq . (Q S^T) + Aqk V_new through a [64 r][128 j] bf16 staging tile,
-        // then coalesced 16-B stores
+        // O = fq . (Q S^T) + Aqk V_new = D2B - fq . D2A; the accumulators are re-zeroed
+        // for the next chunk, then O goes through a [64 r][128 j] bf16 staging tile (in
+        // the chunk's late stage, whose operands the finished c product no longer needs)
+        // to coalesced 16-B stores.
         const int j = 32 * (warp & 3) + lane;   // output column j0 + j
         const bool leader = (warp == 10 && lane == 0);
         auto osync = [&](bool bad) -> bool { return group_sync_or(2, 128, bad); };
+        auto zero_d2 = [&]() {
+            uint32_t z[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) z[e] = 0u;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) tmem_st16(lane_base + TM_D2A + q * 16, z);   // D2A and D2B
+            tmem_wait_st();
+        };
+        zero_d2();   // phase 0 of RB_OFREE: the accumulators start at zero
+        fence_before_sync();
+        if (!osync(*abort_flag) && leader && nch > 0) mbar_arrive(bar(RB_OFREE));
         for (int c = 0; c < nch; ++c) {
             const float *fq = reinterpret_cast<const float *>(sm + R_SCR + (c % kScSlots) * 1024);
             bool ok = true;
             if (leader) {
                 ok = wait_spin(bar(RB_SCF + c % kScSlots), (c / kScSlots) & 1, abort_flag, p.err);
-                ok = ok && wait_spin(bar(RB_D2O), c & 1, abort_flag, p.err);
+                ok = ok && wait_spin(bar(RB_D2), c & 1, abort_flag, p.err);
             }
             if (osync(!ok)) break;
+            if (leader) GDN_TR(p.trace, 0, c, 0);
             fence_after_sync();
             uint32_t a[64], b[64];
 #pragma unroll
@@ -885,15 +895,18 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 tmem_ld16(lane_base + TM_D2B + q * 16, *reinterpret_cast<uint32_t(*)[16]>(b + q * 16));
             }
             tmem_wait_ld();
+            zero_d2();
             fence_before_sync();
             if (osync(*abort_flag)) break;
-            if (leader) mbar_arrive(bar(RB_OFREE));   // D2 may be overwritten
-            uint8_t *stg = sm + R_OUT;
+            if (leader && c + 1 < nch) mbar_arrive(bar(RB_OFREE));   // D2A, D2B read and re-zeroed
+            if (leader) GDN_TR(p.trace, 0, c, 1);
+            uint8_t *stg = sm + late(c);
 #pragma unroll
             for (int r = 0; r < 64; ++r)
                 *reinterpret_cast<__nv_bfloat16 *>(stg + (r * 128 + j) * 2) =
-                    __float2bfloat16_rn(fq[r] * __uint_as_float(a[r]) + __uint_as_float(b[r]));
+                    __float2bfloat16_rn(__uint_as_float(b[r]) - fq[r] * __uint_as_float(a[r]));
             if (osync(*abort_flag)) break;
+            if (leader) GDN_TR(p.trace, 0, c, 2);
             const int rows = min(kChunk, len - c * kChunk);
             __nv_bfloat16 *obase = p.out + (size_t)(tok0 + (int64_t)c * kChunk) * H * dv + (size_t)h * dv + j0;
 #pragma unroll
@@ -904,7 +917,10 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                         *reinterpret_cast<const uint4 *>(stg + r * 256 + ch * 16);
             }
             if (osync(*abort_flag)) break;
-            if (leader) mbar_arrive(bar(RB_SCE + c % kScSlots));   // the factor slot may be refilled
+            if (leader) {
+                mbar_arrive(bar(RB_LE + c % kLate));       // the late stage may be refilled
+                mbar_arrive(bar(RB_SCE + c % kScSlots));   // and the factor slot
+            }
             if (leader) GDN_TR(p.trace, 2, c, 3);
         }
     }
@@ -990,7 +1006,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st)
     rp.final_state = a.final_state; rp.err = err; rp.gm = a.gm; rp.trace = trace;
     e = cudaFuncSetAttribute(recur_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemRc);
     if (e != cudaSuccess) return e;
-    recur_tc_kernel<<<dim3(a.gm.N, a.gm.H, a.gm.dv / 128), kThreadsRc, kSmemRc, st>>>(tq, tk, tv, rp);
+    recur_tc_kernel<<<dim3(a.gm.N, a.gm.H, a.gm.dv / 128), kThreadsRc, kSmemRc, st>>>(tq, tv, rp);
     return cudaGetLastError();
 }
 
