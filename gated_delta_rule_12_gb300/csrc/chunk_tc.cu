@@ -73,16 +73,19 @@ static_assert(U_A % 16 == 0 && U_SC % 16 == 0, "alignment");
 static_assert(3 * (kSmemUt + 1024) <= 233472, "three UT CTAs per SM");
 
 // ---- recur_tc_kernel shared memory.  Operands are staged by lifetime:
-//   "early" stages (3): T' and V (a1), [W~ | Q] interleaved (the merged a2 product)
-//   "late"  stages (2): [Aqk^T | K->] (the merged c product); then the output staging tile
-// plus a ring of the per-chunk factors, fetched further ahead.
+//   "early" stages (2): T' and V (a1), [W~ | Q] interleaved (the merged a2 product)
+//   "late"  stages (2): [Aqk^T | K->] (even chunks) or [K-> | Aqk^T] (odd chunks) for the
+//                       merged c product; afterwards the chunk's output staging tile
+//   the bf16 state (A of a2) and the bf16 V_new^T (A of c), and a ring of per-chunk factors.
 constexpr int kThreadsRc = 448;        // warp 0: loads, TMEM; warp 1: MMA; warps 2-9: state; 10-13: outputs
-constexpr int kEarly = 3, kLate = 2, kScSlots = 4;
+constexpr int kEarly = 2, kLate = 2, kScSlots = 4;
 constexpr uint32_t E_TP = 0, E_V = 8192, E_WQ = 24576, kEarlyBytes = 57344;
 constexpr uint32_t kLateBytes = 24576;
 constexpr uint32_t R_EARLY = 0;
 constexpr uint32_t R_LATE = R_EARLY + kEarly * kEarlyBytes;
-constexpr uint32_t R_SCR = R_LATE + kLate * kLateBytes;   // factor ring: kScSlots x 1 KB
+constexpr uint32_t R_SBF = R_LATE + kLate * kLateBytes;   // S bf16, [d-block][128 j][64 d] x 2
+constexpr uint32_t R_X = R_SBF + 32768;                   // V_new^T bf16, [128 j][64 r]
+constexpr uint32_t R_SCR = R_X + 16384;                   // factor ring: kScSlots x 1 KB
 constexpr uint32_t kScBytes = 528;                        // fq[64], fk[64], e^{b_C} (+ pad)
 constexpr uint32_t R_BAR = R_SCR + kScSlots * 1024;
 constexpr uint32_t R_MISC = R_BAR + 32 * 8;
@@ -91,17 +94,20 @@ static_assert(kEarlyBytes % 1024 == 0 && kLateBytes % 1024 == 0 && kSmemRc <= 23
 constexpr uint32_t kEarlyTx = 8192 + 16384 + 32768;     // T', V, W~ and Q
 constexpr uint32_t kLateTx = 24576;                     // Aqk^T and K->
 
-// recurrence tensor-memory columns (512)
-constexpr uint32_t TM_D1 = 0;     // V_new^T accumulator, 64      } the merged a2 product
-constexpr uint32_t TM_D2A = 64;   // -S Q^T accumulator, 64       } writes D1 | D2A
-constexpr uint32_t TM_D2B = 128;  // V_new^T Aqk^T accumulator, 64   } the merged c product
-constexpr uint32_t TM_S = 192;    // fp32 state, 128                 } writes D2B | S
-constexpr uint32_t TM_X = 320;    // V_new^T bf16 (A operand), 32
-constexpr uint32_t TM_SBF = 384;  // bf16 state (A operand), 64
+// recurrence tensor-memory columns (512).  The two output accumulators alternate by
+// chunk parity so the output warps may drain one while the next chunk runs:
+//   even chunk: a2 -> [D1_0 | D2A_0] (0..127),   c -> [D2B_0 | S] (128..319)
+//   odd  chunk: a2 -> [D1_1 | D2A_1] (384..511), c -> [S | D2B_1] (192..383)
+constexpr uint32_t TM_S = 192;
+__device__ __forceinline__ uint32_t tm_d1(int c) { return (c & 1) ? 384u : 0u; }
+__device__ __forceinline__ uint32_t tm_d2a(int c) { return (c & 1) ? 448u : 64u; }
+__device__ __forceinline__ uint32_t tm_d2b(int c) { return (c & 1) ? 320u : 128u; }
+__device__ __forceinline__ uint32_t tm_c(int c) { return (c & 1) ? 192u : 128u; }
 
-enum : int { RB_EF = 0, RB_EE = 3, RB_LF = 6, RB_LE = 8, RB_SCF = 10, RB_SCE = 14,   // rings
-             RB_D1 = 18, RB_X = 19, RB_S = 20, RB_SP = 21, RB_D2 = 22, RB_OFREE = 23, RB_FIN = 24,
-             RB_COUNT = 25 };
+enum : int { RB_EF = 0, RB_EE = 2, RB_LF = 4, RB_LE = 6, RB_SCF = 8, RB_SCE = 12,   // rings
+             RB_D1 = 16, RB_X = 17, RB_S = 18, RB_SP = 19, RB_D2 = 20,
+             RB_D2O = 21, RB_OFREE = 23,                                         // [2] by parity
+             RB_FIN = 25, RB_COUNT = 26 };
 enum : int { UB_QK = 0, UB_P1 = 1, UB_TRDY = 2, UB_P2 = 3, UB_FIN = 4 };
 
 // Development-only phase timestamps (SM clock) of the first CTA; compiled out
@@ -642,7 +648,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
 
     if (warp == 0) {
         // ------------------------------------------------------------ loads
-        // lane 0: early ring (T', V, W~ | Q); lane 1: factor ring; lane 2: late ring (Aqk^T | K->)
+        // lane 0: early ring (T', V, W~ | Q); lane 1: factor ring; lane 2: late ring (Aqk^T, K->)
         if (lane < 3 && nch > 0) {
             if (lane == 0) { prefetch_tmap(&tmq); prefetch_tmap(&tmv); }
             const int slots = lane == 0 ? kEarly : (lane == 1 ? kScSlots : kLate);
@@ -669,8 +675,14 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     mbar_expect_tx(fb, kScBytes);
                     bulk_load(sb + R_SCR + s * 1024, blk + PB_SC, kScBytes, fb);
                 } else {
+                    const uint32_t base = sb + late(c);
                     mbar_expect_tx(fb, kLateTx);
-                    bulk_load(sb + late(c), blk + PB_AQT, kLateTx, fb);
+                    if ((c & 1) == 0) {
+                        bulk_load(base, blk + PB_AQT, kLateTx, fb);          // [Aqk^T | K->]
+                    } else {
+                        bulk_load(base, blk + PB_KT, 16384, fb);             // [K-> | Aqk^T]
+                        bulk_load(base + 16384, blk + PB_AQT, 8192, fb);
+                    }
                 }
                 last = c;
             }
@@ -682,10 +694,10 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
         // Per chunk three products (16 instructions):
-        //   a1 : D1        = V^T T'^T                      (N = 64,  K = 64)
-        //   a2 : [D1|D2A] -= S [W~ ; Q]^T                  (N = 128, K = 128)  V_new^T and -S Q^T
-        //   c  : [D2B|S]  += V_new^T [Aqk^T | K->]          (N = 192, K = 64)   outputs and state
-        // D2A and D2B are re-zeroed by the output warps once they have read them.
+        //   a1 : D1       = V^T T'^T                       (N = 64,  K = 64)
+        //   a2 : D1|D2A  -= S [W~ ; Q]^T                   (N = 128, K = 128)  V_new^T and -S Q^T
+        //   c  : D2B|S   += V_new^T [Aqk^T | K->]           (N = 192, K = 64)   outputs and state
+        // D2A and D2B (one pair per chunk parity) are re-zeroed by the output warps.
         if (lane == 0 && nch > 0) {
             const uint32_t id_a1 = idesc_bf16(128, 64, true, false);
             const uint32_t id_a2 = idesc_bf16(128, 128, false, false, true);   // negated B
@@ -696,19 +708,19 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_ss(tb + TM_D1, smem_desc(eb + E_V + ks * 2048, 8192, 1024),
+                    mma_ss(tb + tm_d1(c), smem_desc(eb + E_V + ks * 2048, 8192, 1024),
                            smem_desc(eb + E_TP + ks * 32, 16, 1024), id_a1, ks > 0);
                 return true;
             };
             auto issue_a2 = [&](int c) -> bool {
                 const uint32_t eb = sb + early(c);
+                if (!wait_spin(bar(RB_OFREE + (c & 1)), (c >> 1) & 1, abort_flag, p.err)) return false;
                 if (!wait_spin(bar(RB_S), c & 1, abort_flag, p.err)) return false;
-                if (!wait_spin(bar(RB_OFREE), c & 1, abort_flag, p.err)) return false;   // D2A, D2B zero
                 GDN_TR(p.trace, 1, c, 0);
                 fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_ts(tb + TM_D1, tb + TM_SBF + ks * 8,
+                    mma_ss(tb + tm_d1(c), smem_desc(sb + R_SBF + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                            smem_desc(eb + E_WQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id_a2, 1);
                 commit(bar(RB_D1));
                 commit(bar(RB_EE + c % kEarly));
@@ -727,8 +739,10 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_ts(tb + TM_D2B, tb + TM_X + ks * 8, smem_desc(lb + ks * 2048, 8192, 1024), id_c, 1);
+                    mma_ss(tb + tm_c(c), smem_desc(sb + R_X + ks * 32, 16, 1024), smem_desc(lb + ks * 2048, 8192, 1024),
+                           id_c, 1);
                 commit(bar(RB_D2));
+                commit(bar(RB_D2O + (c & 1)));
                 if (c + 1 < nch && !(ok = issue_a1(c + 1) && issue_a2(c + 1))) break;
             }
             commit(bar(RB_FIN));   // every MMA must complete before tensor memory is released
@@ -739,8 +753,8 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
         // ------------------------------------------------------------ state epilogue (warps 2-9)
         // Each tensor-memory lane (row j of S) is served by two threads: half 0 owns
         // the first half of every row's columns, half 1 the second.  Per chunk:
-        //   X : V_new^T -> bf16 (gates the merged c product)
-        //   S : S -> bf16 (gates the next a2), then S <- e^{b_C} S (gates the next c)
+        //   X : V_new^T -> bf16 shared tile (A of the merged c product)
+        //   S : S -> bf16 shared tile (A of the next a2), then S <- e^{b_C} S (gates the next c)
         const int j = 32 * (warp & 3) + lane;
         const int hf = warp >= 6 ? 1 : 0;
         const bool leader = (warp == 2 && lane == 0);
@@ -750,6 +764,19 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             bool ok = true;
             if (leader) ok = wait_spin(bar(b), parity, abort_flag, p.err);
             return !gsync(!ok);
+        };
+        // 64 fp32 state entries (this thread's half of row j) -> the bf16 A tile of a2
+        auto put_sbf = [&](const uint32_t (&sv)[64]) {
+            uint8_t *row = sm + R_SBF + hf * 16384;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                uint4 w;
+                w.x = pack_bf16(__uint_as_float(sv[ch * 8 + 0]), __uint_as_float(sv[ch * 8 + 1]));
+                w.y = pack_bf16(__uint_as_float(sv[ch * 8 + 2]), __uint_as_float(sv[ch * 8 + 3]));
+                w.z = pack_bf16(__uint_as_float(sv[ch * 8 + 4]), __uint_as_float(sv[ch * 8 + 5]));
+                w.w = pack_bf16(__uint_as_float(sv[ch * 8 + 6]), __uint_as_float(sv[ch * 8 + 7]));
+                *reinterpret_cast<uint4 *>(row + sw128_offset(j, ch * 8)) = w;
+            }
         };
         if (nch == 0) {
             if (p.final_state)
@@ -762,29 +789,23 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             bool ok = wait_spin(bar(RB_SCF), 0, abort_flag, p.err);
             {   // initial state: this thread's 64 entries of row j
                 const float e0 = reinterpret_cast<const float *>(sm + R_SCR)[128];
+                uint32_t sv[64];
 #pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) {
-                    const int d0 = hf * 64 + q2 * 32;
-                    float v[32];
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        float4 v4 = p.init_state ? *reinterpret_cast<const float4 *>(p.init_state + srow + d0 + e)
-                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-                        v[e] = v4.x; v[e + 1] = v4.y; v[e + 2] = v4.z; v[e + 3] = v4.w;
-                    }
-                    uint32_t pk[16], s0[16], s1[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        pk[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
-                        s0[e] = __float_as_uint(e0 * v[e]);
-                        s1[e] = __float_as_uint(e0 * v[16 + e]);
-                    }
-                    tmem_st16(lane_base + TM_SBF + d0 / 2, pk);
-                    tmem_st16(lane_base + TM_S + d0, s0);
-                    tmem_st16(lane_base + TM_S + d0 + 16, s1);
+                for (int e = 0; e < 64; e += 4) {
+                    float4 v4 = p.init_state ? *reinterpret_cast<const float4 *>(p.init_state + srow + hf * 64 + e)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                    sv[e] = __float_as_uint(v4.x); sv[e + 1] = __float_as_uint(v4.y);
+                    sv[e + 2] = __float_as_uint(v4.z); sv[e + 3] = __float_as_uint(v4.w);
                 }
+                put_sbf(sv);
+#pragma unroll
+                for (int e = 0; e < 64; ++e) sv[e] = __float_as_uint(e0 * __uint_as_float(sv[e]));
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    tmem_st16(lane_base + TM_S + hf * 64 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(sv + q * 16));
                 tmem_wait_st();
             }
+            fence_proxy_async();
             fence_before_sync();
             if (gsync(!ok || *abort_flag)) break;
             if (leader) { mbar_arrive(bar(RB_S)); mbar_arrive(bar(RB_SP)); }
@@ -794,15 +815,21 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 if (leader) GDN_TR(p.trace, 2, c, 0);
                 fence_after_sync();
                 {
-                    uint32_t a[32], pk[16];
-                    tmem_ld16(lane_base + TM_D1 + hf * 32, *reinterpret_cast<uint32_t(*)[16]>(a));
-                    tmem_ld16(lane_base + TM_D1 + hf * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(a + 16));
+                    uint32_t a[32];
+                    tmem_ld16(lane_base + tm_d1(c) + hf * 32, *reinterpret_cast<uint32_t(*)[16]>(a));
+                    tmem_ld16(lane_base + tm_d1(c) + hf * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(a + 16));
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
-                    tmem_st16(lane_base + TM_X + hf * 16, pk);
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint4 w;
+                        w.x = pack_bf16(__uint_as_float(a[ch * 8 + 0]), __uint_as_float(a[ch * 8 + 1]));
+                        w.y = pack_bf16(__uint_as_float(a[ch * 8 + 2]), __uint_as_float(a[ch * 8 + 3]));
+                        w.z = pack_bf16(__uint_as_float(a[ch * 8 + 4]), __uint_as_float(a[ch * 8 + 5]));
+                        w.w = pack_bf16(__uint_as_float(a[ch * 8 + 6]), __uint_as_float(a[ch * 8 + 7]));
+                        *reinterpret_cast<uint4 *>(sm + R_X + sw128_offset(j, hf * 32 + ch * 8)) = w;
+                    }
                 }
-                tmem_wait_st();
+                fence_proxy_async();
                 fence_before_sync();
                 if (gsync(*abort_flag)) break;
                 if (leader) mbar_arrive(bar(RB_X));
@@ -820,16 +847,8 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     for (int q = 0; q < 4; ++q)
                         tmem_ld16(lane_base + TM_S + hf * 64 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(sv + q * 16));
                     tmem_wait_ld();
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            pk[e] = pack_bf16(__uint_as_float(sv[q * 32 + 2 * e]), __uint_as_float(sv[q * 32 + 2 * e + 1]));
-                        tmem_st16(lane_base + TM_SBF + hf * 32 + q * 16, pk);
-                    }
-                    tmem_wait_st();
-                    fence_before_sync();
+                    put_sbf(sv);
+                    fence_proxy_async();
                     if (gsync(*abort_flag)) break;
                     if (leader) mbar_arrive(bar(RB_S));   // the bf16 state is ready: the next a2 may start
                     if (leader) GDN_TR(p.trace, 2, c, 2);
@@ -860,53 +879,60 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
         } while (false);
     } else {
         // ------------------------------------------------------------ output epilogue (warps 10-13)
-        // O = fq . (Q S^T) + Aqk V_new = D2B - fq . D2A; the accumulators are re-zeroed
-        // for the next chunk, then O goes through a [64 r][128 j] bf16 staging tile (in
-        // the chunk's late stage, whose operands the finished c product no longer needs)
-        // to coalesced 16-B stores.
+        // O = fq . (Q S^T) + Aqk V_new = D2B - fq . D2A; the chunk-parity accumulators are
+        // re-zeroed for the chunk after next, then O goes through a [64 r][128 j] bf16 staging
+        // tile (in the chunk's late stage, whose operands the finished c product no longer
+        // needs) to coalesced 16-B stores.
         const int j = 32 * (warp & 3) + lane;   // output column j0 + j
         const bool leader = (warp == 10 && lane == 0);
         auto osync = [&](bool bad) -> bool { return group_sync_or(2, 128, bad); };
-        auto zero_d2 = [&]() {
+        auto zero_d2 = [&](int c) {
             uint32_t z[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) z[e] = 0u;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) tmem_st16(lane_base + TM_D2A + q * 16, z);   // D2A and D2B
+            for (int q = 0; q < 4; ++q) {
+                tmem_st16(lane_base + tm_d2a(c) + q * 16, z);
+                tmem_st16(lane_base + tm_d2b(c) + q * 16, z);
+            }
             tmem_wait_st();
         };
-        zero_d2();   // phase 0 of RB_OFREE: the accumulators start at zero
+        zero_d2(0);
+        zero_d2(1);
         fence_before_sync();
-        if (!osync(*abort_flag) && leader && nch > 0) mbar_arrive(bar(RB_OFREE));
+        if (!osync(*abort_flag) && leader && nch > 0) {   // phase 0 of each parity: zero accumulators
+            mbar_arrive(bar(RB_OFREE));
+            mbar_arrive(bar(RB_OFREE + 1));
+        }
         for (int c = 0; c < nch; ++c) {
             const float *fq = reinterpret_cast<const float *>(sm + R_SCR + (c % kScSlots) * 1024);
             bool ok = true;
             if (leader) {
                 ok = wait_spin(bar(RB_SCF + c % kScSlots), (c / kScSlots) & 1, abort_flag, p.err);
-                ok = ok && wait_spin(bar(RB_D2), c & 1, abort_flag, p.err);
+                ok = ok && wait_spin(bar(RB_D2O + (c & 1)), (c >> 1) & 1, abort_flag, p.err);
             }
             if (osync(!ok)) break;
             if (leader) GDN_TR(p.trace, 0, c, 0);
             fence_after_sync();
-            uint32_t a[64], b[64];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                tmem_ld16(lane_base + TM_D2A + q * 16, *reinterpret_cast<uint32_t(*)[16]>(a + q * 16));
-                tmem_ld16(lane_base + TM_D2B + q * 16, *reinterpret_cast<uint32_t(*)[16]>(b + q * 16));
-            }
-            tmem_wait_ld();
-            zero_d2();
-            fence_before_sync();
-            if (osync(*abort_flag)) break;
-            if (leader && c + 1 < nch) mbar_arrive(bar(RB_OFREE));   // D2A, D2B read and re-zeroed
-            if (leader) GDN_TR(p.trace, 0, c, 1);
             uint8_t *stg = sm + late(c);
 #pragma unroll
-            for (int r = 0; r < 64; ++r)
-                *reinterpret_cast<__nv_bfloat16 *>(stg + (r * 128 + j) * 2) =
-                    __float2bfloat16_rn(__uint_as_float(b[r]) - fq[r] * __uint_as_float(a[r]));
+            for (int q = 0; q < 4; ++q) {
+                uint32_t a[16], b[16];
+                tmem_ld16(lane_base + tm_d2a(c) + q * 16, a);
+                tmem_ld16(lane_base + tm_d2b(c) + q * 16, b);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int r = q * 16 + e;
+                    *reinterpret_cast<__nv_bfloat16 *>(stg + (r * 128 + j) * 2) =
+                        __float2bfloat16_rn(__uint_as_float(b[e]) - fq[r] * __uint_as_float(a[e]));
+                }
+            }
+            zero_d2(c);
+            fence_before_sync();
             if (osync(*abort_flag)) break;
-            if (leader) GDN_TR(p.trace, 0, c, 2);
+            if (leader && c + 2 < nch) mbar_arrive(bar(RB_OFREE + (c & 1)));   // drained and re-zeroed
+            if (leader) GDN_TR(p.trace, 0, c, 1);
             const int rows = min(kChunk, len - c * kChunk);
             __nv_bfloat16 *obase = p.out + (size_t)(tok0 + (int64_t)c * kChunk) * H * dv + (size_t)h * dv + j0;
 #pragma unroll
@@ -921,7 +947,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 mbar_arrive(bar(RB_LE + c % kLate));       // the late stage may be refilled
                 mbar_arrive(bar(RB_SCE + c % kScSlots));   // and the factor slot
             }
-            if (leader) GDN_TR(p.trace, 2, c, 3);
+            if (leader) GDN_TR(p.trace, 0, c, 2);
         }
     }
 
