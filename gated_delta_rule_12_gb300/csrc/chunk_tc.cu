@@ -114,6 +114,11 @@ enum : int { UB_QK = 0, UB_P1 = 1, UB_TRDY = 2, UB_P2 = 3, UB_FIN = 4 };
 // of the library unless GDN_KERNEL_TRACE is defined.
 #ifdef GDN_KERNEL_TRACE
 long long *g_trace_buffer = nullptr;
+// UT kernel: phase stamps of CTA (slot 0, head 0) in row 15 of role 3
+#define GDN_UTR(trace, ev)                                                                          \
+    do {                                                                                             \
+        if ((trace) && blockIdx.x == 0 && blockIdx.y == 0) (trace)[(3 * 16 + 15) * 16 + (ev)] = clock64(); \
+    } while (0)
 #define GDN_TR(trace, role, c, ev)                                                                   \
     do {                                                                                             \
         if ((trace) && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (c) < 16)            \
@@ -121,6 +126,7 @@ long long *g_trace_buffer = nullptr;
     } while (0)
 #else
 #define GDN_TR(trace, role, c, ev) do { } while (0)
+#define GDN_UTR(trace, ev) do { } while (0)
 #endif
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned *err)
@@ -418,6 +424,7 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         float *bsum = sc, *bet = sc + 64, *rk = sc + 128, *rq = sc + 192, *cw = sc + 256, *ecol = sc + 320;
         const uint32_t lane_base = tb + ((uint32_t)(32 * (warp & 3)) << 16);
         uint8_t *st = sm + U_QK;
+        if (prow == 0) GDN_UTR(p.trace, 0);
         do {
             // (1) gates: chunk-local cumulative log-gate in base 2, beta
             {
@@ -439,7 +446,9 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 if (prow < 64) bsum[prow] = x + ((prow >= 32) ? Mt[0] : 0.f);
             }
             // (2) inverse norms from the landed tiles
+            if (prow == 0) GDN_UTR(p.trace, 1);
             bool ok = wait_bar(bar(UB_QK), 0, abort_flag, p.err);
+            if (prow == 0) GDN_UTR(p.trace, 2);
             {
                 const int r = prow & 63;
                 const bool isq = prow >= 64;
@@ -461,7 +470,9 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
             group_sync(1, 128);
 
             // (3) masks: L (rows 0-63, into A), Aqk (rows 64-127, to the workspace)
+            if (prow == 0) GDN_UTR(p.trace, 3);
             ok = wait_bar(bar(UB_P1), 0, abort_flag, p.err);
+            if (prow == 0) GDN_UTR(p.trace, 4);
             fence_after_sync();
             {
                 const int r = prow & 63, R = r >> 4;
@@ -510,9 +521,11 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 reinterpret_cast<uint4 *>(blk + PB_AQT)[idx] = reinterpret_cast<const uint4 *>(sm + U_TPP)[idx];
             }
             group_sync(1, 128);   // the staging area becomes the solve's scratch
+            if (prow == 0) GDN_UTR(p.trace, 5);
 
             // (4) T = (I + L)^{-1} in place;  T' -> workspace,  T'' -> shared memory
             solve_in_place(Am, Mt, prow, warp - 1, lane);
+            if (prow == 0) GDN_UTR(p.trace, 6);
             {
                 const int r = prow >> 1, i0 = (prow & 1) * 32;
 #pragma unroll
@@ -536,6 +549,7 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
             fence_proxy_async();
             if (group_sync_or(2, 128, !ok || *abort_flag)) break;
             if (prow == 0) mbar_arrive(bar(UB_TRDY));
+            if (prow == 0) GDN_UTR(p.trace, 7);
 
             // (5) W~^T and the per-row factors to the workspace
             {
@@ -569,7 +583,9 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                     }
                 }
             }
+            if (prow == 0) GDN_UTR(p.trace, 8);
             ok = wait_bar(bar(UB_P2), 0, abort_flag, p.err);
+            if (prow == 0) GDN_UTR(p.trace, 9);
             fence_after_sync();
             if (prow < 64) {   // row r of W~ (128 d), K-major tiles of 64 d
 #pragma unroll
@@ -592,8 +608,10 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
             fence_before_sync();
         } while (false);
     }
+    if (tid == 32) GDN_UTR(p.trace, 10);
     fence_before_sync();
     __syncthreads();
+    if (tid == 32) GDN_UTR(p.trace, 11);
     if (warp == 0) {
         fence_after_sync();
         tmem_dealloc(tb, 128);
