@@ -62,11 +62,11 @@ constexpr uint32_t kWsHeader = 1024;   // device error word + padding
 // ---- ut_tc_kernel shared memory
 constexpr int kThreadsUt = 160;        // warp 0: TMA, MMA, TMEM; warps 1-4: 128 "prep" threads
 constexpr uint32_t U_QK = 0;           // [K kb0][Q kb0][K kb1][Q kb1], 8 KB each
-constexpr uint32_t U_TPP = 32768;      // Aqk^T staging, then solve scratch, then T'' (8 KB)
-constexpr uint32_t U_ZERO = 40960;     // 8 KB of zeros: rows 64-127 of the padded A = [T''; 0]
-constexpr uint32_t U_A = 49152;        // L, then T, in place: fp32 [64][LDL]
-constexpr uint32_t U_SC = U_A + 64 * LDL * 4;     // b, beta, rk, rq, cw, ecol [6][64] fp32
-constexpr uint32_t U_BAR = U_SC + 6 * 64 * 4;
+constexpr uint32_t U_TPP = 32768;      // solve scratch, then T'' (8 KB); rows 64-127 of the
+                                       // padded A = [T''; *] of the W~ product read U_A (don't care)
+constexpr uint32_t U_A = 40960;        // L, then T, in place: fp32 [64][LDL]
+constexpr uint32_t U_SC = U_A + 64 * LDL * 4;     // b, beta, rk, rq, cw, ecol, cq[3] [9][64] fp32
+constexpr uint32_t U_BAR = U_SC + 9 * 64 * 4;
 constexpr uint32_t U_MISC = U_BAR + 8 * 8;
 constexpr uint32_t kSmemUt = U_MISC + 64 + 1024;
 static_assert(U_A % 16 == 0 && U_SC % 16 == 0, "alignment");
@@ -374,15 +374,12 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         *abort_flag = 0;
         fence_mbar_init();
     }
-    for (int i = tid; i < 8192 / 16; i += kThreadsUt)
-        reinterpret_cast<uint4 *>(sm + U_ZERO)[i] = make_uint4(0u, 0u, 0u, 0u);
-    fence_proxy_async();
     if (warp == 0) tmem_alloc(tmem_sh, 128);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tb = *tmem_sh;
-    const uint32_t TP1 = 0, TP2 = 0;   // P2 reuses P1's columns once the masks are read
+    const uint32_t TP1 = 0, TP2 = 0;   // the W~ product reuses the Gram columns once they are read
 
     if (warp == 0) {
         if (lane == 0) {
@@ -393,9 +390,9 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
             tma_load_3d(sb + U_QK + 16384, &tmk, 64, h, z, bar(UB_QK));
             tma_load_3d(sb + U_QK + 24576, &tmq, 64, h, z, bar(UB_QK));
             if (wait_bar(bar(UB_QK), 0, abort_flag, p.err)) {
-                const uint32_t id_p1 = idesc_bf16(128, 64, false, false);
+                const uint32_t id_p1 = idesc_bf16(128, 128, false, false);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {   // G = [K; Q] K^T
+                for (int ks = 0; ks < 8; ++ks) {   // G = [K; Q] [K; Q]^T  (rows 0-63: K K^T | K Q^T)
                     const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
                     mma_ss(tb + TP1, smem_desc(sb + U_QK + off, 16, 1024), smem_desc(sb + U_QK + off, 16, 1024),
                            id_p1, ks > 0);
@@ -422,6 +419,7 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         float *Mt = reinterpret_cast<float *>(sm + U_TPP);
         float *sc = reinterpret_cast<float *>(sm + U_SC);
         float *bsum = sc, *bet = sc + 64, *rk = sc + 128, *rq = sc + 192, *cw = sc + 256, *ecol = sc + 320;
+        float *cq = sc + 384;   // [3][64]: e^{b_m - b_p} rq_m for the block ends p = 15, 31, 47
         const uint32_t lane_base = tb + ((uint32_t)(32 * (warp & 3)) << 16);
         uint8_t *st = sm + U_QK;
         if (prow == 0) GDN_UTR(p.trace, 0);
@@ -466,61 +464,113 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 const int i = prow;
                 cw[i] = exp2f(bsum[i | 15] - bsum[i]) * rk[i];
                 ecol[i] = exp2f(bsum[i]) * rk[i];
+#pragma unroll
+                for (int I = 0; I < 3; ++I) cq[I * 64 + i] = (i > I * 16 + 15) ? exp2f(bsum[i] - bsum[I * 16 + 15]) * rq[i] : 0.f;
             }
             group_sync(1, 128);
 
-            // (3) masks: L (rows 0-63, into A), Aqk (rows 64-127, to the workspace)
+            // (3) masks from the Gram rows of K: lane i holds k_i . k_m and k_i . q_m.
+            //     L_im  = beta_i e^{b_i - b_m} rk_i rk_m (k_i . k_m),    m <  i   (into A)
+            //     AqkT_im = e^{b_m - b_i} rq_m rk_i (k_i . q_m),          m >= i   (to the workspace)
+            //   Rows 64-127 (Q rows) are not needed; their threads write K-> meanwhile.
             if (prow == 0) GDN_UTR(p.trace, 3);
             ok = wait_bar(bar(UB_P1), 0, abort_flag, p.err);
             if (prow == 0) GDN_UTR(p.trace, 4);
             fence_after_sync();
-            {
-                const int r = prow & 63, R = r >> 4;
-                const bool isq = prow >= 64;
-                const float br = bsum[r];
-                const float f = isq ? rq[r] : bet[r] * rk[r];
-                const int lim = isq ? r + 1 : r;   // columns i < lim
+            if (prow < 64) {
+                const int i = prow, I = i >> 4;
+                uint32_t u[64];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t u[16];
-                    tmem_ld16(lane_base + q * 16, u);
-                    tmem_wait_ld();
-                    float v[16];
-                    if (q < R) {
-                        const float fu = f * exp2f(br - bsum[q * 16 + 15]);
+                for (int q = 0; q < 4; ++q) tmem_ld16(lane_base + TP1 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(u + q * 16));
+                tmem_wait_ld();
+                const float bi = bsum[i];
+                // L row i: columns m < i
+                {
+                    const float f = bet[i] * rk[i];
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) v[e] = fu * cw[q * 16 + e] * __uint_as_float(u[e]);
-                    } else if (q == R) {
+                    for (int q = 0; q < 4; ++q) {
+                        float v[16];
+                        if (q < I) {
+                            const float fu = f * exp2f(bi - bsum[q * 16 + 15]);
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int i = q * 16 + e;
-                            v[e] = (i < lim) ? f * exp2f(br - bsum[i]) * rk[i] * __uint_as_float(u[e]) : 0.f;
+                            for (int e = 0; e < 16; ++e) v[e] = fu * cw[q * 16 + e] * __uint_as_float(u[q * 16 + e]);
+                        } else if (q == I) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const int m = q * 16 + e;
+                                v[e] = (m < i) ? f * exp2f(bi - bsum[m]) * rk[m] * __uint_as_float(u[m]) : 0.f;
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) v[e] = 0.f;
                         }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) v[e] = 0.f;
-                    }
-                    if (!isq) {
-                        float4 *dst = reinterpret_cast<float4 *>(Am + r * LDL + q * 16);
+                        float4 *dst = reinterpret_cast<float4 *>(Am + i * LDL + q * 16);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-                    } else {
-                        // row r of Q K^T o Gamma is column r of the transposed tile
+                    }
+                }
+                // Aqk^T row i: columns m >= i, e^{b_m - b_i} = e^{b_m - b_p} e^{b_p - b_i} with p the
+                // end of i's 16-block for m beyond it (both factors <= 1), direct inside the block
+                {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            *reinterpret_cast<__nv_bfloat16 *>(sm + U_TPP + sw128_offset(q * 16 + e, r)) =
-                                __float2bfloat16_rn(v[e]);
+                    for (int q = 0; q < 4; ++q)
+                        tmem_ld16(lane_base + TP1 + 64 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(u + q * 16));
+                    tmem_wait_ld();
+                    const float fi = rk[i];
+                    const float wi = exp2f(bsum[i | 15] - bi);   // e^{b_p - b_i}
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float v[16];
+                        if (q > I) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const int m = q * 16 + e;
+                                v[e] = fi * wi * cq[I * 64 + m] * __uint_as_float(u[m]);
+                            }
+                        } else if (q == I) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const int m = q * 16 + e;
+                                v[e] = (m >= i) ? fi * exp2f(bsum[m] - bi) * rq[m] * __uint_as_float(u[m]) : 0.f;
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) v[e] = 0.f;
+                        }
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) w[e] = pack_bf16(v[hh * 8 + 2 * e], v[hh * 8 + 2 * e + 1]);
+                            *reinterpret_cast<uint4 *>(blk + PB_AQT + sw128_offset(i, q * 16 + hh * 8)) =
+                                make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
+            } else {   // K-> = diag(fk) K, written in the K tile's own layout
+                const int r = prow - 64;
+                const float fk = (r < rows) ? exp2f(bsum[63] - bsum[r]) * rk[r] : 0.f;
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+                    const uint8_t *src = st + kb * 16384 + r * 128;
+                    uint8_t *dst = blk + PB_KT + kb * 8192 + r * 128;
+#pragma unroll
+                    for (int ch0 = 0; ch0 < 8; ++ch0) {
+                        const int ch = (ch0 ^ r) & 7;
+                        const uint4 uu = *reinterpret_cast<const uint4 *>(src + ch * 16);
+                        const uint32_t w[4] = {uu.x, uu.y, uu.z, uu.w};
+                        uint32_t o[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 x = unpack_bf16(w[e]);
+                            o[e] = pack_bf16(x.x * fk, x.y * fk);
+                        }
+                        *reinterpret_cast<uint4 *>(dst + ch * 16) = make_uint4(o[0], o[1], o[2], o[3]);
                     }
                 }
             }
             fence_before_sync();
             if (group_sync_or(2, 128, !ok || *abort_flag)) break;
-#pragma unroll
-            for (int it = 0; it < 4; ++it) {   // Aqk^T tile -> workspace
-                const int idx = it * 128 + prow;
-                reinterpret_cast<uint4 *>(blk + PB_AQT)[idx] = reinterpret_cast<const uint4 *>(sm + U_TPP)[idx];
-            }
-            group_sync(1, 128);   // the staging area becomes the solve's scratch
             if (prow == 0) GDN_UTR(p.trace, 5);
 
             // (4) T = (I + L)^{-1} in place;  T' -> workspace,  T'' -> shared memory
@@ -560,27 +610,6 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 } else {
                     reinterpret_cast<float *>(blk + PB_SC)[64 + r] = (r < rows) ? exp2f(bC - bsum[r]) * rk[r] : 0.f;
                     if (r == 0) reinterpret_cast<float *>(blk + PB_SC)[128] = exp2f(bC);
-                }
-            }
-            if (prow >= 64) {   // K-> = diag(fk) K, written in the K tile's own layout
-                const int r = prow - 64;
-                const float fk = (r < rows) ? exp2f(bsum[63] - bsum[r]) * rk[r] : 0.f;
-#pragma unroll
-                for (int kb = 0; kb < 2; ++kb) {
-                    const uint8_t *src = st + kb * 16384 + r * 128;
-                    uint8_t *dst = blk + PB_KT + kb * 8192 + r * 128;
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        const uint4 u = *reinterpret_cast<const uint4 *>(src + ch * 16);
-                        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-                        uint32_t o[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 x = unpack_bf16(w[e]);
-                            o[e] = pack_bf16(x.x * fk, x.y * fk);
-                        }
-                        *reinterpret_cast<uint4 *>(dst + ch * 16) = make_uint4(o[0], o[1], o[2], o[3]);
-                    }
                 }
             }
             if (prow == 0) GDN_UTR(p.trace, 8);
