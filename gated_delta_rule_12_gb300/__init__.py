@@ -11,6 +11,7 @@ Entry points (same names as the C ABI, without the ``gdn_`` prefix):
     chunk_fwd(q, k, v, g, beta, ...)      -> (out, final_state)
     decode_step(state, q, k, v, g, beta)  -> out            (state updated in place)
     chunk_fwd_workspace_size(...)         -> bytes
+    chunk_fwd_kernel_count(...)           -> kernels one chunk_fwd call launches
     check_device_error(workspace)         -> None or raises
 """
 from __future__ import annotations
@@ -30,8 +31,8 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "G
 GDN_F32, GDN_BF16 = 0, 1
 CHUNK = 64
 
-EXPORTS = ["gdn_status_string", "gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd", "gdn_decode_step",
-           "gdn_check_device_error", "gdn_chunk_fwd_noalloc"]
+EXPORTS = ["gdn_status_string", "gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd_kernel_count", "gdn_chunk_fwd",
+           "gdn_decode_step", "gdn_check_device_error", "gdn_chunk_fwd_noalloc"]
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -67,6 +68,8 @@ def load_library(path: str = LIB_PATH, build_if_missing: bool = False) -> ctypes
         lib.gdn_status_string.restype = ctypes.c_char_p
         lib.gdn_chunk_fwd_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_int]
         lib.gdn_chunk_fwd_workspace_size.restype = _sz
+        lib.gdn_chunk_fwd_kernel_count.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_int]
+        lib.gdn_chunk_fwd_kernel_count.restype = _i32
         lib.gdn_chunk_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
                                       _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _f32, _i32, _i32,
                                       _vp, _sz, _vp]
@@ -115,6 +118,12 @@ def _stream(stream):
 def chunk_fwd_workspace_size(B, T, H, dk, dv, num_seqs=0, dtype=torch.bfloat16) -> int:
     dt = GDN_BF16 if dtype == torch.bfloat16 else GDN_F32
     return int(load_library().gdn_chunk_fwd_workspace_size(B, T, H, dk, dv, num_seqs, dt))
+
+
+def chunk_fwd_kernel_count(B, T, H, dk, dv, num_seqs=0, dtype=torch.bfloat16) -> int:
+    """Kernels one ``chunk_fwd`` call of this size launches (0 if unsupported)."""
+    dt = GDN_BF16 if dtype == torch.bfloat16 else GDN_F32
+    return int(load_library().gdn_chunk_fwd_kernel_count(B, T, H, dk, dv, num_seqs, dt))
 
 
 def chunk_fwd(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale=None, use_qk_l2norm=True,

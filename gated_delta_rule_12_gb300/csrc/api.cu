@@ -51,6 +51,15 @@ size_t gdn_chunk_fwd_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk,
     return chunk_workspace_layout(slots, H, dk, dv).total;
 }
 
+int32_t gdn_chunk_fwd_kernel_count(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv,
+                                   int32_t num_seqs, gdn_dtype dt)
+{
+    if (gdn_chunk_fwd_workspace_size(B, T, H, dk, dv, num_seqs, dt) == 0) return 0;
+    const int64_t tokens = (int64_t)B * T;
+    if (chunk_tc_supported(dt == GDN_BF16 ? 1 : 0, dk, dv, tokens)) return 2;   // UT + recurrence
+    return tokens > 0 ? 3 : 1;   // prologue + UT + recurrence, or the state copy alone
+}
+
 gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
                          const float *beta, const float *init_state, const int32_t *cu_seqlens,
                          int32_t num_seqs, void *out, float *final_state, int32_t B, int32_t T,

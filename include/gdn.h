@@ -70,6 +70,16 @@ size_t gdn_chunk_fwd_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk,
                                     int32_t num_seqs, gdn_dtype dt);
 
 /*
+ * Number of kernels one gdn_chunk_fwd call of this problem size enqueues on
+ * its stream (same arguments as gdn_chunk_fwd_workspace_size): 2 on the
+ * tensor-core path (bf16, dk = 128, dv a multiple of 128), 3 on the CUDA-core
+ * path, 1 when there are no tokens.  Returns 0 for an invalid or unsupported
+ * size.  Host-only; touches no device.
+ */
+int32_t gdn_chunk_fwd_kernel_count(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv,
+                                   int32_t num_seqs, gdn_dtype dt);
+
+/*
  * Chunked forward pass (prefill / training forward) of the gated delta rule.
  * "Gated Delta Networks: Improving Mamba2 with Delta Rule", §3.3: per chunk
  * of C = chunk_size tokens the UT transform

@@ -64,6 +64,17 @@ def test_workspace_size_rules(lib):
     assert ws(1, 0, 2, 64, 64, 0, 0) >= 256
 
 
+def test_kernel_count_rules(lib):
+    kc = lib.gdn_chunk_fwd_kernel_count
+    assert kc(4, 2048, 16, 128, 128, 0, gdn.GDN_BF16) == 2      # tensor-core path: UT + recurrence
+    assert kc(8, 8192, 32, 128, 256, 0, gdn.GDN_BF16) == 2
+    assert kc(1, 256, 2, 64, 64, 0, gdn.GDN_F32) == 3           # CUDA-core path
+    assert kc(4, 2048, 16, 128, 128, 0, gdn.GDN_F32) == 3
+    assert kc(2, 0, 2, 64, 64, 0, gdn.GDN_F32) == 1             # no tokens: the state copy alone
+    assert kc(1, 64, 1, 96, 64, 0, gdn.GDN_F32) == 0            # unsupported
+    assert kc(4, 100, 2, 128, 128, 8, gdn.GDN_BF16) == 0
+
+
 def _call_chunk(lib, **over):
     fake = 1 << 20  # 256-aligned, never dereferenced: validation fails first
     args = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, s0=None, cu=None, nseq=0, out=fake, sf=None,
