@@ -114,10 +114,10 @@ enum : int { UB_QK = 0, UB_P1 = 1, UB_TRDY = 2, UB_P2 = 3, UB_FIN = 4 };
 // of the library unless GDN_KERNEL_TRACE is defined.
 #ifdef GDN_KERNEL_TRACE
 long long *g_trace_buffer = nullptr;
-// UT kernel: phase stamps of CTA (slot 0, head 0) in row 15 of role 3
+// UT kernel: up to 48 phase stamps of CTA (slot 0, head 0) in rows 13-15 of role 3
 #define GDN_UTR(trace, ev)                                                                          \
     do {                                                                                             \
-        if ((trace) && blockIdx.x == 0 && blockIdx.y == 0) (trace)[(3 * 16 + 15) * 16 + (ev)] = clock64(); \
+        if ((trace) && blockIdx.x == 0 && blockIdx.y == 0) (trace)[(3 * 16 + 13) * 16 + (ev)] = clock64(); \
     } while (0)
 #define GDN_TR(trace, role, c, ev)                                                                   \
     do {                                                                                             \
@@ -193,25 +193,6 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t u)
     return __bfloat1622float2(v);
 }
 
-// Sum of squares of the 64 bf16 of one 128-B row segment (row index r, used
-// only to visit the 16-B chunks in an order that spreads consecutive rows
-// over all shared-memory banks).
-__device__ __forceinline__ float row_sumsq(const uint8_t *row, int r)
-{
-    float ss = 0.f;
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(row + ((ch ^ r) & 7) * 16);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 f = unpack_bf16(w[e]);
-            ss += f.x * f.x + f.y * f.y;
-        }
-    }
-    return ss;
-}
-
 __device__ __forceinline__ uint32_t to_tf32(float x)
 {
     uint32_t r;
@@ -227,111 +208,140 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// One warp: D (16 x 16) = X (16 x K) * Y (K x 16) on the tensor cores (tf32),
-// X(r, k) = X0[r * xp + k], Y(k, c) = Y0[k * yp + c]; written as -D (negate)
-// or D to Z0[r * zp + c].
-template <int K>
-__device__ __forceinline__ void warp_gemm16(const float *X0, int xp, const float *Y0, int yp, float *Z0, int zp,
-                                            bool negate, int lane)
+// tf32 A fragments of one 16-row strip of X (m16n8k8 layout) for the k-steps
+// 8ks >= kbeg: X(r, k) = X0[r * xp + k].
+template <int KS>
+__device__ __forceinline__ void load_a_tf32(uint32_t (&fa)[KS][4], const float *X0, int xp, int kbeg, int g, int t)
 {
-    const int g = lane >> 2, t = lane & 3;
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-    for (int k0 = 0; k0 < K; k0 += 8) {
-        uint32_t a[4];
-        a[0] = to_tf32(X0[g * xp + k0 + t]);
-        a[1] = to_tf32(X0[(g + 8) * xp + k0 + t]);
-        a[2] = to_tf32(X0[g * xp + k0 + t + 4]);
-        a[3] = to_tf32(X0[(g + 8) * xp + k0 + t + 4]);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const uint32_t b0 = to_tf32(Y0[(k0 + t) * yp + nt * 8 + g]);
-            const uint32_t b1 = to_tf32(Y0[(k0 + t + 4) * yp + nt * 8 + g]);
-            mma_tf32(acc[nt], a, b0, b1);
-        }
-    }
-    const float sg = negate ? -1.f : 1.f;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        Z0[g * zp + nt * 8 + 2 * t] = sg * acc[nt][0];
-        Z0[g * zp + nt * 8 + 2 * t + 1] = sg * acc[nt][1];
-        Z0[(g + 8) * zp + nt * 8 + 2 * t] = sg * acc[nt][2];
-        Z0[(g + 8) * zp + nt * 8 + 2 * t + 1] = sg * acc[nt][3];
+    for (int ks = 0; ks < KS; ++ks) {
+        const int k0 = 8 * ks;
+        if (k0 < kbeg) continue;
+        fa[ks][0] = to_tf32(X0[g * xp + k0 + t]);
+        fa[ks][1] = to_tf32(X0[(g + 8) * xp + k0 + t]);
+        fa[ks][2] = to_tf32(X0[g * xp + k0 + t + 4]);
+        fa[ks][3] = to_tf32(X0[(g + 8) * xp + k0 + t + 4]);
     }
 }
 
-// In place: A (64 x 64, pitch LDL) holds the strictly lower L on entry (zeros
-// elsewhere) and T = (I + L)^{-1} on exit; 128 threads (4 warps), Mt >= 32 x 36
-// floats of scratch.  Diagonal 4x4 blocks by forward substitution, then the
-// block rule [A 0; C B]^{-1} = [A^-1 0; -B^-1 C A^-1  B^-1] for the 4->8 and
-// 8->16 merges (CUDA cores) and the 16->32 and 32->64 merges (tensor cores, tf32).
-__device__ __forceinline__ void solve_in_place(float *__restrict__ A, float *__restrict__ Mt, int tid, int warp,
-                                               int lane)
+// acc (16 x 8) += X Y over the k-steps 8ks >= kbeg, X given as fragments,
+// Y(k, n) = Y0[k * yp + n].
+template <int KS>
+__device__ __forceinline__ void mma_a_tf32(float (&acc)[4], const uint32_t (&fa)[KS][4], const float *Y0, int yp,
+                                           int kbeg, int g, int t)
 {
-    // level 0: 16 diagonal 4x4 blocks, one thread per column
-    float x[4] = {0.f, 0.f, 0.f, 0.f};
-    const int base0 = (tid >> 2) * 4, c0 = tid & 3;
-    if (tid < 64) {
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
+    for (int ks = 0; ks < KS; ++ks) {
+        const int k0 = 8 * ks;
+        if (k0 < kbeg) continue;
+        mma_tf32(acc, fa[ks], to_tf32(Y0[(k0 + t) * yp + g]), to_tf32(Y0[(k0 + t + 4) * yp + g]));
+    }
+}
+
+// Store a 16 x 8 accumulator tile, scaled by sg, to Z0[r * zp + n].
+__device__ __forceinline__ void store_16x8(const float (&acc)[4], float *Z0, int zp, float sg, int g, int t)
+{
+    *reinterpret_cast<float2 *>(Z0 + g * zp + 2 * t) = make_float2(sg * acc[0], sg * acc[1]);
+    *reinterpret_cast<float2 *>(Z0 + (g + 8) * zp + 2 * t) = make_float2(sg * acc[2], sg * acc[3]);
+}
+
+// In place: A (64 x 64, pitch LDL) holds the strictly lower L on entry (zeros
+// elsewhere) and T = (I + L)^{-1} on exit; 128 threads (4 warps, `warp` 0-3),
+// Mt >= 4 x 256 floats of scratch.  Block rule
+//   [A 0; C B]^{-1} = [A^-1 0; -B^-1 (C A^-1)  B^-1]
+// in three steps with one barrier after each:
+//   (i)   warp w inverts the unit-lower 16 x 16 diagonal block w by forward
+//         substitution, one column per lane, the column in registers;
+//   (ii)  the 16 -> 32 merges of blocks (0,1) and (2,3), warp w taking the
+//         8-column half (w & 1) of merge (w >> 1);
+//   (iii) the 32 -> 64 merge, warp w taking columns 8w..8w+7.
+// The off-diagonal blocks of L that (ii) and (iii) overwrite are read into
+// registers before the first barrier, and each warp's two products touch only
+// its own columns of C A^-1, so no other synchronisation is needed.
+__device__ __forceinline__ void solve_in_place(float *__restrict__ A, float *__restrict__ Mt, int warp, int lane,
+                                               long long *trace)
+{
+    (void)trace;
+    const bool stamp = warp == 3 && lane == 0;
+    const int g = lane >> 2, t = lane & 3;
+    const int m2 = warp >> 1, h2 = warp & 1, a2 = 32 * m2, b2 = a2 + 16, n2 = a2 + 8 * h2;   // step (ii)
+    const int n3 = 8 * warp;                                                               // step (iii)
+    uint32_t c2[2][4], c3[2][4][4];
+    // C of step (ii): L rows b2.., columns a2..; A^-1 is lower triangular, so
+    // k-steps below this warp's first column contribute nothing
+    load_a_tf32<2>(c2, A + b2 * LDL + a2, LDL, 8 * h2, g, t);
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) load_a_tf32<4>(c3[mt], A + (32 + 16 * mt) * LDL, LDL, n3, g, t);
+    {   // (i) diagonal block `warp`, column c of its inverse
+        const int o = 16 * warp, c = lane & 15;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.f : 0.f;
+#pragma unroll
+        for (int r = 1; r < 16; ++r) {
+            const float *row = A + (o + r) * LDL + o;
             float acc = 0.f;
 #pragma unroll
-            for (int i = 0; i < r; ++i) acc += A[(base0 + r) * LDL + base0 + i] * x[i];
-            x[r] = (r == c0) ? 1.f : ((r < c0) ? 0.f : -acc);
+            for (int i4 = 0; i4 < r; i4 += 4) {
+                const float4 l4 = *reinterpret_cast<const float4 *>(row + i4);
+                acc = fmaf(l4.x, x[i4], acc);
+                if (i4 + 1 < r) acc = fmaf(l4.y, x[i4 + 1], acc);
+                if (i4 + 2 < r) acc = fmaf(l4.z, x[i4 + 2], acc);
+                if (i4 + 3 < r) acc = fmaf(l4.w, x[i4 + 3], acc);
+            }
+            if (r > c) x[r] = -acc;
+        }
+        if (stamp) GDN_UTR(trace, 9);
+        group_sync(1, 128);   // every warp has read its L fragments and diagonal rows
+        if (stamp) GDN_UTR(trace, 10);
+        if (lane < 16) {
+#pragma unroll
+            for (int r = 0; r < 16; ++r) A[(o + r) * LDL + o + c] = x[r];
         }
     }
     group_sync(1, 128);
-    if (tid < 64) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) A[(base0 + r) * LDL + base0 + c0] = x[r];
+    if (stamp) GDN_UTR(trace, 11);
+    float *M = Mt + warp * 256;   // this warp's C A^-1 columns: up to 32 x 8, pitch 8
+    {   // (ii)
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_a_tf32<2>(acc, c2, A + a2 * LDL + n2, LDL, 8 * h2, g, t);
+        store_16x8(acc, M, 8, 1.f, g, t);
+        __syncwarp();
+        float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t tb[2][4];
+        load_a_tf32<2>(tb, A + b2 * LDL + b2, LDL, 0, g, t);
+        mma_a_tf32<2>(acc2, tb, M, 8, 0, g, t);
+        store_16x8(acc2, A + b2 * LDL + n2, LDL, -1.f, g, t);
     }
+    if (stamp) GDN_UTR(trace, 12);
     group_sync(1, 128);
-    // levels 1, 2: merges of size s = 4 and 8 on the CUDA cores
+    if (stamp) GDN_UTR(trace, 13);
+    {   // (iii)
 #pragma unroll
-    for (int s = 4; s <= 8; s *= 2) {
-        const int epp = s / 4;   // entries per thread: 32*s entries over 128 threads
-        float m[2];
-#pragma unroll
-        for (int k = 0; k < epp; ++k) {
-            const int idx = tid * epp + k, c = idx % s, r = (idx / s) % s, a0 = (idx / (s * s)) * 2 * s, b0 = a0 + s;
-            float acc = 0.f;
-            for (int i = c; i < s; ++i) acc += A[(b0 + r) * LDL + a0 + i] * A[(a0 + i) * LDL + a0 + c];
-            m[k] = acc;
+        for (int mt = 0; mt < 2; ++mt) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_a_tf32<4>(acc, c3[mt], A + n3, LDL, n3, g, t);
+            store_16x8(acc, M + 16 * mt * 8, 8, 1.f, g, t);
         }
-#pragma unroll
-        for (int k = 0; k < epp; ++k) Mt[tid * epp + k] = m[k];
-        group_sync(1, 128);
-#pragma unroll
-        for (int k = 0; k < epp; ++k) {
-            const int idx = tid * epp + k, c = idx % s, r = (idx / s) % s, mm = idx / (s * s);
-            const int a0 = mm * 2 * s, b0 = a0 + s;
-            float acc = 0.f;
-            for (int i = 0; i <= r; ++i) acc += A[(b0 + r) * LDL + b0 + i] * Mt[mm * s * s + i * s + c];
-            A[(b0 + r) * LDL + a0 + c] = -acc;
+        __syncwarp();
+        {   // rows 32-47: B^-1 is lower triangular, k < 16
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t tb[2][4];
+            load_a_tf32<2>(tb, A + 32 * LDL + 32, LDL, 0, g, t);
+            mma_a_tf32<2>(acc, tb, M, 8, 0, g, t);
+            store_16x8(acc, A + 32 * LDL + n3, LDL, -1.f, g, t);
         }
-        group_sync(1, 128);
+        {   // rows 48-63
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t tb[4][4];
+            load_a_tf32<4>(tb, A + 48 * LDL + 32, LDL, 0, g, t);
+            mma_a_tf32<4>(acc, tb, M, 8, 0, g, t);
+            store_16x8(acc, A + 48 * LDL + n3, LDL, -1.f, g, t);
+        }
     }
-    // level 3: the two 16 -> 32 merges; warp w: merge w >> 1, 8-column half... (16 x 16 per merge)
-    {
-        const int mm = warp >> 1;          // merge index (rows/cols 32*mm ...)
-        const int a0 = mm * 32, b0 = a0 + 16;
-        if ((warp & 1) == 0)   // M = L_ba T_aa   (16 x 16 x 16)
-            warp_gemm16<16>(A + b0 * LDL + a0, LDL, A + a0 * LDL + a0, LDL, Mt + mm * 16 * 20, 20, false, lane);
-        group_sync(1, 128);
-        if ((warp & 1) == 0)   // T_ba = -T_bb M
-            warp_gemm16<16>(A + b0 * LDL + b0, LDL, Mt + mm * 16 * 20, 20, A + b0 * LDL + a0, LDL, true, lane);
-        group_sync(1, 128);
-    }
-    // level 4: the 32 -> 64 merge; warp w computes the 16 x 16 quadrant (w & 1, w >> 1)
-    {
-        const int r0 = (warp & 1) * 16, q0 = (warp >> 1) * 16;
-        // M2 = L_BA T_AA  (32 x 32 x 32)
-        warp_gemm16<32>(A + (32 + r0) * LDL, LDL, A + q0, LDL, Mt + r0 * 36 + q0, 36, false, lane);
-        group_sync(1, 128);
-        // T_BA = -T_BB M2
-        warp_gemm16<32>(A + (32 + r0) * LDL + 32, LDL, Mt + q0, 36, A + (32 + r0) * LDL + q0, LDL, true, lane);
-        group_sync(1, 128);
-    }
+    if (stamp) GDN_UTR(trace, 14);
+    group_sync(1, 128);
+    if (stamp) GDN_UTR(trace, 15);
 }
 
 // ===========================================================================
@@ -442,47 +452,58 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 }
                 group_sync(1, 128);
                 if (prow < 64) bsum[prow] = x + ((prow >= 32) ? Mt[0] : 0.f);
+                group_sync(1, 128);
             }
-            // (2) inverse norms from the landed tiles
+            // (2) inverse norms from the diagonal of the Gram product: thread p reads
+            //     G_pp (= ||k_p||^2 or ||q_{p-64}||^2, fp32 sums of exact bf16 products)
+            //     from column p of its own tensor-memory lane
             if (prow == 0) GDN_UTR(p.trace, 1);
-            bool ok = wait_bar(bar(UB_QK), 0, abort_flag, p.err);
+            bool ok = wait_bar(bar(UB_P1), 0, abort_flag, p.err);
+            ok = ok && wait_bar(bar(UB_QK), 0, abort_flag, p.err);   // (already complete) the K tile for K->
             if (prow == 0) GDN_UTR(p.trace, 2);
+            fence_after_sync();
             {
                 const int r = prow & 63;
                 const bool isq = prow >= 64;
-                const uint8_t *row = st + (isq ? 8192 : 0) + r * 128;
-                const float ss = row_sumsq(row, r) + row_sumsq(row + 16384, r);
+                uint32_t d[32];
+                tmem_ld16(lane_base + TP1 + 32 * (warp & 3), *reinterpret_cast<uint32_t(*)[16]>(d));
+                tmem_ld16(lane_base + TP1 + 32 * (warp & 3) + 16, *reinterpret_cast<uint32_t(*)[16]>(d + 16));
+                tmem_wait_ld();
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) ss = (e == lane) ? __uint_as_float(d[e]) : ss;
                 float inv = p.l2 ? 1.f / sqrtf(ss + kL2Eps) : 1.f;
                 if (isq) inv *= p.scale;
-                (isq ? rq : rk)[r] = (r < rows) ? inv : 0.f;
+                inv = (r < rows) ? inv : 0.f;
+                // column factors of the masks: decay of column i to the end of its
+                // 16-block (off-diagonal blocks, where e^{b_r - b_i} = e^{b_r - b_p} e^{b_p - b_i}
+                // with both factors <= 1) and e^{b_i} rk_i (for T'');  for the query
+                // columns m, e^{b_m - b_p} rq_m for the block ends p = 15, 31, 47
+                if (!isq) {
+                    rk[r] = inv;
+                    cw[r] = exp2f(bsum[r | 15] - bsum[r]) * inv;
+                    ecol[r] = exp2f(bsum[r]) * inv;
+                } else {
+                    rq[r] = inv;
+#pragma unroll
+                    for (int I = 0; I < 3; ++I) cq[I * 64 + r] = (r > I * 16 + 15) ? exp2f(bsum[r] - bsum[I * 16 + 15]) * inv : 0.f;
+                }
             }
             if (group_sync_or(2, 128, !ok || *abort_flag)) break;
-            // column factors: decay of column i to the end of its 16-block (for the
-            // off-diagonal blocks, where e^{b_r - b_i} = e^{b_r - b_p} e^{b_p - b_i}
-            // with both factors <= 1), and e^{b_i} rk_i (for T'')
-            if (prow < 64) {
-                const int i = prow;
-                cw[i] = exp2f(bsum[i | 15] - bsum[i]) * rk[i];
-                ecol[i] = exp2f(bsum[i]) * rk[i];
-#pragma unroll
-                for (int I = 0; I < 3; ++I) cq[I * 64 + i] = (i > I * 16 + 15) ? exp2f(bsum[i] - bsum[I * 16 + 15]) * rq[i] : 0.f;
-            }
-            group_sync(1, 128);
 
             // (3) masks from the Gram rows of K: lane i holds k_i . k_m and k_i . q_m.
             //     L_im  = beta_i e^{b_i - b_m} rk_i rk_m (k_i . k_m),    m <  i   (into A)
             //     AqkT_im = e^{b_m - b_i} rq_m rk_i (k_i . q_m),          m >= i   (to the workspace)
             //   Rows 64-127 (Q rows) are not needed; their threads write K-> meanwhile.
             if (prow == 0) GDN_UTR(p.trace, 3);
-            ok = wait_bar(bar(UB_P1), 0, abort_flag, p.err);
             if (prow == 0) GDN_UTR(p.trace, 4);
-            fence_after_sync();
             if (prow < 64) {
                 const int i = prow, I = i >> 4;
                 uint32_t u[64];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) tmem_ld16(lane_base + TP1 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(u + q * 16));
                 tmem_wait_ld();
+                if (prow == 0) GDN_UTR(p.trace, 5);
                 const float bi = bsum[i];
                 // L row i: columns m < i
                 {
@@ -509,6 +530,7 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                         for (int e = 0; e < 4; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
                     }
                 }
+                if (prow == 0) GDN_UTR(p.trace, 6);
                 // Aqk^T row i: columns m >= i, e^{b_m - b_i} = e^{b_m - b_p} e^{b_p - b_i} with p the
                 // end of i's 16-block for m beyond it (both factors <= 1), direct inside the block
                 {
@@ -516,6 +538,7 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                     for (int q = 0; q < 4; ++q)
                         tmem_ld16(lane_base + TP1 + 64 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(u + q * 16));
                     tmem_wait_ld();
+                    if (prow == 0) GDN_UTR(p.trace, 7);
                     const float fi = rk[i];
                     const float wi = exp2f(bsum[i | 15] - bi);   // e^{b_p - b_i}
 #pragma unroll
@@ -547,6 +570,7 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                         }
                     }
                 }
+                if (prow == 0) GDN_UTR(p.trace, 22);
             } else {   // K-> = diag(fk) K, written in the K tile's own layout
                 const int r = prow - 64;
                 const float fk = (r < rows) ? exp2f(bsum[63] - bsum[r]) * rk[r] : 0.f;
@@ -568,14 +592,15 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                         *reinterpret_cast<uint4 *>(dst + ch * 16) = make_uint4(o[0], o[1], o[2], o[3]);
                     }
                 }
+                if (prow == 64) GDN_UTR(p.trace, 23);
             }
             fence_before_sync();
             if (group_sync_or(2, 128, !ok || *abort_flag)) break;
-            if (prow == 0) GDN_UTR(p.trace, 5);
+            if (prow == 0) GDN_UTR(p.trace, 8);
 
             // (4) T = (I + L)^{-1} in place;  T' -> workspace,  T'' -> shared memory
-            solve_in_place(Am, Mt, prow, warp - 1, lane);
-            if (prow == 0) GDN_UTR(p.trace, 6);
+            solve_in_place(Am, Mt, (warp + 3) & 3, lane, p.trace);
+            if (prow == 0) GDN_UTR(p.trace, 16);
             {
                 const int r = prow >> 1, i0 = (prow & 1) * 32;
 #pragma unroll
@@ -599,7 +624,7 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
             fence_proxy_async();
             if (group_sync_or(2, 128, !ok || *abort_flag)) break;
             if (prow == 0) mbar_arrive(bar(UB_TRDY));
-            if (prow == 0) GDN_UTR(p.trace, 7);
+            if (prow == 0) GDN_UTR(p.trace, 17);
 
             // (5) W~^T and the per-row factors to the workspace
             {
@@ -612,9 +637,9 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                     if (r == 0) reinterpret_cast<float *>(blk + PB_SC)[128] = exp2f(bC);
                 }
             }
-            if (prow == 0) GDN_UTR(p.trace, 8);
+            if (prow == 0) GDN_UTR(p.trace, 18);
             ok = wait_bar(bar(UB_P2), 0, abort_flag, p.err);
-            if (prow == 0) GDN_UTR(p.trace, 9);
+            if (prow == 0) GDN_UTR(p.trace, 19);
             fence_after_sync();
             if (prow < 64) {   // row r of W~ (128 d), K-major tiles of 64 d
 #pragma unroll
@@ -637,10 +662,10 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
             fence_before_sync();
         } while (false);
     }
-    if (tid == 32) GDN_UTR(p.trace, 10);
+    if (tid == 32) GDN_UTR(p.trace, 20);
     fence_before_sync();
     __syncthreads();
-    if (tid == 32) GDN_UTR(p.trace, 11);
+    if (tid == 32) GDN_UTR(p.trace, 21);
     if (warp == 0) {
         fence_after_sync();
         tmem_dealloc(tb, 128);
