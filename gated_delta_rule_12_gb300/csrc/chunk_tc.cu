@@ -62,15 +62,17 @@ constexpr uint32_t kWsHeader = 1024;   // device error word + padding
 // ---- ut_tc_kernel shared memory
 constexpr int kThreadsUt = 160;        // warp 0: TMA, MMA, TMEM; warps 1-4: 128 "prep" threads
 constexpr uint32_t U_QK = 0;           // [K kb0][Q kb0][K kb1][Q kb1], 8 KB each
-constexpr uint32_t U_TPP = 32768;      // solve scratch, then T'' (8 KB); rows 64-127 of the
-                                       // padded A = [T''; *] of the W~ product read U_A (don't care)
-constexpr uint32_t U_A = 40960;        // L, then T, in place: fp32 [64][LDL]
-constexpr uint32_t U_SC = U_A + 64 * LDL * 4;     // b, beta, rk, rq, cw, ecol, cq[3] [9][64] fp32
-constexpr uint32_t U_BAR = U_SC + 9 * 64 * 4;
+// Once the Gram product has read Q, its two tiles are reused:
+constexpr uint32_t U_TPP = 8192;       // T'' (bf16, 8 KB): A of the W~ product; its padding rows
+                                       // 64-127 read the K tile behind it (results not used)
+constexpr uint32_t U_MT = 24576;       // solve scratch (4 KB)
+constexpr uint32_t U_A = 32768;        // L, then T, in place: fp32 [64][LDL]
+constexpr uint32_t U_SC = U_A + 64 * LDL * 4;     // b, beta, rk, rq, cw, ecol, cq[3], misc  [10][64] fp32
+constexpr uint32_t U_BAR = U_SC + 10 * 64 * 4;
 constexpr uint32_t U_MISC = U_BAR + 8 * 8;
 constexpr uint32_t kSmemUt = U_MISC + 64 + 1024;
 static_assert(U_A % 16 == 0 && U_SC % 16 == 0, "alignment");
-static_assert(3 * (kSmemUt + 1024) <= 233472, "three UT CTAs per SM");
+static_assert(4 * (kSmemUt + 1024) <= 233472, "four UT CTAs per SM");
 
 // ---- recur_tc_kernel shared memory.  Operands are staged by lifetime:
 //   "early" stages (2): T' and V (a1), [W~ | Q] interleaved (the merged a2 product)
@@ -357,7 +359,7 @@ struct UtParams {
     long long *trace;
 };
 
-__global__ void __launch_bounds__(kThreadsUt, 3)
+__global__ void __launch_bounds__(kThreadsUt, 4)
 ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk, const UtParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -426,7 +428,7 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
     } else {
         const int prow = 32 * (warp & 3) + lane;   // tensor-memory lane of this thread
         float *Am = reinterpret_cast<float *>(sm + U_A);
-        float *Mt = reinterpret_cast<float *>(sm + U_TPP);
+        float *Mt = reinterpret_cast<float *>(sm + U_MT);
         float *sc = reinterpret_cast<float *>(sm + U_SC);
         float *bsum = sc, *bet = sc + 64, *rk = sc + 128, *rq = sc + 192, *cw = sc + 256, *ecol = sc + 320;
         float *cq = sc + 384;   // [3][64]: e^{b_m - b_p} rq_m for the block ends p = 15, 31, 47
@@ -446,12 +448,12 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                         const float y = __shfl_up_sync(0xffffffffu, x, o);
                         if (lane >= o) x += y;
                     }
-                    if (lane == 31) Mt[prow >> 5] = x;
+                    if (lane == 31) sc[576 + (prow >> 5)] = x;
                 } else {
                     bet[r] = (r < rows) ? p.beta[t] : 0.f;
                 }
                 group_sync(1, 128);
-                if (prow < 64) bsum[prow] = x + ((prow >= 32) ? Mt[0] : 0.f);
+                if (prow < 64) bsum[prow] = x + ((prow >= 32) ? sc[576] : 0.f);
                 group_sync(1, 128);
             }
             // (2) inverse norms from the diagonal of the Gram product: thread p reads
@@ -498,28 +500,44 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
             if (prow == 0) GDN_UTR(p.trace, 3);
             if (prow == 0) GDN_UTR(p.trace, 4);
             if (prow < 64) {
-                const int i = prow, I = i >> 4;
+                // Thread i (TMEM lane i) holds row i of K [K; Q]^T.  Warp quarter wq covers
+                // rows 32wq..32wq+31 (16-blocks 2wq, 2wq+1): the "near" column blocks 2wq and
+                // 2wq+1 take the exact factor e^{+-(b_i - b_m)} per entry (masked by a select),
+                // the far blocks the factorised one, so every branch is uniform over the warp.
+                const int i = prow, I = i >> 4, wq = warp & 3;
+                const float bi = bsum[i];
                 uint32_t u[64];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) tmem_ld16(lane_base + TP1 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(u + q * 16));
                 tmem_wait_ld();
                 if (prow == 0) GDN_UTR(p.trace, 5);
-                const float bi = bsum[i];
-                // L row i: columns m < i
-                {
+                {   // L row i, columns m < i: beta_i e^{b_i - b_m} rk_i rk_m G_im
                     const float f = bet[i] * rk[i];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         float v[16];
-                        if (q < I) {
+                        if (q < 2 * wq) {
                             const float fu = f * exp2f(bi - bsum[q * 16 + 15]);
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) v[e] = fu * cw[q * 16 + e] * __uint_as_float(u[q * 16 + e]);
-                        } else if (q == I) {
+                            for (int e4 = 0; e4 < 16; e4 += 4) {
+                                const float4 c4 = *reinterpret_cast<const float4 *>(cw + q * 16 + e4);
+                                v[e4 + 0] = fu * c4.x * __uint_as_float(u[q * 16 + e4 + 0]);
+                                v[e4 + 1] = fu * c4.y * __uint_as_float(u[q * 16 + e4 + 1]);
+                                v[e4 + 2] = fu * c4.z * __uint_as_float(u[q * 16 + e4 + 2]);
+                                v[e4 + 3] = fu * c4.w * __uint_as_float(u[q * 16 + e4 + 3]);
+                            }
+                        } else if (q <= 2 * wq + 1) {
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const int m = q * 16 + e;
-                                v[e] = (m < i) ? f * exp2f(bi - bsum[m]) * rk[m] * __uint_as_float(u[m]) : 0.f;
+                            for (int e4 = 0; e4 < 16; e4 += 4) {
+                                const float4 b4 = *reinterpret_cast<const float4 *>(bsum + q * 16 + e4);
+                                const float4 r4 = *reinterpret_cast<const float4 *>(rk + q * 16 + e4);
+                                const float bb[4] = {b4.x, b4.y, b4.z, b4.w}, rr[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int m = q * 16 + e4 + e;
+                                    const float x = f * rr[e] * __uint_as_float(u[m]) * exp2f(bi - bb[e]);
+                                    v[e4 + e] = (m < i) ? x : 0.f;
+                                }
                             }
                         } else {
 #pragma unroll
@@ -531,30 +549,41 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                     }
                 }
                 if (prow == 0) GDN_UTR(p.trace, 6);
-                // Aqk^T row i: columns m >= i, e^{b_m - b_i} = e^{b_m - b_p} e^{b_p - b_i} with p the
-                // end of i's 16-block for m beyond it (both factors <= 1), direct inside the block
-                {
+                // Aqk^T row i, columns m >= i: e^{b_m - b_i} rq_m rk_i G_(i, 64+m); far blocks
+                // as e^{b_m - b_p} e^{b_p - b_i} with p the end of i's 16-block
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        tmem_ld16(lane_base + TP1 + 64 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(u + q * 16));
-                    tmem_wait_ld();
-                    if (prow == 0) GDN_UTR(p.trace, 7);
+                for (int q = 0; q < 4; ++q)
+                    tmem_ld16(lane_base + TP1 + 64 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(u + q * 16));
+                tmem_wait_ld();
+                if (prow == 0) GDN_UTR(p.trace, 7);
+                {
                     const float fi = rk[i];
-                    const float wi = exp2f(bsum[i | 15] - bi);   // e^{b_p - b_i}
+                    const float fw = fi * exp2f(bsum[i | 15] - bi);   // rk_i e^{b_p - b_i}
+                    const float *cqi = cq + (I < 3 ? I : 2) * 64;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         float v[16];
-                        if (q > I) {
+                        if (q > 2 * wq + 1) {
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const int m = q * 16 + e;
-                                v[e] = fi * wi * cq[I * 64 + m] * __uint_as_float(u[m]);
+                            for (int e4 = 0; e4 < 16; e4 += 4) {
+                                const float4 c4 = *reinterpret_cast<const float4 *>(cqi + q * 16 + e4);
+                                v[e4 + 0] = fw * c4.x * __uint_as_float(u[q * 16 + e4 + 0]);
+                                v[e4 + 1] = fw * c4.y * __uint_as_float(u[q * 16 + e4 + 1]);
+                                v[e4 + 2] = fw * c4.z * __uint_as_float(u[q * 16 + e4 + 2]);
+                                v[e4 + 3] = fw * c4.w * __uint_as_float(u[q * 16 + e4 + 3]);
                             }
-                        } else if (q == I) {
+                        } else if (q >= 2 * wq) {
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const int m = q * 16 + e;
-                                v[e] = (m >= i) ? fi * exp2f(bsum[m] - bi) * rq[m] * __uint_as_float(u[m]) : 0.f;
+                            for (int e4 = 0; e4 < 16; e4 += 4) {
+                                const float4 b4 = *reinterpret_cast<const float4 *>(bsum + q * 16 + e4);
+                                const float4 r4 = *reinterpret_cast<const float4 *>(rq + q * 16 + e4);
+                                const float bb[4] = {b4.x, b4.y, b4.z, b4.w}, rr[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int m = q * 16 + e4 + e;
+                                    const float x = fi * rr[e] * __uint_as_float(u[m]) * exp2f(bb[e] - bi);
+                                    v[e4 + e] = (m >= i) ? x : 0.f;
+                                }
                             }
                         } else {
 #pragma unroll
