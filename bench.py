@@ -1,8 +1,8 @@
 #!/usr/bin/env python
 """Benchmark of the gated delta rule hot path on GB300.
 
-One step = one chunked forward (prologue, UT transform, inter-chunk
-recurrence, final-state write) over the headline workload
+One step = one chunked forward (gate cumsum and norms, UT transform,
+inter-chunk recurrence, final-state write) over the headline workload
   B=4, H=16, L=2048, d_k=d_v=128, chunk 64, bf16 q/k/v, fp32 gates/state,
 with inputs resident in HBM.  The decode half of the metric (64 successive
 single-token steps on N=256, H=16, d=128, fp32 state) is measured in the same
@@ -14,8 +14,8 @@ before every timed step, outside the events.  Under torchrun every rank runs
 its own replica of the workload (independent sequences: weak scaling, no
 collective on the data path); rank 0 prints the max over ranks.
 
---impl reference times the fp64 CPU oracle on the host cores instead, on a
-bounded sample of the same workload, and prints the same JSON line.
+--impl reference times the fp64 CPU oracle on the host cores instead, on the
+same workload, and prints the same JSON line.
 """
 from __future__ import annotations
 
@@ -75,33 +75,53 @@ def decode_algorithmic_bytes(w: inputs.Workload) -> int:
 
 
 class ClockSampler:
-    """Samples nvidia-smi SM clocks and throttle reasons while the timed region runs."""
+    """Samples nvidia-smi SM clocks and throttle reasons around the timed region.
+
+    nvidia-smi polls every `interval_ms`; each line is stamped with the host
+    clock.  The timed region of one step is far shorter than a poll, so the
+    summary keeps the samples within `margin_s` of the region (the bench marks
+    its start and end with `mark()`), and the sampler is started, and has
+    produced its first line, before the warm-up steps run.
+    """
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, interval_ms: int = 50, margin_s: float = 0.5):
         self.index = index
+        self.interval_ms = interval_ms
+        self.margin_s = margin_s
         self.proc = None
         self.lines = []
+        self.marks = []
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.interval_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
+            t0 = time.monotonic()
+            while not self.lines and time.monotonic() - t0 < 5.0:
+                time.sleep(0.01)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.monotonic())
 
     def __exit__(self, *exc):
         if self.proc is not None:
+            # one more poll after the region ends
+            t0 = time.monotonic()
+            while time.monotonic() - t0 < 3 * self.interval_ms / 1e3:
+                time.sleep(0.01)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -111,7 +131,11 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lo = (min(self.marks) - self.margin_s) if self.marks else float("-inf")
+        hi = (max(self.marks) + self.margin_s) if self.marks else float("inf")
+        for ts, ln in self.lines:
+            if not (lo <= ts <= hi):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -123,10 +147,12 @@ class ClockSampler:
             for nm, val in zip(names, parts[4:8]):
                 if val.lower() == "active":
                     reasons.add(nm)
+        window = (f"nvidia-smi every {self.interval_ms} ms, samples within {self.margin_s} s of the timed region"
+                  if self.marks else f"nvidia-smi every {self.interval_ms} ms")
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": window}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": window}
 
 
 def traffic_record(kernel: str):
@@ -173,6 +199,11 @@ def max_over_ranks(dist, x: float) -> float:
     return float(t.item())
 
 
+def job_throughput(units_per_rank: float, world_size: int, ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time (ms)."""
+    return units_per_rank * world_size / (ms * 1e-3)
+
+
 def barrier(dist):
     if dist is not None:
         dist.barrier()
@@ -205,27 +236,29 @@ def bench_ours(args):
         gdn.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], init_state=d["init_state"], scale=w.scale,
                       use_qk_l2norm=True, out=out, final_state=sf, workspace=work)
 
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
-    barrier(dist)
-    torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(local) as clk:
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+        barrier(dist)
+        torch.cuda.synchronize()
+        clk.mark()
         for i in range(args.steps):
             flush.zero_()
             evs[i][0].record(stream)
             step()
             evs[i][1].record(stream)
         torch.cuda.synchronize()
+        clk.mark()
     barrier(dist)
     ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
     ms = max_over_ranks(dist, ms)
     clocks = clk.summary()
 
     tokens = w.B * w.L
-    value = tokens * ws_n / (ms * 1e-3)
+    value = job_throughput(tokens, ws_n, ms)
     algo_bytes = prefill_algorithmic_bytes(w)
     achieved = algo_bytes / (ms * 1e-3) / 1e9
     launches_per_step = gdn.chunk_fwd_kernel_count(w.B, w.L, w.H, w.dk, w.dv, 0, torch.bfloat16)
@@ -304,10 +337,10 @@ def bench_ours(args):
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_record("chunk_fwd"),
                          "kernel": "one gdn_chunk_fwd call (ut_tc_kernel + recur_tc_kernel)",
                          "algorithmic_bytes": algo_bytes, "peak_source": peaks["source"]},
-            "e2e": {"value": tokens * ws_n / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": job_throughput(tokens, ws_n, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "decode": {"workload": DECODE, "value": 1e3 / dms * ws_n, "unit": "steps/s",
-                       "tokens_per_s": wd.num_seqs * 1e3 / dms * ws_n, "ms_per_step": dms,
+            "decode": {"workload": DECODE, "value": job_throughput(1, ws_n, dms), "unit": "steps/s",
+                       "tokens_per_s": job_throughput(wd.num_seqs, ws_n, dms), "ms_per_step": dms,
                        "roofline": {"bound": "hbm", "achieved": d_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                     "frac": d_ach / peaks["hbm_gbs"], "traffic": traffic_record("decode"),
                                     "algorithmic_bytes": dbytes},
@@ -333,15 +366,23 @@ def oracle_sample(w: inputs.Workload, host=None, seqs=1, heads=None):
     return {k: sel(host[k]) for k in ("q", "k", "v", "g", "beta")}, seqs * w.L * hs
 
 
-def cpu_baseline(w: inputs.Workload, host=None):
+def cpu_baseline(w: inputs.Workload, host=None, budget_s: float = 10.0):
+    """The fp64 oracle on the host cores over the whole workload, repeated for about `budget_s`."""
     import oracle
-    s, token_heads = oracle_sample(w, host, seqs=1)
-    t0 = time.perf_counter()
-    oracle.recurrent_fwd(s["q"], s["k"], s["v"], s["g"], s["beta"], scale=w.scale, use_qk_l2norm=True)
-    dt = time.perf_counter() - t0
-    cores = min(oracle.num_threads(), w.H)
-    return {"value": token_heads / w.H / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"1 of {w.B} sequences ({w.L} tokens x {w.H} heads), fp64 recurrence, {dt:.2f} s"}
+    s, token_heads = oracle_sample(w, host, seqs=w.B)
+
+    def one_pass() -> float:
+        t0 = time.perf_counter()
+        oracle.recurrent_fwd(s["q"], s["k"], s["v"], s["g"], s["beta"], scale=w.scale, use_qk_l2norm=True)
+        return time.perf_counter() - t0
+
+    dt = one_pass()
+    reps = max(1, int(budget_s / dt))   # the first pass sizes the sample
+    dt += sum(one_pass() for _ in range(reps - 1))
+    cores = min(oracle.num_threads(), w.B * w.H)
+    return {"value": token_heads / w.H * reps / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"the whole workload ({w.B} x {w.L} tokens x {w.H} heads), fp64 recurrence, "
+                      f"{reps} passes in {dt:.1f} s"}
 
 
 def bench_reference(args):
@@ -352,8 +393,8 @@ def bench_reference(args):
     oracle.build()
     w = inputs.WORKLOADS[PREFILL]
     host = inputs.make(w)
-    s, token_heads = oracle_sample(w, host, seqs=1)
-    cores = min(oracle.num_threads(), w.H)
+    s, token_heads = oracle_sample(w, host, seqs=w.B)
+    cores = min(oracle.num_threads(), w.B * w.H)
 
     def step():
         oracle.recurrent_fwd(s["q"], s["k"], s["v"], s["g"], s["beta"], scale=w.scale, use_qk_l2norm=True)
@@ -371,7 +412,7 @@ def bench_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": PREFILL, "B": w.B, "T": w.L, "H": w.H, "dk": w.dk, "dv": w.dv, "chunk": w.chunk_size},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"per step: 1 of {w.B} sequences ({w.H} heads x {w.L} tokens) of the workload, fp64 recurrence"},
+                         "sample": f"per step: the whole workload ({w.B} x {w.L} tokens x {w.H} heads), fp64 recurrence"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -433,7 +433,7 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         float *bsum = sc, *bet = sc + 64, *rk = sc + 128, *rq = sc + 192, *cw = sc + 256, *ecol = sc + 320;
         float *cq = sc + 384;   // [3][64]: e^{b_m - b_p} rq_m for the block ends p = 15, 31, 47
         const uint32_t lane_base = tb + ((uint32_t)(32 * (warp & 3)) << 16);
-        uint8_t *st = sm + U_QK;
+        const uint8_t *st = sm + U_QK;
         if (prow == 0) GDN_UTR(p.trace, 0);
         do {
             // (1) gates: chunk-local cumulative log-gate in base 2, beta
