@@ -40,6 +40,7 @@ from gated_delta_rule_12_gb300 import inputs  # noqa: E402
 METRIC = "tokens/s chunked fwd (H=16,d=128,L=2048) + decode steps/s; % roofline"
 PREFILL = "prefill_b4_h16_l2048_d128_bf16"
 DECODE = "decode_n256_h16_d128_bf16"
+MULTI_T = 4          # tokens per call of the multi-token decode line
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
@@ -65,6 +66,13 @@ def prefill_algorithmic_bytes(w: inputs.Workload) -> int:
 def prefill_algorithmic_flops(w: inputs.Workload) -> int:
     C = w.chunk_size
     return w.B * w.L * w.H * (2 * C * (3 * w.dk + 2 * w.dv) + 6 * w.dk * w.dv)
+
+
+def decode_multi_algorithmic_bytes(w: inputs.Workload, T: int) -> int:
+    """Per call of T tokens: the fp32 state read and written once, plus T tokens of q, k, v, out, g, beta."""
+    s = 2 if w.dtype == "bf16" else 4
+    nh = w.num_seqs * w.H
+    return nh * (2 * w.dv * w.dk * 4 + T * ((2 * w.dk + 2 * w.dv) * s + 8))
 
 
 def decode_algorithmic_bytes(w: inputs.Workload) -> int:
@@ -324,6 +332,40 @@ def bench_ours(args):
     dbytes = decode_algorithmic_bytes(wd)
     d_ach = dbytes / (dms * 1e-3) / 1e9
 
+    # several tokens per call: the same 64 tokens as MULTI_T tokens x (64 / MULTI_T) calls,
+    # the state read and written once per call
+    tmaj = lambda x: x.transpose(0, 1).contiguous()          # [steps, N, ...] -> [N, steps, ...]
+    dm = {k2: tmaj(dd[k2]) for k2 in ("q", "k", "v", "g", "beta")}
+    calls = wd.steps // MULTI_T
+    mstate = dd["state0"].clone()
+    mout = torch.empty((wd.num_seqs, MULTI_T, wd.H, wd.dv), dtype=torch.bfloat16, device=dev)
+    msl = [{k2: dm[k2][:, c * MULTI_T:(c + 1) * MULTI_T].contiguous() for k2 in dm} for c in range(calls)]
+
+    def decode_multi_all():
+        for c in range(calls):
+            x = msl[c]
+            gdn.decode_multi(mstate, x["q"], x["k"], x["v"], x["g"], x["beta"], scale=wd.scale, out=mout)
+
+    for _ in range(max(1, args.warmup)):
+        decode_multi_all()
+    torch.cuda.synchronize()
+    mgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(mgraph):
+        decode_multi_all()
+    mgraph.replay()
+    torch.cuda.synchronize()
+    m_ms = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        mgraph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        m_ms.append(a.elapsed_time(b) / calls)
+    mms = max_over_ranks(dist, statistics.median(m_ms))
+    mbytes = decode_multi_algorithmic_bytes(wd, MULTI_T)
+    m_ach = mbytes / (mms * 1e-3) / 1e9
+
     if rank == 0:
         cpu = cpu_baseline(w) if ws_n == 1 else None
         line = {
@@ -345,6 +387,12 @@ def bench_ours(args):
                                     "frac": d_ach / peaks["hbm_gbs"], "traffic": traffic_record("decode"),
                                     "algorithmic_bytes": dbytes},
                        "timing": f"{wd.steps} steps in one CUDA graph, median of {reps}"},
+            "decode_multi": {"workload": DECODE, "tokens_per_call": MULTI_T,
+                             "value": job_throughput(wd.num_seqs * MULTI_T, ws_n, mms), "unit": "tokens/s",
+                             "ms_per_call": mms,
+                             "roofline": {"bound": "hbm", "achieved": m_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                          "frac": m_ach / peaks["hbm_gbs"], "algorithmic_bytes": mbytes},
+                             "timing": f"{wd.steps} tokens as {calls} calls in one CUDA graph, median of {reps}"},
             "gpu_launches": args.steps * launches_per_step,
             "clocks": clocks,
             "cpu_baseline": cpu,

@@ -10,6 +10,7 @@ be loaded the calls raise: there is no fallback.
 Entry points (same names as the C ABI, without the ``gdn_`` prefix):
     chunk_fwd(q, k, v, g, beta, ...)      -> (out, final_state)
     decode_step(state, q, k, v, g, beta)  -> out            (state updated in place)
+    decode_multi(state, q, k, v, g, beta) -> out [N,T,H,dv] (T tokens per call, state in place)
     chunk_fwd_workspace_size(...)         -> bytes
     chunk_fwd_kernel_count(...)           -> kernels one chunk_fwd call launches
     check_device_error(workspace)         -> None or raises
@@ -32,7 +33,7 @@ GDN_F32, GDN_BF16 = 0, 1
 CHUNK = 64
 
 EXPORTS = ["gdn_status_string", "gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd_kernel_count", "gdn_chunk_fwd",
-           "gdn_decode_step", "gdn_check_device_error", "gdn_chunk_fwd_noalloc"]
+           "gdn_decode_step", "gdn_decode_multi", "gdn_check_device_error", "gdn_chunk_fwd_noalloc"]
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -77,6 +78,9 @@ def load_library(path: str = LIB_PATH, build_if_missing: bool = False) -> ctypes
         lib.gdn_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                         _i32, _i32, _i32, _i32, ctypes.c_int, _f32, _i32, _vp]
         lib.gdn_decode_step.restype = ctypes.c_int
+        lib.gdn_decode_multi.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                         _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _f32, _i32, _vp]
+        lib.gdn_decode_multi.restype = ctypes.c_int
         lib.gdn_check_device_error.argtypes = [_vp, _vp]
         lib.gdn_check_device_error.restype = ctypes.c_int
         lib.gdn_chunk_fwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
@@ -184,6 +188,32 @@ def decode_step(state, q, k, v, g, beta, scale=None, use_qk_l2norm=True, out=Non
                              N, H, dk, dv, _dt(q), float(scale), int(bool(use_qk_l2norm)), _stream(stream))
     if rc != GDN_OK:
         raise GDNError(rc, "gdn_decode_step")
+    return out
+
+
+def decode_multi(state, q, k, v, g, beta, scale=None, use_qk_l2norm=True, out=None, stream=None):
+    """T decode tokens per (sequence, head) in one call; ``state`` [N,H,dv,dk] fp32 is updated in place.
+
+    q, k [N,T,H,dk], v [N,T,H,dv] (fp32 or bf16); g, beta [N,T,H] fp32.  Returns out [N,T,H,dv],
+    the same as T successive ``decode_step`` calls.
+    """
+    lib = load_library()
+    N, H, dv, dk = state.shape
+    T = q.shape[1]
+    if scale is None:
+        scale = dk ** -0.5
+    if out is None:
+        out = torch.empty((N, T, H, dv), dtype=q.dtype, device=q.device)
+    if state.dtype != torch.float32 or g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("state, g and beta must be float32")
+    if q.shape != (N, T, H, dk) or k.shape != (N, T, H, dk) or v.shape != (N, T, H, dv) or g.shape != (N, T, H) \
+            or beta.shape != (N, T, H) or out.shape != (N, T, H, dv):
+        raise ValueError("decode_multi: inconsistent shapes")
+    _need_cuda(state, q, k, v, g, beta, out)
+    rc = lib.gdn_decode_multi(_ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(out),
+                              N, T, H, dk, dv, _dt(q), float(scale), int(bool(use_qk_l2norm)), _stream(stream))
+    if rc != GDN_OK:
+        raise GDNError(rc, "gdn_decode_multi")
     return out
 
 

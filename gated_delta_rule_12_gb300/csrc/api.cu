@@ -106,15 +106,15 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-gdn_status gdn_decode_step(float *state, const void *q, const void *k, const void *v,
-                           const float *g, const float *beta, void *out, int32_t N, int32_t H,
-                           int32_t dk, int32_t dv, gdn_dtype dt, float scale,
-                           int32_t use_qk_l2norm, void *stream)
+static gdn_status decode_common(float *state, const void *q, const void *k, const void *v, const float *g,
+                                const float *beta, void *out, int32_t N, int32_t T, int32_t H, int32_t dk,
+                                int32_t dv, gdn_dtype dt, float scale, int32_t use_qk_l2norm, void *stream)
 {
-    if (N < 0 || H < 1 || dk < 1 || dv < 1) return GDN_ERR_INVALID_ARG;
+    if (N < 0 || T < 0 || H < 1 || dk < 1 || dv < 1) return GDN_ERR_INVALID_ARG;
     if (dt != GDN_F32 && dt != GDN_BF16) return GDN_ERR_INVALID_ARG;
     if (!(dk == 64 || dk == 128 || dk == 256) || dv % 8 != 0) return GDN_ERR_UNSUPPORTED;
-    if (N == 0) return GDN_OK;
+    if (N == 0 || T == 0) return GDN_OK;
+    if ((int64_t)N * T * H * (dk > dv ? dk : dv) >= ((int64_t)1 << 62)) return GDN_ERR_INVALID_ARG;
     const void *ptrs[] = {state, q, k, v, g, beta, out};
     for (const void *p : ptrs)
         if (!p) return GDN_ERR_INVALID_ARG;
@@ -125,9 +125,26 @@ gdn_status gdn_decode_step(float *state, const void *q, const void *k, const voi
     DecodeArgs a;
     a.state = state; a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = out;
     a.N = N; a.H = H; a.dk = dk; a.dv = dv; a.dt = (dt == GDN_BF16) ? 1 : 0;
+    a.ntok = T;
     a.scale = scale; a.l2 = use_qk_l2norm ? 1 : 0;
     cudaError_t e = launch_decode(a, (cudaStream_t)stream);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status gdn_decode_step(float *state, const void *q, const void *k, const void *v,
+                           const float *g, const float *beta, void *out, int32_t N, int32_t H,
+                           int32_t dk, int32_t dv, gdn_dtype dt, float scale,
+                           int32_t use_qk_l2norm, void *stream)
+{
+    return decode_common(state, q, k, v, g, beta, out, N, 1, H, dk, dv, dt, scale, use_qk_l2norm, stream);
+}
+
+gdn_status gdn_decode_multi(float *state, const void *q, const void *k, const void *v,
+                            const float *g, const float *beta, void *out, int32_t N, int32_t T,
+                            int32_t H, int32_t dk, int32_t dv, gdn_dtype dt, float scale,
+                            int32_t use_qk_l2norm, void *stream)
+{
+    return decode_common(state, q, k, v, g, beta, out, N, T, H, dk, dv, dt, scale, use_qk_l2norm, stream);
 }
 
 gdn_status gdn_check_device_error(void *workspace, void *stream)

@@ -65,7 +65,8 @@ constexpr uint32_t U_QK = 0;           // [K kb0][Q kb0][K kb1][Q kb1], 8 KB eac
 // Once the Gram product has read Q, its two tiles are reused:
 constexpr uint32_t U_TPP = 8192;       // T'' (bf16, 8 KB): A of the W~ product; its padding rows
                                        // 64-127 read the K tile behind it (results not used)
-constexpr uint32_t U_MT = 24576;       // solve scratch (4 KB)
+constexpr uint32_t U_MT = 24576;       // solve scratch (4 KB), then
+constexpr uint32_t U_TPL = 24576;      // T''_lo (bf16, 8 KB): T'' - T''_hi; its padding rows read U_A
 constexpr uint32_t U_A = 32768;        // L, then T, in place: fp32 [64][LDL]
 constexpr uint32_t U_SC = U_A + 64 * LDL * 4;     // b, beta, rk, rq, cw, ecol, cq[3], misc  [10][64] fp32
 constexpr uint32_t U_BAR = U_SC + 10 * 64 * 4;
@@ -414,9 +415,9 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                     fence_after_sync();
                     const uint32_t id_p2 = idesc_bf16(128, 128, false, true);
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)   // [W~; 0] = [T''; 0] K   (rows 0-63 are W~)
-                        mma_ss(tb + TP2, smem_desc(sb + U_TPP + ks * 32, 16, 1024),
-                               smem_desc(sb + U_QK + ks * 2048, 16384, 1024), id_p2, ks > 0);
+                    for (int ks = 0; ks < 8; ++ks)   // [W~; 0] = [T''_hi; 0] K + [T''_lo; 0] K  (rows 0-63 are W~)
+                        mma_ss(tb + TP2, smem_desc(sb + ((ks < 4) ? U_TPP : U_TPL) + (ks & 3) * 32, 16, 1024),
+                               smem_desc(sb + U_QK + (ks & 3) * 2048, 16384, 1024), id_p2, ks > 0);
                     commit(bar(UB_P2));
                 }
             }
@@ -638,16 +639,22 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                     const float4 t0 = *reinterpret_cast<const float4 *>(Am + r * LDL + ib);
                     const float4 t1 = *reinterpret_cast<const float4 *>(Am + r * LDL + ib + 4);
                     const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
-                    uint32_t w1[4], w2[4];
+                    uint32_t w1[4], w2[4], w3[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float p0 = tv[2 * e] * bet[ib + 2 * e], p1 = tv[2 * e + 1] * bet[ib + 2 * e + 1];
                         w1[e] = pack_bf16(p0, p1);
-                        w2[e] = pack_bf16(p0 * ecol[ib + 2 * e], p1 * ecol[ib + 2 * e + 1]);
+                        // T'' as a sum of two bf16 terms: W~ = T'' K can cancel heavily (nearly
+                        // parallel keys), so its operand carries ~16 bits
+                        const float t0 = p0 * ecol[ib + 2 * e], t1 = p1 * ecol[ib + 2 * e + 1];
+                        w2[e] = pack_bf16(t0, t1);
+                        const float2 h2 = unpack_bf16(w2[e]);
+                        w3[e] = pack_bf16(t0 - h2.x, t1 - h2.y);
                     }
                     const uint32_t off = sw128_offset(r, ib);
                     *reinterpret_cast<uint4 *>(blk + PB_TP + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
                     *reinterpret_cast<uint4 *>(sm + U_TPP + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+                    *reinterpret_cast<uint4 *>(sm + U_TPL + off) = make_uint4(w3[0], w3[1], w3[2], w3[3]);
                 }
             }
             fence_proxy_async();

@@ -1,4 +1,4 @@
-// decode.cu -- single-token decode step of the gated delta rule.
+// decode.cu -- decode steps of the gated delta rule (one or a few tokens per call).
 //
 // "Gated DeltaNet：先忘一点，再按误差更新记忆", "为什么再加一个遗忘门？":
 //     Sbar = alpha S,   S <- Sbar + beta (v - Sbar k) k^T,   o = S q.
@@ -15,6 +15,12 @@
 // (R * dk * 4 bytes).  Warps stride over all groups of the call, so the load
 // is balanced whatever N*H is.  Each lane holds dk/32 consecutive entries of
 // a row (16-byte vector loads when dk >= 128).
+//
+// Several tokens per call ("Decode 递归": the ordered composition of steps):
+// the group's rows stay in registers while the T tokens of the call are
+// applied in order, so the state is still read once and written once per call
+// however many tokens it carries.  Token t of sequence n, head h is at
+// ((n T + t) H + h) of the token-major inputs; T = 1 is the single step.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -52,18 +58,42 @@ __device__ __forceinline__ void store_row(float *p, const float (&x)[VEC])
     }
 }
 
-template <typename T, int DK, int R>
+// Sums of eight per-lane partials x[0..7] (one per row) over the warp, reduced
+// together: three exchange stages halve the rows a lane carries (xor 16, 8, 4),
+// two more finish the sum (xor 2, 1).  Afterwards lane l holds the total of
+// row l >> 2 (9 shuffles for 8 rows instead of 5 per row).
+__device__ __forceinline__ float warp_sum8_transposed(const float (&x)[8], int lane)
+{
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float w4[4], w2[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        w4[i] = (b4 ? x[i + 4] : x[i]) + __shfl_xor_sync(0xffffffffu, b4 ? x[i] : x[i + 4], 16);
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        w2[i] = (b3 ? w4[i + 2] : w4[i]) + __shfl_xor_sync(0xffffffffu, b3 ? w4[i] : w4[i + 2], 8);
+    float w = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
+    w += __shfl_xor_sync(0xffffffffu, w, 2);
+    w += __shfl_xor_sync(0xffffffffu, w, 1);
+    return w;
+}
+
+// MULTI = false compiles the single-token step as straight-line code.
+template <typename T, int DK, bool MULTI>
 __global__ void __launch_bounds__(256)
 decode_kernel(float *__restrict__ state, const T *__restrict__ q, const T *__restrict__ k,
               const T *__restrict__ v, const float *__restrict__ g, const float *__restrict__ beta,
-              T *__restrict__ out, int NH, int dv, float scale, int l2)
+              T *__restrict__ out, int NH, int H, int ntok, int dv, float scale, int l2)
 {
+    constexpr int R = 8;           // rows of S per warp group
     constexpr int VEC = DK / 32;   // entries of a row per lane
     const int lane = threadIdx.x & 31;
+    const int myrow = lane >> 2;   // the row whose reductions this lane ends up holding
     const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int groups_per_head = dv / R;
     const int64_t total = (int64_t)NH * groups_per_head;
+    const int nt = MULTI ? ntok : 1;
 
     for (int64_t grp = warp0; grp < total; grp += nwarps) {
         const int64_t nh = grp / groups_per_head;
@@ -74,78 +104,91 @@ decode_kernel(float *__restrict__ state, const T *__restrict__ q, const T *__res
 #pragma unroll
         for (int r = 0; r < R; ++r) load_row<VEC>(S + (size_t)r * DK, s[r]);
 
-        // normalised key and scaled, normalised query for this head
-        float kv[VEC], qv[VEC];
-        float sk = 0.f, sq = 0.f;
-#pragma unroll
-        for (int i = 0; i < VEC; ++i) {
-            kv[i] = to_f32(k[nh * DK + lane * VEC + i]);
-            qv[i] = to_f32(q[nh * DK + lane * VEC + i]);
-            sk += kv[i] * kv[i];
-            sq += qv[i] * qv[i];
-        }
-        float rk = 1.f, rq = scale;
-        if (l2) {
-            sk = warp_sum(sk);
-            sq = warp_sum(sq);
-            rk = 1.f / sqrtf(sk + kL2Eps);
-            rq = scale / sqrtf(sq + kL2Eps);
-        }
-        float kq = 0.f;
-#pragma unroll
-        for (int i = 0; i < VEC; ++i) {
-            kv[i] *= rk;
-            qv[i] *= rq;
-            kq += kv[i] * qv[i];
-        }
-        kq = warp_sum(kq);
-        const float alpha = expf(g[nh]);
-        const float b = beta[nh];
-
-        float ov = 0.f;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            float pk = 0.f, pq = 0.f;
+        const int64_t n = MULTI ? nh / H : nh, h = MULTI ? nh % H : 0;
+#pragma unroll 1
+        for (int t = 0; t < nt; ++t) {
+            const int64_t tok = MULTI ? (n * ntok + t) * H + h : nh;   // token-head index
+            // normalised key and scaled, normalised query of this token
+            float kv[VEC], qv[VEC];
+            float sk = 0.f, sq = 0.f;
 #pragma unroll
             for (int i = 0; i < VEC; ++i) {
-                pk += s[r][i] * kv[i];
-                pq += s[r][i] * qv[i];
+                kv[i] = to_f32(k[tok * DK + lane * VEC + i]);
+                qv[i] = to_f32(q[tok * DK + lane * VEC + i]);
+                sk += kv[i] * kv[i];
+                sq += qv[i] * qv[i];
             }
-            pk = warp_sum(pk);
-            pq = warp_sum(pq);
-            const float vj = to_f32(v[nh * dv + j0 + r]);
-            const float e = b * (vj - alpha * pk);
+            const float vj = to_f32(v[tok * dv + j0 + myrow]);
+            const float alpha = expf(g[tok]);
+            const float b = beta[tok];
+            float rk = 1.f, rq = scale;
+            if (l2) {
+                sk = warp_sum(sk);
+                sq = warp_sum(sq);
+                rk = 1.f / sqrtf(sk + kL2Eps);
+                rq = scale / sqrtf(sq + kL2Eps);
+            }
+            float kq = 0.f;
 #pragma unroll
-            for (int i = 0; i < VEC; ++i) s[r][i] = alpha * s[r][i] + e * kv[i];
-            const float o = alpha * pq + e * kq;
-            if (lane == r) ov = o;
+            for (int i = 0; i < VEC; ++i) {
+                kv[i] *= rk;
+                qv[i] *= rq;
+                kq += kv[i] * qv[i];
+            }
+            kq = warp_sum(kq);
+
+            float pk[R], pq[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                pk[r] = 0.f;
+                pq[r] = 0.f;
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) {
+                    pk[r] += s[r][i] * kv[i];
+                    pq[r] += s[r][i] * qv[i];
+                }
+            }
+            const float pkm = warp_sum8_transposed(pk, lane);   // (S k) of row myrow
+            const float pqm = warp_sum8_transposed(pq, lane);   // (S q) of row myrow
+            const float em = b * (vj - alpha * pkm);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float e = __shfl_sync(0xffffffffu, em, 4 * r);
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) s[r][i] = alpha * s[r][i] + e * kv[i];
+            }
+            if ((lane & 3) == 0) out[tok * dv + j0 + myrow] = from_f32<T>(alpha * pqm + em * kq);
         }
 #pragma unroll
         for (int r = 0; r < R; ++r) store_row<VEC>(S + (size_t)r * DK, s[r]);
-        if (lane < R) out[nh * dv + j0 + lane] = from_f32<T>(ov);
     }
 }
 
-template <typename T, int DK>
-static cudaError_t launch_decode_typed(const DecodeArgs &a, cudaStream_t st)
+template <typename T, int DK, bool MULTI>
+static cudaError_t launch_decode_kernel(const DecodeArgs &a, cudaStream_t st)
 {
-    constexpr int R = 8;
     const int NH = a.N * a.H;
-    const int64_t groups = (int64_t)NH * (a.dv / R);
+    const int64_t groups = (int64_t)NH * (a.dv / 8);
     int dev = 0, sms = 152;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<T, DK, R>, 256, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<T, DK, MULTI>, 256, 0);
     if (per_sm < 1) per_sm = 1;
     int64_t blocks = (groups + 7) / 8;
     const int64_t cap = (int64_t)sms * per_sm;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    decode_kernel<T, DK, R><<<(unsigned)blocks, 256, 0, st>>>(
-        a.state, (const T *)a.q, (const T *)a.k, (const T *)a.v, a.g, a.beta, (T *)a.out, NH, a.dv,
-        a.scale, a.l2);
+    decode_kernel<T, DK, MULTI><<<(unsigned)blocks, 256, 0, st>>>(
+        a.state, (const T *)a.q, (const T *)a.k, (const T *)a.v, a.g, a.beta, (T *)a.out, NH, a.H, a.ntok,
+        a.dv, a.scale, a.l2);
     return cudaGetLastError();
+}
+
+template <typename T, int DK>
+static cudaError_t launch_decode_typed(const DecodeArgs &a, cudaStream_t st)
+{
+    return a.ntok > 1 ? launch_decode_kernel<T, DK, true>(a, st) : launch_decode_kernel<T, DK, false>(a, st);
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st)

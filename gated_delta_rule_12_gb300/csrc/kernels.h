@@ -28,6 +28,7 @@ struct DecodeArgs {
     const float *g, *beta;
     void *out;
     int N, H, dk, dv, dt;
+    int ntok;        // tokens per sequence in this call (1 = single step)
     float scale;
     int l2;
 };

@@ -95,16 +95,18 @@ def _round(x: torch.Tensor, dtype: str) -> torch.Tensor:
     return x.to(torch.bfloat16) if dtype == "bf16" else x.to(torch.float32)
 
 
-def draw_gates(shape, decay, gen):
+def draw_gates(shape, decay, gen, beta_max=1.0):
+    """g = -decay * softplus(z), beta = beta_max * sigmoid(z').  beta_max = 2 gives the
+    negative-eigenvalue range beta in (0, 2)."""
     z = torch.randn(shape, generator=gen, dtype=torch.float32)
     zb = torch.randn(shape, generator=gen, dtype=torch.float32)
     g = -decay * torch.nn.functional.softplus(z)
-    beta = torch.sigmoid(zb)
+    beta = beta_max * torch.sigmoid(zb)
     return g.contiguous(), beta.contiguous()
 
 
 def make_prefill(B, L, H, dk, dv, dtype="bf16", seed=0, decay=0.1, init_state=False,
-                 num_seqs=0, lengths=None):
+                 num_seqs=0, lengths=None, beta_max=1.0):
     """Inputs of one chunked-forward call.
 
     Returns a dict with q, k [B,T,H,dk], v [B,T,H,dv], g, beta [B,T,H] (fp32),
@@ -123,14 +125,14 @@ def make_prefill(B, L, H, dk, dv, dtype="bf16", seed=0, decay=0.1, init_state=Fa
     q = torch.randn((B, L, H, dk), generator=gen, dtype=torch.float32)
     k = torch.randn((B, L, H, dk), generator=gen, dtype=torch.float32)
     v = torch.randn((B, L, H, dv), generator=gen, dtype=torch.float32)
-    g, beta = draw_gates((B, L, H), decay, gen)
+    g, beta = draw_gates((B, L, H), decay, gen, beta_max)
     N = num_seqs if num_seqs else B
     s0 = (0.02 * torch.randn((N, H, dv, dk), generator=gen, dtype=torch.float32)) if init_state else None
     return dict(q=_round(q, dtype), k=_round(k, dtype), v=_round(v, dtype), g=g, beta=beta,
                 init_state=s0, cu_seqlens=cu)
 
 
-def make_decode(N, H, dk, dv, steps, dtype="bf16", seed=0, decay=0.1):
+def make_decode(N, H, dk, dv, steps, dtype="bf16", seed=0, decay=0.1, beta_max=1.0):
     """Inputs of ``steps`` successive decode calls.
 
     Returns q, k [steps,N,H,dk], v [steps,N,H,dv], g, beta [steps,N,H],
@@ -140,7 +142,7 @@ def make_decode(N, H, dk, dv, steps, dtype="bf16", seed=0, decay=0.1):
     q = torch.randn((steps, N, H, dk), generator=gen, dtype=torch.float32)
     k = torch.randn((steps, N, H, dk), generator=gen, dtype=torch.float32)
     v = torch.randn((steps, N, H, dv), generator=gen, dtype=torch.float32)
-    g, beta = draw_gates((steps, N, H), decay, gen)
+    g, beta = draw_gates((steps, N, H), decay, gen, beta_max)
     s0 = 0.02 * torch.randn((N, H, dv, dk), generator=gen, dtype=torch.float32)
     return dict(q=_round(q, dtype), k=_round(k, dtype), v=_round(v, dtype), g=g, beta=beta, state0=s0)
 

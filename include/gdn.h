@@ -25,7 +25,7 @@
  *         states      [N, H, dv, dk]    fp32 (row j of S holds dk entries)
  *         cu_seqlens  [N + 1]           int32, device
  *   - Alignment: q, k, v, out and states 16 bytes (gdn_chunk_fwd); state
- *     16 bytes and q, k, v, out their element size (gdn_decode_step); g, beta
+ *     16 bytes and q, k, v, out their element size (decode); g, beta
  *     and cu_seqlens 4 bytes; the workspace 256 bytes.
  *   - q is multiplied by `scale` after the optional per-token-head L2
  *     normalisation of q and k (use_qk_l2norm != 0: x / sqrt(sum x^2 + 1e-6)).
@@ -139,6 +139,26 @@ gdn_status gdn_decode_step(float *state,
                            void *out,
                            int32_t N, int32_t H, int32_t dk, int32_t dv, gdn_dtype dt,
                            float scale, int32_t use_qk_l2norm, void *stream);
+
+/*
+ * T successive decode tokens per (sequence, head) in one call (speculative or
+ * multi-token decode), state updated in place.  "Gated DeltaNet：先忘一点，再按
+ * 误差更新记忆", "Decode 递归": the steps compose in order, so the result is
+ * exactly that of T gdn_decode_step calls on tokens 0..T-1 (and of
+ * gdn_chunk_fwd over the same T tokens with init_state = state).  The state
+ * is read once and written once per call, whatever T is.
+ *   state   [N, H, dv, dk] fp32.
+ *   q, k    [N, T, H, dk] dtype dt (token-major within each sequence);
+ *   v, out  [N, T, H, dv] dtype dt;  g, beta [N, T, H] fp32.
+ *   T >= 0 (T = 0 or N = 0: nothing is enqueued); other rules as gdn_decode_step.
+ * Errors: GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA.
+ */
+gdn_status gdn_decode_multi(float *state,
+                            const void *q, const void *k, const void *v,
+                            const float *g, const float *beta,
+                            void *out,
+                            int32_t N, int32_t T, int32_t H, int32_t dk, int32_t dv, gdn_dtype dt,
+                            float scale, int32_t use_qk_l2norm, void *stream);
 
 /*
  * Reads and clears the device error word at the start of `workspace`

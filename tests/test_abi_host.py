@@ -122,6 +122,20 @@ def test_decode_validation(lib):
     assert d(fake, fake, fake, fake, fake, fake, fake, 0, 2, 128, 64, 0, 1.0, 1, None) == 0  # nothing to do
 
 
+def test_decode_multi_validation(lib):
+    fake = 1 << 20
+    d = lib.gdn_decode_multi
+    #            state q     k     v     g     beta  out   N  T  H  dk   dv  dt scale l2 stream
+    assert d(fake, fake, fake, fake, fake, fake, fake, 4, 3, 2, 96, 64, 0, 1.0, 1, None) == 2    # dk
+    assert d(fake, fake, fake, fake, fake, fake, fake, 4, 3, 2, 128, 12, 0, 1.0, 1, None) == 2   # dv % 8
+    assert d(fake, fake, fake, fake, fake, fake, fake, 4, -1, 2, 128, 64, 0, 1.0, 1, None) == 1  # T < 0
+    assert d(fake, fake, fake, fake, None, fake, fake, 4, 3, 2, 128, 64, 0, 1.0, 1, None) == 1   # g
+    assert d(fake + 8, fake, fake, fake, fake, fake, fake, 4, 3, 2, 128, 64, 0, 1.0, 1, None) == 1   # state
+    assert d(fake, fake, fake, fake + 1, fake, fake, fake, 4, 3, 2, 128, 64, 1, 1.0, 1, None) == 1   # bf16 v
+    assert d(fake, fake, fake, fake, fake, fake, fake, 4, 0, 2, 128, 64, 0, 1.0, 1, None) == 0   # T = 0
+    assert d(None, None, None, None, None, None, None, 0, 3, 2, 128, 64, 0, 1.0, 1, None) == 0   # N = 0
+
+
 def test_check_device_error_validation(lib):
     assert lib.gdn_check_device_error(None, None) == 1
     assert lib.gdn_check_device_error((1 << 20) + 8, None) == 1

@@ -67,3 +67,81 @@ def test_decode_full_workload_sampled_sequences_and_chunked_agreement():
     torch.cuda.synchronize()
     assert_close(sc, st.double().cpu().numpy(), "bf16", "chunked vs decode state")
     assert_close(oc, perm(O).double().cpu().numpy(), "bf16", "chunked vs decode out")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_beta_up_to_two(dtype):
+    """beta in (0, 2) (negative eigenvalues along k) over 16 steps."""
+    steps = 16
+    d = inputs.make_decode(N=5, H=2, dk=128, dv=128, steps=steps, dtype=dtype, seed=25, beta_max=2.0)
+    dd = cuda(d)
+    st = dd["state0"].clone()
+    ref = d["state0"].double().numpy()
+    for t in range(steps):
+        o = gdn.decode_step(st, dd["q"][t], dd["k"][t], dd["v"][t], dd["g"][t], dd["beta"][t], scale=128 ** -0.5)
+        ro, ref = oracle.decode_step(ref, d["q"][t], d["k"][t], d["v"][t], d["g"][t], d["beta"][t],
+                                     scale=128 ** -0.5, use_qk_l2norm=True)
+        assert_close(o, ro, dtype, f"out step {t}")
+    torch.cuda.synchronize()
+    assert_close(st, ref, dtype, "state")
+
+
+# ---------------------------------------------------------------------------
+# several tokens per call ("Decode 递归": ordered composition of steps)
+# ---------------------------------------------------------------------------
+
+def _multi_inputs(N, T, H, dk, dv, dtype, seed, beta_max=1.0):
+    """Token-major [N, T, H, d] inputs of one multi-token call, from the decode generator."""
+    d = inputs.make_decode(N=N, H=H, dk=dk, dv=dv, steps=T, dtype=dtype, seed=seed, beta_max=beta_max)
+    tm = lambda x: x.transpose(0, 1).contiguous()     # [T, N, ...] -> [N, T, ...]
+    return {"q": tm(d["q"]), "k": tm(d["k"]), "v": tm(d["v"]), "g": tm(d["g"]), "beta": tm(d["beta"]),
+            "state0": d["state0"]}
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T", [1, 2, 4, 7, 16])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 64), (256, 64)])
+def test_decode_multi_against_oracle_and_single_steps(dtype, T, dk, dv):
+    d = _multi_inputs(N=6, T=T, H=3, dk=dk, dv=dv, dtype=dtype, seed=26, beta_max=2.0)
+    dd = cuda(d)
+    scale = dk ** -0.5
+    st = dd["state0"].clone()
+    out = gdn.decode_multi(st, dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], scale=scale)
+    # the same T tokens as T single steps: identical arithmetic per token, so identical bits
+    st1 = dd["state0"].clone()
+    outs = [gdn.decode_step(st1, dd["q"][:, t].contiguous(), dd["k"][:, t].contiguous(),
+                            dd["v"][:, t].contiguous(), dd["g"][:, t].contiguous(),
+                            dd["beta"][:, t].contiguous(), scale=scale) for t in range(T)]
+    torch.cuda.synchronize()
+    assert torch.equal(out, torch.stack(outs, 1))
+    assert torch.equal(st, st1)
+    # and the fp64 recurrence over the T tokens
+    ro, rs = oracle.recurrent_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], init_state=d["state0"],
+                                  scale=scale, use_qk_l2norm=True)
+    assert_close(out, ro, dtype, "out")
+    assert_close(st, rs, dtype, "state")
+
+
+def test_decode_multi_full_size_matches_chunked_forward():
+    """N=256, H=16, d=128, 4 tokens per call x 16 calls against the chunked forward over the same
+    64 tokens, and sampled sequences against the oracle."""
+    N, H, d_, T, calls = 256, 16, 128, 4, 16
+    d = _multi_inputs(N=N, T=T * calls, H=H, dk=d_, dv=d_, dtype="bf16", seed=27)
+    dd = cuda(d)
+    st = dd["state0"].clone()
+    outs = []
+    for c in range(calls):
+        sl = lambda x: x[:, c * T:(c + 1) * T].contiguous()
+        outs.append(gdn.decode_multi(st, sl(dd["q"]), sl(dd["k"]), sl(dd["v"]), sl(dd["g"]), sl(dd["beta"])))
+    O = torch.cat(outs, 1)
+    co, cs = gdn.chunk_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], init_state=dd["state0"],
+                           scale=d_ ** -0.5)
+    torch.cuda.synchronize()
+    assert_close(O, co.float().cpu().double().numpy(), "bf16", "out vs chunked")
+    assert_close(st, cs.cpu().double().numpy(), "bf16", "state vs chunked")
+    for n in (0, 99, 255):
+        sel = lambda x: x[n:n + 1]
+        ro, rs = oracle.recurrent_fwd(sel(d["q"]), sel(d["k"]), sel(d["v"]), sel(d["g"]), sel(d["beta"]),
+                                      init_state=d["state0"][n:n + 1], scale=d_ ** -0.5, use_qk_l2norm=True)
+        assert_close(O[n:n + 1], ro, "bf16", f"out seq {n}")
+        assert_close(st[n:n + 1], rs, "bf16", f"state seq {n}")

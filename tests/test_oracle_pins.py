@@ -368,3 +368,90 @@ def test_rejects_bad_geometry():
     q, k, v, g, beta = rand_inputs(rng, 1, 8, 1, 4, 4)
     with pytest.raises(ValueError):
         oracle.recurrent_fwd(q, k, v, g, beta, cu_seqlens=np.array([0, 5, 7], np.int32))  # does not end at T
+
+
+# --------------------------------------------------------------------------
+# beta in (0, 2): the negative-eigenvalue range (paper page, §2.2, translator's
+# note).  No new arithmetic; these pin the sign structure and the solve.
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("b", [1.3, 1.9, 2.0])
+def test_beta_up_to_two_negative_eigenvalue_along_key(b):
+    """Unit k, v = 0: S_t k = alpha (1 - beta) S_{t-1} k (negative for beta > 1, a reflection at 2)
+    and S_t x = alpha S_{t-1} x for x orthogonal to k."""
+    rng = np.random.default_rng(17)
+    dk, dv = 9, 4
+    st = rng.standard_normal((1, 1, dv, dk))
+    k = rng.standard_normal(dk)
+    k /= np.linalg.norm(k)
+    x = rng.standard_normal(dk)
+    x -= (x @ k) * k
+    alpha = 0.9
+    _, new = oracle.decode_step(st, x[None, None], k[None, None], np.zeros((1, 1, dv)),
+                                np.array([[math.log(alpha)]]), np.array([[b]]))
+    np.testing.assert_allclose(new[0, 0] @ k, alpha * (1 - b) * (st[0, 0] @ k), atol=1e-12)
+    np.testing.assert_allclose(new[0, 0] @ x, alpha * (st[0, 0] @ x), atol=1e-12)
+
+
+def test_beta_up_to_two_is_nonexpansive_without_writes():
+    """With v = 0 and unit keys, ||I - beta k k^T||_2 = max(1, |1 - beta|) = 1 for beta in [0, 2],
+    so the spectral norm of S never grows faster than alpha; beyond 2 it grows by |1 - beta|."""
+    rng = np.random.default_rng(18)
+    dk, dv, steps = 6, 5, 40
+    st = rng.standard_normal((1, 1, dv, dk))
+    for _ in range(steps):
+        k = rng.standard_normal(dk)
+        k /= np.linalg.norm(k)
+        g = -0.05 * abs(rng.standard_normal())
+        b = rng.uniform(0.0, 2.0)
+        _, new = oracle.decode_step(st, k[None, None], k[None, None], np.zeros((1, 1, dv)),
+                                    np.array([[g]]), np.array([[b]]))
+        assert np.linalg.norm(new[0, 0], 2) <= math.exp(g) * np.linalg.norm(st[0, 0], 2) * (1 + 1e-12)
+        st = new
+    # contrast: a rank-one state along k is scaled by exactly alpha |1 - beta| (here 1.5 at beta = 2.5)
+    k = rng.standard_normal(dk)
+    k /= np.linalg.norm(k)
+    s1 = np.outer(rng.standard_normal(dv), k)[None, None]
+    _, new = oracle.decode_step(s1, k[None, None], k[None, None], np.zeros((1, 1, dv)),
+                                np.array([[0.0]]), np.array([[2.5]]))
+    np.testing.assert_allclose(new[0, 0], -1.5 * s1[0, 0], atol=1e-12)
+
+
+@pytest.mark.parametrize("C", [4, 16, 64])
+@pytest.mark.parametrize("w_form", [0, 1])
+def test_chunked_equals_recurrent_beta_up_to_two(C, w_form):
+    rng = np.random.default_rng(19)
+    B, T, H, dk, dv = 1, 70, 2, 8, 5
+    q, k, v, g, beta = rand_inputs(rng, B, T, H, dk, dv, decay=0.5)
+    beta = 2.0 * beta
+    S0 = rng.standard_normal((B, H, dv, dk))
+    o1, s1 = oracle.recurrent_fwd(q, k, v, g, beta, init_state=S0, scale=0.5)
+    o2, s2 = oracle.chunked_fwd(q, k, v, g, beta, init_state=S0, scale=0.5, chunk_size=C, w_form=w_form)
+    np.testing.assert_allclose(o2, o1, atol=1e-9)
+    np.testing.assert_allclose(s2, s1, atol=1e-9)
+
+
+def test_ut_solve_with_nearly_parallel_keys_and_beta_near_two():
+    """The stress case of the (I + L) solve: |L_ij| approaches beta_i |k_i . k_j| ~ 2.  The UT
+    transform still satisfies its defining systems, and the chunked form still equals the recurrence."""
+    rng = np.random.default_rng(20)
+    C, dk, dv = 64, 16, 8
+    base = rng.standard_normal(dk)
+    K = base[None, :] + 0.05 * rng.standard_normal((C, dk))
+    K /= np.linalg.norm(K, axis=1, keepdims=True)
+    V = rng.standard_normal((C, dv))
+    alpha = np.exp(-0.01 * np.abs(rng.standard_normal(C)))
+    beta = rng.uniform(1.8, 2.0, C)
+    W, U = oracle.ut_transform(K, V, alpha, beta, w_form=0)
+    b = np.cumsum(np.log(alpha))
+    Gamma = np.tril(np.exp(b[:, None] - b[None, :]))
+    LG = np.eye(C) + np.tril(np.diag(beta) @ (Gamma * (K @ K.T)), -1)
+    assert np.abs(LG - np.eye(C)).max() > 1.7                     # the regime this test is for
+    np.testing.assert_allclose(LG @ U, beta[:, None] * V, atol=1e-9 * max(1.0, np.abs(U).max()))
+    np.testing.assert_allclose(LG @ W, (beta * np.exp(b))[:, None] * K, atol=1e-9 * max(1.0, np.abs(W).max()))
+    q = rng.standard_normal((1, C, 1, dk))
+    g = np.log(alpha)[None, :, None]
+    o1, s1 = oracle.recurrent_fwd(q, K[None, :, None], V[None, :, None], g, beta[None, :, None])
+    o2, s2 = oracle.chunked_fwd(q, K[None, :, None], V[None, :, None], g, beta[None, :, None], chunk_size=64)
+    np.testing.assert_allclose(o2, o1, atol=1e-8)
+    np.testing.assert_allclose(s2, s1, atol=1e-8)
