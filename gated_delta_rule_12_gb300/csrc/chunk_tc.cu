@@ -68,8 +68,8 @@ constexpr uint32_t U_TPP = 8192;       // T'' (bf16, 8 KB): A of the W~ product;
 constexpr uint32_t U_MT = 24576;       // solve scratch (4 KB), then
 constexpr uint32_t U_TPL = 24576;      // T''_lo (bf16, 8 KB): T'' - T''_hi; its padding rows read U_A
 constexpr uint32_t U_A = 32768;        // L, then T, in place: fp32 [64][LDL]
-constexpr uint32_t U_SC = U_A + 64 * LDL * 4;     // b, beta, rk, rq, cw, ecol, cq[3], misc  [10][64] fp32
-constexpr uint32_t U_BAR = U_SC + 10 * 64 * 4;
+constexpr uint32_t U_SC = U_A + 64 * LDL * 4;     // b, beta, rk, rq, cw, ecol, cq[3], misc, fk  [11][64] fp32
+constexpr uint32_t U_BAR = U_SC + 11 * 64 * 4;
 constexpr uint32_t U_MISC = U_BAR + 8 * 8;
 constexpr uint32_t kSmemUt = U_MISC + 64 + 1024;
 static_assert(U_A % 16 == 0 && U_SC % 16 == 0, "alignment");
@@ -433,6 +433,7 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         float *sc = reinterpret_cast<float *>(sm + U_SC);
         float *bsum = sc, *bet = sc + 64, *rk = sc + 128, *rq = sc + 192, *cw = sc + 256, *ecol = sc + 320;
         float *cq = sc + 384;   // [3][64]: e^{b_m - b_p} rq_m for the block ends p = 15, 31, 47
+        float *fkt = sc + 640;  // fk_r = e^{b_C - b_r} rk_r
         const uint32_t lane_base = tb + ((uint32_t)(32 * (warp & 3)) << 16);
         const uint8_t *st = sm + U_QK;
         if (prow == 0) GDN_UTR(p.trace, 0);
@@ -486,6 +487,7 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                     rk[r] = inv;
                     cw[r] = exp2f(bsum[r | 15] - bsum[r]) * inv;
                     ecol[r] = exp2f(bsum[r]) * inv;
+                    fkt[r] = (r < rows) ? exp2f(bsum[63] - bsum[r]) * inv : 0.f;
                 } else {
                     rq[r] = inv;
 #pragma unroll
@@ -595,63 +597,70 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                             uint32_t w[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) w[e] = pack_bf16(v[hh * 8 + 2 * e], v[hh * 8 + 2 * e + 1]);
-                            *reinterpret_cast<uint4 *>(blk + PB_AQT + sw128_offset(i, q * 16 + hh * 8)) =
+                            *reinterpret_cast<uint4 *>(sm + U_TPP + sw128_offset(i, q * 16 + hh * 8)) =
                                 make_uint4(w[0], w[1], w[2], w[3]);
                         }
                     }
                 }
                 if (prow == 0) GDN_UTR(p.trace, 22);
-            } else {   // K-> = diag(fk) K, written in the K tile's own layout
-                const int r = prow - 64;
-                const float fk = (r < rows) ? exp2f(bsum[63] - bsum[r]) * rk[r] : 0.f;
+            } else {   // K-> = diag(fk) K in the K tile's own layout; 16-B chunk u of the two
+                       // 8-KB tiles per step, so a warp writes 512 contiguous bytes
+                const int t = prow - 64;
+#pragma unroll 4
+                for (int k2 = 0; k2 < 16; ++k2) {
+                    const int u = t + 64 * k2, kb = u >> 9, r = (u >> 3) & 63, pc = u & 7;
+                    const float fk = fkt[r];
+                    const uint4 uu = *reinterpret_cast<const uint4 *>(st + kb * 16384 + r * 128 + pc * 16);
+                    const uint32_t w[4] = {uu.x, uu.y, uu.z, uu.w};
+                    uint32_t o[4];
 #pragma unroll
-                for (int kb = 0; kb < 2; ++kb) {
-                    const uint8_t *src = st + kb * 16384 + r * 128;
-                    uint8_t *dst = blk + PB_KT + kb * 8192 + r * 128;
-#pragma unroll
-                    for (int ch0 = 0; ch0 < 8; ++ch0) {
-                        const int ch = (ch0 ^ r) & 7;
-                        const uint4 uu = *reinterpret_cast<const uint4 *>(src + ch * 16);
-                        const uint32_t w[4] = {uu.x, uu.y, uu.z, uu.w};
-                        uint32_t o[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 x = unpack_bf16(w[e]);
-                            o[e] = pack_bf16(x.x * fk, x.y * fk);
-                        }
-                        *reinterpret_cast<uint4 *>(dst + ch * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 x = unpack_bf16(w[e]);
+                        o[e] = pack_bf16(x.x * fk, x.y * fk);
                     }
+                    *reinterpret_cast<uint4 *>(blk + PB_KT + kb * 8192 + r * 128 + pc * 16) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
                 if (prow == 64) GDN_UTR(p.trace, 23);
             }
             fence_before_sync();
             if (group_sync_or(2, 128, !ok || *abort_flag)) break;
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2) {   // Aqk^T: staging tile -> workspace, 512 B per warp store
+                const int o = 16 * (prow + 128 * k2);
+                *reinterpret_cast<uint4 *>(blk + PB_AQT + o) = *reinterpret_cast<const uint4 *>(sm + U_TPP + o);
+            }
             if (prow == 0) GDN_UTR(p.trace, 8);
 
             // (4) T = (I + L)^{-1} in place;  T' -> workspace,  T'' -> shared memory
             solve_in_place(Am, Mt, (warp + 3) & 3, lane, p.trace);
             if (prow == 0) GDN_UTR(p.trace, 16);
-            {
-                const int r = prow >> 1, i0 = (prow & 1) * 32;
+            {   // 16-B chunk u = (row r, physical chunk pc) per step: consecutive threads write
+                // consecutive bytes of T' (and of T''); columns ib..ib+7 of row r
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    const int ib = i0 + ch * 8;
+                for (int k2 = 0; k2 < 4; ++k2) {
+                    const int u = prow + 128 * k2, r = u >> 3, pc = u & 7, ib = 8 * (pc ^ (r & 7));
                     const float4 t0 = *reinterpret_cast<const float4 *>(Am + r * LDL + ib);
                     const float4 t1 = *reinterpret_cast<const float4 *>(Am + r * LDL + ib + 4);
+                    const float4 b0 = *reinterpret_cast<const float4 *>(bet + ib);
+                    const float4 b1 = *reinterpret_cast<const float4 *>(bet + ib + 4);
+                    const float4 e0 = *reinterpret_cast<const float4 *>(ecol + ib);
+                    const float4 e1 = *reinterpret_cast<const float4 *>(ecol + ib + 4);
                     const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+                    const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                    const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
                     uint32_t w1[4], w2[4], w3[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float p0 = tv[2 * e] * bet[ib + 2 * e], p1 = tv[2 * e + 1] * bet[ib + 2 * e + 1];
+                        const float p0 = tv[2 * e] * bv[2 * e], p1 = tv[2 * e + 1] * bv[2 * e + 1];
                         w1[e] = pack_bf16(p0, p1);
                         // T'' as a sum of two bf16 terms: W~ = T'' K can cancel heavily (nearly
                         // parallel keys), so its operand carries ~16 bits
-                        const float t0 = p0 * ecol[ib + 2 * e], t1 = p1 * ecol[ib + 2 * e + 1];
-                        w2[e] = pack_bf16(t0, t1);
+                        const float q0 = p0 * ev[2 * e], q1 = p1 * ev[2 * e + 1];
+                        w2[e] = pack_bf16(q0, q1);
                         const float2 h2 = unpack_bf16(w2[e]);
-                        w3[e] = pack_bf16(t0 - h2.x, t1 - h2.y);
+                        w3[e] = pack_bf16(q0 - h2.x, q1 - h2.y);
                     }
-                    const uint32_t off = sw128_offset(r, ib);
+                    const uint32_t off = (uint32_t)(r * 128 + pc * 16);   // = sw128_offset(r, ib)
                     *reinterpret_cast<uint4 *>(blk + PB_TP + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
                     *reinterpret_cast<uint4 *>(sm + U_TPP + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
                     *reinterpret_cast<uint4 *>(sm + U_TPL + off) = make_uint4(w3[0], w3[1], w3[2], w3[3]);
@@ -669,7 +678,7 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 if (prow < 64) {
                     reinterpret_cast<float *>(blk + PB_SC)[r] = (r < rows) ? exp2f(bsum[r]) * rq[r] : 0.f;
                 } else {
-                    reinterpret_cast<float *>(blk + PB_SC)[64 + r] = (r < rows) ? exp2f(bC - bsum[r]) * rk[r] : 0.f;
+                    reinterpret_cast<float *>(blk + PB_SC)[64 + r] = fkt[r];
                     if (r == 0) reinterpret_cast<float *>(blk + PB_SC)[128] = exp2f(bC);
                 }
             }
@@ -677,7 +686,8 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
             ok = wait_bar(bar(UB_P2), 0, abort_flag, p.err);
             if (prow == 0) GDN_UTR(p.trace, 19);
             fence_after_sync();
-            if (prow < 64) {   // row r of W~ (128 d), K-major tiles of 64 d
+            if (prow < 64) {   // row r of W~ (128 d) -> staging [d-block][64 r][64 d] in the dead T area
+                uint8_t *wst = sm + U_A;
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     uint32_t u[16];
@@ -690,10 +700,16 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                         for (int e = 0; e < 4; ++e)
                             w[e] = pack_bf16(__uint_as_float(u[hh * 8 + 2 * e]), __uint_as_float(u[hh * 8 + 2 * e + 1]));
                         const int d = q * 16 + hh * 8;
-                        *reinterpret_cast<uint4 *>(blk + PB_W + (d >> 6) * 8192 + sw128_offset(prow, d & 63)) =
+                        *reinterpret_cast<uint4 *>(wst + (d >> 6) * 8192 + sw128_offset(prow, d & 63)) =
                             make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
+            }
+            if (group_sync_or(2, 128, !ok || *abort_flag)) break;
+#pragma unroll
+            for (int k2 = 0; k2 < 8; ++k2) {   // W~: staging -> workspace, 512 B per warp store
+                const int o = 16 * (prow + 128 * k2);
+                *reinterpret_cast<uint4 *>(blk + PB_W + o) = *reinterpret_cast<const uint4 *>(sm + U_A + o);
             }
             fence_before_sync();
         } while (false);
