@@ -41,6 +41,7 @@ METRIC = "tokens/s chunked fwd (H=16,d=128,L=2048) + decode steps/s; % roofline"
 PREFILL = "prefill_b4_h16_l2048_d128_bf16"
 DECODE = "decode_n256_h16_d128_bf16"
 MULTI_T = 4          # tokens per call of the multi-token decode line
+PROLOGUE_K = 4       # short-convolution width of the prologue line
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
@@ -366,6 +367,10 @@ def bench_ours(args):
     mbytes = decode_multi_algorithmic_bytes(wd, MULTI_T)
     m_ach = mbytes / (mms * 1e-3) / 1e9
 
+    # block prologue (short conv + SiLU for q, k, v; gate activations) on the bench shape
+    pro = bench_prologue(w, dev, flush, stream, reps, peaks)
+    pro["value"] = job_throughput(w.B * w.L, ws_n, max_over_ranks(dist, pro["ms_per_call"]))
+
     if rank == 0:
         cpu = cpu_baseline(w) if ws_n == 1 else None
         line = {
@@ -393,6 +398,7 @@ def bench_ours(args):
                              "roofline": {"bound": "hbm", "achieved": m_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                           "frac": m_ach / peaks["hbm_gbs"], "algorithmic_bytes": mbytes},
                              "timing": f"{wd.steps} tokens as {calls} calls in one CUDA graph, median of {reps}"},
+            "prologue": pro,
             "gpu_launches": args.steps * launches_per_step,
             "clocks": clocks,
             "cpu_baseline": cpu,
@@ -400,6 +406,48 @@ def bench_ours(args):
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def bench_prologue(w: inputs.Workload, dev, flush, stream, reps: int, peaks, K: int = PROLOGUE_K):
+    """One gdn_prologue call on the workload's shape: raw projections in, q, k, v, g, beta out."""
+    import gated_delta_rule_12_gb300 as gdn
+    gen = torch.Generator().manual_seed(w.seed + 100)
+    rn = lambda *shape: torch.randn(shape, generator=gen, dtype=torch.float32)
+    B, T, H, dk, dv = w.B, w.L, w.H, w.dk, w.dv
+    x = [rn(B, T, H, dk).to(torch.bfloat16).to(dev), rn(B, T, H, dk).to(torch.bfloat16).to(dev),
+         rn(B, T, H, dv).to(torch.bfloat16).to(dev)]
+    wts = [(0.5 * rn(H, dk, K)).to(dev), (0.5 * rn(H, dk, K)).to(dev), (0.5 * rn(H, dv, K)).to(dev)]
+    ab = [rn(B, T, H).to(dev), rn(B, T, H).to(dev)]
+    par = [(0.5 * rn(H)).to(dev), (0.5 * rn(H)).to(dev)]
+    s_in = torch.zeros((B, K - 1, H, 2 * dk + dv), dtype=torch.bfloat16, device=dev)
+    s_out = torch.empty_like(s_in)
+    outs = (torch.empty_like(x[0]), torch.empty_like(x[1]), torch.empty_like(x[2]),
+            torch.empty((B, T, H), dtype=torch.float32, device=dev),
+            torch.empty((B, T, H), dtype=torch.float32, device=dev))
+
+    def call():
+        gdn.prologue(*x, *wts, *ab, *par, conv_state_in=s_in, conv_state_out=s_out, out=outs)
+
+    for _ in range(3):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    t = []
+    for _ in range(max(reps, 5)):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        t.append(a.elapsed_time(b))
+    ms = statistics.median(t)
+    nbytes = B * T * H * ((2 * dk + dv) * 2 * 2 + 16) + 2 * B * (K - 1) * H * (2 * dk + dv) * 2
+    ach = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"{PREFILL} projections, conv width {K}", "unit": "tokens/s", "ms_per_call": ms,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / peaks["hbm_gbs"], "algorithmic_bytes": nbytes},
+            "timing": f"median of {max(reps, 5)} calls, L2 flushed before each"}
 
 
 # ---------------------------------------------------------------------------

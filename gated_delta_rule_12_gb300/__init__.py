@@ -11,6 +11,7 @@ Entry points (same names as the C ABI, without the ``gdn_`` prefix):
     chunk_fwd(q, k, v, g, beta, ...)      -> (out, final_state)
     decode_step(state, q, k, v, g, beta)  -> out            (state updated in place)
     decode_multi(state, q, k, v, g, beta) -> out [N,T,H,dv] (T tokens per call, state in place)
+    prologue(xq, xk, xv, wq, wk, wv, a, b, A_log, dt_bias, ...) -> (q, k, v, g, beta)
     chunk_fwd_workspace_size(...)         -> bytes
     chunk_fwd_kernel_count(...)           -> kernels one chunk_fwd call launches
     check_device_error(workspace)         -> None or raises
@@ -33,7 +34,7 @@ GDN_F32, GDN_BF16 = 0, 1
 CHUNK = 64
 
 EXPORTS = ["gdn_status_string", "gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd_kernel_count", "gdn_chunk_fwd",
-           "gdn_decode_step", "gdn_decode_multi", "gdn_check_device_error", "gdn_chunk_fwd_noalloc"]
+           "gdn_decode_step", "gdn_decode_multi", "gdn_prologue", "gdn_check_device_error", "gdn_chunk_fwd_noalloc"]
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -81,6 +82,8 @@ def load_library(path: str = LIB_PATH, build_if_missing: bool = False) -> ctypes
         lib.gdn_decode_multi.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                          _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _f32, _i32, _vp]
         lib.gdn_decode_multi.restype = ctypes.c_int
+        lib.gdn_prologue.argtypes = [_vp] * 12 + [_vp, _i32] + [_vp] * 5 + [_i32] * 6 + [ctypes.c_int, _vp]
+        lib.gdn_prologue.restype = ctypes.c_int
         lib.gdn_check_device_error.argtypes = [_vp, _vp]
         lib.gdn_check_device_error.restype = ctypes.c_int
         lib.gdn_chunk_fwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
@@ -215,6 +218,41 @@ def decode_multi(state, q, k, v, g, beta, scale=None, use_qk_l2norm=True, out=No
     if rc != GDN_OK:
         raise GDNError(rc, "gdn_decode_multi")
     return out
+
+
+def prologue(xq, xk, xv, wq, wk, wv, a, b, A_log, dt_bias, conv_state_in=None, conv_state_out=None,
+             cu_seqlens=None, out=None, stream=None):
+    """Block prologue (``gdn_prologue``): q, k, v = SiLU(short causal conv of the projections),
+    g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b), in one pass.
+
+    xq, xk [B,T,H,dk], xv [B,T,H,dv] (fp32 or bf16); wq, wk [H,dk,K], wv [H,dv,K] fp32;
+    a, b [B,T,H] fp32; A_log, dt_bias [H] fp32; conv states [N,K-1,H,2dk+dv] (dtype of x) or None.
+    Returns ``(q, k, v, g, beta)``; ``out`` may pass those five tensors preallocated.
+    """
+    lib = load_library()
+    B, T, H, dk = xq.shape
+    dv = xv.shape[-1]
+    K = wq.shape[-1]
+    if out is None:
+        out = (torch.empty_like(xq), torch.empty_like(xk), torch.empty_like(xv),
+               torch.empty((B, T, H), dtype=torch.float32, device=xq.device),
+               torch.empty((B, T, H), dtype=torch.float32, device=xq.device))
+    q, k, v, g, beta = out
+    for t in (wq, wk, wv, a, b, A_log, dt_bias, g, beta):
+        if t.dtype != torch.float32:
+            raise TypeError("filters, gate projections, gate parameters and g, beta must be float32")
+    if wq.shape != (H, dk, K) or wk.shape != (H, dk, K) or wv.shape != (H, dv, K):
+        raise ValueError("prologue: filters must be [H, d, K]")
+    _need_cuda(xq, xk, xv, wq, wk, wv, a, b, A_log, dt_bias, conv_state_in, conv_state_out, cu_seqlens,
+               q, k, v, g, beta)
+    num_seqs = (cu_seqlens.numel() - 1) if cu_seqlens is not None else 0
+    rc = lib.gdn_prologue(_ptr(xq), _ptr(xk), _ptr(xv), _ptr(wq), _ptr(wk), _ptr(wv), _ptr(a), _ptr(b),
+                          _ptr(A_log), _ptr(dt_bias), _ptr(conv_state_in), _ptr(conv_state_out),
+                          _ptr(cu_seqlens), num_seqs, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                          B, T, H, dk, dv, K, _dt(xq), _stream(stream))
+    if rc != GDN_OK:
+        raise GDNError(rc, "gdn_prologue")
+    return q, k, v, g, beta
 
 
 def check_device_error(workspace, stream=None):

@@ -147,6 +147,52 @@ gdn_status gdn_decode_multi(float *state, const void *q, const void *k, const vo
     return decode_common(state, q, k, v, g, beta, out, N, T, H, dk, dv, dt, scale, use_qk_l2norm, stream);
 }
 
+gdn_status gdn_prologue(const void *xq, const void *xk, const void *xv, const float *wq, const float *wk,
+                        const float *wv, const float *a, const float *b, const float *A_log,
+                        const float *dt_bias, const void *conv_state_in, void *conv_state_out,
+                        const int32_t *cu_seqlens, int32_t num_seqs, void *q, void *k, void *v, float *g,
+                        float *beta, int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, int32_t K,
+                        gdn_dtype dt, void *stream)
+{
+    if (B < 1 || T < 0 || H < 1 || dk < 1 || dv < 1) return GDN_ERR_INVALID_ARG;
+    if (dt != GDN_F32 && dt != GDN_BF16) return GDN_ERR_INVALID_ARG;
+    if (K < 1 || K > 4 || dk % 8 != 0 || dv % 8 != 0 || dk > 256 || dv > 256) return GDN_ERR_UNSUPPORTED;
+    const bool varlen = cu_seqlens != nullptr;
+    if (varlen && (B != 1 || num_seqs < 1)) return GDN_ERR_INVALID_ARG;
+    if (!varlen && num_seqs != 0 && num_seqs != B) return GDN_ERR_INVALID_ARG;
+    const int N = varlen ? num_seqs : B;
+    if ((int64_t)B * T * H >= ((int64_t)1 << 40)) return GDN_ERR_INVALID_ARG;
+    const bool have_tokens = (int64_t)B * T > 0;
+    if (have_tokens) {
+        const void *need[] = {xq, xk, xv, wq, wk, wv, a, b, A_log, dt_bias, q, k, v, g, beta};
+        for (const void *p : need)
+            if (!p) return GDN_ERR_INVALID_ARG;
+    }
+    const void *al16[] = {xq, xk, xv, q, k, v, conv_state_in, conv_state_out};
+    for (const void *p : al16)
+        if (p && !aligned16(p)) return GDN_ERR_INVALID_ARG;
+    const void *al4[] = {wq, wk, wv, a, b, A_log, dt_bias, g, beta, cu_seqlens};
+    for (const void *p : al4)
+        if (p && !aligned_to(p, 4)) return GDN_ERR_INVALID_ARG;
+    if (conv_state_in && conv_state_out && K > 1) {   // the two state buffers must not overlap
+        const size_t bytes = (size_t)N * (K - 1) * H * (2 * dk + dv) * (dt == GDN_BF16 ? 2 : 4);
+        const uintptr_t i0 = (uintptr_t)conv_state_in, o0 = (uintptr_t)conv_state_out;
+        if (i0 < o0 + bytes && o0 < i0 + bytes) return GDN_ERR_INVALID_ARG;
+    }
+    if (!have_tokens && !conv_state_out) return GDN_OK;
+    PrologueArgs pa;
+    pa.xq = xq; pa.xk = xk; pa.xv = xv; pa.wq = wq; pa.wk = wk; pa.wv = wv;
+    pa.a = a; pa.b = b; pa.A_log = A_log; pa.dt_bias = dt_bias;
+    pa.state_in = K > 1 ? conv_state_in : nullptr;
+    pa.state_out = K > 1 ? conv_state_out : nullptr;
+    pa.cu = cu_seqlens;
+    pa.q = q; pa.k = k; pa.v = v; pa.g = g; pa.beta = beta;
+    pa.B = B; pa.T = T; pa.H = H; pa.dk = dk; pa.dv = dv; pa.N = N; pa.K = K;
+    pa.dt = (dt == GDN_BF16) ? 1 : 0;
+    cudaError_t e = launch_prologue(pa, (cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 gdn_status gdn_check_device_error(void *workspace, void *stream)
 {
     if (!workspace || ((uintptr_t)workspace & 255u) != 0) return GDN_ERR_INVALID_ARG;

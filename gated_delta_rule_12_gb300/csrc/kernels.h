@@ -33,7 +33,20 @@ struct DecodeArgs {
     int l2;
 };
 
+struct PrologueArgs {
+    const void *xq, *xk, *xv;                 // raw projections [B, T, H, dk|dk|dv], dtype dt
+    const float *wq, *wk, *wv;                // convolution filters [H, d, K]
+    const float *a, *b, *A_log, *dt_bias;     // gate projections [B, T, H]; per-head parameters [H]
+    const void *state_in;                     // [N, K-1, H, 2 dk + dv] dtype dt, or null
+    void *state_out;                          // same layout, or null
+    const int32_t *cu;                        // [N + 1] or null
+    void *q, *k, *v;                          // outputs [B, T, H, dk|dk|dv], dtype dt
+    float *g, *beta;                          // outputs [B, T, H]
+    int B, T, H, dk, dv, N, K, dt;
+};
+
 cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t st);
+cudaError_t launch_prologue(const PrologueArgs &a, cudaStream_t st);
 bool chunk_tc_supported(int dt, int dk, int dv, int64_t tokens);
 size_t chunk_tc_workspace_bytes(int64_t slots, int H);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st);

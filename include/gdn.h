@@ -168,6 +168,40 @@ gdn_status gdn_decode_multi(float *state,
 gdn_status gdn_check_device_error(void *workspace, void *stream);
 
 /*
+ * Block prologue: q, k, v, g, beta from their linear projections, in one pass.
+ * "Gated Delta Networks: Improving Mamba2 with Delta Rule", §3.4 "Token mixing
+ * block" and Fig. 1: q, k, v = SiLU(short causal depthwise convolution of the
+ * projection); alpha from its projection in Mamba2's parameterisation, beta
+ * from its projection through a sigmoid:
+ *     y_t    = silu(sum_{j<K} w[h][c][j] x_{t-K+1+j})   (tap K-1: current token)
+ *     g_t    = log alpha_t = -exp(A_log[h]) softplus(a_t + dt_bias[h])
+ *     beta_t = 1 / (1 + exp(-b_t))
+ * The outputs are the q, k, v, g, beta of gdn_chunk_fwd / gdn_decode_multi
+ * (whose use_qk_l2norm applies the L2 normalisation of q and k).
+ *   xq, xk        [B, T, H, dk] dtype dt;  xv [B, T, H, dv] dtype dt.
+ *   wq, wk        [H, dk, K] fp32;  wv [H, dv, K] fp32 (one filter per channel).
+ *   a, b          [B, T, H] fp32;  A_log, dt_bias [H] fp32.
+ *   conv_state_in [N, K-1, H, 2 dk + dv] dtype dt: the K-1 inputs before each
+ *                 sequence (oldest first; channels ordered q, k, v), or NULL
+ *                 for zeros.  conv_state_out, same layout, receives the K-1
+ *                 most recent inputs of each sequence (NULL to skip); it must
+ *                 not overlap conv_state_in.
+ *   cu_seqlens    as gdn_chunk_fwd (NULL: N = B sequences of T tokens).
+ *   q, k, v       outputs [B, T, H, dk|dk|dv] dtype dt;  g, beta [B, T, H] fp32.
+ *   K in 1..4; dk, dv multiples of 8 up to 256; x*, q, k, v and the states
+ *   16-byte aligned, the fp32 arrays 4-byte aligned.
+ * Errors: GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA.
+ */
+gdn_status gdn_prologue(const void *xq, const void *xk, const void *xv,
+                        const float *wq, const float *wk, const float *wv,
+                        const float *a, const float *b, const float *A_log, const float *dt_bias,
+                        const void *conv_state_in, void *conv_state_out,
+                        const int32_t *cu_seqlens, int32_t num_seqs,
+                        void *q, void *k, void *v, float *g, float *beta,
+                        int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, int32_t K,
+                        gdn_dtype dt, void *stream);
+
+/*
  * gdn_chunk_fwd_noalloc -- gdn_chunk_fwd for callers that cannot allocate.
  * The pages have no counterpart of this call: it exists for callers that may
  * not call cudaMalloc or any allocating routine where they run the operator

@@ -58,6 +58,10 @@ def _load():
                                                _i32, _i32, _i32, _i32, _i32,
                                                ctypes.c_double, _i32, _i32, _i32, _i32]
             lib.oracle_chunked_fwd.restype = ctypes.c_int
+            lib.oracle_short_conv_silu.argtypes = [_D, _D, _D, _I32P, _i32, _i32, _i32, _i32, _i32, _i32, _D, _D]
+            lib.oracle_short_conv_silu.restype = ctypes.c_int
+            lib.oracle_gate_activations.argtypes = [_D, _D, _D, _D, ctypes.c_int64, _i32, _D, _D]
+            lib.oracle_gate_activations.restype = ctypes.c_int
             lib.oracle_decode_step.argtypes = [_D, _D, _D, _D, _D, _D, _D,
                                                _i32, _i32, _i32, _i32,
                                                ctypes.c_double, _i32, _i32]
@@ -182,3 +186,44 @@ def ut_transform(K, V, alpha, beta, w_form=0):
                                      int(w_form), _ptr(W), _ptr(U))
     _check(rc, "ut_transform")
     return W, U
+
+
+def short_conv_silu(x, w, state_in=None, cu_seqlens=None):
+    """Block prologue of one of q, k, v: short causal depthwise convolution, then SiLU.
+
+    x [B,T,H,d]; w [H,d,K] (tap K-1 multiplies the current token); state_in
+    [N,K-1,H,d] (the K-1 inputs before each sequence, oldest first) or None for
+    zeros.  Returns ``(y [B,T,H,d], state_out [N,K-1,H,d])``.
+    """
+    x, w = _f64(x), _f64(w)
+    B, T, H, d = x.shape
+    K = w.shape[-1]
+    if w.shape != (H, d, K):
+        raise ValueError("oracle: w must be [H, d, K]")
+    cu, cup = _cu(cu_seqlens)
+    N = (len(cu) - 1) if cu is not None else B
+    si = _f64(state_in)
+    if si is not None and si.shape != (N, K - 1, H, d):
+        raise ValueError("oracle: state_in must be [N, K-1, H, d]")
+    y = np.zeros_like(x)
+    so = np.zeros((N, K - 1, H, d), np.float64)
+    rc = _load().oracle_short_conv_silu(_ptr(x), _ptr(w), _ptr(si), cup, N, B, T, H, d, K, _ptr(y), _ptr(so))
+    _check(rc, "short_conv_silu")
+    return y, so
+
+
+def gate_activations(a, b, A_log, dt_bias):
+    """alpha (as g = log alpha) in Mamba2's parameterisation and beta = sigmoid(b).
+
+    a, b [..., H]; A_log, dt_bias [H].  Returns ``(g, beta)`` shaped like a.
+    """
+    a, b, A_log, dt_bias = _f64(a), _f64(b), _f64(A_log), _f64(dt_bias)
+    H = a.shape[-1]
+    if b.shape != a.shape or A_log.shape != (H,) or dt_bias.shape != (H,):
+        raise ValueError("oracle: gate shapes")
+    g = np.zeros_like(a)
+    beta = np.zeros_like(a)
+    rc = _load().oracle_gate_activations(_ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), a.size // H, H,
+                                         _ptr(g), _ptr(beta))
+    _check(rc, "gate_activations")
+    return g, beta

@@ -38,6 +38,12 @@
  *                          independent algorithm used to cross-check the
  *                          definition and to debug stage by stage.
  *   oracle_ut_transform    the per-chunk UT transform alone (W and U~).
+ *   oracle_short_conv_silu the block prologue of q, k, v: short causal
+ *                          depthwise convolution then SiLU ([paper] §3.4
+ *                          "Token mixing block" and Fig. 1).
+ *   oracle_gate_activations alpha in Mamba2's parameterisation and beta by a
+ *                          sigmoid, from their linear projections (same
+ *                          section).
  */
 #include <math.h>
 #include <pthread.h>
@@ -480,3 +486,75 @@ int oracle_chunked_fwd(const double *q, const double *k, const double *v,
 }
 
 int oracle_num_threads(void) { return resolve_threads(0); }
+
+
+/* ------------------------------------------------------------------ */
+/* Block prologue ([paper] §3.4 "Token mixing block", Fig. 1)          */
+/* ------------------------------------------------------------------ */
+
+/*
+ * q, k, v are produced from their linear projections x by a short causal
+ * convolution (depthwise: one filter of K taps per channel) followed by SiLU.
+ * Readings (the page gives neither): tap j of the filter multiplies
+ * x_{t-K+1+j}, so tap K-1 is the current token; no bias.  Before the first
+ * token of a sequence the history comes from state_in (the K-1 most recent
+ * earlier inputs, oldest first) or is zero.  state_out receives the K-1 most
+ * recent inputs of each sequence in the same layout.
+ *
+ *   x          [B, T, H, d]        raw projections of one of q, k, v
+ *   w          [H, d, K]
+ *   state_in   [N, K-1, H, d] or NULL;  state_out [N, K-1, H, d] or NULL
+ *   y          [B, T, H, d]        silu(conv(x))
+ */
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+int oracle_short_conv_silu(const double *x, const double *w, const double *state_in, const int32_t *cu,
+                           int32_t N, int32_t B, int32_t T, int32_t H, int32_t d, int32_t K,
+                           double *y, double *state_out)
+{
+    if (B < 1 || T < 0 || H < 1 || d < 1 || K < 1) return -1;
+    if (cu && B != 1) return -1;
+    if (!cu) N = B;
+    geom_t gm = {B, T, H, d, d, N, cu};
+    if (cu && check_geom(&gm) != 0) return -1;
+    const int64_t HD = (int64_t)H * d;
+    for (int n = 0; n < N; ++n) {
+        int64_t row0, len;
+        seq_span(&gm, n, &row0, &len);
+        for (int64_t hc = 0; hc < HD; ++hc) {
+            /* value of the input at position p (relative to the sequence start) */
+#define XAT(p) ((p) >= 0 ? x[(row0 + (p)) * HD + hc]                                              \
+                         : (state_in ? state_in[((int64_t)n * (K - 1) + (K - 1) + (p)) * HD + hc] : 0.0))
+            for (int64_t t = 0; t < len; ++t) {
+                double z = 0.0;
+                for (int j = 0; j < K; ++j) z += w[hc * K + j] * XAT(t - (K - 1) + j);
+                y[(row0 + t) * HD + hc] = silu(z);
+            }
+            if (state_out)
+                for (int m = 0; m < K - 1; ++m)
+                    state_out[((int64_t)n * (K - 1) + m) * HD + hc] = XAT(len - (K - 1) + m);
+#undef XAT
+        }
+    }
+    return 0;
+}
+
+/*
+ * alpha in Mamba2's parameterisation and beta by a sigmoid ([paper] §3.4: alpha
+ * and beta come from linear projections only, alpha "with Mamba2's
+ * parameterisation"):  g = log alpha = -exp(A_log[h]) * softplus(a + dt_bias[h]),
+ * beta = sigmoid(b).   a, b, g, beta [B, T, H];  A_log, dt_bias [H].
+ */
+static double softplus(double z) { return z > 30.0 ? z : log1p(exp(z)); }
+
+int oracle_gate_activations(const double *a, const double *b, const double *A_log, const double *dt_bias,
+                            int64_t BT, int32_t H, double *g, double *beta)
+{
+    for (int64_t t = 0; t < BT; ++t)
+        for (int h = 0; h < H; ++h) {
+            const int64_t i = t * H + h;
+            g[i] = -exp(A_log[h]) * softplus(a[i] + dt_bias[h]);
+            beta[i] = 1.0 / (1.0 + exp(-b[i]));
+        }
+    return 0;
+}

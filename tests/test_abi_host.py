@@ -136,6 +136,30 @@ def test_decode_multi_validation(lib):
     assert d(None, None, None, None, None, None, None, 0, 3, 2, 128, 64, 0, 1.0, 1, None) == 0   # N = 0
 
 
+def test_prologue_validation(lib):
+    fake = 1 << 20
+    P = lib.gdn_prologue
+
+    def call(**o):
+        a = dict(xq=fake, xk=fake, xv=fake, wq=fake, wk=fake, wv=fake, ga=fake, gb=fake, al=fake, dtb=fake,
+                 si=None, so=None, cu=None, nseq=0, q=fake, k=fake, v=fake, g=fake, beta=fake,
+                 B=2, T=64, H=2, dk=64, dv=64, K=4, dt=gdn.GDN_BF16)
+        a.update(o)
+        return P(a["xq"], a["xk"], a["xv"], a["wq"], a["wk"], a["wv"], a["ga"], a["gb"], a["al"], a["dtb"],
+                 a["si"], a["so"], a["cu"], a["nseq"], a["q"], a["k"], a["v"], a["g"], a["beta"],
+                 a["B"], a["T"], a["H"], a["dk"], a["dv"], a["K"], a["dt"], None)
+
+    assert call(K=5) == 2 and call(K=0) == 2          # filter width 1..4
+    assert call(dk=12) == 2 and call(dv=264) == 2    # multiples of 8 up to 256
+    assert call(xq=fake + 8) == 1                    # 16-byte aligned projections
+    assert call(g=fake + 2) == 1                     # 4-byte aligned fp32 arrays
+    assert call(wq=None) == 1
+    assert call(cu=fake, nseq=2) == 1                # varlen needs B == 1
+    bytes_ = 2 * 3 * 2 * (2 * 64 + 64) * 2
+    assert call(si=fake, so=fake + bytes_ - 16) == 1   # overlapping convolution states
+    assert call(T=0, so=None) == 0                   # nothing to do
+
+
 def test_check_device_error_validation(lib):
     assert lib.gdn_check_device_error(None, None) == 1
     assert lib.gdn_check_device_error((1 << 20) + 8, None) == 1
