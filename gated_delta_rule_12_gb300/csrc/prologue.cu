@@ -52,7 +52,7 @@ __device__ __forceinline__ float softplus(float z) { return z > 20.f ? z : log1p
 // 2 cp, 2 cp + 1 of the concatenated [q | k | v] channel axis of head h.
 template <typename T, int K>
 __global__ void __launch_bounds__(kThreads)
-prologue_kernel(const PrologueArgs p)
+block_prologue_kernel(const PrologueArgs p)
 {
     constexpr int KH = K > 1 ? K - 1 : 1;   // history registers (unused when K == 1)
     const int H = p.H, dk = p.dk, dv = p.dv, Cw = 2 * dk + dv, G = Cw / 2;
@@ -185,10 +185,10 @@ cudaError_t launch_typed(const PrologueArgs &a, cudaStream_t st)
     const int64_t items = strips * a.H * ((2 * a.dk + a.dv) / 2);
     const unsigned blocks = (unsigned)((items + kThreads - 1) / kThreads);
     switch (a.K) {
-        case 1: prologue_kernel<T, 1><<<blocks, kThreads, 0, st>>>(a); break;
-        case 2: prologue_kernel<T, 2><<<blocks, kThreads, 0, st>>>(a); break;
-        case 3: prologue_kernel<T, 3><<<blocks, kThreads, 0, st>>>(a); break;
-        default: prologue_kernel<T, 4><<<blocks, kThreads, 0, st>>>(a); break;
+        case 1: block_prologue_kernel<T, 1><<<blocks, kThreads, 0, st>>>(a); break;
+        case 2: block_prologue_kernel<T, 2><<<blocks, kThreads, 0, st>>>(a); break;
+        case 3: block_prologue_kernel<T, 3><<<blocks, kThreads, 0, st>>>(a); break;
+        default: block_prologue_kernel<T, 4><<<blocks, kThreads, 0, st>>>(a); break;
     }
     return cudaGetLastError();
 }
