@@ -58,6 +58,10 @@ def _load():
                                                _i32, _i32, _i32, _i32, _i32,
                                                ctypes.c_double, _i32, _i32, _i32, _i32]
             lib.oracle_chunked_fwd.restype = ctypes.c_int
+            lib.oracle_recurrent_bwd.argtypes = [_D, _D, _D, _D, _D, _D, _I32P, _i32, _D, _D,
+                                                 _D, _D, _D, _D, _D, _D,
+                                                 _i32, _i32, _i32, _i32, _i32, ctypes.c_double, _i32, _i32]
+            lib.oracle_recurrent_bwd.restype = ctypes.c_int
             lib.oracle_short_conv_silu.argtypes = [_D, _D, _D, _I32P, _i32, _i32, _i32, _i32, _i32, _i32, _D, _D]
             lib.oracle_short_conv_silu.restype = ctypes.c_int
             lib.oracle_gate_activations.argtypes = [_D, _D, _D, _D, ctypes.c_int64, _i32, _D, _D]
@@ -186,6 +190,29 @@ def ut_transform(K, V, alpha, beta, w_form=0):
                                      int(w_form), _ptr(W), _ptr(U))
     _check(rc, "ut_transform")
     return W, U
+
+
+def recurrent_bwd(q, k, v, g, beta, dout, init_state=None, dfinal=None, cu_seqlens=None, scale=1.0,
+                  use_qk_l2norm=False, nthreads=0):
+    """Gradients of the token recurrence (reverse mode) for the loss
+    sum(dout * out) + sum(dfinal * final_state).
+
+    Returns a dict with dq, dk [B,T,H,dk], dv [B,T,H,dv], dg, dbeta [B,T,H] and dinit [N,H,dv,dk].
+    """
+    q, k, v, g, beta, s0, cu, cup, B, T, H, dk, dv, N = _prep(q, k, v, g, beta, init_state, cu_seqlens)
+    dout = _f64(dout)
+    dsf = _f64(dfinal)
+    if dout.shape != (B, T, H, dv) or (dsf is not None and dsf.shape != (N, H, dv, dk)):
+        raise ValueError("oracle: dout must be [B,T,H,dv] and dfinal [N,H,dv,dk]")
+    r = {n: np.zeros(shape, np.float64) for n, shape in (("dq", (B, T, H, dk)), ("dk", (B, T, H, dk)),
+                                                          ("dv", (B, T, H, dv)), ("dg", (B, T, H)),
+                                                          ("dbeta", (B, T, H)), ("dinit", (N, H, dv, dk)))}
+    rc = _load().oracle_recurrent_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(s0), cup, N,
+                                      _ptr(dout), _ptr(dsf), _ptr(r["dq"]), _ptr(r["dk"]), _ptr(r["dv"]),
+                                      _ptr(r["dg"]), _ptr(r["dbeta"]), _ptr(r["dinit"]), B, T, H, dk, dv,
+                                      float(scale), int(bool(use_qk_l2norm)), int(nthreads))
+    _check(rc, "recurrent_bwd")
+    return r
 
 
 def short_conv_silu(x, w, state_in=None, cu_seqlens=None):

@@ -38,6 +38,10 @@
  *                          independent algorithm used to cross-check the
  *                          definition and to debug stage by stage.
  *   oracle_ut_transform    the per-chunk UT transform alone (W and U~).
+ *   oracle_recurrent_bwd   gradients of eq. 10 with respect to q, k, v, g,
+ *                          beta and the initial state, by reverse-mode
+ *                          differentiation of the token recurrence (the
+ *                          states are recomputed forward and kept).
  *   oracle_short_conv_silu the block prologue of q, k, v: short causal
  *                          depthwise convolution then SiLU ([paper] §3.4
  *                          "Token mixing block" and Fig. 1).
@@ -557,4 +561,149 @@ int oracle_gate_activations(const double *a, const double *b, const double *A_lo
             beta[i] = 1.0 / (1.0 + exp(-b[i]));
         }
     return 0;
+}
+
+
+/* ------------------------------------------------------------------ */
+/* Backward of the token recurrence (reverse mode)                     */
+/* ------------------------------------------------------------------ */
+
+/*
+ * With q^ = scale q r_q, k^ = k r_k (r = (|x|^2 + eps)^{-1/2} when use_qk_l2norm,
+ * else 1), one step of eq. 10 in the decay-then-correct form is
+ *     Sbar = alpha S_{t-1},  e = beta (v - Sbar k^),  S_t = Sbar + e k^T,  o_t = S_t q^.
+ * Given D = dL/dS_t (after adding dO_t q^T for the output), the step's adjoint is
+ *     de = D k^,  dv = beta de,  dbeta = de . (v - Sbar k^),
+ *     dk^ = D^T e - beta Sbar^T de,   dq^ = S_t^T dO_t,
+ *     dSbar = D - beta de k^T,  dg = <dSbar, Sbar>,  dS_{t-1} = alpha dSbar,
+ * then the normalisations: dx = r dx^ - r^3 (x . dx^) x (times scale for q).
+ * dout [B,T,H,dv] and dfinal [N,H,dv,dk] (or NULL) are the loss gradients of the
+ * outputs; results dq, dk [B,T,H,dk], dv [B,T,H,dv], dg, dbeta [B,T,H],
+ * dinit [N,H,dv,dk] (or NULL).
+ */
+typedef struct {
+    geom_t gm;
+    const double *q, *k, *v, *g, *beta, *s0, *dout, *dsf;
+    double *dq, *dk, *dv, *dg, *dbeta, *ds0;
+    double scale;
+    int l2;
+    int err;
+} bwd_ctx_t;
+
+static void bwd_unit(void *vctx, int64_t unit, double *scratch)
+{
+    bwd_ctx_t *c = (bwd_ctx_t *)vctx;
+    const geom_t *gm = &c->gm;
+    const int H = gm->H, dk = gm->dk, dv = gm->dv;
+    const int n = (int)(unit / H), h = (int)(unit % H);
+    const int64_t sz = (int64_t)dv * dk;
+    int64_t row0, len;
+    seq_span(gm, n, &row0, &len);
+    double *St = (double *)malloc(sizeof(double) * (size_t)((len + 1) * sz));   /* S_0 .. S_len */
+    double *qh = (double *)malloc(sizeof(double) * (size_t)(len > 0 ? len * dk : 1));
+    double *kh = (double *)malloc(sizeof(double) * (size_t)(len > 0 ? len * dk : 1));
+    if (!St || !qh || !kh) { c->err = 1; free(St); free(qh); free(kh); return; }
+    double *D = scratch, *dSb = D + sz, *Sb = dSb + sz, *p = Sb + sz, *e = p + dv, *de = e + dv;
+    double *dqh = de + dv, *dkh = dqh + dk;
+
+    /* forward, keeping every state */
+    if (c->s0) memcpy(St, c->s0 + ((int64_t)n * H + h) * sz, sizeof(double) * (size_t)sz);
+    else memset(St, 0, sizeof(double) * (size_t)sz);
+    for (int64_t t = 0; t < len; ++t) {
+        const int64_t th = (row0 + t) * H + h;
+        load_vec(c->q + th * dk, qh + t * dk, dk, c->l2, c->scale);
+        load_vec(c->k + th * dk, kh + t * dk, dk, c->l2, 1.0);
+        memcpy(St + (t + 1) * sz, St + t * sz, sizeof(double) * (size_t)sz);
+        gdr_step(St + (t + 1) * sz, qh + t * dk, kh + t * dk, c->v + th * dv, exp(c->g[th]), c->beta[th],
+                 NULL, dk, dv);
+    }
+
+    /* reverse */
+    if (c->dsf) memcpy(D, c->dsf + ((int64_t)n * H + h) * sz, sizeof(double) * (size_t)sz);
+    else memset(D, 0, sizeof(double) * (size_t)sz);
+    for (int64_t t = len - 1; t >= 0; --t) {
+        const int64_t th = (row0 + t) * H + h;
+        const double *S1 = St + (t + 1) * sz, *S0 = St + t * sz;
+        const double *qq = qh + t * dk, *kk = kh + t * dk, *vv = c->v + th * dv, *dO = c->dout + th * dv;
+        const double alpha = exp(c->g[th]), b = c->beta[th];
+        for (int j = 0; j < dv; ++j)
+            for (int d = 0; d < dk; ++d) D[j * dk + d] += dO[j] * qq[d];
+        for (int d = 0; d < dk; ++d) {
+            double acc = 0.0;
+            for (int j = 0; j < dv; ++j) acc += S1[j * dk + d] * dO[j];
+            dqh[d] = acc;
+        }
+        for (int64_t i = 0; i < sz; ++i) Sb[i] = alpha * S0[i];
+        double dbeta = 0.0;
+        for (int j = 0; j < dv; ++j) {
+            double pj = 0.0, dej = 0.0;
+            for (int d = 0; d < dk; ++d) { pj += Sb[j * dk + d] * kk[d]; dej += D[j * dk + d] * kk[d]; }
+            p[j] = pj;
+            e[j] = b * (vv[j] - pj);
+            de[j] = dej;
+            dbeta += dej * (vv[j] - pj);
+            c->dv[th * dv + j] = b * dej;
+        }
+        for (int d = 0; d < dk; ++d) {
+            double acc = 0.0;
+            for (int j = 0; j < dv; ++j) acc += D[j * dk + d] * e[j] - b * Sb[j * dk + d] * de[j];
+            dkh[d] = acc;
+        }
+        double dg = 0.0;
+        for (int j = 0; j < dv; ++j)
+            for (int d = 0; d < dk; ++d) {
+                const double x = D[j * dk + d] - b * de[j] * kk[d];
+                dSb[j * dk + d] = x;
+                dg += x * Sb[j * dk + d];
+            }
+        for (int64_t i = 0; i < sz; ++i) D[i] = alpha * dSb[i];
+        c->dbeta[th] = dbeta;
+        c->dg[th] = dg;
+        /* through the normalisations (and scale on q) */
+        const double *qr = c->q + th * dk, *kr = c->k + th * dk;
+        if (c->l2) {
+            double sq = 0.0, sk = 0.0, qd = 0.0, kd = 0.0;
+            for (int d = 0; d < dk; ++d) { sq += qr[d] * qr[d]; sk += kr[d] * kr[d]; qd += qr[d] * dqh[d]; kd += kr[d] * dkh[d]; }
+            const double rq = 1.0 / sqrt(sq + ORACLE_L2_EPS), rk = 1.0 / sqrt(sk + ORACLE_L2_EPS);
+            for (int d = 0; d < dk; ++d) {
+                c->dq[th * dk + d] = c->scale * (rq * dqh[d] - rq * rq * rq * qd * qr[d]);
+                c->dk[th * dk + d] = rk * dkh[d] - rk * rk * rk * kd * kr[d];
+            }
+        } else {
+            for (int d = 0; d < dk; ++d) {
+                c->dq[th * dk + d] = c->scale * dqh[d];
+                c->dk[th * dk + d] = dkh[d];
+            }
+        }
+        (void)p;
+    }
+    if (c->ds0) memcpy(c->ds0 + ((int64_t)n * H + h) * sz, D, sizeof(double) * (size_t)sz);
+    free(St);
+    free(qh);
+    free(kh);
+}
+
+int oracle_recurrent_bwd(const double *q, const double *k, const double *v, const double *g, const double *beta,
+                         const double *init_state, const int32_t *cu_seqlens, int32_t num_seqs,
+                         const double *dout, const double *dfinal,
+                         double *dq, double *dk, double *dv, double *dg, double *dbeta, double *dinit,
+                         int32_t B, int32_t T, int32_t H, int32_t dkk, int32_t dvv,
+                         double scale, int32_t use_qk_l2norm, int32_t nthreads)
+{
+    bwd_ctx_t c;
+    c.gm.B = B; c.gm.T = T; c.gm.H = H; c.gm.dk = dkk; c.gm.dv = dvv;
+    c.gm.cu = cu_seqlens; c.gm.N = cu_seqlens ? num_seqs : B;
+    if (check_geom(&c.gm)) return -1;
+    c.q = q; c.k = k; c.v = v; c.g = g; c.beta = beta; c.s0 = init_state; c.dout = dout; c.dsf = dfinal;
+    c.dq = dq; c.dk = dk; c.dv = dv; c.dg = dg; c.dbeta = dbeta; c.ds0 = dinit;
+    c.scale = scale; c.l2 = use_qk_l2norm; c.err = 0;
+    /* tokens outside every sequence get zero gradients */
+    memset(dq, 0, sizeof(double) * (size_t)B * T * H * dkk);
+    memset(dk, 0, sizeof(double) * (size_t)B * T * H * dkk);
+    memset(dv, 0, sizeof(double) * (size_t)B * T * H * dvv);
+    memset(dg, 0, sizeof(double) * (size_t)B * T * H);
+    memset(dbeta, 0, sizeof(double) * (size_t)B * T * H);
+    size_t scratch = 3 * (size_t)dvv * dkk + 3 * (size_t)dvv + 2 * (size_t)dkk;
+    int rc = run_pool(bwd_unit, &c, (int64_t)c.gm.N * H, scratch, nthreads);
+    return rc ? rc : (c.err ? -2 : 0);
 }
