@@ -367,6 +367,10 @@ def bench_ours(args):
     mbytes = decode_multi_algorithmic_bytes(wd, MULTI_T)
     m_ach = mbytes / (mms * 1e-3) / 1e9
 
+    # backward of the chunked forward on the bench shape
+    bwd = bench_backward(w, d, dev, flush, stream, reps, peaks)
+    bwd["value"] = job_throughput(w.B * w.L, ws_n, max_over_ranks(dist, bwd["ms_per_call"]))
+
     # block prologue (short conv + SiLU for q, k, v; gate activations) on the bench shape
     pro = bench_prologue(w, dev, flush, stream, reps, peaks)
     pro["value"] = job_throughput(w.B * w.L, ws_n, max_over_ranks(dist, pro["ms_per_call"]))
@@ -399,6 +403,7 @@ def bench_ours(args):
                                           "frac": m_ach / peaks["hbm_gbs"], "algorithmic_bytes": mbytes},
                              "timing": f"{wd.steps} tokens as {calls} calls in one CUDA graph, median of {reps}"},
             "prologue": pro,
+            "backward": bwd,
             "gpu_launches": args.steps * launches_per_step,
             "clocks": clocks,
             "cpu_baseline": cpu,
@@ -406,6 +411,43 @@ def bench_ours(args):
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def bench_backward(w: inputs.Workload, d, dev, flush, stream, reps: int, peaks):
+    """One gdn_chunk_bwd call on the workload (inputs resident, L2 flushed before each call)."""
+    import gated_delta_rule_12_gb300 as gdn
+    gen = torch.Generator().manual_seed(w.seed + 200)
+    dO = torch.randn((w.B, w.L, w.H, w.dv), generator=gen).to(torch.bfloat16).to(dev)
+    dS = torch.randn((w.B, w.H, w.dv, w.dk), generator=gen).to(dev)
+    need = gdn.load_library().gdn_chunk_bwd_workspace_size(w.B, w.L, w.H, w.dk, w.dv, 0, gdn.GDN_BF16)
+    work = torch.empty(need, dtype=torch.uint8, device=dev)
+
+    def call():
+        gdn.chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], dO, init_state=d["init_state"], dfinal_state=dS,
+                      scale=w.scale, workspace=work)
+
+    for _ in range(2):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    t = []
+    for _ in range(max(3, reps)):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        t.append(a.elapsed_time(b))
+    ms = statistics.median(t)
+    s = 2
+    per_th = (2 * w.dk + 2 * w.dv) * s + 8 + (2 * w.dk + w.dv) * s + 8   # q, k, v, dO, g, beta in; dq, dk, dv, dg, dbeta out
+    nbytes = w.B * w.L * w.H * per_th + 2 * w.B * w.H * w.dv * w.dk * 4
+    ach = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": PREFILL, "unit": "tokens/s", "ms_per_call": ms, "kernels": 4,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / peaks["hbm_gbs"], "algorithmic_bytes": nbytes},
+            "timing": f"median of {max(3, reps)} calls, L2 flushed before each"}
 
 
 def bench_prologue(w: inputs.Workload, dev, flush, stream, reps: int, peaks, K: int = PROLOGUE_K):

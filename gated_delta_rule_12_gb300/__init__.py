@@ -14,6 +14,7 @@ Entry points (same names as the C ABI, without the ``gdn_`` prefix):
     prologue(xq, xk, xv, wq, wk, wv, a, b, A_log, dt_bias, ...) -> (q, k, v, g, beta)
     chunk_fwd_workspace_size(...)         -> bytes
     chunk_fwd_kernel_count(...)           -> kernels one chunk_fwd call launches
+    chunk_bwd(q, k, v, g, beta, dout, ...) -> (dq, dk, dv, dg, dbeta, dinit_state)
     check_device_error(workspace)         -> None or raises
 """
 from __future__ import annotations
@@ -34,7 +35,8 @@ GDN_F32, GDN_BF16 = 0, 1
 CHUNK = 64
 
 EXPORTS = ["gdn_status_string", "gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd_kernel_count", "gdn_chunk_fwd",
-           "gdn_decode_step", "gdn_decode_multi", "gdn_prologue", "gdn_check_device_error", "gdn_chunk_fwd_noalloc"]
+           "gdn_chunk_bwd_workspace_size", "gdn_chunk_bwd", "gdn_decode_step", "gdn_decode_multi", "gdn_prologue",
+           "gdn_check_device_error", "gdn_chunk_fwd_noalloc"]
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -76,6 +78,11 @@ def load_library(path: str = LIB_PATH, build_if_missing: bool = False) -> ctypes
                                       _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _f32, _i32, _i32,
                                       _vp, _sz, _vp]
         lib.gdn_chunk_fwd.restype = ctypes.c_int
+        lib.gdn_chunk_bwd_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_int]
+        lib.gdn_chunk_bwd_workspace_size.restype = _sz
+        lib.gdn_chunk_bwd.argtypes = [_vp] * 6 + [_vp, _i32] + [_vp] * 8 + [_i32] * 5 + [ctypes.c_int, _f32, _i32, _i32,
+                                                                                         _vp, _sz, _vp]
+        lib.gdn_chunk_bwd.restype = ctypes.c_int
         lib.gdn_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                         _i32, _i32, _i32, _i32, ctypes.c_int, _f32, _i32, _vp]
         lib.gdn_decode_step.restype = ctypes.c_int
@@ -171,6 +178,41 @@ def chunk_fwd(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale=None, us
     if rc != GDN_OK:
         raise GDNError(rc, "gdn_chunk_fwd")
     return out, final_state
+
+
+def chunk_bwd(q, k, v, g, beta, dout, init_state=None, dfinal_state=None, cu_seqlens=None, scale=None,
+              use_qk_l2norm=True, want_dinit=True, workspace=None, chunk_size=CHUNK, stream=None):
+    """Backward of ``chunk_fwd`` (``gdn_chunk_bwd``): returns ``(dq, dk, dv, dg, dbeta, dinit_state)``
+    for the loss gradients ``dout`` [B,T,H,dv] and ``dfinal_state`` [N,H,dv,dk] (or None)."""
+    lib = load_library()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else B
+    if scale is None:
+        scale = dk ** -0.5
+    dq, dkk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dg = torch.empty((B, T, H), dtype=torch.float32, device=q.device)
+    db = torch.empty((B, T, H), dtype=torch.float32, device=q.device)
+    dinit = torch.empty((N, H, dv, dk), dtype=torch.float32, device=q.device) if want_dinit else None
+    for t in (g, beta, init_state, dfinal_state):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError("g, beta and states must be float32")
+    if dout.dtype != q.dtype:
+        raise TypeError("dout must have the dtype of q")
+    _need_cuda(q, k, v, g, beta, dout, init_state, dfinal_state, cu_seqlens)
+    dt = _dt(q)
+    num_seqs = N if cu_seqlens is not None else 0
+    need = int(lib.gdn_chunk_bwd_workspace_size(B, T, H, dk, dv, num_seqs, dt))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    rc = lib.gdn_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state), _ptr(cu_seqlens),
+                           num_seqs, _ptr(dout), _ptr(dfinal_state), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dg),
+                           _ptr(db), _ptr(dinit), B, T, H, dk, dv, dt, float(scale), int(bool(use_qk_l2norm)),
+                           int(chunk_size), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                           _stream(stream))
+    if rc != GDN_OK:
+        raise GDNError(rc, "gdn_chunk_bwd")
+    return dq, dkk, dvv, dg, db, dinit
 
 
 def decode_step(state, q, k, v, g, beta, scale=None, use_qk_l2norm=True, out=None, stream=None):

@@ -106,6 +106,63 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v, const floa
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+size_t gdn_chunk_bwd_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv,
+                                    int32_t num_seqs, gdn_dtype dt)
+{
+    if (B < 1 || T < 0 || H < 1 || num_seqs < 0) return 0;
+    if (dt != GDN_F32 && dt != GDN_BF16) return 0;
+    if (!chunk_dims_supported(dk, dv)) return 0;
+    const bool varlen = num_seqs > 0;
+    if (varlen && B != 1) return 0;
+    return chunk_bwd_workspace_bytes(num_slots(B, T, varlen ? num_seqs : B, varlen), H, dk, dv);
+}
+
+gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                         const float *init_state, const int32_t *cu_seqlens, int32_t num_seqs,
+                         const void *dout, const float *dfinal_state,
+                         void *dq, void *dk_, void *dv_, float *dg, float *dbeta, float *dinit_state,
+                         int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, gdn_dtype dt, float scale,
+                         int32_t use_qk_l2norm, int32_t chunk_size, void *workspace, size_t workspace_bytes,
+                         void *stream)
+{
+    if (B < 1 || T < 0 || H < 1 || dk < 1 || dv < 1) return GDN_ERR_INVALID_ARG;
+    if (dt != GDN_F32 && dt != GDN_BF16) return GDN_ERR_INVALID_ARG;
+    if (chunk_size != kChunk) return GDN_ERR_UNSUPPORTED;
+    if (!chunk_dims_supported(dk, dv)) return GDN_ERR_UNSUPPORTED;
+    const bool varlen = cu_seqlens != nullptr;
+    if (varlen && (B != 1 || num_seqs < 1)) return GDN_ERR_INVALID_ARG;
+    if (!varlen && num_seqs != 0 && num_seqs != B) return GDN_ERR_INVALID_ARG;
+    const int N = varlen ? num_seqs : B;
+    const bool have_tokens = (int64_t)B * T > 0;
+    if (have_tokens && (!q || !k || !v || !g || !beta || !dout || !dq || !dk_ || !dv_ || !dg || !dbeta))
+        return GDN_ERR_INVALID_ARG;
+    const void *ptrs16[] = {q, k, v, init_state, dout, dfinal_state, dq, dk_, dv_, dinit_state};
+    for (const void *p : ptrs16)
+        if (p && !aligned16(p)) return GDN_ERR_INVALID_ARG;
+    const void *ptrs4[] = {g, beta, cu_seqlens, dg, dbeta};
+    for (const void *p : ptrs4)
+        if (p && !aligned_to(p, 4)) return GDN_ERR_INVALID_ARG;
+    if (!workspace || ((uintptr_t)workspace & 255u) != 0) return GDN_ERR_WORKSPACE;
+    const size_t need = gdn_chunk_bwd_workspace_size(B, T, H, dk, dv, varlen ? num_seqs : 0, dt);
+    if (need == 0) return GDN_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return GDN_ERR_WORKSPACE;
+
+    BwdArgs a;
+    a.q = q; a.k = k; a.v = v; a.dout = dout; a.g = g; a.beta = beta;
+    a.init_state = init_state; a.dfinal = dfinal_state;
+    a.dq = dq; a.dk = dk_; a.dv = dv_; a.dg = dg; a.dbeta = dbeta; a.dinit = dinit_state;
+    a.gm.B = B; a.gm.T = T; a.gm.H = H; a.gm.dk = dk; a.gm.dv = dv; a.gm.N = N;
+    a.gm.cu = cu_seqlens;
+    a.gm.nct = ceil_div(T, kChunk);
+    a.slots = have_tokens ? num_slots(B, T, N, varlen) : 0;
+    a.dt = (dt == GDN_BF16) ? 1 : 0;
+    a.scale = scale;
+    a.l2 = use_qk_l2norm ? 1 : 0;
+    a.workspace = workspace;
+    cudaError_t e = launch_chunk_bwd(a, (cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 static gdn_status decode_common(float *state, const void *q, const void *k, const void *v, const float *g,
                                 const float *beta, void *out, int32_t N, int32_t T, int32_t H, int32_t dk,
                                 int32_t dv, gdn_dtype dt, float scale, int32_t use_qk_l2norm, void *stream)

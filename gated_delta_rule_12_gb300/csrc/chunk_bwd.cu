@@ -1,0 +1,559 @@
+// chunk_bwd.cu -- backward pass of the chunked gated delta rule (CUDA cores, fp32).
+//
+// "Gated Delta Networks: Improving Mamba2 with Delta Rule", §3.3 (the chunkwise
+// form; the training forward whose gradients these are).  Per chunk, with
+// q^ = scale q / |q|, k^ = k / |k| (when normalising), b the chunk-local
+// cumulative log-gate, gam = e^b, gC = e^{b_last}, Gamma_ri = e^{b_r - b_i} (i <= r):
+//     L = strictLower(diag(beta)(Gamma o K^K^T)),  T = (I + L)^{-1}
+//     U = T diag(beta) V,   W = T diag(beta gam) K^,   A = (Q^ K^T) o Gamma
+//     V_new = U - W S^T,    O = diag(gam) Q^ S^T + A V_new
+//     S' = gC S + V_new^T diag(gC / gam) K^
+// Reverse mode, chunk by chunk from the last one, with dS' the gradient of the
+// state after the chunk:
+//     dV_new = Kd dS'^T + A^T dO                     (Kd = diag(gC/gam) K^, Qd = diag(gam) Q^)
+//     dS     = gC dS' + dO^T Qd - dV_new^T W          (the gradient of the state before it)
+// and, in parallel over chunks, the local gradients through A, Qd, Kd, U, W, T, L,
+// Gamma and the gates (see bwd_local_kernel), then through the normalisations.
+//
+// Four kernels: bwd_prep_kernel (per chunk: q^, k^, b, T, U, W, A),
+// bwd_fwd_scan_kernel (per sequence and head: the state at every chunk start and
+// V_new), bwd_bwd_scan_kernel (reverse: dS' per chunk, dV_new, dS_0) and
+// bwd_local_kernel (per chunk: dq, dk, dv, dg, dbeta).  Everything is fp32 on the
+// CUDA cores, matrices staged through shared memory by one block-level GEMM.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kBT = 256;   // threads per block of every backward kernel
+
+// ---------------------------------------------------------------------------
+// per (slot, head) fp32 workspace block
+// ---------------------------------------------------------------------------
+struct BwdLayout {
+    int64_t qh, kh, b, t, u, w, a, s, vn, dvn, dsn, dqh, dkh, dw, total;   // float offsets
+};
+
+__host__ __device__ inline BwdLayout bwd_layout(int dk, int dv)
+{
+    BwdLayout L;
+    int64_t o = 0;
+    L.qh = o;  o += 64 * dk;
+    L.kh = o;  o += 64 * dk;
+    L.b = o;   o += 64;
+    L.t = o;   o += 64 * 64;
+    L.u = o;   o += 64 * dv;
+    L.w = o;   o += 64 * dk;
+    L.a = o;   o += 64 * 64;
+    L.s = o;   o += (int64_t)dv * dk;
+    L.vn = o;  o += 64 * dv;
+    L.dvn = o; o += 64 * dv;
+    L.dsn = o; o += (int64_t)dv * dk;
+    L.dqh = o; o += 64 * dk;             // scratch of bwd_local_kernel
+    L.dkh = o; o += 64 * dk;
+    L.dw = o;  o += 64 * dk;
+    L.total = o;
+    return L;
+}
+
+// ---------------------------------------------------------------------------
+// block GEMM: out(i, j, sum_k A(i, k) B(k, j)) for i < M <= 16 MT, j < N <= 16 NT,
+// all kBT threads of the block (a 16 x 16 grid, MT x NT outputs each).  A and B
+// are read through functors; AK / BK say whether consecutive k are contiguous in
+// memory (then the tile loads run along k), so the staging loads coalesce.
+// ---------------------------------------------------------------------------
+template <int MT, int NT, bool AK, bool BK, class FA, class FB, class FO>
+__device__ __forceinline__ void block_gemm(int M, int N, int K, FA fa, FB fb, FO fo, float *sA, float *sB)
+{
+    constexpr int MR = 16 * MT, NR = 16 * NT;
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    float acc[MT][NT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int n = 0; n < NT; ++n) acc[m][n] = 0.f;
+    for (int k0 = 0; k0 < K; k0 += 16) {
+        for (int e = tid; e < 16 * MR; e += kBT) {
+            const int kk = AK ? (e & 15) : (e / MR), i = AK ? (e >> 4) : (e % MR);
+            sA[kk * MR + i] = (i < M && k0 + kk < K) ? fa(i, k0 + kk) : 0.f;
+        }
+        for (int e = tid; e < 16 * NR; e += kBT) {
+            const int kk = BK ? (e & 15) : (e / NR), j = BK ? (e >> 4) : (e % NR);
+            sB[kk * NR + j] = (j < N && k0 + kk < K) ? fb(k0 + kk, j) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int kk = 0; kk < 16; ++kk) {
+            float a[MT], b[NT];
+#pragma unroll
+            for (int m = 0; m < MT; ++m) a[m] = sA[kk * MR + ty + 16 * m];
+#pragma unroll
+            for (int n = 0; n < NT; ++n) b[n] = sB[kk * NR + tx + 16 * n];
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int n = 0; n < NT; ++n) acc[m][n] = fmaf(a[m], b[n], acc[m][n]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const int i = ty + 16 * m, j = tx + 16 * n;
+            if (i < M && j < N) fo(i, j, acc[m][n]);
+        }
+}
+
+// shared staging of block_gemm: up to 16 x 256 floats for A and for B
+constexpr int kStage = 16 * 256;
+
+// The chunk (sequence n, chunk c) of `slot` and its token range; false if none.
+__device__ __forceinline__ bool chunk_of(const Geometry &gm, int64_t slot, int &n, int &c, int64_t &tok0, int &rows)
+{
+    return slot_to_chunk(gm, slot, n, c, tok0, rows);
+}
+
+struct BwdParams {
+    const void *q, *k, *v, *dout;   // dtype dt
+    const float *g, *beta, *init_state, *dfinal;
+    void *dq, *dk, *dv;             // dtype dt
+    float *dg, *dbeta, *dinit;
+    float *ws;                      // per (slot, head) blocks of BwdLayout
+    Geometry gm;
+    float scale;
+    int l2;
+};
+
+template <typename T>
+__device__ __forceinline__ float ld(const void *p, int64_t i) { return to_f32(reinterpret_cast<const T *>(p)[i]); }
+
+// ---------------------------------------------------------------------------
+// bwd_prep_kernel: per (slot, head) -- q^, k^, b, T = (I + L)^{-1}, U, W, A
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kBT)
+bwd_prep_kernel(const BwdParams p)
+{
+    extern __shared__ float smb[];
+    const Geometry gm = p.gm;
+    const int H = gm.H, dk = gm.dk, dv = gm.dv, h = blockIdx.y, tid = threadIdx.x;
+    const int64_t slot = blockIdx.x;
+    int n, c, rows;
+    int64_t tok0;
+    if (!chunk_of(gm, slot, n, c, tok0, rows)) return;
+    const BwdLayout LY = bwd_layout(dk, dv);
+    float *blk = p.ws + (slot * H + h) * LY.total;
+    float *sA = smb, *sB = sA + kStage;
+    float *sL = sB + kStage;             // [64][65]: L, then T (column solve)
+    float *sb = sL + 64 * 65, *sbe = sb + 64, *sgam = sbe + 64;   // b, beta, gam
+
+    // gates: chunk-local cumulative log-gate (padding rows: g = 0, beta = 0)
+    if (tid < 64) {
+        const int64_t th = (tok0 + tid) * H + h;
+        sb[tid] = tid < rows ? p.g[th] : 0.f;
+        sbe[tid] = tid < rows ? p.beta[th] : 0.f;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float acc = 0.f;
+        for (int r = 0; r < 64; ++r) { acc += sb[r]; sb[r] = acc; }
+    }
+    __syncthreads();
+    if (tid < 64) {
+        sgam[tid] = expf(sb[tid]);
+        blk[LY.b + tid] = sb[tid];
+    }
+    // normalised q^ (scaled) and k^: one warp per row, rows tid>>5 + 8 i
+    for (int r = tid >> 5; r < 64; r += kBT / 32) {
+        const int lane = tid & 31;
+        const int64_t th = (tok0 + r) * H + h;
+        float sq = 0.f, sk = 0.f;
+        for (int d = lane; d < dk; d += 32) {
+            const float qv = r < rows ? ld<T>(p.q, th * dk + d) : 0.f, kv = r < rows ? ld<T>(p.k, th * dk + d) : 0.f;
+            sq += qv * qv;
+            sk += kv * kv;
+        }
+        sq = warp_sum(sq);
+        sk = warp_sum(sk);
+        const float rq = (p.l2 ? rsqrtf(sq + kL2Eps) : 1.f) * p.scale, rk = p.l2 ? rsqrtf(sk + kL2Eps) : 1.f;
+        for (int d = lane; d < dk; d += 32) {
+            blk[LY.qh + r * dk + d] = r < rows ? ld<T>(p.q, th * dk + d) * rq : 0.f;
+            blk[LY.kh + r * dk + d] = r < rows ? ld<T>(p.k, th * dk + d) * rk : 0.f;
+        }
+    }
+    __syncthreads();
+    const float *qh = blk + LY.qh, *kh = blk + LY.kh;
+    // KK = K^ K^T -> L (strictly lower, beta_r Gamma_ri KK_ri) into sL;  A = (Q^ K^T) o Gamma
+    block_gemm<4, 4, true, true>(64, 64, dk, [&](int i, int k) { return kh[i * dk + k]; },
+                                 [&](int k, int j) { return kh[j * dk + k]; },
+                                 [&](int i, int j, float x) {
+                                     sL[i * 65 + j] = j < i ? sbe[i] * expf(sb[i] - sb[j]) * x : 0.f;
+                                 }, sA, sB);
+    block_gemm<4, 4, true, true>(64, 64, dk, [&](int i, int k) { return qh[i * dk + k]; },
+                                 [&](int k, int j) { return kh[j * dk + k]; },
+                                 [&](int i, int j, float x) {
+                                     blk[LY.a + i * 64 + j] = j <= i ? expf(sb[i] - sb[j]) * x : 0.f;
+                                 }, sA, sB);
+    __syncthreads();
+    // T = (I + L)^{-1}: thread c < 64 solves column c by forward substitution
+    if (tid < 64) {
+        const int col = tid;
+        float x[64];
+#pragma unroll
+        for (int r = 0; r < 64; ++r) {
+            float acc = r == col ? 1.f : 0.f;
+            for (int i = col; i < r; ++i) acc -= sL[r * 65 + i] * x[i];
+            x[r] = r < col ? 0.f : acc;
+        }
+#pragma unroll
+        for (int r = 0; r < 64; ++r) blk[LY.t + r * 64 + col] = x[r];
+    }
+    __syncthreads();
+    const float *Tm = blk + LY.t;
+    // U = T diag(beta) V,  W = T diag(beta gam) K^
+    block_gemm<4, 16, true, false>(64, dv, 64, [&](int i, int k) { return Tm[i * 64 + k]; },
+                                   [&](int k, int j) {
+                                       return k < rows ? sbe[k] * ld<T>(p.v, ((tok0 + k) * H + h) * dv + j) : 0.f;
+                                   },
+                                   [&](int i, int j, float x) { blk[LY.u + i * dv + j] = x; }, sA, sB);
+    block_gemm<4, 16, true, false>(64, dk, 64, [&](int i, int k) { return Tm[i * 64 + k]; },
+                                   [&](int k, int j) { return sbe[k] * sgam[k] * kh[k * dk + j]; },
+                                   [&](int i, int j, float x) { blk[LY.w + i * dk + j] = x; }, sA, sB);
+}
+
+// ---------------------------------------------------------------------------
+// bwd_fwd_scan_kernel: per (sequence, head) -- the state at every chunk start
+// (S_c, saved) and V_new = U - W S_c^T (saved), S_{c+1} = gC S_c + V_new^T Kd.
+// The state lives in shared memory.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kBT)
+bwd_fwd_scan_kernel(const BwdParams p)
+{
+    extern __shared__ float smb[];
+    const Geometry gm = p.gm;
+    const int H = gm.H, dk = gm.dk, dv = gm.dv, n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    const BwdLayout LY = bwd_layout(dk, dv);
+    float *sA = smb, *sB = sA + kStage, *S = sB + kStage;   // S [dv][dk]
+    const int64_t SZ = (int64_t)dv * dk;
+    for (int64_t e = tid; e < SZ; e += kBT)
+        S[e] = p.init_state ? p.init_state[((int64_t)n * H + h) * SZ + e] : 0.f;
+    int64_t tok0;
+    int len;
+    seq_span(gm, n, tok0, len);
+    const int nch = ceil_div(len, kChunk);
+    const int64_t slot0 = slot_base(gm, n);
+    __syncthreads();
+    for (int c = 0; c < nch; ++c) {
+        float *blk = p.ws + ((slot0 + c) * H + h) * LY.total;
+        const float *b = blk + LY.b, *W = blk + LY.w, *U = blk + LY.u, *kh = blk + LY.kh;
+        for (int64_t e = tid; e < SZ; e += kBT) blk[LY.s + e] = S[e];
+        float *vn = blk + LY.vn;
+        block_gemm<4, 16, true, true>(64, dv, dk, [&](int i, int k) { return W[i * dk + k]; },
+                                      [&](int k, int j) { return S[j * dk + k]; },
+                                      [&](int i, int j, float x) { vn[i * dv + j] = U[i * dv + j] - x; }, sA, sB);
+        __syncthreads();
+        const float gC = expf(b[63]);
+        for (int j0 = 0; j0 < dv; j0 += 128)   // S <- gC S + V_new^T Kd, 128 state rows per pass
+            block_gemm<8, 8, false, false>(min(128, dv - j0), dk, 64,
+                                           [&](int i, int r) { return vn[r * dv + j0 + i]; },
+                                           [&](int r, int d) { return expf(b[63] - b[r]) * kh[r * dk + d]; },
+                                           [&](int i, int d, float x) {
+                                               float &s_ = S[(int64_t)(j0 + i) * dk + d];
+                                               s_ = gC * s_ + x;
+                                           }, sA, sB);
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// bwd_bwd_scan_kernel: per (sequence, head), chunks in reverse -- dS' (saved per
+// chunk), dV_new = Kd dS'^T + A^T dO (saved), dS = gC dS' + dO^T Qd - dV_new^T W;
+// the gradient of the initial state at the end.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kBT)
+bwd_bwd_scan_kernel(const BwdParams p)
+{
+    extern __shared__ float smb[];
+    const Geometry gm = p.gm;
+    const int H = gm.H, dk = gm.dk, dv = gm.dv, n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    const BwdLayout LY = bwd_layout(dk, dv);
+    float *sA = smb, *sB = sA + kStage, *dS = sB + kStage;   // dS [dv][dk]
+    const int64_t SZ = (int64_t)dv * dk;
+    for (int64_t e = tid; e < SZ; e += kBT)
+        dS[e] = p.dfinal ? p.dfinal[((int64_t)n * H + h) * SZ + e] : 0.f;
+    int64_t tok0;
+    int len;
+    seq_span(gm, n, tok0, len);
+    const int nch = ceil_div(len, kChunk);
+    const int64_t slot0 = slot_base(gm, n);
+    __syncthreads();
+    for (int c = nch - 1; c >= 0; --c) {
+        float *blk = p.ws + ((slot0 + c) * H + h) * LY.total;
+        const float *b = blk + LY.b, *W = blk + LY.w, *A = blk + LY.a, *kh = blk + LY.kh, *qh = blk + LY.qh;
+        const int64_t t0 = tok0 + (int64_t)c * kChunk;
+        const int rows = min(kChunk, len - c * kChunk);
+        for (int64_t e = tid; e < SZ; e += kBT) blk[LY.dsn + e] = dS[e];
+        float *dvn = blk + LY.dvn;
+        auto dO = [&](int r, int j) { return r < rows ? ld<T>(p.dout, ((t0 + r) * H + h) * dv + j) : 0.f; };
+        // dV_new = Kd dS'^T + A^T dO
+        block_gemm<4, 16, true, true>(64, dv, dk + 64,
+                                      [&](int r, int k) {
+                                          return k < dk ? expf(b[63] - b[r]) * kh[r * dk + k] : A[(k - dk) * 64 + r];
+                                      },
+                                      [&](int k, int j) { return k < dk ? dS[(int64_t)j * dk + k] : dO(k - dk, j); },
+                                      [&](int r, int j, float x) { dvn[r * dv + j] = x; }, sA, sB);
+        __syncthreads();
+        // dS <- gC dS' + dO^T Qd - dV_new^T W
+        const float gC = expf(b[63]);
+        for (int j0 = 0; j0 < dv; j0 += 128)
+            block_gemm<8, 8, false, false>(min(128, dv - j0), dk, 128,
+                                           [&](int i, int k) { return k < 64 ? dO(k, j0 + i) : -dvn[(k - 64) * dv + j0 + i]; },
+                                           [&](int k, int d) {
+                                               return k < 64 ? expf(b[k]) * qh[k * dk + d] : W[(k - 64) * dk + d];
+                                           },
+                                           [&](int i, int d, float x) {
+                                               float &s_ = dS[(int64_t)(j0 + i) * dk + d];
+                                               s_ = gC * s_ + x;
+                                           }, sA, sB);
+        __syncthreads();
+    }
+    if (p.dinit)
+        for (int64_t e = tid; e < SZ; e += kBT) p.dinit[((int64_t)n * H + h) * SZ + e] = dS[e];
+}
+
+// ---------------------------------------------------------------------------
+// bwd_local_kernel: per (slot, head) -- the gradients of the chunk's inputs given
+// S (state at the chunk start), V_new, dV_new and dS' (gradient after the chunk):
+//   dQd = dO S,  dKd = V_new dS',  dW = -dV_new S,  dA = tril(dO V_new^T)
+//   dV = diag(beta) T^T dV_new,  T^T dW -> dK, dbeta, dgam
+//   dT = dV_new (diag(beta) V)^T + dW (diag(beta gam) K^)^T,  dL = strictLower(-T^T dT T^T)
+//   through L = diag(beta)(Gamma o K^K^T) and A = (Q^K^T) o Gamma: dQ^, dK^, dbeta, dGamma
+//   db from Gamma, gam, gC/gam and gC (= e^{b_last}), dg = reverse cumsum of db,
+//   then dq, dk through the normalisations.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kBT)
+bwd_local_kernel(const BwdParams p)
+{
+    extern __shared__ float smb[];
+    const Geometry gm = p.gm;
+    const int H = gm.H, dk = gm.dk, dv = gm.dv, h = blockIdx.y, tid = threadIdx.x;
+    const int64_t slot = blockIdx.x;
+    int n, c, rows;
+    int64_t tok0;
+    if (!chunk_of(gm, slot, n, c, tok0, rows)) return;
+    const BwdLayout LY = bwd_layout(dk, dv);
+    float *blk = p.ws + (slot * H + h) * LY.total;
+    float *sA = smb, *sB = sA + kStage;
+    float *sDA = sB + kStage, *sDT = sDA + 4096, *sX = sDT + 4096, *sDL = sX + 4096, *sGG = sDL + 4096;
+    float *sb = sGG + 4096, *sbe = sb + 64, *sgam = sbe + 64, *sdgam = sgam + 64, *sdkdf = sdgam + 64,
+          *sdbeta = sdkdf + 64, *st = sdbeta + 64, *sred = st + 64;   // sred [kBT]
+    const float *qh = blk + LY.qh, *kh = blk + LY.kh, *Tm = blk + LY.t, *S = blk + LY.s, *Vn = blk + LY.vn,
+                *dVn = blk + LY.dvn, *dSn = blk + LY.dsn;
+    float *dQ = blk + LY.dqh, *dK = blk + LY.dkh, *dW = blk + LY.dw;
+    if (tid < 64) {
+        sb[tid] = blk[LY.b + tid];
+        sbe[tid] = tid < rows ? p.beta[(tok0 + tid) * H + h] : 0.f;
+        sgam[tid] = expf(sb[tid]);
+        sdgam[tid] = 0.f;
+        sdkdf[tid] = 0.f;
+        sdbeta[tid] = 0.f;
+    }
+    __syncthreads();
+    const float gC = expf(sb[63]);
+    auto dOf = [&](int r, int j) { return r < rows ? ld<T>(p.dout, ((tok0 + r) * H + h) * dv + j) : 0.f; };
+    auto Vf = [&](int r, int j) { return r < rows ? ld<T>(p.v, ((tok0 + r) * H + h) * dv + j) : 0.f; };
+    auto Gam = [&](int r, int i) { return i <= r ? expf(sb[r] - sb[i]) : 0.f; };
+
+    // dQd = dO S  ->  dQ = gam dQd,  dgam += Q^ . dQd
+    block_gemm<4, 16, true, false>(64, dk, dv, [&](int r, int j) { return dOf(r, j); },
+                                   [&](int j, int d) { return S[(int64_t)j * dk + d]; },
+                                   [&](int r, int d, float x) {
+                                       dQ[r * dk + d] = sgam[r] * x;
+                                       atomicAdd(&sdgam[r], qh[r * dk + d] * x);
+                                   }, sA, sB);
+    // dKd = V_new dS'  ->  dK = (gC / gam) dKd,  dkdf += K^ . dKd
+    block_gemm<4, 16, true, false>(64, dk, dv, [&](int r, int j) { return Vn[r * dv + j]; },
+                                   [&](int j, int d) { return dSn[(int64_t)j * dk + d]; },
+                                   [&](int r, int d, float x) {
+                                       dK[r * dk + d] = expf(sb[63] - sb[r]) * x;
+                                       atomicAdd(&sdkdf[r], kh[r * dk + d] * x);
+                                   }, sA, sB);
+    // dW = -dV_new S
+    block_gemm<4, 16, true, false>(64, dk, dv, [&](int r, int j) { return dVn[r * dv + j]; },
+                                   [&](int j, int d) { return S[(int64_t)j * dk + d]; },
+                                   [&](int r, int d, float x) { dW[r * dk + d] = -x; }, sA, sB);
+    // dA = tril(dO V_new^T) (diagonal included)
+    block_gemm<4, 4, true, true>(64, 64, dv, [&](int r, int j) { return dOf(r, j); },
+                                 [&](int j, int i) { return Vn[i * dv + j]; },
+                                 [&](int r, int i, float x) { sDA[r * 64 + i] = i <= r ? x : 0.f; }, sA, sB);
+    __syncthreads();
+    // T^T dV_new -> dv = beta T^T dV_new,  dbeta += (T^T dV_new) . V
+    block_gemm<4, 16, false, false>(64, dv, 64, [&](int i, int r) { return Tm[r * 64 + i]; },
+                                    [&](int r, int j) { return dVn[r * dv + j]; },
+                                    [&](int i, int j, float x) {
+                                        if (i < rows) {
+                                            reinterpret_cast<T *>(p.dv)[((tok0 + i) * H + h) * dv + j] = from_f32<T>(sbe[i] * x);
+                                            atomicAdd(&sdbeta[i], x * Vf(i, j));
+                                        }
+                                    }, sA, sB);
+    // T^T dW -> dK += beta gam T^T dW,  dbeta += gam (T^T dW) . K^,  dgam += beta (T^T dW) . K^
+    block_gemm<4, 16, false, false>(64, dk, 64, [&](int i, int r) { return Tm[r * 64 + i]; },
+                                    [&](int r, int d) { return dW[r * dk + d]; },
+                                    [&](int i, int d, float x) {
+                                        dK[i * dk + d] += sbe[i] * sgam[i] * x;
+                                        const float t = x * kh[i * dk + d];
+                                        atomicAdd(&sdbeta[i], sgam[i] * t);
+                                        atomicAdd(&sdgam[i], sbe[i] * t);
+                                    }, sA, sB);
+    // dT = dV_new (diag(beta) V)^T + dW (diag(beta gam) K^)^T
+    block_gemm<4, 4, true, true>(64, 64, dv + dk,
+                                 [&](int i, int k) { return k < dv ? dVn[i * dv + k] : dW[i * dk + k - dv]; },
+                                 [&](int k, int j) {
+                                     return k < dv ? sbe[j] * Vf(j, k) : sbe[j] * sgam[j] * kh[j * dk + k - dv];
+                                 },
+                                 [&](int i, int j, float x) { sDT[i * 64 + j] = x; }, sA, sB);
+    __syncthreads();
+    // X = T^T dT;  dL = strictLower(-X T^T)
+    block_gemm<4, 4, false, false>(64, 64, 64, [&](int i, int r) { return Tm[r * 64 + i]; },
+                                   [&](int r, int j) { return sDT[r * 64 + j]; },
+                                   [&](int i, int j, float x) { sX[i * 64 + j] = x; }, sA, sB);
+    __syncthreads();
+    block_gemm<4, 4, true, true>(64, 64, 64, [&](int i, int r) { return sX[i * 64 + r]; },
+                                 [&](int r, int j) { return Tm[j * 64 + r]; },
+                                 [&](int i, int j, float x) { sDL[i * 64 + j] = j < i ? -x : 0.f; }, sA, sB);
+    __syncthreads();
+    // K^K^T: dbeta += sum_{i<r} dL Gamma KK;  GG = Gamma o dGamma starts with dL beta_r KK
+    block_gemm<4, 4, true, true>(64, 64, dk, [&](int r, int d) { return kh[r * dk + d]; },
+                                 [&](int d, int i) { return kh[i * dk + d]; },
+                                 [&](int r, int i, float x) {
+                                     const float G = Gam(r, i), dl = sDL[r * 64 + i];
+                                     sGG[r * 64 + i] = G * dl * sbe[r] * x;
+                                     if (i < r) atomicAdd(&sdbeta[r], dl * G * x);
+                                 }, sA, sB);
+    __syncthreads();
+    // Q^K^T: GG += Gamma dA QK
+    block_gemm<4, 4, true, true>(64, 64, dk, [&](int r, int d) { return qh[r * dk + d]; },
+                                 [&](int d, int i) { return kh[i * dk + d]; },
+                                 [&](int r, int i, float x) { sGG[r * 64 + i] += Gam(r, i) * sDA[r * 64 + i] * x; },
+                                 sA, sB);
+    __syncthreads();
+    // dA -> dA o Gamma;  dL -> M = dL o beta_r Gamma
+    for (int e = tid; e < 4096; e += kBT) {
+        const int r = e >> 6, i = e & 63;
+        const float G = Gam(r, i);
+        sDA[e] *= G;
+        sDL[e] *= sbe[r] * G;
+    }
+    __syncthreads();
+    // dQ += (dA o Gamma) K^;   dK += (dA o Gamma)^T Q^ + M K^ + M^T K^
+    block_gemm<4, 16, true, false>(64, dk, 64, [&](int r, int i) { return sDA[r * 64 + i]; },
+                                   [&](int i, int d) { return kh[i * dk + d]; },
+                                   [&](int r, int d, float x) { dQ[r * dk + d] += x; }, sA, sB);
+    block_gemm<4, 16, false, false>(64, dk, 192,
+                                    [&](int i, int k) {
+                                        return k < 64 ? sDA[k * 64 + i]
+                                                      : (k < 128 ? sDL[i * 64 + k - 64] : sDL[(k - 128) * 64 + i]);
+                                    },
+                                    [&](int k, int d) { return k < 64 ? qh[k * dk + d] : kh[(k & 63) * dk + d]; },
+                                    [&](int i, int d, float x) { dK[i * dk + d] += x; }, sA, sB);
+    // dgC = <dS', S>
+    float part = 0.f;
+    for (int64_t e = tid; e < (int64_t)dv * dk; e += kBT) part += dSn[e] * S[e];
+    sred[tid] = part;
+    __syncthreads();
+    for (int off = kBT / 2; off > 0; off >>= 1) {
+        if (tid < off) sred[tid] += sred[tid + off];
+        __syncthreads();
+    }
+    const float dgC = sred[0];
+    // db_r, then dg = reverse cumsum within the chunk
+    if (tid < 64) {
+        const int r = tid;
+        float dbr = 0.f;
+        for (int i = 0; i < 64; ++i) dbr += sGG[r * 64 + i] - sGG[i * 64 + r];
+        const float t = sdkdf[r] * expf(sb[63] - sb[r]);
+        st[r] = t;
+        sb[r] = dbr + sdgam[r] * sgam[r] - t;   // sb is no longer needed as b
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float tsum = 0.f;
+        for (int r = 0; r < 64; ++r) tsum += st[r];
+        sb[63] += tsum + dgC * gC;
+        float acc = 0.f;
+        for (int r = 63; r >= 0; --r) { acc += sb[r]; sb[r] = acc; }
+    }
+    __syncthreads();
+    if (tid < rows) {
+        const int64_t th = (tok0 + tid) * H + h;
+        p.dg[th] = sb[tid];
+        p.dbeta[th] = sdbeta[tid];
+    }
+    // dq, dk through the normalisations (and scale on q): one warp per row
+    for (int r = tid >> 5; r < rows; r += kBT / 32) {
+        const int lane = tid & 31;
+        const int64_t th = (tok0 + r) * H + h;
+        float sq = 0.f, sk = 0.f, qd = 0.f, kd = 0.f;
+        for (int d = lane; d < dk; d += 32) {
+            const float qv = ld<T>(p.q, th * dk + d), kv = ld<T>(p.k, th * dk + d);
+            sq += qv * qv; sk += kv * kv;
+            qd += qv * dQ[r * dk + d]; kd += kv * dK[r * dk + d];
+        }
+        sq = warp_sum(sq); sk = warp_sum(sk); qd = warp_sum(qd); kd = warp_sum(kd);
+        const float rq = p.l2 ? rsqrtf(sq + kL2Eps) : 1.f, rk = p.l2 ? rsqrtf(sk + kL2Eps) : 1.f;
+        for (int d = lane; d < dk; d += 32) {
+            const float qv = ld<T>(p.q, th * dk + d), kv = ld<T>(p.k, th * dk + d);
+            const float gq = p.l2 ? p.scale * (rq * dQ[r * dk + d] - rq * rq * rq * qd * qv) : p.scale * dQ[r * dk + d];
+            const float gk = p.l2 ? rk * dK[r * dk + d] - rk * rk * rk * kd * kv : dK[r * dk + d];
+            reinterpret_cast<T *>(p.dq)[th * dk + d] = from_f32<T>(gq);
+            reinterpret_cast<T *>(p.dk)[th * dk + d] = from_f32<T>(gk);
+        }
+    }
+}
+
+template <typename T>
+cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t st)
+{
+    BwdParams p;
+    p.q = a.q; p.k = a.k; p.v = a.v; p.dout = a.dout; p.g = a.g; p.beta = a.beta;
+    p.init_state = a.init_state; p.dfinal = a.dfinal;
+    p.dq = a.dq; p.dk = a.dk; p.dv = a.dv; p.dg = a.dg; p.dbeta = a.dbeta; p.dinit = a.dinit;
+    p.ws = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(a.workspace) + 256);
+    p.gm = a.gm; p.scale = a.scale; p.l2 = a.l2;
+    const size_t stage = 2 * (size_t)kStage * sizeof(float);
+    const size_t sm_prep = stage + sizeof(float) * (64 * 65 + 3 * 64);
+    const size_t sm_scan = stage + sizeof(float) * (size_t)a.gm.dv * a.gm.dk;
+    const size_t sm_local = stage + sizeof(float) * (5 * 4096 + 7 * 64 + kBT);
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(bwd_prep_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_prep)))
+        return e;
+    if ((e = cudaFuncSetAttribute(bwd_fwd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_scan)))
+        return e;
+    if ((e = cudaFuncSetAttribute(bwd_bwd_scan_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_scan)))
+        return e;
+    if ((e = cudaFuncSetAttribute(bwd_local_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_local)))
+        return e;
+    if (a.slots > 0) bwd_prep_kernel<T><<<dim3((unsigned)a.slots, a.gm.H), kBT, sm_prep, st>>>(p);
+    bwd_fwd_scan_kernel<<<dim3(a.gm.N, a.gm.H), kBT, sm_scan, st>>>(p);
+    bwd_bwd_scan_kernel<T><<<dim3(a.gm.N, a.gm.H), kBT, sm_scan, st>>>(p);
+    if (a.slots > 0) bwd_local_kernel<T><<<dim3((unsigned)a.slots, a.gm.H), kBT, sm_local, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t chunk_bwd_workspace_bytes(int64_t slots, int H, int dk, int dv)
+{
+    return 256 + (size_t)slots * H * bwd_layout(dk, dv).total * sizeof(float);
+}
+
+cudaError_t launch_chunk_bwd(const BwdArgs &a, cudaStream_t st)
+{
+    return a.dt == 1 ? launch_bwd_typed<__nv_bfloat16>(a, st) : launch_bwd_typed<float>(a, st);
+}
+
+}  // namespace gdn

@@ -45,7 +45,22 @@ struct PrologueArgs {
     int B, T, H, dk, dv, N, K, dt;
 };
 
+struct BwdArgs {
+    const void *q, *k, *v, *dout;            // dtype dt
+    const float *g, *beta, *init_state, *dfinal;
+    void *dq, *dk, *dv;                      // dtype dt
+    float *dg, *dbeta, *dinit;
+    Geometry gm;
+    int64_t slots;
+    int dt;
+    float scale;
+    int l2;
+    void *workspace;
+};
+
 cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t st);
+cudaError_t launch_chunk_bwd(const BwdArgs &a, cudaStream_t st);
+size_t chunk_bwd_workspace_bytes(int64_t slots, int H, int dk, int dv);
 cudaError_t launch_prologue(const PrologueArgs &a, cudaStream_t st);
 bool chunk_tc_supported(int dt, int dk, int dv, int64_t tokens);
 size_t chunk_tc_workspace_bytes(int64_t slots, int H);

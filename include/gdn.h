@@ -123,6 +123,41 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
                          void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Backward pass of gdn_chunk_fwd: the gradients of a loss L with respect to q,
+ * k, v, g, beta and the initial state, given dL/dout and dL/dfinal_state.
+ * "Gated Delta Networks: Improving Mamba2 with Delta Rule", §3.3: the chunkwise
+ * form is differentiated chunk by chunk -- a reverse scan over the chunks
+ * carries the state gradient dS = gamma^C dS' + dO^T Q<- - dV_new^T W<- with
+ * dV_new = K-> dS'^T + (Q K^T o Gamma)^T dO, and each chunk's inputs get their
+ * gradients through the UT transform in parallel.  The forward states are
+ * recomputed from the inputs (nothing from the forward call is needed).
+ *   q, k, v, g, beta, init_state, cu_seqlens, B, T, H, dk, dv, dt, scale,
+ *   use_qk_l2norm, chunk_size   as in gdn_chunk_fwd.
+ *   dout          [B, T, H, dv] dtype dt: dL/dout.
+ *   dfinal_state  [N, H, dv, dk] fp32: dL/dfinal_state, or NULL for zeros.
+ *   dq, dk, dv    outputs [B, T, H, dk|dk|dv] dtype dt.
+ *   dg, dbeta     outputs [B, T, H] fp32.
+ *   dinit_state   output [N, H, dv, dk] fp32, or NULL to skip.
+ *   workspace     at least gdn_chunk_bwd_workspace_size() bytes, 256-byte aligned
+ *                 (fp32 intermediates, about 0.35 MB per chunk and head at
+ *                 dk = dv = 128).
+ * The kernels are fp32 on the CUDA cores.
+ * Errors: GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA.
+ */
+size_t gdn_chunk_bwd_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv,
+                                    int32_t num_seqs, gdn_dtype dt);
+
+gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v,
+                         const float *g, const float *beta,
+                         const float *init_state,
+                         const int32_t *cu_seqlens, int32_t num_seqs,
+                         const void *dout, const float *dfinal_state,
+                         void *dq, void *dk_, void *dv_, float *dg, float *dbeta, float *dinit_state,
+                         int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv,
+                         gdn_dtype dt, float scale, int32_t use_qk_l2norm, int32_t chunk_size,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * One decode step per (sequence, head), state updated in place.
  * "Gated DeltaNet：先忘一点，再按误差更新记忆", "为什么再加一个遗忘门？" and
  * "Decode 递归":  Sbar = alpha S;  S <- Sbar + beta (v - Sbar k) k^T;
