@@ -32,7 +32,7 @@ constexpr int kBT = 256;   // threads per block of every backward kernel
 // per (slot, head) fp32 workspace block
 // ---------------------------------------------------------------------------
 struct BwdLayout {
-    int64_t qh, kh, b, t, u, w, a, s, vn, dvn, dsn, dqh, dkh, dw, total;   // float offsets
+    int64_t qh, kh, qd, kd, b, t, u, w, a, s, vn, dvn, dsn, dqh, dkh, dw, total;   // float offsets
 };
 
 __host__ __device__ inline BwdLayout bwd_layout(int dk, int dv)
@@ -41,6 +41,8 @@ __host__ __device__ inline BwdLayout bwd_layout(int dk, int dv)
     int64_t o = 0;
     L.qh = o;  o += 64 * dk;
     L.kh = o;  o += 64 * dk;
+    L.qd = o;  o += 64 * dk;             // diag(gam) Q^
+    L.kd = o;  o += 64 * dk;             // diag(gC / gam) K^
     L.b = o;   o += 64;
     L.t = o;   o += 64 * 64;
     L.u = o;   o += 64 * dv;
@@ -73,16 +75,45 @@ __device__ __forceinline__ void block_gemm(int M, int N, int K, FA fa, FB fb, FO
     for (int m = 0; m < MT; ++m)
 #pragma unroll
         for (int n = 0; n < NT; ++n) acc[m][n] = 0.f;
-    for (int k0 = 0; k0 < K; k0 += 16) {
-        for (int e = tid; e < 16 * MR; e += kBT) {
+    static_assert((16 * MR) % kBT == 0 && (16 * NR) % kBT == 0, "tile sizes");
+    constexpr int EA = 16 * MR / kBT, EB = 16 * NR / kBT;   // tile elements per thread
+    float va[EA], vb[EB];
+    // the loads of a k-tile are all issued before any is stored, and the next tile's
+    // loads are in flight while the current one is multiplied
+    auto load = [&](int k0) {
+#pragma unroll
+        for (int u = 0; u < EA; ++u) {
+            const int e = tid + u * kBT;
             const int kk = AK ? (e & 15) : (e / MR), i = AK ? (e >> 4) : (e % MR);
-            sA[kk * MR + i] = (i < M && k0 + kk < K) ? fa(i, k0 + kk) : 0.f;
+            va[u] = (i < M && k0 + kk < K) ? fa(i, k0 + kk) : 0.f;
         }
-        for (int e = tid; e < 16 * NR; e += kBT) {
+#pragma unroll
+        for (int u = 0; u < EB; ++u) {
+            const int e = tid + u * kBT;
             const int kk = BK ? (e & 15) : (e / NR), j = BK ? (e >> 4) : (e % NR);
-            sB[kk * NR + j] = (j < N && k0 + kk < K) ? fb(k0 + kk, j) : 0.f;
+            vb[u] = (j < N && k0 + kk < K) ? fb(k0 + kk, j) : 0.f;
         }
-        __syncthreads();
+    };
+    auto store = [&]() {
+#pragma unroll
+        for (int u = 0; u < EA; ++u) {
+            const int e = tid + u * kBT;
+            const int kk = AK ? (e & 15) : (e / MR), i = AK ? (e >> 4) : (e % MR);
+            sA[kk * MR + i] = va[u];
+        }
+#pragma unroll
+        for (int u = 0; u < EB; ++u) {
+            const int e = tid + u * kBT;
+            const int kk = BK ? (e & 15) : (e / NR), j = BK ? (e >> 4) : (e % NR);
+            sB[kk * NR + j] = vb[u];
+        }
+    };
+    load(0);
+    store();
+    __syncthreads();
+    for (int k0 = 0; k0 < K; k0 += 16) {
+        const bool more = k0 + 16 < K;
+        if (more) load(k0 + 16);
 #pragma unroll 4
         for (int kk = 0; kk < 16; ++kk) {
             float a[MT], b[NT];
@@ -96,6 +127,10 @@ __device__ __forceinline__ void block_gemm(int M, int N, int K, FA fa, FB fb, FO
                 for (int n = 0; n < NT; ++n) acc[m][n] = fmaf(a[m], b[n], acc[m][n]);
         }
         __syncthreads();
+        if (more) {
+            store();
+            __syncthreads();
+        }
     }
 #pragma unroll
     for (int m = 0; m < MT; ++m)
@@ -185,6 +220,11 @@ bwd_prep_kernel(const BwdParams p)
     }
     __syncthreads();
     const float *qh = blk + LY.qh, *kh = blk + LY.kh;
+    for (int e = tid; e < 64 * dk; e += kBT) {
+        const int r = e / dk;
+        blk[LY.qd + e] = sgam[r] * qh[e];
+        blk[LY.kd + e] = expf(sb[63] - sb[r]) * kh[e];
+    }
     // KK = K^ K^T -> L (strictly lower, beta_r Gamma_ri KK_ri) into sL;  A = (Q^ K^T) o Gamma
     block_gemm<4, 4, true, true>(64, 64, dk, [&](int i, int k) { return kh[i * dk + k]; },
                                  [&](int k, int j) { return kh[j * dk + k]; },
@@ -224,21 +264,25 @@ bwd_prep_kernel(const BwdParams p)
 }
 
 // ---------------------------------------------------------------------------
-// bwd_fwd_scan_kernel: per (sequence, head) -- the state at every chunk start
-// (S_c, saved) and V_new = U - W S_c^T (saved), S_{c+1} = gC S_c + V_new^T Kd.
-// The state lives in shared memory.
+// bwd_fwd_scan_kernel: per (sequence, head, 32 rows of the state) -- the state at
+// every chunk start (S_c, saved) and V_new = U - W S_c^T (saved), then
+// S_{c+1} = gC S_c + V_new^T Kd.  State rows evolve independently, so each block
+// owns 32 of them, in shared memory.
 // ---------------------------------------------------------------------------
+constexpr int kScanRows = 32;
+
 __global__ void __launch_bounds__(kBT)
 bwd_fwd_scan_kernel(const BwdParams p)
 {
     extern __shared__ float smb[];
     const Geometry gm = p.gm;
     const int H = gm.H, dk = gm.dk, dv = gm.dv, n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    const int j0 = blockIdx.z * kScanRows;
     const BwdLayout LY = bwd_layout(dk, dv);
-    float *sA = smb, *sB = sA + kStage, *S = sB + kStage;   // S [dv][dk]
-    const int64_t SZ = (int64_t)dv * dk;
+    float *sA = smb, *sB = sA + kStage, *S = sB + kStage;   // S [32][dk]: rows j0 .. j0 + 31
+    const int64_t SZ = (int64_t)kScanRows * dk, so = (int64_t)j0 * dk;
     for (int64_t e = tid; e < SZ; e += kBT)
-        S[e] = p.init_state ? p.init_state[((int64_t)n * H + h) * SZ + e] : 0.f;
+        S[e] = p.init_state ? p.init_state[((int64_t)n * H + h) * dv * dk + so + e] : 0.f;
     int64_t tok0;
     int len;
     seq_span(gm, n, tok0, len);
@@ -247,30 +291,30 @@ bwd_fwd_scan_kernel(const BwdParams p)
     __syncthreads();
     for (int c = 0; c < nch; ++c) {
         float *blk = p.ws + ((slot0 + c) * H + h) * LY.total;
-        const float *b = blk + LY.b, *W = blk + LY.w, *U = blk + LY.u, *kh = blk + LY.kh;
-        for (int64_t e = tid; e < SZ; e += kBT) blk[LY.s + e] = S[e];
+        const float *b = blk + LY.b, *W = blk + LY.w, *U = blk + LY.u, *kd = blk + LY.kd;
+        for (int64_t e = tid; e < SZ; e += kBT) blk[LY.s + so + e] = S[e];
         float *vn = blk + LY.vn;
-        block_gemm<4, 16, true, true>(64, dv, dk, [&](int i, int k) { return W[i * dk + k]; },
-                                      [&](int k, int j) { return S[j * dk + k]; },
-                                      [&](int i, int j, float x) { vn[i * dv + j] = U[i * dv + j] - x; }, sA, sB);
+        block_gemm<4, 2, true, true>(64, kScanRows, dk, [&](int i, int k) { return W[i * dk + k]; },
+                                     [&](int k, int j) { return S[j * dk + k]; },
+                                     [&](int i, int j, float x) {
+                                         vn[i * dv + j0 + j] = U[i * dv + j0 + j] - x;
+                                     }, sA, sB);
         __syncthreads();
         const float gC = expf(b[63]);
-        for (int j0 = 0; j0 < dv; j0 += 128)   // S <- gC S + V_new^T Kd, 128 state rows per pass
-            block_gemm<8, 8, false, false>(min(128, dv - j0), dk, 64,
-                                           [&](int i, int r) { return vn[r * dv + j0 + i]; },
-                                           [&](int r, int d) { return expf(b[63] - b[r]) * kh[r * dk + d]; },
-                                           [&](int i, int d, float x) {
-                                               float &s_ = S[(int64_t)(j0 + i) * dk + d];
-                                               s_ = gC * s_ + x;
-                                           }, sA, sB);
+        block_gemm<2, 8, false, false>(kScanRows, dk, 64, [&](int i, int r) { return vn[r * dv + j0 + i]; },
+                                       [&](int r, int d) { return kd[r * dk + d]; },
+                                       [&](int i, int d, float x) {
+                                           float &s_ = S[(int64_t)i * dk + d];
+                                           s_ = gC * s_ + x;
+                                       }, sA, sB);
         __syncthreads();
     }
 }
 
 // ---------------------------------------------------------------------------
-// bwd_bwd_scan_kernel: per (sequence, head), chunks in reverse -- dS' (saved per
-// chunk), dV_new = Kd dS'^T + A^T dO (saved), dS = gC dS' + dO^T Qd - dV_new^T W;
-// the gradient of the initial state at the end.
+// bwd_bwd_scan_kernel: per (sequence, head, 32 state rows), chunks in reverse --
+// dS' (saved per chunk), dV_new = Kd dS'^T + A^T dO (saved),
+// dS = gC dS' + dO^T Qd - dV_new^T W; the gradient of the initial state at the end.
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(kBT)
@@ -279,11 +323,12 @@ bwd_bwd_scan_kernel(const BwdParams p)
     extern __shared__ float smb[];
     const Geometry gm = p.gm;
     const int H = gm.H, dk = gm.dk, dv = gm.dv, n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    const int j0 = blockIdx.z * kScanRows;
     const BwdLayout LY = bwd_layout(dk, dv);
-    float *sA = smb, *sB = sA + kStage, *dS = sB + kStage;   // dS [dv][dk]
-    const int64_t SZ = (int64_t)dv * dk;
+    float *sA = smb, *sB = sA + kStage, *dS = sB + kStage;   // dS [32][dk]
+    const int64_t SZ = (int64_t)kScanRows * dk, so = (int64_t)j0 * dk;
     for (int64_t e = tid; e < SZ; e += kBT)
-        dS[e] = p.dfinal ? p.dfinal[((int64_t)n * H + h) * SZ + e] : 0.f;
+        dS[e] = p.dfinal ? p.dfinal[((int64_t)n * H + h) * dv * dk + so + e] : 0.f;
     int64_t tok0;
     int len;
     seq_span(gm, n, tok0, len);
@@ -292,36 +337,35 @@ bwd_bwd_scan_kernel(const BwdParams p)
     __syncthreads();
     for (int c = nch - 1; c >= 0; --c) {
         float *blk = p.ws + ((slot0 + c) * H + h) * LY.total;
-        const float *b = blk + LY.b, *W = blk + LY.w, *A = blk + LY.a, *kh = blk + LY.kh, *qh = blk + LY.qh;
+        const float *b = blk + LY.b, *W = blk + LY.w, *A = blk + LY.a, *kd = blk + LY.kd, *qd = blk + LY.qd;
         const int64_t t0 = tok0 + (int64_t)c * kChunk;
         const int rows = min(kChunk, len - c * kChunk);
-        for (int64_t e = tid; e < SZ; e += kBT) blk[LY.dsn + e] = dS[e];
+        for (int64_t e = tid; e < SZ; e += kBT) blk[LY.dsn + so + e] = dS[e];
         float *dvn = blk + LY.dvn;
         auto dO = [&](int r, int j) { return r < rows ? ld<T>(p.dout, ((t0 + r) * H + h) * dv + j) : 0.f; };
-        // dV_new = Kd dS'^T + A^T dO
-        block_gemm<4, 16, true, true>(64, dv, dk + 64,
-                                      [&](int r, int k) {
-                                          return k < dk ? expf(b[63] - b[r]) * kh[r * dk + k] : A[(k - dk) * 64 + r];
-                                      },
-                                      [&](int k, int j) { return k < dk ? dS[(int64_t)j * dk + k] : dO(k - dk, j); },
-                                      [&](int r, int j, float x) { dvn[r * dv + j] = x; }, sA, sB);
+        // dV_new = Kd dS'^T + A^T dO  (columns j0 .. j0 + 31)
+        block_gemm<4, 2, true, true>(64, kScanRows, dk + 64,
+                                     [&](int r, int k) { return k < dk ? kd[r * dk + k] : A[(k - dk) * 64 + r]; },
+                                     [&](int k, int j) {
+                                         return k < dk ? dS[(int64_t)j * dk + k] : dO(k - dk, j0 + j);
+                                     },
+                                     [&](int r, int j, float x) { dvn[r * dv + j0 + j] = x; }, sA, sB);
         __syncthreads();
         // dS <- gC dS' + dO^T Qd - dV_new^T W
         const float gC = expf(b[63]);
-        for (int j0 = 0; j0 < dv; j0 += 128)
-            block_gemm<8, 8, false, false>(min(128, dv - j0), dk, 128,
-                                           [&](int i, int k) { return k < 64 ? dO(k, j0 + i) : -dvn[(k - 64) * dv + j0 + i]; },
-                                           [&](int k, int d) {
-                                               return k < 64 ? expf(b[k]) * qh[k * dk + d] : W[(k - 64) * dk + d];
-                                           },
-                                           [&](int i, int d, float x) {
-                                               float &s_ = dS[(int64_t)(j0 + i) * dk + d];
-                                               s_ = gC * s_ + x;
-                                           }, sA, sB);
+        block_gemm<2, 8, false, false>(kScanRows, dk, 128,
+                                       [&](int i, int k) {
+                                           return k < 64 ? dO(k, j0 + i) : -dvn[(k - 64) * dv + j0 + i];
+                                       },
+                                       [&](int k, int d) { return k < 64 ? qd[k * dk + d] : W[(k - 64) * dk + d]; },
+                                       [&](int i, int d, float x) {
+                                           float &s_ = dS[(int64_t)i * dk + d];
+                                           s_ = gC * s_ + x;
+                                       }, sA, sB);
         __syncthreads();
     }
     if (p.dinit)
-        for (int64_t e = tid; e < SZ; e += kBT) p.dinit[((int64_t)n * H + h) * SZ + e] = dS[e];
+        for (int64_t e = tid; e < SZ; e += kBT) p.dinit[((int64_t)n * H + h) * dv * dk + so + e] = dS[e];
 }
 
 // ---------------------------------------------------------------------------
@@ -335,7 +379,7 @@ bwd_bwd_scan_kernel(const BwdParams p)
 //   then dq, dk through the normalisations.
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(kBT)
+__global__ void __launch_bounds__(kBT, 2)
 bwd_local_kernel(const BwdParams p)
 {
     extern __shared__ float smb[];
@@ -348,7 +392,8 @@ bwd_local_kernel(const BwdParams p)
     const BwdLayout LY = bwd_layout(dk, dv);
     float *blk = p.ws + (slot * H + h) * LY.total;
     float *sA = smb, *sB = sA + kStage;
-    float *sDA = sB + kStage, *sDT = sDA + 4096, *sX = sDT + 4096, *sDL = sX + 4096, *sGG = sDL + 4096;
+    float *sDA = sB + kStage, *sDT = sDA + 4096, *sX = sDT + 4096, *sGG = sX + 4096;
+    float *sDL = sDT;   // dT is dead once X = T^T dT is formed
     float *sb = sGG + 4096, *sbe = sb + 64, *sgam = sbe + 64, *sdgam = sgam + 64, *sdkdf = sdgam + 64,
           *sdbeta = sdkdf + 64, *st = sdbeta + 64, *sred = st + 64;   // sred [kBT]
     const float *qh = blk + LY.qh, *kh = blk + LY.kh, *Tm = blk + LY.t, *S = blk + LY.s, *Vn = blk + LY.vn,
@@ -526,8 +571,8 @@ cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t st)
     p.gm = a.gm; p.scale = a.scale; p.l2 = a.l2;
     const size_t stage = 2 * (size_t)kStage * sizeof(float);
     const size_t sm_prep = stage + sizeof(float) * (64 * 65 + 3 * 64);
-    const size_t sm_scan = stage + sizeof(float) * (size_t)a.gm.dv * a.gm.dk;
-    const size_t sm_local = stage + sizeof(float) * (5 * 4096 + 7 * 64 + kBT);
+    const size_t sm_scan = stage + sizeof(float) * (size_t)kScanRows * a.gm.dk;
+    const size_t sm_local = stage + sizeof(float) * (4 * 4096 + 7 * 64 + kBT);
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(bwd_prep_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_prep)))
         return e;
@@ -538,8 +583,9 @@ cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t st)
     if ((e = cudaFuncSetAttribute(bwd_local_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_local)))
         return e;
     if (a.slots > 0) bwd_prep_kernel<T><<<dim3((unsigned)a.slots, a.gm.H), kBT, sm_prep, st>>>(p);
-    bwd_fwd_scan_kernel<<<dim3(a.gm.N, a.gm.H), kBT, sm_scan, st>>>(p);
-    bwd_bwd_scan_kernel<T><<<dim3(a.gm.N, a.gm.H), kBT, sm_scan, st>>>(p);
+    const dim3 sgrid(a.gm.N, a.gm.H, a.gm.dv / kScanRows);
+    bwd_fwd_scan_kernel<<<sgrid, kBT, sm_scan, st>>>(p);
+    bwd_bwd_scan_kernel<T><<<sgrid, kBT, sm_scan, st>>>(p);
     if (a.slots > 0) bwd_local_kernel<T><<<dim3((unsigned)a.slots, a.gm.H), kBT, sm_local, st>>>(p);
     return cudaGetLastError();
 }
