@@ -488,7 +488,8 @@ def bench_prologue(w: inputs.Workload, dev, flush, stream, reps: int, peaks, K: 
     ach = nbytes / (ms * 1e-3) / 1e9
     return {"workload": f"{PREFILL} projections, conv width {K}", "unit": "tokens/s", "ms_per_call": ms,
             "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": ach / peaks["hbm_gbs"], "algorithmic_bytes": nbytes},
+                         "frac": ach / peaks["hbm_gbs"], "traffic": traffic_record("prologue"),
+                         "algorithmic_bytes": nbytes},
             "timing": f"median of {max(reps, 5)} calls, L2 flushed before each"}
 
 
