@@ -910,9 +910,9 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     *reinterpret_cast<float4 *>(p.final_state + srow + d) = v4;
                 }
         } else do {
-            bool ok = wait_spin(bar(RB_SCF), 0, abort_flag, p.err);
-            {   // initial state: this thread's 64 entries of row j
-                const float e0 = reinterpret_cast<const float *>(sm + R_SCR)[128];
+            {   // initial state: this thread's 64 entries of row j.  The bf16 copy (A of the
+                // first a2) goes out before the first factor slot is waited for; the
+                // pre-decayed fp32 state (gating the first c) after it.
                 uint32_t sv[64];
 #pragma unroll
                 for (int e = 0; e < 64; e += 4) {
@@ -922,6 +922,11 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     sv[e + 2] = __float_as_uint(v4.z); sv[e + 3] = __float_as_uint(v4.w);
                 }
                 put_sbf(sv);
+                fence_proxy_async();
+                if (gsync(*abort_flag)) break;
+                if (leader) mbar_arrive(bar(RB_S));
+                if (!gwait(RB_SCF, 0)) break;
+                const float e0 = reinterpret_cast<const float *>(sm + R_SCR)[128];
 #pragma unroll
                 for (int e = 0; e < 64; ++e) sv[e] = __float_as_uint(e0 * __uint_as_float(sv[e]));
 #pragma unroll
@@ -929,10 +934,9 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     tmem_st16(lane_base + TM_S + hf * 64 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(sv + q * 16));
                 tmem_wait_st();
             }
-            fence_proxy_async();
             fence_before_sync();
-            if (gsync(!ok || *abort_flag)) break;
-            if (leader) { mbar_arrive(bar(RB_S)); mbar_arrive(bar(RB_SP)); }
+            if (gsync(*abort_flag)) break;
+            if (leader) mbar_arrive(bar(RB_SP));
             for (int c = 0; c < nch; ++c) {
                 // ---- X: this thread's 32 tokens of V_new^T row j
                 if (!gwait(RB_D1, c & 1)) break;
@@ -986,18 +990,17 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     if (gsync(*abort_flag)) break;
                     if (leader) mbar_arrive(bar(RB_SP));  // the fp32 state is pre-decayed for the next c
                     if (leader) GDN_TR(p.trace, 2, c, 5);
-                } else if (p.final_state) {
+                } else if (p.final_state) {   // one tensor-memory round trip, then 16-B stores
+                    uint32_t u[64];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t u[16];
-                        tmem_ld16(lane_base + TM_S + hf * 64 + q * 16, u);
-                        tmem_wait_ld();
+                    for (int q = 0; q < 4; ++q)
+                        tmem_ld16(lane_base + TM_S + hf * 64 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(u + q * 16));
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 16; e += 4)
-                            *reinterpret_cast<float4 *>(p.final_state + srow + hf * 64 + q * 16 + e) =
-                                make_float4(__uint_as_float(u[e]), __uint_as_float(u[e + 1]),
-                                            __uint_as_float(u[e + 2]), __uint_as_float(u[e + 3]));
-                    }
+                    for (int e = 0; e < 64; e += 4)
+                        *reinterpret_cast<float4 *>(p.final_state + srow + hf * 64 + e) =
+                            make_float4(__uint_as_float(u[e]), __uint_as_float(u[e + 1]),
+                                        __uint_as_float(u[e + 2]), __uint_as_float(u[e + 3]));
                 }
             }
         } while (false);
