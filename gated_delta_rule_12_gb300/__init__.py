@@ -93,6 +93,8 @@ def load_library(path: str = LIB_PATH, build_if_missing: bool = False) -> ctypes
         lib.gdn_prologue.restype = ctypes.c_int
         lib.gdn_check_device_error.argtypes = [_vp, _vp]
         lib.gdn_check_device_error.restype = ctypes.c_int
+        lib.gdn_selftest_wait_timeout.argtypes = [_vp, ctypes.c_uint32, _vp]
+        lib.gdn_selftest_wait_timeout.restype = ctypes.c_int
         lib.gdn_chunk_fwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
                                               _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _f32, _i32, _i32,
                                               _vp]
@@ -301,6 +303,16 @@ def check_device_error(workspace, stream=None):
     rc = load_library().gdn_check_device_error(_ptr(workspace), _stream(stream))
     if rc != GDN_OK:
         raise GDNError(rc, "gdn_check_device_error")
+
+
+def selftest_wait_timeout(workspace, limit_us=20000, stream=None):
+    """``gdn_selftest_wait_timeout``: enqueue a kernel whose bounded wait on a phase that nothing
+    completes gives up after ``limit_us`` and records the timeout in ``workspace``'s error word
+    (read back by ``check_device_error``, which then raises GDN_ERR_DEVICE_TIMEOUT)."""
+    _need_cuda(workspace)
+    rc = load_library().gdn_selftest_wait_timeout(_ptr(workspace), int(limit_us), _stream(stream))
+    if rc != GDN_OK:
+        raise GDNError(rc, "gdn_selftest_wait_timeout")
 
 
 def chunk_fwd_noalloc(q, k, v, g, beta, out, final_state=None, init_state=None, cu_seqlens=None, scale=None,

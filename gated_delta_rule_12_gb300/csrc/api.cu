@@ -250,6 +250,16 @@ gdn_status gdn_prologue(const void *xq, const void *xk, const void *xv, const fl
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+gdn_status gdn_selftest_wait_timeout(void *workspace, uint32_t limit_us, void *stream)
+{
+    if (!workspace || ((uintptr_t)workspace & 255u) != 0) return GDN_ERR_INVALID_ARG;
+    if (limit_us < 1 || limit_us > 1000000u) return GDN_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemsetAsync(workspace, 0, sizeof(unsigned), st) != cudaSuccess) return GDN_ERR_CUDA;
+    cudaError_t e = launch_wait_selftest(reinterpret_cast<unsigned *>(workspace), (uint64_t)limit_us * 1000u, st);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 gdn_status gdn_check_device_error(void *workspace, void *stream)
 {
     if (!workspace || ((uintptr_t)workspace & 255u) != 0) return GDN_ERR_INVALID_ARG;

@@ -132,14 +132,15 @@ long long *g_trace_buffer = nullptr;
 #define GDN_UTR(trace, ev) do { } while (0)
 #endif
 
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned *err)
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned *err,
+                                         uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             *abort_flag = 1;
             atomicExch(err, kDevErrTimeout);
             return false;
@@ -1086,6 +1087,30 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     }
 }
 
+// ===========================================================================
+// self-test of the bounded wait
+// ===========================================================================
+// One CTA waits, through the same bounded wait as the kernels above, on an mbarrier
+// phase that nothing completes.  The wait gives up after limit_ns, records
+// kDevErrTimeout in the error word and raises the CTA's abort flag, and every thread
+// leaves; nothing faults and the context stays usable.
+__global__ void __launch_bounds__(128)
+wait_selftest_kernel(unsigned *err, uint64_t limit_ns)
+{
+    __shared__ uint64_t barrier_word;
+    __shared__ int abort_word;
+    const uint32_t b = smem_u32(&barrier_word);
+    volatile int *abort_flag = &abort_word;
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) wait_bar(b, 0, abort_flag, err, limit_ns);   // no arrival ever comes
+    __syncthreads();
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -1126,6 +1151,12 @@ extern "C" void gdn_debug_set_trace(long long *buf) { g_trace_buffer = buf; }
 bool chunk_tc_supported(int dt, int dk, int dv, int64_t tokens)
 {
     return dt == 1 && dk == 128 && dv % 128 == 0 && tokens > 0 && tokens < ((int64_t)1 << 31);
+}
+
+cudaError_t launch_wait_selftest(unsigned *err, uint64_t limit_ns, cudaStream_t st)
+{
+    wait_selftest_kernel<<<1, 128, 0, st>>>(err, limit_ns);
+    return cudaGetLastError();
 }
 
 size_t chunk_tc_workspace_bytes(int64_t slots, int H)

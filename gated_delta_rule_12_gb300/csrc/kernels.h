@@ -66,5 +66,7 @@ bool chunk_tc_supported(int dt, int dk, int dv, int64_t tokens);
 size_t chunk_tc_workspace_bytes(int64_t slots, int H);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
+// one CTA whose bounded wait on a never-completed mbarrier phase gives up after limit_ns
+cudaError_t launch_wait_selftest(unsigned *err, uint64_t limit_ns, cudaStream_t st);
 
 }  // namespace gdn

@@ -203,6 +203,20 @@ gdn_status gdn_decode_multi(float *state,
 gdn_status gdn_check_device_error(void *workspace, void *stream);
 
 /*
+ * Self-test of the failure path (no counterpart on the pages).  Enqueues on
+ * `stream` one kernel that waits, with the same bounded wait the tensor-core
+ * kernels use for every mbarrier phase, on a phase that nothing completes.
+ * After limit_us microseconds (1 .. 1e6) the wait gives up and the kernel
+ * records the timeout in the device error word at the start of `workspace`
+ * (256-byte aligned, at least 256 bytes; the word is cleared first), then
+ * exits: nothing faults, and a following gdn_check_device_error on the same
+ * workspace returns GDN_ERR_DEVICE_TIMEOUT (and clears the word).  Returns
+ * GDN_OK once enqueued, GDN_ERR_INVALID_ARG for a bad pointer or limit,
+ * GDN_ERR_CUDA if the launch fails.
+ */
+gdn_status gdn_selftest_wait_timeout(void *workspace, uint32_t limit_us, void *stream);
+
+/*
  * Block prologue: q, k, v, g, beta from their linear projections, in one pass.
  * "Gated Delta Networks: Improving Mamba2 with Delta Rule", §3.4 "Token mixing
  * block" and Fig. 1: q, k, v = SiLU(short causal depthwise convolution of the

@@ -117,6 +117,33 @@ def test_device_error_word_clear_after_call():
     gdn.check_device_error(ws)   # raises if the word is not clear
 
 
+def test_bounded_wait_gives_up_and_reports_timeout():
+    """The failure path without a fault: a kernel whose bounded wait (the one every mbarrier wait of
+    the tensor-core kernels uses) sees a phase that nothing completes gives up after its limit, the
+    error word reads back as GDN_ERR_DEVICE_TIMEOUT, and a chunked-forward call on the same workspace
+    afterwards runs and matches the oracle: the context stays usable."""
+    import time
+    ws = torch.zeros((gdn.chunk_fwd_workspace_size(1, 128, 2, 128, 128, 0, torch.bfloat16),),
+                     dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    gdn.selftest_wait_timeout(ws, limit_us=20000)
+    with pytest.raises(gdn.GDNError) as err:
+        gdn.check_device_error(ws)
+    assert err.value.code == 5, err.value            # GDN_ERR_DEVICE_TIMEOUT
+    assert time.perf_counter() - t0 >= 0.02          # it waited out its limit
+    gdn.check_device_error(ws)                        # reading the word cleared it
+    d = inputs.make_prefill(B=1, L=128, H=2, dk=128, dv=128, dtype="bf16", seed=31, init_state=True)
+    dd = cuda(d)
+    out, sf = gdn.chunk_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], init_state=dd["init_state"],
+                            workspace=ws)
+    gdn.check_device_error(ws)
+    ro, rs = oracle.recurrent_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], init_state=d["init_state"],
+                                  scale=128 ** -0.5, use_qk_l2norm=True)
+    assert_close(out, ro, "bf16", "out after the timeout")
+    assert_close(sf, rs, "bf16", "final_state after the timeout")
+
+
 # ---------------------------------------------------------------------------
 # full-size workloads
 # ---------------------------------------------------------------------------
