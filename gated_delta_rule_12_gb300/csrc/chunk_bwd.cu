@@ -61,20 +61,51 @@ __host__ __device__ inline BwdLayout bwd_layout(int dk, int dv)
 
 // ---------------------------------------------------------------------------
 // block GEMM: out(i, j, sum_k A(i, k) B(k, j)) for i < M <= 16 MT, j < N <= 16 NT,
-// all kBT threads of the block (a 16 x 16 grid, MT x NT outputs each).  A and B
-// are read through functors; AK / BK say whether consecutive k are contiguous in
-// memory (then the tile loads run along k), so the staging loads coalesce.
+// all kBT threads of the block.  A and B are read through functors; AK / BK say
+// whether consecutive k are contiguous in memory (then the tile loads run along k),
+// so the staging loads coalesce.  Each 16-wide k-tile is staged in shared memory
+// (pitch MR + 4 and NR + 4, which makes the fragment loads below conflict-free) and
+// multiplied on the tensor cores: mma.sync m16n8k8 in tf32, each operand split into
+// a tf32 head and a tf32 tail and the three products head*head + head*tail +
+// tail*head accumulated in fp32, which keeps fp32 accuracy (the tail*tail term is
+// below fp32 rounding).  The 8 warps tile the output as (MR / 16) x (8 / (MR / 16))
+// blocks of 16 rows.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t tf32_of(float x)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo)
+{
+    hi = tf32_of(x);
+    lo = tf32_of(x - __uint_as_float(hi));
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2])
+{
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 "
+                 "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 template <int MT, int NT, bool AK, bool BK, class FA, class FB, class FO>
 __device__ __forceinline__ void block_gemm(int M, int N, int K, FA fa, FB fb, FO fo, float *sA, float *sB)
 {
-    constexpr int MR = 16 * MT, NR = 16 * NT;
-    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-    float acc[MT][NT];
+    constexpr int MR = 16 * MT, NR = 16 * NT, MRP = MR + 4, NRP = NR + 4;
+    constexpr int WM = MR / 16, WN = 8 / WM;          // warps along M and N
+    static_assert(WM * WN == kBT / 32 && NR % (8 * WN) == 0, "warp tiling");
+    constexpr int NTW = NR / WN / 8;                  // n8 tiles per warp
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int m0 = 16 * (warp % WM), n0 = (NR / WN) * (warp / WM);
+    float acc[NTW][4];
 #pragma unroll
-    for (int m = 0; m < MT; ++m)
+    for (int n = 0; n < NTW; ++n)
 #pragma unroll
-        for (int n = 0; n < NT; ++n) acc[m][n] = 0.f;
+        for (int q = 0; q < 4; ++q) acc[n][q] = 0.f;
     static_assert((16 * MR) % kBT == 0 && (16 * NR) % kBT == 0, "tile sizes");
     constexpr int EA = 16 * MR / kBT, EB = 16 * NR / kBT;   // tile elements per thread
     float va[EA], vb[EB];
@@ -99,13 +130,13 @@ __device__ __forceinline__ void block_gemm(int M, int N, int K, FA fa, FB fb, FO
         for (int u = 0; u < EA; ++u) {
             const int e = tid + u * kBT;
             const int kk = AK ? (e & 15) : (e / MR), i = AK ? (e >> 4) : (e % MR);
-            sA[kk * MR + i] = va[u];
+            sA[kk * MRP + i] = va[u];
         }
 #pragma unroll
         for (int u = 0; u < EB; ++u) {
             const int e = tid + u * kBT;
             const int kk = BK ? (e & 15) : (e / NR), j = BK ? (e >> 4) : (e % NR);
-            sB[kk * NR + j] = vb[u];
+            sB[kk * NRP + j] = vb[u];
         }
     };
     load(0);
@@ -114,17 +145,22 @@ __device__ __forceinline__ void block_gemm(int M, int N, int K, FA fa, FB fb, FO
     for (int k0 = 0; k0 < K; k0 += 16) {
         const bool more = k0 + 16 < K;
         if (more) load(k0 + 16);
-#pragma unroll 4
-        for (int kk = 0; kk < 16; ++kk) {
-            float a[MT], b[NT];
 #pragma unroll
-            for (int m = 0; m < MT; ++m) a[m] = sA[kk * MR + ty + 16 * m];
+        for (int ks = 0; ks < 16; ks += 8) {
+            uint32_t ah[4], al[4];
+            split_tf32(sA[(ks + t) * MRP + m0 + g], ah[0], al[0]);
+            split_tf32(sA[(ks + t) * MRP + m0 + g + 8], ah[1], al[1]);
+            split_tf32(sA[(ks + t + 4) * MRP + m0 + g], ah[2], al[2]);
+            split_tf32(sA[(ks + t + 4) * MRP + m0 + g + 8], ah[3], al[3]);
 #pragma unroll
-            for (int n = 0; n < NT; ++n) b[n] = sB[kk * NR + tx + 16 * n];
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-#pragma unroll
-                for (int n = 0; n < NT; ++n) acc[m][n] = fmaf(a[m], b[n], acc[m][n]);
+            for (int n = 0; n < NTW; ++n) {
+                uint32_t bh[2], bl[2];
+                split_tf32(sB[(ks + t) * NRP + n0 + 8 * n + g], bh[0], bl[0]);
+                split_tf32(sB[(ks + t + 4) * NRP + n0 + 8 * n + g], bh[1], bl[1]);
+                mma_tf32(acc[n], al, bh);
+                mma_tf32(acc[n], ah, bl);
+                mma_tf32(acc[n], ah, bh);
+            }
         }
         __syncthreads();
         if (more) {
@@ -133,16 +169,16 @@ __device__ __forceinline__ void block_gemm(int M, int N, int K, FA fa, FB fb, FO
         }
     }
 #pragma unroll
-    for (int m = 0; m < MT; ++m)
+    for (int n = 0; n < NTW; ++n)
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-            const int i = ty + 16 * m, j = tx + 16 * n;
-            if (i < M && j < N) fo(i, j, acc[m][n]);
+        for (int q = 0; q < 4; ++q) {
+            const int i = m0 + g + 8 * (q >> 1), j = n0 + 8 * n + 2 * t + (q & 1);
+            if (i < M && j < N) fo(i, j, acc[n][q]);
         }
 }
 
-// shared staging of block_gemm: up to 16 x 256 floats for A and for B
-constexpr int kStage = 16 * 256;
+// shared staging of block_gemm: up to 16 x (256 + 4) floats for A and for B
+constexpr int kStage = 16 * (256 + 4);
 
 // The chunk (sequence n, chunk c) of `slot` and its token range; false if none.
 __device__ __forceinline__ bool chunk_of(const Geometry &gm, int64_t slot, int &n, int &c, int64_t &tok0, int &rows)
