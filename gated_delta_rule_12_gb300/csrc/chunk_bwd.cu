@@ -204,7 +204,7 @@ __device__ __forceinline__ float ld(const void *p, int64_t i) { return to_f32(re
 // bwd_prep_kernel: per (slot, head) -- q^, k^, b, T = (I + L)^{-1}, U, W, A
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(kBT)
+__global__ void __launch_bounds__(kBT, 2)
 bwd_prep_kernel(const BwdParams p)
 {
     extern __shared__ float smb[];
