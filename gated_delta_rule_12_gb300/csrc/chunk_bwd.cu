@@ -92,10 +92,18 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-template <int MT, int NT, bool AK, bool BK, class FA, class FB, class FO>
-__device__ __forceinline__ void block_gemm(int M, int N, int K, FA fa, FB fb, FO fo, float *sA, float *sB)
+// shared staging of block_gemm: up to 16 x (128 + 4) floats for A and for B
+constexpr int kStage = 16 * (128 + 4);
+
+// NRS > 0: fo also returns NRS per-element contributions (a float2) to row sums,
+// which are reduced in registers and across the 4 lanes that share a row, then added
+// to rs0[i] (and rs1[i]) with one shared-memory atomic per row and warp.
+template <int MT, int NT, bool AK, bool BK, int NRS = 0, class FA, class FB, class FO>
+__device__ __forceinline__ void block_gemm(int M, int N, int K, FA fa, FB fb, FO fo, float *sA, float *sB,
+                                           float *rs0 = nullptr, float *rs1 = nullptr)
 {
     constexpr int MR = 16 * MT, NR = 16 * NT, MRP = MR + 4, NRP = NR + 4;
+    static_assert(16 * MRP <= kStage && 16 * NRP <= kStage, "staging size");
     constexpr int WM = MR / 16, WN = 8 / WM;          // warps along M and N
     static_assert(WM * WN == kBT / 32 && NR % (8 * WN) == 0, "warp tiling");
     constexpr int NTW = NR / WN / 8;                  // n8 tiles per warp
@@ -168,17 +176,55 @@ __device__ __forceinline__ void block_gemm(int M, int N, int K, FA fa, FB fb, FO
             __syncthreads();
         }
     }
+    float rsum[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
     for (int n = 0; n < NTW; ++n)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int i = m0 + g + 8 * (q >> 1), j = n0 + 8 * n + 2 * t + (q & 1);
-            if (i < M && j < N) fo(i, j, acc[n][q]);
+            if (i < M && j < N) {
+                if constexpr (NRS > 0) {
+                    const float2 c = fo(i, j, acc[n][q]);
+                    rsum[q >> 1][0] += c.x;
+                    rsum[q >> 1][1] += c.y;
+                } else {
+                    fo(i, j, acc[n][q]);
+                }
+            }
         }
+    if constexpr (NRS > 0) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int s = 0; s < NRS; ++s) {
+                float v = rsum[hh][s];
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                rsum[hh][s] = v;
+            }
+        if (t == 0)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int i = m0 + g + 8 * hh;
+                if (i < M) {
+                    atomicAdd(&rs0[i], rsum[hh][0]);
+                    if constexpr (NRS > 1) atomicAdd(&rs1[i], rsum[hh][1]);
+                }
+            }
+    }
 }
 
-// shared staging of block_gemm: up to 16 x (256 + 4) floats for A and for B
-constexpr int kStage = 16 * (256 + 4);
+// block_gemm over column blocks of 128 (N up to 256): fb and fo see global column indices.
+template <int MT, bool AK, bool BK, int NRS = 0, class FA, class FB, class FO>
+__device__ __forceinline__ void block_gemm_cols(int M, int N, int K, FA fa, FB fb, FO fo, float *sA, float *sB,
+                                                float *rs0 = nullptr, float *rs1 = nullptr)
+{
+    for (int j0 = 0; j0 < N; j0 += 128) {
+        block_gemm<MT, 8, AK, BK, NRS>(
+            M, min(N - j0, 128), K, fa, [&](int k, int j) { return fb(k, j0 + j); },
+            [&](int i, int j, float x) { return fo(i, j0 + j, x); }, sA, sB, rs0, rs1);
+    }   // block_gemm ends with a barrier after its last shared reads, so the next block may restage
+}
 
 // The chunk (sequence n, chunk c) of `slot` and its token range; false if none.
 __device__ __forceinline__ bool chunk_of(const Geometry &gm, int64_t slot, int &n, int &c, int64_t &tok0, int &rows)
@@ -289,14 +335,14 @@ bwd_prep_kernel(const BwdParams p)
     __syncthreads();
     const float *Tm = blk + LY.t;
     // U = T diag(beta) V,  W = T diag(beta gam) K^
-    block_gemm<4, 16, true, false>(64, dv, 64, [&](int i, int k) { return Tm[i * 64 + k]; },
-                                   [&](int k, int j) {
-                                       return k < rows ? sbe[k] * ld<T>(p.v, ((tok0 + k) * H + h) * dv + j) : 0.f;
-                                   },
-                                   [&](int i, int j, float x) { blk[LY.u + i * dv + j] = x; }, sA, sB);
-    block_gemm<4, 16, true, false>(64, dk, 64, [&](int i, int k) { return Tm[i * 64 + k]; },
-                                   [&](int k, int j) { return sbe[k] * sgam[k] * kh[k * dk + j]; },
-                                   [&](int i, int j, float x) { blk[LY.w + i * dk + j] = x; }, sA, sB);
+    block_gemm_cols<4, true, false>(64, dv, 64, [&](int i, int k) { return Tm[i * 64 + k]; },
+                                    [&](int k, int j) {
+                                        return k < rows ? sbe[k] * ld<T>(p.v, ((tok0 + k) * H + h) * dv + j) : 0.f;
+                                    },
+                                    [&](int i, int j, float x) { blk[LY.u + i * dv + j] = x; }, sA, sB);
+    block_gemm_cols<4, true, false>(64, dk, 64, [&](int i, int k) { return Tm[i * 64 + k]; },
+                                    [&](int k, int j) { return sbe[k] * sgam[k] * kh[k * dk + j]; },
+                                    [&](int i, int j, float x) { blk[LY.w + i * dk + j] = x; }, sA, sB);
 }
 
 // ---------------------------------------------------------------------------
@@ -431,7 +477,7 @@ bwd_local_kernel(const BwdParams p)
     float *sDA = sB + kStage, *sDT = sDA + 4096, *sX = sDT + 4096, *sGG = sX + 4096;
     float *sDL = sDT;   // dT is dead once X = T^T dT is formed
     float *sb = sGG + 4096, *sbe = sb + 64, *sgam = sbe + 64, *sdgam = sgam + 64, *sdkdf = sdgam + 64,
-          *sdbeta = sdkdf + 64, *st = sdbeta + 64, *sred = st + 64;   // sred [kBT]
+          *sdbeta = sdkdf + 64, *st = sdbeta + 64, *sfk = st + 64, *sred = sfk + 64;   // sred [kBT]
     const float *qh = blk + LY.qh, *kh = blk + LY.kh, *Tm = blk + LY.t, *S = blk + LY.s, *Vn = blk + LY.vn,
                 *dVn = blk + LY.dvn, *dSn = blk + LY.dsn;
     float *dQ = blk + LY.dqh, *dK = blk + LY.dkh, *dW = blk + LY.dw;
@@ -444,52 +490,55 @@ bwd_local_kernel(const BwdParams p)
         sdbeta[tid] = 0.f;
     }
     __syncthreads();
+    if (tid < 64) sfk[tid] = expf(sb[63] - sb[tid]);   // gC / gam
     const float gC = expf(sb[63]);
     auto dOf = [&](int r, int j) { return r < rows ? ld<T>(p.dout, ((tok0 + r) * H + h) * dv + j) : 0.f; };
     auto Vf = [&](int r, int j) { return r < rows ? ld<T>(p.v, ((tok0 + r) * H + h) * dv + j) : 0.f; };
     auto Gam = [&](int r, int i) { return i <= r ? expf(sb[r] - sb[i]) : 0.f; };
 
     // dQd = dO S  ->  dQ = gam dQd,  dgam += Q^ . dQd
-    block_gemm<4, 16, true, false>(64, dk, dv, [&](int r, int j) { return dOf(r, j); },
-                                   [&](int j, int d) { return S[(int64_t)j * dk + d]; },
-                                   [&](int r, int d, float x) {
-                                       dQ[r * dk + d] = sgam[r] * x;
-                                       atomicAdd(&sdgam[r], qh[r * dk + d] * x);
-                                   }, sA, sB);
+    block_gemm_cols<4, true, false, 1>(64, dk, dv, [&](int r, int j) { return dOf(r, j); },
+                                       [&](int j, int d) { return S[(int64_t)j * dk + d]; },
+                                       [&](int r, int d, float x) {
+                                           dQ[r * dk + d] = sgam[r] * x;
+                                           return make_float2(qh[r * dk + d] * x, 0.f);
+                                       }, sA, sB, sdgam);
     // dKd = V_new dS'  ->  dK = (gC / gam) dKd,  dkdf += K^ . dKd
-    block_gemm<4, 16, true, false>(64, dk, dv, [&](int r, int j) { return Vn[r * dv + j]; },
-                                   [&](int j, int d) { return dSn[(int64_t)j * dk + d]; },
-                                   [&](int r, int d, float x) {
-                                       dK[r * dk + d] = expf(sb[63] - sb[r]) * x;
-                                       atomicAdd(&sdkdf[r], kh[r * dk + d] * x);
-                                   }, sA, sB);
+    block_gemm_cols<4, true, false, 1>(64, dk, dv, [&](int r, int j) { return Vn[r * dv + j]; },
+                                       [&](int j, int d) { return dSn[(int64_t)j * dk + d]; },
+                                       [&](int r, int d, float x) {
+                                           dK[r * dk + d] = sfk[r] * x;
+                                           return make_float2(kh[r * dk + d] * x, 0.f);
+                                       }, sA, sB, sdkdf);
     // dW = -dV_new S
-    block_gemm<4, 16, true, false>(64, dk, dv, [&](int r, int j) { return dVn[r * dv + j]; },
-                                   [&](int j, int d) { return S[(int64_t)j * dk + d]; },
-                                   [&](int r, int d, float x) { dW[r * dk + d] = -x; }, sA, sB);
+    block_gemm_cols<4, true, false>(64, dk, dv, [&](int r, int j) { return dVn[r * dv + j]; },
+                                    [&](int j, int d) { return S[(int64_t)j * dk + d]; },
+                                    [&](int r, int d, float x) { dW[r * dk + d] = -x; }, sA, sB);
     // dA = tril(dO V_new^T) (diagonal included)
     block_gemm<4, 4, true, true>(64, 64, dv, [&](int r, int j) { return dOf(r, j); },
                                  [&](int j, int i) { return Vn[i * dv + j]; },
                                  [&](int r, int i, float x) { sDA[r * 64 + i] = i <= r ? x : 0.f; }, sA, sB);
     __syncthreads();
     // T^T dV_new -> dv = beta T^T dV_new,  dbeta += (T^T dV_new) . V
-    block_gemm<4, 16, false, false>(64, dv, 64, [&](int i, int r) { return Tm[r * 64 + i]; },
-                                    [&](int r, int j) { return dVn[r * dv + j]; },
-                                    [&](int i, int j, float x) {
-                                        if (i < rows) {
-                                            reinterpret_cast<T *>(p.dv)[((tok0 + i) * H + h) * dv + j] = from_f32<T>(sbe[i] * x);
-                                            atomicAdd(&sdbeta[i], x * Vf(i, j));
-                                        }
-                                    }, sA, sB);
+    block_gemm_cols<4, false, false, 1>(64, dv, 64, [&](int i, int r) { return Tm[r * 64 + i]; },
+                                        [&](int r, int j) { return dVn[r * dv + j]; },
+                                        [&](int i, int j, float x) {
+                                            float c = 0.f;
+                                            if (i < rows) {
+                                                reinterpret_cast<T *>(p.dv)[((tok0 + i) * H + h) * dv + j] =
+                                                    from_f32<T>(sbe[i] * x);
+                                                c = x * Vf(i, j);
+                                            }
+                                            return make_float2(c, 0.f);
+                                        }, sA, sB, sdbeta);
     // T^T dW -> dK += beta gam T^T dW,  dbeta += gam (T^T dW) . K^,  dgam += beta (T^T dW) . K^
-    block_gemm<4, 16, false, false>(64, dk, 64, [&](int i, int r) { return Tm[r * 64 + i]; },
-                                    [&](int r, int d) { return dW[r * dk + d]; },
-                                    [&](int i, int d, float x) {
-                                        dK[i * dk + d] += sbe[i] * sgam[i] * x;
-                                        const float t = x * kh[i * dk + d];
-                                        atomicAdd(&sdbeta[i], sgam[i] * t);
-                                        atomicAdd(&sdgam[i], sbe[i] * t);
-                                    }, sA, sB);
+    block_gemm_cols<4, false, false, 2>(64, dk, 64, [&](int i, int r) { return Tm[r * 64 + i]; },
+                                        [&](int r, int d) { return dW[r * dk + d]; },
+                                        [&](int i, int d, float x) {
+                                            dK[i * dk + d] += sbe[i] * sgam[i] * x;
+                                            const float t = x * kh[i * dk + d];
+                                            return make_float2(sgam[i] * t, sbe[i] * t);
+                                        }, sA, sB, sdbeta, sdgam);
     // dT = dV_new (diag(beta) V)^T + dW (diag(beta gam) K^)^T
     block_gemm<4, 4, true, true>(64, 64, dv + dk,
                                  [&](int i, int k) { return k < dv ? dVn[i * dv + k] : dW[i * dk + k - dv]; },
@@ -508,13 +557,13 @@ bwd_local_kernel(const BwdParams p)
                                  [&](int i, int j, float x) { sDL[i * 64 + j] = j < i ? -x : 0.f; }, sA, sB);
     __syncthreads();
     // K^K^T: dbeta += sum_{i<r} dL Gamma KK;  GG = Gamma o dGamma starts with dL beta_r KK
-    block_gemm<4, 4, true, true>(64, 64, dk, [&](int r, int d) { return kh[r * dk + d]; },
-                                 [&](int d, int i) { return kh[i * dk + d]; },
-                                 [&](int r, int i, float x) {
-                                     const float G = Gam(r, i), dl = sDL[r * 64 + i];
-                                     sGG[r * 64 + i] = G * dl * sbe[r] * x;
-                                     if (i < r) atomicAdd(&sdbeta[r], dl * G * x);
-                                 }, sA, sB);
+    block_gemm<4, 4, true, true, 1>(64, 64, dk, [&](int r, int d) { return kh[r * dk + d]; },
+                                    [&](int d, int i) { return kh[i * dk + d]; },
+                                    [&](int r, int i, float x) {
+                                        const float G = Gam(r, i), dl = sDL[r * 64 + i];
+                                        sGG[r * 64 + i] = G * dl * sbe[r] * x;
+                                        return make_float2(i < r ? dl * G * x : 0.f, 0.f);
+                                    }, sA, sB, sdbeta);
     __syncthreads();
     // Q^K^T: GG += Gamma dA QK
     block_gemm<4, 4, true, true>(64, 64, dk, [&](int r, int d) { return qh[r * dk + d]; },
@@ -531,10 +580,10 @@ bwd_local_kernel(const BwdParams p)
     }
     __syncthreads();
     // dQ += (dA o Gamma) K^;   dK += (dA o Gamma)^T Q^ + M K^ + M^T K^
-    block_gemm<4, 16, true, false>(64, dk, 64, [&](int r, int i) { return sDA[r * 64 + i]; },
-                                   [&](int i, int d) { return kh[i * dk + d]; },
-                                   [&](int r, int d, float x) { dQ[r * dk + d] += x; }, sA, sB);
-    block_gemm<4, 16, false, false>(64, dk, 192,
+    block_gemm_cols<4, true, false>(64, dk, 64, [&](int r, int i) { return sDA[r * 64 + i]; },
+                                    [&](int i, int d) { return kh[i * dk + d]; },
+                                    [&](int r, int d, float x) { dQ[r * dk + d] += x; }, sA, sB);
+    block_gemm_cols<4, false, false>(64, dk, 192,
                                     [&](int i, int k) {
                                         return k < 64 ? sDA[k * 64 + i]
                                                       : (k < 128 ? sDL[i * 64 + k - 64] : sDL[(k - 128) * 64 + i]);
@@ -556,7 +605,7 @@ bwd_local_kernel(const BwdParams p)
         const int r = tid;
         float dbr = 0.f;
         for (int i = 0; i < 64; ++i) dbr += sGG[r * 64 + i] - sGG[i * 64 + r];
-        const float t = sdkdf[r] * expf(sb[63] - sb[r]);
+        const float t = sdkdf[r] * sfk[r];
         st[r] = t;
         sb[r] = dbr + sdgam[r] * sgam[r] - t;   // sb is no longer needed as b
     }
@@ -608,7 +657,7 @@ cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t st)
     const size_t stage = 2 * (size_t)kStage * sizeof(float);
     const size_t sm_prep = stage + sizeof(float) * (64 * 65 + 3 * 64);
     const size_t sm_scan = stage + sizeof(float) * (size_t)kScanRows * a.gm.dk;
-    const size_t sm_local = stage + sizeof(float) * (4 * 4096 + 7 * 64 + kBT);
+    const size_t sm_local = stage + sizeof(float) * (4 * 4096 + 8 * 64 + kBT);
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(bwd_prep_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_prep)))
         return e;
