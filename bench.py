@@ -519,9 +519,17 @@ def cpu_baseline(w: inputs.Workload, host=None, budget_s: float = 10.0):
     reps = max(1, int(budget_s / dt))   # the first pass sizes the sample
     dt += sum(one_pass() for _ in range(reps - 1))
     cores = min(oracle.num_threads(), w.B * w.H)
+    # one host core: one sequence of the workload (all heads), one pass
+    s1, th1 = oracle_sample(w, host, seqs=1)
+    t0 = time.perf_counter()
+    oracle.recurrent_fwd(s1["q"], s1["k"], s1["v"], s1["g"], s1["beta"], scale=w.scale, use_qk_l2norm=True,
+                         nthreads=1)
+    dt1 = time.perf_counter() - t0
     return {"value": token_heads / w.H * reps / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"the whole workload ({w.B} x {w.L} tokens x {w.H} heads), fp64 recurrence, "
-                      f"{reps} passes in {dt:.1f} s"}
+                      f"{reps} passes in {dt:.1f} s",
+            "single_core": {"value": th1 / w.H / dt1, "unit": "tokens/s", "cores": 1,
+                            "sample": f"one sequence ({w.L} tokens x {w.H} heads), one pass in {dt1:.2f} s"}}
 
 
 def bench_reference(args):
