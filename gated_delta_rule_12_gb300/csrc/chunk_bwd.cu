@@ -263,23 +263,30 @@ bwd_prep_kernel(const BwdParams p)
     const BwdLayout LY = bwd_layout(dk, dv);
     float *blk = p.ws + (slot * H + h) * LY.total;
     float *sA = smb, *sB = sA + kStage;
-    float *sL = sB + kStage;             // [64][65]: L, then T (column solve)
-    float *sb = sL + 64 * 65, *sbe = sb + 64, *sgam = sbe + 64;   // b, beta, gam
+    float *sL = sB + kStage;             // [64][65]: L
+    float *sT = sL + 64 * 65;            // [64][65]: T = (I + L)^{-1}
+    float *sb = sT + 64 * 65, *sbe = sb + 64, *sgam = sbe + 64, *sfk = sgam + 64;   // b, beta, gam, gC / gam
 
-    // gates: chunk-local cumulative log-gate (padding rows: g = 0, beta = 0)
+    // gates: chunk-local cumulative log-gate (padding rows: g = 0, beta = 0), a warp scan
+    // over each half of the chunk, then the first half's total added to the second
     if (tid < 64) {
         const int64_t th = (tok0 + tid) * H + h;
-        sb[tid] = tid < rows ? p.g[th] : 0.f;
+        float x = tid < rows ? p.g[th] : 0.f;
+        const int lane = tid & 31;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        sb[tid] = x;
         sbe[tid] = tid < rows ? p.beta[th] : 0.f;
     }
     __syncthreads();
-    if (tid == 0) {
-        float acc = 0.f;
-        for (int r = 0; r < 64; ++r) { acc += sb[r]; sb[r] = acc; }
-    }
+    if (tid >= 32 && tid < 64) sb[tid] += sb[31];
     __syncthreads();
     if (tid < 64) {
         sgam[tid] = expf(sb[tid]);
+        sfk[tid] = expf(sb[63] - sb[tid]);
         blk[LY.b + tid] = sb[tid];
     }
     // normalised q^ (scaled) and k^: one warp per row, rows tid>>5 + 8 i
@@ -305,7 +312,7 @@ bwd_prep_kernel(const BwdParams p)
     for (int e = tid; e < 64 * dk; e += kBT) {
         const int r = e / dk;
         blk[LY.qd + e] = sgam[r] * qh[e];
-        blk[LY.kd + e] = expf(sb[63] - sb[r]) * kh[e];
+        blk[LY.kd + e] = sfk[r] * kh[e];
     }
     // KK = K^ K^T -> L (strictly lower, beta_r Gamma_ri KK_ri) into sL;  A = (Q^ K^T) o Gamma
     block_gemm<4, 4, true, true>(64, 64, dk, [&](int i, int k) { return kh[i * dk + k]; },
@@ -319,28 +326,56 @@ bwd_prep_kernel(const BwdParams p)
                                      blk[LY.a + i * 64 + j] = j <= i ? expf(sb[i] - sb[j]) * x : 0.f;
                                  }, sA, sB);
     __syncthreads();
-    // T = (I + L)^{-1}: thread c < 64 solves column c by forward substitution
+    // T = (I + L)^{-1} by the block rule [A 0; C B]^{-1} = [A^-1 0; -B^-1 C A^-1  B^-1]:
+    // the four 16 x 16 diagonal blocks by forward substitution (thread tid < 64 owns column
+    // tid & 15 of block tid >> 4, in registers), then the 16 -> 32 and 32 -> 64 merges
+    // as two small products each, X = C A^-1 into scratch, then -B^-1 X
+    for (int e = tid; e < 64 * 64; e += kBT) {   // blocks above the diagonal
+        const int r = e >> 6, c = e & 63;
+        if ((c >> 4) > (r >> 4)) sT[r * 65 + c] = 0.f;
+    }
     if (tid < 64) {
-        const int col = tid;
-        float x[64];
+        const int b0 = 16 * (tid >> 4), c = tid & 15;
+        float x[16];
 #pragma unroll
-        for (int r = 0; r < 64; ++r) {
-            float acc = r == col ? 1.f : 0.f;
-            for (int i = col; i < r; ++i) acc -= sL[r * 65 + i] * x[i];
-            x[r] = r < col ? 0.f : acc;
+        for (int r = 0; r < 16; ++r) {
+            float acc = r == c ? 1.f : 0.f;
+#pragma unroll
+            for (int i = 0; i < r; ++i) acc -= sL[(b0 + r) * 65 + b0 + i] * x[i];
+            x[r] = acc;   // zero above the diagonal (r < c), since then every x[i] is zero
         }
 #pragma unroll
-        for (int r = 0; r < 64; ++r) blk[LY.t + r * 64 + col] = x[r];
+        for (int r = 0; r < 16; ++r) sT[(b0 + r) * 65 + b0 + c] = x[r];
     }
     __syncthreads();
-    const float *Tm = blk + LY.t;
+    auto merge = [&](int n, int a0, int b0, float *X, int e0, int estep) {
+        // block [b0, b0 + n) x [a0, a0 + n) of T from the diagonal blocks at a0 and b0
+        for (int e = e0; e < n * n; e += estep) {
+            const int r = e / n, c = e % n;
+            float acc = 0.f;
+            for (int i = c; i < n; ++i) acc += sL[(b0 + r) * 65 + a0 + i] * sT[(a0 + i) * 65 + a0 + c];
+            X[e] = acc;
+        }
+        __syncthreads();
+        for (int e = e0; e < n * n; e += estep) {
+            const int r = e / n, c = e % n;
+            float acc = 0.f;
+            for (int i = 0; i <= r; ++i) acc += sT[(b0 + r) * 65 + b0 + i] * X[i * n + c];
+            sT[(b0 + r) * 65 + a0 + c] = -acc;
+        }
+        __syncthreads();
+    };
+    merge(16, 32 * (tid >> 7), 32 * (tid >> 7) + 16, sA + 256 * (tid >> 7), tid & 127, 128);   // 16 -> 32, two at once
+    merge(32, 0, 32, sA, tid, kBT);                                                            // 32 -> 64
+    for (int e = tid; e < 64 * 64; e += kBT) blk[LY.t + e] = sT[(e >> 6) * 65 + (e & 63)];
+    const float *Tm = sT;   // pitch 65 below
     // U = T diag(beta) V,  W = T diag(beta gam) K^
-    block_gemm_cols<4, true, false>(64, dv, 64, [&](int i, int k) { return Tm[i * 64 + k]; },
+    block_gemm_cols<4, true, false>(64, dv, 64, [&](int i, int k) { return Tm[i * 65 + k]; },
                                     [&](int k, int j) {
                                         return k < rows ? sbe[k] * ld<T>(p.v, ((tok0 + k) * H + h) * dv + j) : 0.f;
                                     },
                                     [&](int i, int j, float x) { blk[LY.u + i * dv + j] = x; }, sA, sB);
-    block_gemm_cols<4, true, false>(64, dk, 64, [&](int i, int k) { return Tm[i * 64 + k]; },
+    block_gemm_cols<4, true, false>(64, dk, 64, [&](int i, int k) { return Tm[i * 65 + k]; },
                                     [&](int k, int j) { return sbe[k] * sgam[k] * kh[k * dk + j]; },
                                     [&](int i, int j, float x) { blk[LY.w + i * dk + j] = x; }, sA, sB);
 }
@@ -655,7 +690,7 @@ cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t st)
     p.ws = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(a.workspace) + 256);
     p.gm = a.gm; p.scale = a.scale; p.l2 = a.l2;
     const size_t stage = 2 * (size_t)kStage * sizeof(float);
-    const size_t sm_prep = stage + sizeof(float) * (64 * 65 + 3 * 64);
+    const size_t sm_prep = stage + sizeof(float) * (2 * 64 * 65 + 4 * 64);
     const size_t sm_scan = stage + sizeof(float) * (size_t)kScanRows * a.gm.dk;
     const size_t sm_local = stage + sizeof(float) * (4 * 4096 + 8 * 64 + kBT);
     cudaError_t e;
