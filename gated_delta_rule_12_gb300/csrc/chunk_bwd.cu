@@ -31,14 +31,14 @@ constexpr int kBT = 256;   // threads per block of every backward kernel
 // ---------------------------------------------------------------------------
 // per (slot, head) fp32 workspace block
 // ---------------------------------------------------------------------------
-struct BwdLayout {
-    int64_t qh, kh, qd, kd, b, t, u, w, a, s, vn, dvn, dsn, dqh, dkh, dw, total;   // float offsets
+struct BwdLayout {   // float offsets within one block (under 2^31 for every supported head size)
+    int qh, kh, qd, kd, b, t, u, w, a, ado, doq, s, vn, dvn, dsn, dqh, dkh, dw, total;
 };
 
 __host__ __device__ inline BwdLayout bwd_layout(int dk, int dv)
 {
     BwdLayout L;
-    int64_t o = 0;
+    int o = 0;
     L.qh = o;  o += 64 * dk;
     L.kh = o;  o += 64 * dk;
     L.qd = o;  o += 64 * dk;             // diag(gam) Q^
@@ -48,10 +48,12 @@ __host__ __device__ inline BwdLayout bwd_layout(int dk, int dv)
     L.u = o;   o += 64 * dv;
     L.w = o;   o += 64 * dk;
     L.a = o;   o += 64 * 64;
-    L.s = o;   o += (int64_t)dv * dk;
+    L.ado = o; o += 64 * dv;             // A^T dO   (the state-independent part of dV_new)
+    L.doq = o; o += dv * dk;             // dO^T Qd  (the state-independent part of dS)
+    L.s = o;   o += dv * dk;
     L.vn = o;  o += 64 * dv;
     L.dvn = o; o += 64 * dv;
-    L.dsn = o; o += (int64_t)dv * dk;
+    L.dsn = o; o += dv * dk;
     L.dqh = o; o += 64 * dk;             // scratch of bwd_local_kernel
     L.dkh = o; o += 64 * dk;
     L.dw = o;  o += 64 * dk;
@@ -378,6 +380,17 @@ bwd_prep_kernel(const BwdParams p)
     block_gemm_cols<4, true, false>(64, dk, 64, [&](int i, int k) { return Tm[i * 65 + k]; },
                                     [&](int k, int j) { return sbe[k] * sgam[k] * kh[k * dk + j]; },
                                     [&](int i, int j, float x) { blk[LY.w + i * dk + j] = x; }, sA, sB);
+    // the state-independent parts of the reverse scan's two products: A^T dO and dO^T Qd
+    const float *Ag = blk + LY.a, *qd = blk + LY.qd;
+    auto dOf = [&](int r, int j) { return r < rows ? ld<T>(p.dout, ((tok0 + r) * H + h) * dv + j) : 0.f; };
+    block_gemm_cols<4, false, false>(64, dv, 64, [&](int r, int i) { return Ag[i * 64 + r]; },
+                                     [&](int i, int j) { return dOf(i, j); },
+                                     [&](int r, int j, float x) { blk[LY.ado + r * dv + j] = x; }, sA, sB);
+    for (int j0 = 0; j0 < dv; j0 += 64)
+        block_gemm_cols<4, false, false>(min(64, dv - j0), dk, 64, [&](int i, int r) { return dOf(r, j0 + i); },
+                                         [&](int r, int d) { return qd[r * dk + d]; },
+                                         [&](int i, int d, float x) { blk[LY.doq + (int64_t)(j0 + i) * dk + d] = x; },
+                                         sA, sB);
 }
 
 // ---------------------------------------------------------------------------
@@ -454,30 +467,22 @@ bwd_bwd_scan_kernel(const BwdParams p)
     __syncthreads();
     for (int c = nch - 1; c >= 0; --c) {
         float *blk = p.ws + ((slot0 + c) * H + h) * LY.total;
-        const float *b = blk + LY.b, *W = blk + LY.w, *A = blk + LY.a, *kd = blk + LY.kd, *qd = blk + LY.qd;
-        const int64_t t0 = tok0 + (int64_t)c * kChunk;
-        const int rows = min(kChunk, len - c * kChunk);
+        const float *b = blk + LY.b, *W = blk + LY.w, *kd = blk + LY.kd, *ado = blk + LY.ado, *doq = blk + LY.doq;
         for (int64_t e = tid; e < SZ; e += kBT) blk[LY.dsn + so + e] = dS[e];
         float *dvn = blk + LY.dvn;
-        auto dO = [&](int r, int j) { return r < rows ? ld<T>(p.dout, ((t0 + r) * H + h) * dv + j) : 0.f; };
-        // dV_new = Kd dS'^T + A^T dO  (columns j0 .. j0 + 31)
-        block_gemm<4, 2, true, true>(64, kScanRows, dk + 64,
-                                     [&](int r, int k) { return k < dk ? kd[r * dk + k] : A[(k - dk) * 64 + r]; },
-                                     [&](int k, int j) {
-                                         return k < dk ? dS[(int64_t)j * dk + k] : dO(k - dk, j0 + j);
-                                     },
-                                     [&](int r, int j, float x) { dvn[r * dv + j0 + j] = x; }, sA, sB);
+        // dV_new = Kd dS'^T + A^T dO  (columns j0 .. j0 + 31; A^T dO comes from the prep kernel)
+        block_gemm<4, 2, true, true>(64, kScanRows, dk, [&](int r, int k) { return kd[r * dk + k]; },
+                                     [&](int k, int j) { return dS[(int64_t)j * dk + k]; },
+                                     [&](int r, int j, float x) { dvn[r * dv + j0 + j] = x + ado[r * dv + j0 + j]; },
+                                     sA, sB);
         __syncthreads();
-        // dS <- gC dS' + dO^T Qd - dV_new^T W
+        // dS <- gC dS' + dO^T Qd - dV_new^T W  (dO^T Qd comes from the prep kernel)
         const float gC = expf(b[63]);
-        block_gemm<2, 8, false, false>(kScanRows, dk, 128,
-                                       [&](int i, int k) {
-                                           return k < 64 ? dO(k, j0 + i) : -dvn[(k - 64) * dv + j0 + i];
-                                       },
-                                       [&](int k, int d) { return k < 64 ? qd[k * dk + d] : W[(k - 64) * dk + d]; },
+        block_gemm<2, 8, false, false>(kScanRows, dk, 64, [&](int i, int k) { return -dvn[k * dv + j0 + i]; },
+                                       [&](int k, int d) { return W[k * dk + d]; },
                                        [&](int i, int d, float x) {
                                            float &s_ = dS[(int64_t)i * dk + d];
-                                           s_ = gC * s_ + x;
+                                           s_ = gC * s_ + doq[(int64_t)(j0 + i) * dk + d] + x;
                                        }, sA, sB);
         __syncthreads();
     }
