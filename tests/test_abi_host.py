@@ -64,6 +64,22 @@ def test_workspace_size_rules(lib):
     assert ws(1, 0, 2, 64, 64, 0, 0) >= 256
 
 
+def test_backward_workspace_size_rules(lib):
+    ws = lib.gdn_chunk_bwd_workspace_size
+
+    def per_block(dk, dv):
+        # fp32 per (chunk, head): q^, k^, Qd, Kd, W~ and three dk-wide scratch rows (8 x 64 dk),
+        # b (64), T and A (64 x 64 each), U, V_new, dV_new and A^T dO (4 x 64 dv),
+        # and three dv x dk matrices (S, dS', dO^T Qd)
+        return 4 * (8 * 64 * dk + 64 + 2 * 64 * 64 + 4 * 64 * dv + 3 * dv * dk)
+
+    assert ws(4, 2048, 16, 128, 128, 0, gdn.GDN_BF16) == 256 + 4 * 32 * 16 * per_block(128, 128)
+    assert ws(1, 100, 2, 64, 32, 0, gdn.GDN_F32) == 256 + 2 * 2 * per_block(64, 32)   # ragged: 2 chunks
+    assert ws(1, 32768, 16, 128, 128, 8, gdn.GDN_BF16) == 256 + (32768 // 64 + 8 + 1) * 16 * per_block(128, 128)
+    assert ws(4, 100, 2, 128, 128, 8, gdn.GDN_BF16) == 0     # varlen needs B == 1
+    assert ws(1, 64, 1, 96, 64, 0, gdn.GDN_F32) == 0         # unsupported dk
+
+
 def test_kernel_count_rules(lib):
     kc = lib.gdn_chunk_fwd_kernel_count
     assert kc(4, 2048, 16, 128, 128, 0, gdn.GDN_BF16) == 2      # tensor-core path: UT + recurrence
