@@ -32,7 +32,7 @@ constexpr int kBT = 256;   // threads per block of every backward kernel
 // per (slot, head) fp32 workspace block
 // ---------------------------------------------------------------------------
 struct BwdLayout {   // float offsets within one block (under 2^31 for every supported head size)
-    int qh, kh, qd, kd, b, t, u, w, a, ado, doq, s, vn, dvn, dsn, dqh, dkh, dw, total;
+    int qh, kh, qd, kd, b, t, u, w, a, kk, qk, ado, doq, s, vn, dvn, dsn, dqh, dkh, dw, total;
 };
 
 __host__ __device__ inline BwdLayout bwd_layout(int dk, int dv)
@@ -48,6 +48,8 @@ __host__ __device__ inline BwdLayout bwd_layout(int dk, int dv)
     L.u = o;   o += 64 * dv;
     L.w = o;   o += 64 * dk;
     L.a = o;   o += 64 * 64;
+    L.kk = o;  o += 64 * 64;             // K^ K^T and Q^ K^T before masking
+    L.qk = o;  o += 64 * 64;
     L.ado = o; o += 64 * dv;             // A^T dO   (the state-independent part of dV_new)
     L.doq = o; o += dv * dk;             // dO^T Qd  (the state-independent part of dS)
     L.s = o;   o += dv * dk;
@@ -321,11 +323,13 @@ bwd_prep_kernel(const BwdParams p)
                                  [&](int k, int j) { return kh[j * dk + k]; },
                                  [&](int i, int j, float x) {
                                      sL[i * 65 + j] = j < i ? sbe[i] * expf(sb[i] - sb[j]) * x : 0.f;
+                                     blk[LY.kk + i * 64 + j] = x;
                                  }, sA, sB);
     block_gemm<4, 4, true, true>(64, 64, dk, [&](int i, int k) { return qh[i * dk + k]; },
                                  [&](int k, int j) { return kh[j * dk + k]; },
                                  [&](int i, int j, float x) {
                                      blk[LY.a + i * 64 + j] = j <= i ? expf(sb[i] - sb[j]) * x : 0.f;
+                                     blk[LY.qk + i * 64 + j] = x;
                                  }, sA, sB);
     __syncthreads();
     // T = (I + L)^{-1} by the block rule [A 0; C B]^{-1} = [A^-1 0; -B^-1 C A^-1  B^-1]:
@@ -596,27 +600,29 @@ bwd_local_kernel(const BwdParams p)
                                  [&](int r, int j) { return Tm[j * 64 + r]; },
                                  [&](int i, int j, float x) { sDL[i * 64 + j] = j < i ? -x : 0.f; }, sA, sB);
     __syncthreads();
-    // K^K^T: dbeta += sum_{i<r} dL Gamma KK;  GG = Gamma o dGamma starts with dL beta_r KK
-    block_gemm<4, 4, true, true, 1>(64, 64, dk, [&](int r, int d) { return kh[r * dk + d]; },
-                                    [&](int d, int i) { return kh[i * dk + d]; },
-                                    [&](int r, int i, float x) {
-                                        const float G = Gam(r, i), dl = sDL[r * 64 + i];
-                                        sGG[r * 64 + i] = G * dl * sbe[r] * x;
-                                        return make_float2(i < r ? dl * G * x : 0.f, 0.f);
-                                    }, sA, sB, sdbeta);
-    __syncthreads();
-    // Q^K^T: GG += Gamma dA QK
-    block_gemm<4, 4, true, true>(64, 64, dk, [&](int r, int d) { return qh[r * dk + d]; },
-                                 [&](int d, int i) { return kh[i * dk + d]; },
-                                 [&](int r, int i, float x) { sGG[r * 64 + i] += Gam(r, i) * sDA[r * 64 + i] * x; },
-                                 sA, sB);
-    __syncthreads();
-    // dA -> dA o Gamma;  dL -> M = dL o beta_r Gamma
-    for (int e = tid; e < 4096; e += kBT) {
-        const int r = e >> 6, i = e & 63;
-        const float G = Gam(r, i);
-        sDA[e] *= G;
-        sDL[e] *= sbe[r] * G;
+    // One pass over the 64 x 64 entries, with K^K^T and Q^K^T as the prep kernel formed them:
+    //   GG = Gamma o dGamma = Gamma o (dL beta_r KK + dA QK),  dbeta_r += sum_{i<r} dL Gamma KK,
+    //   then dA -> dA o Gamma and dL -> M = dL o beta_r Gamma.
+    // Warp w takes rows 8w .. 8w + 7, lane l columns l and l + 32 of each.
+    static_assert(kBT == 256, "eight warps of eight rows");
+    {
+        const float *KK = blk + LY.kk, *QK = blk + LY.qk;
+        const int warp = tid >> 5, lane = tid & 31;
+        for (int rr = 0; rr < 8; ++rr) {
+            const int r = warp * 8 + rr;
+            float db = 0.f;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int i = lane + 32 * h2, e = r * 64 + i;
+                const float G = Gam(r, i), dl = sDL[e], da = sDA[e], kk = KK[e];
+                sGG[e] = G * (dl * sbe[r] * kk + da * QK[e]);
+                if (i < r) db += dl * G * kk;
+                sDA[e] = da * G;
+                sDL[e] = dl * sbe[r] * G;
+            }
+            db = warp_sum(db);
+            if (lane == 0) sdbeta[r] += db;
+        }
     }
     __syncthreads();
     // dQ += (dA o Gamma) K^;   dK += (dA o Gamma)^T Q^ + M K^ + M^T K^

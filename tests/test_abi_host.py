@@ -69,9 +69,9 @@ def test_backward_workspace_size_rules(lib):
 
     def per_block(dk, dv):
         # fp32 per (chunk, head): q^, k^, Qd, Kd, W~ and three dk-wide scratch rows (8 x 64 dk),
-        # b (64), T and A (64 x 64 each), U, V_new, dV_new and A^T dO (4 x 64 dv),
-        # and three dv x dk matrices (S, dS', dO^T Qd)
-        return 4 * (8 * 64 * dk + 64 + 2 * 64 * 64 + 4 * 64 * dv + 3 * dv * dk)
+        # b (64), T, A and the raw K^K^T, Q^K^T (4 x 64 x 64), U, V_new, dV_new and A^T dO
+        # (4 x 64 dv), and three dv x dk matrices (S, dS', dO^T Qd)
+        return 4 * (8 * 64 * dk + 64 + 4 * 64 * 64 + 4 * 64 * dv + 3 * dv * dk)
 
     assert ws(4, 2048, 16, 128, 128, 0, gdn.GDN_BF16) == 256 + 4 * 32 * 16 * per_block(128, 128)
     assert ws(1, 100, 2, 64, 32, 0, gdn.GDN_F32) == 256 + 2 * 2 * per_block(64, 32)   # ragged: 2 chunks
