@@ -1,4 +1,4 @@
-// chunk_bwd.cu -- backward pass of the chunked gated delta rule (CUDA cores, fp32).
+// chunk_bwd.cu -- backward pass of the chunked gated delta rule (fp32 throughout).
 //
 // "Gated Delta Networks: Improving Mamba2 with Delta Rule", §3.3 (the chunkwise
 // form; the training forward whose gradients these are).  Per chunk, with
@@ -15,11 +15,15 @@
 // and, in parallel over chunks, the local gradients through A, Qd, Kd, U, W, T, L,
 // Gamma and the gates (see bwd_local_kernel), then through the normalisations.
 //
-// Four kernels: bwd_prep_kernel (per chunk: q^, k^, b, T, U, W, A),
-// bwd_fwd_scan_kernel (per sequence and head: the state at every chunk start and
-// V_new), bwd_bwd_scan_kernel (reverse: dS' per chunk, dV_new, dS_0) and
-// bwd_local_kernel (per chunk: dq, dk, dv, dg, dbeta).  Everything is fp32 on the
-// CUDA cores, matrices staged through shared memory by one block-level GEMM.
+// Four kernels:
+//   bwd_prep_kernel      per chunk: q^, k^, b, T, U, W, A, Qd, Kd, the unmasked K^K^T and
+//                        Q^K^T, and the reverse scan's state-independent A^T dO and dO^T Qd
+//   bwd_fwd_scan_kernel  per (sequence, head, 32 state rows): the state at every chunk start
+//                        and V_new
+//   bwd_bwd_scan_kernel  the same units in reverse: dS' per chunk, dV_new, dS_0
+//   bwd_local_kernel     per chunk: dq, dk, dv, dg, dbeta
+// Every intermediate is fp32.  The matrix products go through one block-level GEMM
+// (block_gemm) on the tensor cores with fp32 accuracy (three tf32 products per pair).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -251,7 +255,8 @@ template <typename T>
 __device__ __forceinline__ float ld(const void *p, int64_t i) { return to_f32(reinterpret_cast<const T *>(p)[i]); }
 
 // ---------------------------------------------------------------------------
-// bwd_prep_kernel: per (slot, head) -- q^, k^, b, T = (I + L)^{-1}, U, W, A
+// bwd_prep_kernel: per (slot, head) -- q^, k^, b, T = (I + L)^{-1}, U, W, A, Qd, Kd,
+// K^K^T and Q^K^T unmasked, A^T dO and dO^T Qd
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(kBT, 2)
