@@ -57,6 +57,16 @@ def test_prefill_ragged_with_initial_state(dtype, dk, dv):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("L", [1, 17, 64, 65])
+def test_short_batched_sequences(dtype, L):
+    """Equal-length batches shorter than, equal to and one past a chunk, on both chunk paths."""
+    d = inputs.make_prefill(B=3, L=L, H=2, dk=128, dv=128, dtype=dtype, seed=19, decay=0.3, init_state=True)
+    out, sf, ro, rs = run_both(d, 128)
+    assert_close(out, ro, dtype, "out")
+    assert_close(sf, rs, dtype, "final_state")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_varlen_boundaries(dtype):
     lens = [1, 63, 64, 65, 0, 130, 7, 128]
     d = inputs.make_prefill(B=1, L=sum(lens), H=2, dk=128, dv=128, dtype=dtype, seed=12, decay=0.5,
