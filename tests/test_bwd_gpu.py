@@ -83,6 +83,16 @@ def test_bwd_ragged_with_states(dtype, dk, dv):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("L", [1, 17, 65])
+def test_bwd_short_batched_sequences(dtype, L):
+    """Equal-length batches shorter than a chunk and one past it, with both state gradients."""
+    d = inputs.make_prefill(B=3, L=L, H=2, dk=128, dv=64, dtype=dtype, seed=76, decay=0.3, init_state=True)
+    dO, dS = cotangents(d, 77)
+    out, ref = grads(d, dO, dS, 128)
+    check_all(out, ref, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_bwd_varlen_beta_up_to_two(dtype):
     lens = [1, 63, 64, 65, 0, 130, 7]
     d = inputs.make_prefill(B=1, L=sum(lens), H=2, dk=128, dv=128, dtype=dtype, seed=72, decay=0.5,
