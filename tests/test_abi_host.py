@@ -125,6 +125,43 @@ def test_chunk_fwd_validation(lib, over, code):
     assert _call_chunk(lib, **over) == code
 
 
+def _call_bwd(lib, **over):
+    fake = 1 << 20  # 256-aligned, never dereferenced: validation fails first
+    args = dict(q=fake, k=fake, v=fake, g=fake, beta=fake, s0=None, cu=None, nseq=0, dout=fake, dsf=None,
+                dq=fake, dk_=fake, dv_=fake, dg=fake, db=fake, dinit=None,
+                B=1, T=64, H=1, dk=64, dv=64, dt=gdn.GDN_F32, scale=0.125, l2=1, C=64,
+                ws=fake, wsb=1 << 30, stream=None)
+    args.update(over)
+    a = args
+    return lib.gdn_chunk_bwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["s0"], a["cu"], a["nseq"], a["dout"],
+                             a["dsf"], a["dq"], a["dk_"], a["dv_"], a["dg"], a["db"], a["dinit"],
+                             a["B"], a["T"], a["H"], a["dk"], a["dv"], a["dt"], a["scale"], a["l2"], a["C"],
+                             a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(C=32), 2),                       # chunk size other than 64
+    (dict(dk=96), 2),                      # unsupported head dim
+    (dict(dv=48), 2),
+    (dict(B=0), 1),
+    (dict(H=0), 1),
+    (dict(dt=7), 1),
+    (dict(dout=None), 1),                  # NULL output gradient with tokens present
+    (dict(dg=None), 1),                    # NULL gradient buffer
+    (dict(dq=(1 << 20) + 4), 1),           # misaligned
+    (dict(db=(1 << 20) + 2), 1),
+    (dict(dinit=(1 << 20) + 8), 1),
+    (dict(ws=None), 3),                    # no workspace
+    (dict(ws=(1 << 20) + 16), 3),          # workspace not 256-aligned
+    (dict(wsb=64), 3),                     # workspace too small
+    (dict(cu=1 << 20, nseq=0), 1),         # varlen without a sequence count
+    (dict(cu=1 << 20, nseq=2, B=2), 1),    # varlen needs B == 1
+    (dict(nseq=3), 1),                     # num_seqs inconsistent with B
+])
+def test_chunk_bwd_validation(lib, over, code):
+    assert _call_bwd(lib, **over) == code
+
+
 def test_decode_validation(lib):
     fake = 1 << 20
     d = lib.gdn_decode_step
