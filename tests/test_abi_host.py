@@ -218,6 +218,15 @@ def test_check_device_error_validation(lib):
     assert lib.gdn_check_device_error((1 << 20) + 8, None) == 1
 
 
+def test_selftest_wait_timeout_validation(lib):
+    fake = 1 << 20
+    st = lib.gdn_selftest_wait_timeout
+    assert st(None, 1000, None) == 1              # no workspace
+    assert st(fake + 8, 1000, None) == 1          # not 256-aligned
+    assert st(fake, 0, None) == 1                 # limit below 1 us
+    assert st(fake, 1000001, None) == 1           # limit above 1 s
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     q = torch.zeros(1, 64, 1, 64)
