@@ -45,6 +45,27 @@ def test_exports_every_declared_symbol(lib):
         assert re.search(rf"\bT {n}\b", out), f"{n} missing from the dynamic symbol table"
 
 
+def test_header_compiles_as_plain_c(tmp_path):
+    """include/gdn.h is a C header: a C99 translation unit that takes the address of every
+    declared entry point compiles warning-free with gcc."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    inc = os.path.join(ROOT, "include")
+    with open(os.path.join(inc, "gdn.h")) as f:
+        names = sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", f.read())))
+    assert names, "no entry points found in the header"
+    src = tmp_path / "use_gdn.c"
+    src.write_text('#include "gdn.h"\n'
+                   "void *const gdn_entry_points[] = {\n" + "".join(f"    (void *)&{n},\n" for n in names) + "};\n"
+                   "int gdn_ok(gdn_status s) { return s == GDN_OK; }\n")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", inc, "-c", str(src), "-o",
+                        str(tmp_path / "use_gdn.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_status_strings(lib):
     for code, name in gdn.STATUS.items():
         assert lib.gdn_status_string(code).decode() == name
