@@ -83,6 +83,83 @@ def decode_algorithmic_bytes(w: inputs.Workload) -> int:
     return nh * (2 * w.dv * w.dk * 4 + (2 * w.dk + 2 * w.dv) * s + 8)
 
 
+FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # CUDA-core fp32 FMA rate at the maximum SM clock (nominal)
+
+
+def prefill_roofline(w: inputs.Workload, ms: float, peaks, traffic=None, kernel: str = "") -> dict:
+    """Roofline of one chunked-forward call: the time bound is the larger of the algorithmic bytes at
+    the measured HBM bandwidth and the algorithmic FLOPs at the tensor (bf16 workloads) or fp32 FMA
+    (fp32 workloads) peak; `frac` is that bound over the measured time."""
+    nbytes = prefill_algorithmic_bytes(w)
+    flops = prefill_algorithmic_flops(w)
+    t_bytes = nbytes / (peaks["hbm_gbs"] * 1e9)
+    fpeak = peaks["bf16_tflops"] if w.dtype == "bf16" else FP32_FMA_TFLOPS
+    t_flops = flops / (fpeak * 1e12)
+    t = ms * 1e-3
+    if t_bytes >= t_flops:
+        r = {"bound": "hbm", "achieved": nbytes / t / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        r = {"bound": "tensor" if w.dtype == "bf16" else "alu", "achieved": flops / t / 1e12, "peak": fpeak,
+             "unit": "TFLOP/s"}
+    r.update({"frac": max(t_bytes, t_flops) / t, "traffic": traffic, "algorithmic_bytes": nbytes,
+              "algorithmic_flops": flops, "t_bytes_us": t_bytes * 1e6, "t_flops_us": t_flops * 1e6,
+              "frac_bytes": t_bytes / t, "frac_flops": t_flops / t,
+              "flop_peak_source": "measured bf16" if w.dtype == "bf16" else "nominal fp32 FMA (152 SMs x 128 lanes x 2 x 2.07 GHz)",
+              "peak_source": peaks["source"]})
+    if kernel:
+        r["kernel"] = kernel
+    return r
+
+
+def bench_prefill_workload(name: str, dev, flush, stream, reps: int, peaks) -> dict:
+    """One gdn_chunk_fwd call on another workload of the table (inputs resident in HBM, L2 flushed
+    before each call, CUDA events on the launching stream, median of `reps`)."""
+    import gated_delta_rule_12_gb300 as gdn
+    w = inputs.WORKLOADS[name]
+    host = inputs.make(w)
+    d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in host.items()}
+    del host
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    B = w.B if w.kind != "varlen" else 1
+    N = w.num_seqs if w.kind == "varlen" else w.B
+    num_seqs = N if w.kind == "varlen" else 0
+    out = torch.empty((B, w.L, w.H, w.dv), dtype=tdt, device=dev)
+    sf = torch.empty((N, w.H, w.dv, w.dk), dtype=torch.float32, device=dev)
+    work = torch.empty(gdn.chunk_fwd_workspace_size(B, w.L, w.H, w.dk, w.dv, num_seqs, tdt), dtype=torch.uint8,
+                       device=dev)
+
+    def call():
+        gdn.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], init_state=d["init_state"],
+                      cu_seqlens=d["cu_seqlens"], scale=w.scale, use_qk_l2norm=True, out=out, final_state=sf,
+                      workspace=work)
+
+    for _ in range(3):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    t = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        t.append(a.elapsed_time(b))
+    ms = statistics.median(t)
+    launches = gdn.chunk_fwd_kernel_count(B, w.L, w.H, w.dk, w.dv, num_seqs, tdt)
+    shape = {"B": B, "T": w.L, "H": w.H, "dk": w.dk, "dv": w.dv, "chunk": w.chunk_size, "dtype": w.dtype}
+    if w.kind == "varlen":
+        cu = d["cu_seqlens"].cpu().tolist()
+        shape["lengths"] = [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
+    del d, out, sf, work
+    torch.cuda.empty_cache()
+    return {"workload": name, "shape": shape, "unit": "tokens/s", "value": w.B * w.L / (ms * 1e-3) if w.kind != "varlen" else w.L / (ms * 1e-3),
+            "ms_per_call": ms, "kernels_per_call": launches,
+            "roofline": prefill_roofline(w, ms, peaks, kernel="one gdn_chunk_fwd call"),
+            "timing": f"median of {reps} calls, L2 flushed (512 MiB write) before each"}
+
+
 class ClockSampler:
     """Samples nvidia-smi SM clocks and throttle reasons around the timed region.
 
@@ -418,6 +495,14 @@ def bench_ours(args):
     pro = bench_prologue(w, dev, flush, stream, reps, peaks)
     pro["value"] = job_throughput(w.B * w.L, ws_n, max_over_ranks(dist, pro["ms_per_call"]))
 
+    # the other chunked-forward workloads of the table (parity cases, timed here too)
+    others = {}
+    for key, name in (("small_f32", "prefill_b1_h2_l256_d64_f32"), ("varlen", "varlen_t32768_h16_d128_bf16"),
+                      ("large", "prefill_b8_h32_l8192_dk128_dv256_bf16")):
+        others[key] = bench_prefill_workload(name, dev, flush, stream, max(5, reps), peaks)
+        tokens_w = others[key]["value"] * others[key]["ms_per_call"] * 1e-3
+        others[key]["value"] = job_throughput(tokens_w, ws_n, max_over_ranks(dist, others[key]["ms_per_call"]))
+
     if rank == 0:
         cpu = cpu_baseline(w) if ws_n == 1 else None
         line = {
@@ -427,10 +512,8 @@ def bench_ours(args):
             "config": {"workload": PREFILL, "B": w.B, "T": w.L, "H": w.H, "dk": w.dk, "dv": w.dv,
                        "chunk": w.chunk_size, "tokens_per_step": tokens, "l2": "flushed (512 MiB write) before each timed step",
                        "parallelism": f"replicas x{ws_n}"},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_record("chunk_fwd"),
-                         "kernel": "one gdn_chunk_fwd call (ut_tc_kernel + recur_tc_kernel)",
-                         "algorithmic_bytes": algo_bytes, "peak_source": peaks["source"]},
+            "roofline": prefill_roofline(w, ms, peaks, traffic=traffic_record("chunk_fwd"),
+                                         kernel="one gdn_chunk_fwd call (ut_tc_kernel + recur_tc_kernel)"),
             "e2e": {"value": job_throughput(tokens, ws_n, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "mode": "pipelined: step i+1's inputs in and step i-1's outputs out while step i computes",
@@ -451,6 +534,7 @@ def bench_ours(args):
                              "timing": f"{wd.steps} tokens as {calls} calls in one CUDA graph, median of {reps}"},
             "prologue": pro,
             "backward": bwd,
+            **others,
             "gpu_launches": args.steps * launches_per_step,
             "clocks": clocks,
             "cpu_baseline": cpu,

@@ -30,7 +30,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libgdn.so")
 
 GDN_OK = 0
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_WORKSPACE",
-          4: "GDN_ERR_CUDA", 5: "GDN_ERR_DEVICE_TIMEOUT"}
+          4: "GDN_ERR_CUDA", 5: "GDN_ERR_DEVICE_TIMEOUT", 6: "GDN_ERR_RANGE"}
 GDN_F32, GDN_BF16 = 0, 1
 CHUNK = 64
 
@@ -131,6 +131,43 @@ def _stream(stream):
     return getattr(stream, "cuda_stream", stream)
 
 
+
+def _check_chunk_args(q, k, v, g, beta, init_state, cu_seqlens, out, final_state):
+    """The checks every chunked-forward wrapper makes before it hands raw pointers to the C ABI:
+    dtypes (the kernels read cu_seqlens as int32 and g, beta and the states as fp32, so any other
+    dtype would be misread on the device), shapes, placement and contiguity."""
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
+        raise ValueError("q, k must be [B,T,H,dk] and v [B,T,H,dv]")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    _dt(q)
+    if cu_seqlens is not None:
+        if cu_seqlens.dtype != torch.int32:
+            raise TypeError("cu_seqlens must be int32")
+        if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+            raise ValueError("cu_seqlens must be [N+1] with N >= 1")
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else B
+    for t, what in ((g, "g"), (beta, "beta")):
+        if t.dtype != torch.float32:
+            raise TypeError(f"{what} must be float32")
+        if tuple(t.shape) != (B, T, H):
+            raise ValueError(f"{what} must be [B,T,H]")
+    for t, what in ((init_state, "init_state"), (final_state, "final_state")):
+        if t is None:
+            continue
+        if t.dtype != torch.float32:
+            raise TypeError(f"{what} must be float32")
+        if tuple(t.shape) != (N, H, dv, dk):
+            raise ValueError(f"{what} must be [N,H,dv,dk] = {(N, H, dv, dk)}")
+    if out is not None:
+        if out.dtype != q.dtype:
+            raise TypeError("out must have the dtype of q")
+        if tuple(out.shape) != (B, T, H, dv):
+            raise ValueError(f"out must be [B,T,H,dv] = {(B, T, H, dv)}")
+    _need_cuda(q, k, v, g, beta, init_state, cu_seqlens, out, final_state)
+
 def chunk_fwd_workspace_size(B, T, H, dk, dv, num_seqs=0, dtype=torch.bfloat16) -> int:
     dt = GDN_BF16 if dtype == torch.bfloat16 else GDN_F32
     return int(load_library().gdn_chunk_fwd_workspace_size(B, T, H, dk, dv, num_seqs, dt))
@@ -161,13 +198,7 @@ def chunk_fwd(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale=None, us
         out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
     if final_state is None and output_final_state:
         final_state = torch.empty((N, H, dv, dk), dtype=torch.float32, device=q.device)
-    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
-        raise TypeError("cu_seqlens must be int32")
-    for t, dtp in ((g, torch.float32), (beta, torch.float32), (init_state, torch.float32),
-                   (final_state, torch.float32)):
-        if t is not None and t.dtype != dtp:
-            raise TypeError("g, beta and states must be float32")
-    _need_cuda(q, k, v, g, beta, init_state, cu_seqlens, out, final_state)
+    _check_chunk_args(q, k, v, g, beta, init_state, cu_seqlens, out, final_state)
     dt = _dt(q)
     num_seqs = N if cu_seqlens is not None else 0
     need = int(lib.gdn_chunk_fwd_workspace_size(B, T, H, dk, dv, num_seqs, dt))
@@ -327,7 +358,9 @@ def chunk_fwd_noalloc(q, k, v, g, beta, out, final_state=None, init_state=None, 
     dv = v.shape[-1]
     if scale is None:
         scale = dk ** -0.5
-    _need_cuda(q, k, v, g, beta, init_state, cu_seqlens, out, final_state)
+    if out is None:
+        raise ValueError("chunk_fwd_noalloc allocates nothing: pass out")
+    _check_chunk_args(q, k, v, g, beta, init_state, cu_seqlens, out, final_state)
     num_seqs = (cu_seqlens.numel() - 1) if cu_seqlens is not None else 0
     rc = lib.gdn_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state),
                                    _ptr(cu_seqlens), num_seqs, _ptr(out), _ptr(final_state),

@@ -33,6 +33,7 @@ const char *gdn_status_string(gdn_status s)
         case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
         case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
         case GDN_ERR_DEVICE_TIMEOUT: return "GDN_ERR_DEVICE_TIMEOUT";
+        case GDN_ERR_RANGE: return "GDN_ERR_RANGE";
     }
     return "GDN_UNKNOWN_STATUS";
 }
@@ -271,7 +272,9 @@ gdn_status gdn_check_device_error(void *workspace, void *stream)
     if (word == kDevErrNone) return GDN_OK;
     if (cudaMemsetAsync(workspace, 0, sizeof(word), st) != cudaSuccess) return GDN_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return GDN_ERR_CUDA;
-    return word == kDevErrTimeout ? GDN_ERR_DEVICE_TIMEOUT : GDN_ERR_CUDA;
+    if (word == kDevErrTimeout) return GDN_ERR_DEVICE_TIMEOUT;
+    if (word == kDevErrRange) return GDN_ERR_RANGE;
+    return GDN_ERR_CUDA;
 }
 
 }  // extern "C"

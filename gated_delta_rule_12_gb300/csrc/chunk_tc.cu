@@ -34,6 +34,7 @@
 // raises a CTA-wide abort flag, and all roles unwind to the common exit, where
 // tensor memory is released.
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -51,12 +52,16 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s: legitimate waits are 
 
 // Per (chunk, head) block of the workspace written by ut_tc_kernel.
 // All tiles are 128-B-swizzled rows of 64 bf16 (8 KB per 64 rows).
-constexpr uint32_t PB_TP = 0;          // T'    [64 r][64 i]                  (K-major B of a1)
-constexpr uint32_t PB_W = 8192;        // W~    [d-block][64 r][64 d]  x 2    (K-major B of a2)
-constexpr uint32_t PB_AQT = 24576;     // Aqk^T [64 i][64 r]                  (MN-major B of c)
-constexpr uint32_t PB_KT = 32768;      // K->   [d-block][64 r][64 d]  x 2    (MN-major B of c)
-constexpr uint32_t PB_SC = 49152;      // fq[64], fk[64], e^{b_C}  (fp32)
-constexpr uint32_t kPrepBlock = 50176;
+// T' is carried as a bf16 hi + lo pair (the two K-major B tiles of a1, back to back); the
+// operands of the c product (Aqk^T, K->, and V_new^T in the recurrence) are fp16, whose 11
+// significand bits keep the intra-chunk products accurate where they nearly cancel (nearly
+// parallel keys with beta close to 2).
+constexpr uint32_t PB_TP = 0;          // T'_hi [64 r][64 i] bf16, then T'_lo  (K-major B of a1)
+constexpr uint32_t PB_W = 16384;       // W~    [d-block][64 r][64 d]  x 2    (K-major B of a2), bf16
+constexpr uint32_t PB_AQT = 32768;     // Aqk^T [64 i][64 r] fp16             (MN-major B of c)
+constexpr uint32_t PB_KT = 40960;      // K->   [d-block][64 r][64 d]  x 2    (MN-major B of c), fp16
+constexpr uint32_t PB_SC = 57344;      // fq[64], e^{b_C}, range flag, 2 x 0 (fp32)
+constexpr uint32_t kPrepBlock = 57856;
 constexpr uint32_t kWsHeader = 1024;   // device error word + padding
 
 // ---- ut_tc_kernel shared memory
@@ -82,19 +87,20 @@ static_assert(4 * (kSmemUt + 1024) <= 233472, "four UT CTAs per SM");
 //   the bf16 state (A of a2) and the bf16 V_new^T (A of c), and a ring of per-chunk factors.
 constexpr int kThreadsRc = 448;        // warp 0: loads, TMEM; warp 1: MMA; warps 2-9: state; 10-13: outputs
 constexpr int kEarly = 2, kLate = 2, kScSlots = 4;
-constexpr uint32_t E_TP = 0, E_V = 8192, E_WQ = 24576, kEarlyBytes = 57344;
+constexpr uint32_t E_TP = 0, E_V = 16384, E_WQ = 32768, kEarlyBytes = 65536;
 constexpr uint32_t kLateBytes = 24576;
 constexpr uint32_t R_EARLY = 0;
 constexpr uint32_t R_LATE = R_EARLY + kEarly * kEarlyBytes;
 constexpr uint32_t R_SBF = R_LATE + kLate * kLateBytes;   // S bf16, [d-block][128 j][64 d] x 2
 constexpr uint32_t R_X = R_SBF + 32768;                   // V_new^T bf16, [128 j][64 r]
-constexpr uint32_t R_SCR = R_X + 16384;                   // factor ring: kScSlots x 1 KB
-constexpr uint32_t kScBytes = 528;                        // fq[64], fk[64], e^{b_C} (+ pad)
-constexpr uint32_t R_BAR = R_SCR + kScSlots * 1024;
+constexpr uint32_t R_SCR = R_X + 16384;                   // factor ring: kScSlots x kScStride
+constexpr uint32_t kScBytes = 272;                        // fq[64], e^{b_C}, range flag (+ pad)
+constexpr uint32_t kScStride = 288;
+constexpr uint32_t R_BAR = R_SCR + kScSlots * kScStride;
 constexpr uint32_t R_MISC = R_BAR + 32 * 8;
 constexpr uint32_t kSmemRc = R_MISC + 64 + 1024;
 static_assert(kEarlyBytes % 1024 == 0 && kLateBytes % 1024 == 0 && kSmemRc <= 232448, "recurrence smem");
-constexpr uint32_t kEarlyTx = 8192 + 16384 + 32768;     // T', V, W~ and Q
+constexpr uint32_t kEarlyTx = 16384 + 16384 + 32768;    // T' (hi, lo), V, W~ and Q
 constexpr uint32_t kLateTx = 24576;                     // Aqk^T and K->
 
 // recurrence tensor-memory columns (512).  The two output accumulators alternate by
@@ -191,6 +197,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+__device__ __forceinline__ uint32_t pack_f16(float a, float b)
+{
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Largest magnitude an fp16 operand may carry before it would round to infinity.
+constexpr float kF16Max = 65504.f;
+
 __device__ __forceinline__ float2 unpack_bf16(uint32_t u)
 {
     __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&u);
@@ -212,33 +227,50 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// tf32 A fragments of one 16-row strip of X (m16n8k8 layout) for the k-steps
+// fp32 A fragments of one 16-row strip of X (m16n8k8 layout) for the k-steps
 // 8ks >= kbeg: X(r, k) = X0[r * xp + k].
 template <int KS>
-__device__ __forceinline__ void load_a_tf32(uint32_t (&fa)[KS][4], const float *X0, int xp, int kbeg, int g, int t)
+__device__ __forceinline__ void load_a_f32(float (&fa)[KS][4], const float *X0, int xp, int kbeg, int g, int t)
 {
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
         const int k0 = 8 * ks;
         if (k0 < kbeg) continue;
-        fa[ks][0] = to_tf32(X0[g * xp + k0 + t]);
-        fa[ks][1] = to_tf32(X0[(g + 8) * xp + k0 + t]);
-        fa[ks][2] = to_tf32(X0[g * xp + k0 + t + 4]);
-        fa[ks][3] = to_tf32(X0[(g + 8) * xp + k0 + t + 4]);
+        fa[ks][0] = X0[g * xp + k0 + t];
+        fa[ks][1] = X0[(g + 8) * xp + k0 + t];
+        fa[ks][2] = X0[g * xp + k0 + t + 4];
+        fa[ks][3] = X0[(g + 8) * xp + k0 + t + 4];
     }
 }
 
-// acc (16 x 8) += X Y over the k-steps 8ks >= kbeg, X given as fragments,
-// Y(k, n) = Y0[k * yp + n].
+// x = hi + lo with hi, lo both tf32 (x - hi is exact in fp32), about 22 bits together.
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo)
+{
+    hi = to_tf32(x);
+    lo = to_tf32(x - __uint_as_float(hi));
+}
+
+// acc (16 x 8) += X Y over the k-steps 8ks >= kbeg, X given as fp32 fragments,
+// Y(k, n) = Y0[k * yp + n], as three tf32 products (X_lo Y_hi + X_hi Y_lo + X_hi Y_hi): the
+// lo x lo term is below fp32 rounding, so the result has fp32 accuracy.  The solve's merges need
+// it: with nearly parallel keys and beta close to 2 the entries of T alternate in sign and a
+// single tf32 pass loses about three decimal digits of the intra-chunk products.
 template <int KS>
-__device__ __forceinline__ void mma_a_tf32(float (&acc)[4], const uint32_t (&fa)[KS][4], const float *Y0, int yp,
-                                           int kbeg, int g, int t)
+__device__ __forceinline__ void mma_a_3xtf32(float (&acc)[4], const float (&fa)[KS][4], const float *Y0, int yp,
+                                             int kbeg, int g, int t)
 {
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
         const int k0 = 8 * ks;
         if (k0 < kbeg) continue;
-        mma_tf32(acc, fa[ks], to_tf32(Y0[(k0 + t) * yp + g]), to_tf32(Y0[(k0 + t + 4) * yp + g]));
+        uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split_tf32(fa[ks][e], ah[e], al[e]);
+        split_tf32(Y0[(k0 + t) * yp + g], bh0, bl0);
+        split_tf32(Y0[(k0 + t + 4) * yp + g], bh1, bl1);
+        mma_tf32(acc, al, bh0, bh1);
+        mma_tf32(acc, ah, bl0, bl1);
+        mma_tf32(acc, ah, bh0, bh1);
     }
 }
 
@@ -270,12 +302,12 @@ __device__ __forceinline__ void solve_in_place(float *__restrict__ A, float *__r
     const int g = lane >> 2, t = lane & 3;
     const int m2 = warp >> 1, h2 = warp & 1, a2 = 32 * m2, b2 = a2 + 16, n2 = a2 + 8 * h2;   // step (ii)
     const int n3 = 8 * warp;                                                               // step (iii)
-    uint32_t c2[2][4], c3[2][4][4];
+    float c2[2][4], c3[2][4][4];
     // C of step (ii): L rows b2.., columns a2..; A^-1 is lower triangular, so
     // k-steps below this warp's first column contribute nothing
-    load_a_tf32<2>(c2, A + b2 * LDL + a2, LDL, 8 * h2, g, t);
+    load_a_f32<2>(c2, A + b2 * LDL + a2, LDL, 8 * h2, g, t);
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) load_a_tf32<4>(c3[mt], A + (32 + 16 * mt) * LDL, LDL, n3, g, t);
+    for (int mt = 0; mt < 2; ++mt) load_a_f32<4>(c3[mt], A + (32 + 16 * mt) * LDL, LDL, n3, g, t);
     {   // (i) diagonal block `warp`, column c of its inverse
         const int o = 16 * warp, c = lane & 15;
         float x[16];
@@ -308,13 +340,13 @@ __device__ __forceinline__ void solve_in_place(float *__restrict__ A, float *__r
     float *M = Mt + warp * 256;   // this warp's C A^-1 columns: up to 32 x 8, pitch 8
     {   // (ii)
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_a_tf32<2>(acc, c2, A + a2 * LDL + n2, LDL, 8 * h2, g, t);
+        mma_a_3xtf32<2>(acc, c2, A + a2 * LDL + n2, LDL, 8 * h2, g, t);
         store_16x8(acc, M, 8, 1.f, g, t);
         __syncwarp();
         float acc2[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t tb[2][4];
-        load_a_tf32<2>(tb, A + b2 * LDL + b2, LDL, 0, g, t);
-        mma_a_tf32<2>(acc2, tb, M, 8, 0, g, t);
+        float tb[2][4];
+        load_a_f32<2>(tb, A + b2 * LDL + b2, LDL, 0, g, t);
+        mma_a_3xtf32<2>(acc2, tb, M, 8, 0, g, t);
         store_16x8(acc2, A + b2 * LDL + n2, LDL, -1.f, g, t);
     }
     if (stamp) GDN_UTR(trace, 12);
@@ -324,22 +356,22 @@ __device__ __forceinline__ void solve_in_place(float *__restrict__ A, float *__r
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_a_tf32<4>(acc, c3[mt], A + n3, LDL, n3, g, t);
+            mma_a_3xtf32<4>(acc, c3[mt], A + n3, LDL, n3, g, t);
             store_16x8(acc, M + 16 * mt * 8, 8, 1.f, g, t);
         }
         __syncwarp();
         {   // rows 32-47: B^-1 is lower triangular, k < 16
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t tb[2][4];
-            load_a_tf32<2>(tb, A + 32 * LDL + 32, LDL, 0, g, t);
-            mma_a_tf32<2>(acc, tb, M, 8, 0, g, t);
+            float tb[2][4];
+            load_a_f32<2>(tb, A + 32 * LDL + 32, LDL, 0, g, t);
+            mma_a_3xtf32<2>(acc, tb, M, 8, 0, g, t);
             store_16x8(acc, A + 32 * LDL + n3, LDL, -1.f, g, t);
         }
         {   // rows 48-63
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t tb[4][4];
-            load_a_tf32<4>(tb, A + 48 * LDL + 32, LDL, 0, g, t);
-            mma_a_tf32<4>(acc, tb, M, 8, 0, g, t);
+            float tb[4][4];
+            load_a_f32<4>(tb, A + 48 * LDL + 32, LDL, 0, g, t);
+            mma_a_3xtf32<4>(acc, tb, M, 8, 0, g, t);
             store_16x8(acc, A + 48 * LDL + n3, LDL, -1.f, g, t);
         }
     }
@@ -380,12 +412,14 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
     const int H = gm.H;
     uint32_t *tmem_sh = reinterpret_cast<uint32_t *>(sm + U_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + U_MISC + 4);
+    volatile int *range_flag = reinterpret_cast<volatile int *>(sm + U_MISC + 8);
     auto bar = [&](int i) -> uint32_t { return sb + U_BAR + 8u * (uint32_t)i; };
     uint8_t *blk = p.blocks + ((size_t)slot * H + h) * kPrepBlock;
 
     if (tid == 0) {
         for (int i = 0; i < 5; ++i) mbar_init(bar(i), 1);
         *abort_flag = 0;
+        *range_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tmem_sh, 128);
@@ -510,6 +544,7 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 // the far blocks the factorised one, so every branch is uniform over the warp.
                 const int i = prow, I = i >> 4, wq = warp & 3;
                 const float bi = bsum[i];
+                float amax = 0.f;   // largest |Aqk| this thread converts to fp16
                 uint32_t u[64];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) tmem_ld16(lane_base + TP1 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(u + q * 16));
@@ -597,16 +632,21 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                         for (int hh = 0; hh < 2; ++hh) {
                             uint32_t w[4];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) w[e] = pack_bf16(v[hh * 8 + 2 * e], v[hh * 8 + 2 * e + 1]);
+                            for (int e = 0; e < 4; ++e) {
+                                amax = fmaxf(amax, fmaxf(fabsf(v[hh * 8 + 2 * e]), fabsf(v[hh * 8 + 2 * e + 1])));
+                                w[e] = pack_f16(v[hh * 8 + 2 * e], v[hh * 8 + 2 * e + 1]);
+                            }
                             *reinterpret_cast<uint4 *>(sm + U_TPP + sw128_offset(i, q * 16 + hh * 8)) =
                                 make_uint4(w[0], w[1], w[2], w[3]);
                         }
                     }
                 }
+                if (amax > kF16Max) *range_flag = 1;
                 if (prow == 0) GDN_UTR(p.trace, 22);
             } else {   // K-> = diag(fk) K in the K tile's own layout; 16-B chunk u of the two
                        // 8-KB tiles per step, so a warp writes 512 contiguous bytes
                 const int t = prow - 64;
+                float kmax = 0.f;   // largest |K->| this thread converts to fp16
 #pragma unroll 4
                 for (int k2 = 0; k2 < 16; ++k2) {
                     const int u = t + 64 * k2, kb = u >> 9, r = (u >> 3) & 63, pc = u & 7;
@@ -617,10 +657,12 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 x = unpack_bf16(w[e]);
-                        o[e] = pack_bf16(x.x * fk, x.y * fk);
+                        kmax = fmaxf(kmax, fmaxf(fabsf(x.x * fk), fabsf(x.y * fk)));
+                        o[e] = pack_f16(x.x * fk, x.y * fk);
                     }
                     *reinterpret_cast<uint4 *>(blk + PB_KT + kb * 8192 + r * 128 + pc * 16) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
+                if (kmax > kF16Max) *range_flag = 1;
                 if (prow == 64) GDN_UTR(p.trace, 23);
             }
             fence_before_sync();
@@ -649,11 +691,13 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                     const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
                     const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
                     const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-                    uint32_t w1[4], w2[4], w3[4];
+                    uint32_t w1[4], w1l[4], w2[4], w3[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float p0 = tv[2 * e] * bv[2 * e], p1 = tv[2 * e + 1] * bv[2 * e + 1];
-                        w1[e] = pack_bf16(p0, p1);
+                        w1[e] = pack_bf16(p0, p1);   // T' = T'_hi + T'_lo, each bf16
+                        const float2 h1 = unpack_bf16(w1[e]);
+                        w1l[e] = pack_bf16(p0 - h1.x, p1 - h1.y);
                         // T'' as a sum of two bf16 terms: W~ = T'' K can cancel heavily (nearly
                         // parallel keys), so its operand carries ~16 bits
                         const float q0 = p0 * ev[2 * e], q1 = p1 * ev[2 * e + 1];
@@ -663,6 +707,7 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                     }
                     const uint32_t off = (uint32_t)(r * 128 + pc * 16);   // = sw128_offset(r, ib)
                     *reinterpret_cast<uint4 *>(blk + PB_TP + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+                    *reinterpret_cast<uint4 *>(blk + PB_TP + 8192 + off) = make_uint4(w1l[0], w1l[1], w1l[2], w1l[3]);
                     *reinterpret_cast<uint4 *>(sm + U_TPP + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
                     *reinterpret_cast<uint4 *>(sm + U_TPL + off) = make_uint4(w3[0], w3[1], w3[2], w3[3]);
                 }
@@ -678,9 +723,9 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 const float bC = bsum[63];
                 if (prow < 64) {
                     reinterpret_cast<float *>(blk + PB_SC)[r] = (r < rows) ? exp2f(bsum[r]) * rq[r] : 0.f;
-                } else {
-                    reinterpret_cast<float *>(blk + PB_SC)[64 + r] = fkt[r];
-                    if (r == 0) reinterpret_cast<float *>(blk + PB_SC)[128] = exp2f(bC);
+                } else if (r < 4) {   // [65]: 1 if an fp16 operand of this block overflowed
+                    reinterpret_cast<float *>(blk + PB_SC)[64 + r] =
+                        (r == 0) ? exp2f(bC) : ((r == 1 && *range_flag) ? 1.f : 0.f);
                 }
             }
             if (prow == 0) GDN_UTR(p.trace, 18);
@@ -789,7 +834,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 if (lane == 0) {
                     const uint32_t base = sb + early(c);
                     mbar_expect_tx(fb, kEarlyTx);
-                    bulk_load(base + E_TP, blk + PB_TP, 8192, fb);
+                    bulk_load(base + E_TP, blk + PB_TP, 16384, fb);                 // T'_hi, T'_lo
                     tma_load_3d(base + E_V, &tmv, j0, h, z, fb);
                     tma_load_3d(base + E_V + 8192, &tmv, j0 + 64, h, z, fb);
                     bulk_load(base + E_WQ, blk + PB_W, 8192, fb);                 // W~ d 0-63   -> rows 0-63
@@ -798,7 +843,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     tma_load_3d(base + E_WQ + 24576, &tmq, 64, h, z, fb);         // Q  d 64-127
                 } else if (lane == 1) {
                     mbar_expect_tx(fb, kScBytes);
-                    bulk_load(sb + R_SCR + s * 1024, blk + PB_SC, kScBytes, fb);
+                    bulk_load(sb + R_SCR + s * kScStride, blk + PB_SC, kScBytes, fb);
                 } else {
                     const uint32_t base = sb + late(c);
                     mbar_expect_tx(fb, kLateTx);
@@ -818,23 +863,23 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
-        // Per chunk three products (16 instructions):
-        //   a1 : D1       = V^T T'^T                       (N = 64,  K = 64)
+        // Per chunk three products (20 instructions):
+        //   a1 : D1       = V^T T'_hi^T + V^T T'_lo^T       (N = 64,  K = 2 x 64)
         //   a2 : D1|D2A  -= S [W~ ; Q]^T                   (N = 128, K = 128)  V_new^T and -S Q^T
         //   c  : D2B|S   += V_new^T [Aqk^T | K->]           (N = 192, K = 64)   outputs and state
         // D2A and D2B (one pair per chunk parity) are re-zeroed by the output warps.
         if (lane == 0 && nch > 0) {
             const uint32_t id_a1 = idesc_bf16(128, 64, true, false);
             const uint32_t id_a2 = idesc_bf16(128, 128, false, false, true);   // negated B
-            const uint32_t id_c = idesc_bf16(128, 192, false, true);
+            const uint32_t id_c = idesc_f16(128, 192, false, true);          // fp16 operands
             auto issue_a1 = [&](int c) -> bool {
                 const uint32_t eb = sb + early(c);
                 if (!wait_spin(bar(RB_EF + c % kEarly), (c / kEarly) & 1, abort_flag, p.err)) return false;
                 fence_after_sync();
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_ss(tb + tm_d1(c), smem_desc(eb + E_V + ks * 2048, 8192, 1024),
-                           smem_desc(eb + E_TP + ks * 32, 16, 1024), id_a1, ks > 0);
+                for (int ks = 0; ks < 8; ++ks)   // K-steps 0-3 against T'_hi, 4-7 against T'_lo
+                    mma_ss(tb + tm_d1(c), smem_desc(eb + E_V + (ks & 3) * 2048, 8192, 1024),
+                           smem_desc(eb + E_TP + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), id_a1, ks > 0);
                 return true;
             };
             auto issue_a2 = [&](int c) -> bool {
@@ -927,7 +972,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 if (gsync(*abort_flag)) break;
                 if (leader) mbar_arrive(bar(RB_S));
                 if (!gwait(RB_SCF, 0)) break;
-                const float e0 = reinterpret_cast<const float *>(sm + R_SCR)[128];
+                const float e0 = reinterpret_cast<const float *>(sm + R_SCR)[64];
 #pragma unroll
                 for (int e = 0; e < 64; ++e) sv[e] = __float_as_uint(e0 * __uint_as_float(sv[e]));
 #pragma unroll
@@ -948,15 +993,19 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     tmem_ld16(lane_base + tm_d1(c) + hf * 32, *reinterpret_cast<uint32_t(*)[16]>(a));
                     tmem_ld16(lane_base + tm_d1(c) + hf * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(a + 16));
                     tmem_wait_ld();
+                    float xmax = 0.f;
 #pragma unroll
                     for (int ch = 0; ch < 4; ++ch) {
                         uint4 w;
-                        w.x = pack_bf16(__uint_as_float(a[ch * 8 + 0]), __uint_as_float(a[ch * 8 + 1]));
-                        w.y = pack_bf16(__uint_as_float(a[ch * 8 + 2]), __uint_as_float(a[ch * 8 + 3]));
-                        w.z = pack_bf16(__uint_as_float(a[ch * 8 + 4]), __uint_as_float(a[ch * 8 + 5]));
-                        w.w = pack_bf16(__uint_as_float(a[ch * 8 + 6]), __uint_as_float(a[ch * 8 + 7]));
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) xmax = fmaxf(xmax, fabsf(__uint_as_float(a[ch * 8 + e])));
+                        w.x = pack_f16(__uint_as_float(a[ch * 8 + 0]), __uint_as_float(a[ch * 8 + 1]));
+                        w.y = pack_f16(__uint_as_float(a[ch * 8 + 2]), __uint_as_float(a[ch * 8 + 3]));
+                        w.z = pack_f16(__uint_as_float(a[ch * 8 + 4]), __uint_as_float(a[ch * 8 + 5]));
+                        w.w = pack_f16(__uint_as_float(a[ch * 8 + 6]), __uint_as_float(a[ch * 8 + 7]));
                         *reinterpret_cast<uint4 *>(sm + R_X + sw128_offset(j, hf * 32 + ch * 8)) = w;
                     }
+                    if (xmax > kF16Max) atomicExch(p.err, kDevErrRange);
                 }
                 fence_proxy_async();
                 fence_before_sync();
@@ -970,7 +1019,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 if (c + 1 < nch) {
                     const int s1 = (c + 1) % kScSlots;
                     if (!gwait(RB_SCF + s1, ((c + 1) / kScSlots) & 1)) break;
-                    const float e1 = reinterpret_cast<const float *>(sm + R_SCR + s1 * 1024)[128];
+                    const float e1 = reinterpret_cast<const float *>(sm + R_SCR + s1 * kScStride)[64];
                     uint32_t sv[64];
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
@@ -1033,13 +1082,14 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             mbar_arrive(bar(RB_OFREE + 1));
         }
         for (int c = 0; c < nch; ++c) {
-            const float *fq = reinterpret_cast<const float *>(sm + R_SCR + (c % kScSlots) * 1024);
+            const float *fq = reinterpret_cast<const float *>(sm + R_SCR + (c % kScSlots) * kScStride);
             bool ok = true;
             if (leader) {
                 ok = wait_spin(bar(RB_SCF + c % kScSlots), (c / kScSlots) & 1, abort_flag, p.err);
                 ok = ok && wait_spin(bar(RB_D2O + (c & 1)), (c >> 1) & 1, abort_flag, p.err);
             }
             if (osync(!ok)) break;
+            if (leader && fq[65] != 0.f) atomicExch(p.err, kDevErrRange);   // flagged by the chunk-local kernel
             if (leader) GDN_TR(p.trace, 0, c, 0);
             fence_after_sync();
             uint8_t *stg = sm + late(c);

@@ -24,6 +24,7 @@ constexpr float kL2Eps = 1e-6f;
 // Device error word codes (first 4 bytes of the workspace header).
 constexpr unsigned kDevErrNone = 0u;
 constexpr unsigned kDevErrTimeout = 1u;
+constexpr unsigned kDevErrRange = 2u;   // a tensor-core operand exceeded the fp16 range
 
 struct Geometry {
     int B, T, H, dk, dv, N;

@@ -20,9 +20,14 @@
 //   - is one buffer per GPU, so calls that overlap on the GPU (different
 //     streams, or different host threads) race on it: callers must order them.
 // Host code cannot use the array's name as a device address (it names a
-// host-side stand-in), so the first call on each device looks the address
-// up with cudaGetSymbolAddress while that device is current and caches it.
-// That first call should therefore come before any stream capture.
+// host-side stand-in), so every call looks the address up with
+// cudaGetSymbolAddress while the call's device is current.  A device reset
+// (cudaDeviceReset) unloads the module and the array may come back at another
+// address; looking it up on every call keeps the address current.  While the
+// caller's stream is being captured into a graph the lookup is skipped and the
+// address found by the last call on that device outside a capture is used, so
+// at least one call on each device (after any device reset) must come before
+// a capture.
 #include <mutex>
 #include <stdint.h>
 
@@ -41,18 +46,24 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 constexpr int kMaxDevices = 128;
 std::mutex g_setup_mu;
-void *g_scratch_addr[kMaxDevices];   // device address of g_noalloc_scratch, per device
+void *g_scratch_addr[kMaxDevices];   // last looked-up device address of g_noalloc_scratch, per device
 
-// Looks up (once per device, with that device current) the device address of
-// the scratch array.  Returns nullptr on failure.
-void *scratch_on_current_device(cudaError_t *err)
+// The device address of the scratch array on the current device.  Outside a
+// stream capture it is looked up afresh (cudaGetSymbolAddress, which neither
+// allocates nor enqueues work), so it follows a device reset; during a capture
+// of `stream` the last address found on this device is reused.  Returns nullptr
+// on failure.
+void *scratch_on_current_device(cudaStream_t stream, cudaError_t *err)
 {
     int dev = -1;
     *err = cudaGetDevice(&dev);
     if (*err != cudaSuccess) return nullptr;
     if (dev < 0 || dev >= kMaxDevices) { *err = cudaErrorInvalidDevice; return nullptr; }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    *err = cudaStreamIsCapturing(stream, &cs);
+    if (*err != cudaSuccess) return nullptr;
     std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (!g_scratch_addr[dev]) {
+    if (cs == cudaStreamCaptureStatusNone || !g_scratch_addr[dev]) {
         void *p = nullptr;
         *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (*err != cudaSuccess || !p) return nullptr;
@@ -94,7 +105,7 @@ extern "C" gdn_status gdn_chunk_fwd_noalloc(const void *q, const void *k, const 
     if (need > kNoAllocScratchBytes) return GDN_ERR_WORKSPACE;   // problem too large for the fixed array
 
     cudaError_t e = cudaSuccess;
-    void *scratch = scratch_on_current_device(&e);
+    void *scratch = scratch_on_current_device((cudaStream_t)stream, &e);
     if (!scratch) return GDN_ERR_CUDA;
 
     ChunkArgs a;

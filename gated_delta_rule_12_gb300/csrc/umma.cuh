@@ -55,6 +55,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with fp16 A and B (format code 0), fp32 accumulate.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major,
+                                                 bool negate_b = false)
+{
+    return (1u << 4)                       // D format: f32
+         | ((negate_b ? 1u : 0u) << 14)
+         | ((a_mn_major ? 1u : 0u) << 15)
+         | ((b_mn_major ? 1u : 0u) << 16)
+         | ((uint32_t)(N >> 3) << 17)
+         | ((uint32_t)(M >> 4) << 24);
+}
+
 // ---------------------------------------------------------------------------
 // MMA issue (single thread)
 // ---------------------------------------------------------------------------

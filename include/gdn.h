@@ -50,7 +50,8 @@ typedef enum {
     GDN_ERR_UNSUPPORTED = 2,     /* valid but not implemented (e.g. head dims)  */
     GDN_ERR_WORKSPACE = 3,       /* workspace missing or smaller than required  */
     GDN_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed        */
-    GDN_ERR_DEVICE_TIMEOUT = 5   /* a kernel gave up waiting (see check below)  */
+    GDN_ERR_DEVICE_TIMEOUT = 5,  /* a kernel gave up waiting (see check below)  */
+    GDN_ERR_RANGE = 6            /* a value left the range of an fp16 operand   */
 } gdn_status;
 
 typedef enum {
@@ -109,6 +110,18 @@ int32_t gdn_chunk_fwd_kernel_count(int32_t B, int32_t T, int32_t H, int32_t dk, 
  *   workspace     device scratch of at least gdn_chunk_fwd_workspace_size()
  *                 bytes, 256-byte aligned; its first 256 bytes hold the
  *                 device error word read by gdn_check_device_error.
+ * Precision: arithmetic and accumulation are fp32.  On the tensor-core path
+ * (bf16, dk = 128, dv a multiple of 128) the MMA operands are rounded: the
+ * state copy, W<- and the raw q, k, v are bf16, T diag(beta) is a bf16 hi + lo
+ * pair, and the three operands of the intra-chunk product
+ * (U~ - W<- S^T) [Q K^T o Gamma | K->] are fp16, whose 11 significand bits
+ * keep that product accurate where its terms nearly cancel (nearly parallel
+ * keys with beta close to 2).  fp16 holds magnitudes up to 65504: a call in
+ * which U~ - W<- S^T, Q K^T o Gamma or K-> exceeds that records
+ * GDN_ERR_RANGE in the device error word (read by gdn_check_device_error).
+ * Values below about 6e-5 in magnitude are carried with reduced relative
+ * precision (fp16 subnormals), which is negligible against entries of
+ * ordinary size in the same product.
  * Errors: GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE,
  *         GDN_ERR_CUDA.  Nothing is enqueued when an error is returned
  *         before the first launch.
@@ -198,7 +211,8 @@ gdn_status gdn_decode_multi(float *state,
 /*
  * Reads and clears the device error word at the start of `workspace`
  * (synchronises `stream`).  Returns GDN_OK, GDN_ERR_DEVICE_TIMEOUT when a
- * kernel gave up on a bounded wait, or GDN_ERR_CUDA.
+ * kernel gave up on a bounded wait, GDN_ERR_RANGE when a tensor-core operand
+ * left the fp16 range (see gdn_chunk_fwd), or GDN_ERR_CUDA.
  */
 gdn_status gdn_check_device_error(void *workspace, void *stream);
 
@@ -267,9 +281,12 @@ gdn_status gdn_prologue(const void *xq, const void *xk, const void *xv,
  *     than GDN_NOALLOC_SCRATCH_BYTES is rejected with GDN_ERR_WORKSPACE
  *     before any work is enqueued (for example B=1, H=8, T=2048, dk=dv=128
  *     needs 16.2 MiB and fits; H=16 needs 32.4 MiB and does not).
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *   - Every call looks up the array's device address (cudaGetSymbolAddress,
+ *     with the call's device current), so the address stays valid across a
+ *     device reset.  While `stream` is being captured the lookup is skipped and
+ *     the address found by the last uncaptured call on that device is used:
+ *     make at least one call on each device (and one after any cudaDeviceReset)
+ *     before capturing.
  *   - All calls on a device share the one array and it keeps the previous
  *     call's contents (the call clears what must start at zero).  Calls that
  *     overlap on the GPU race on it: order them (one stream, or events).

@@ -28,8 +28,24 @@ def errors(got, ref):
     return maxabs, rel
 
 
+# Every comparison made through assert_close is recorded here (test id, quantity, errors, bounds);
+# conftest.py writes the records to the file named by GDN_PARITY_LOG at the end of the session, so the
+# margins of a GPU run can be kept beside its results.
+RECORDS = []
+CURRENT_TEST = [""]
+
+
+def record(what, dtype, maxabs, rel, bound_rel=None, bound_maxabs=None):
+    RECORDS.append({"test": CURRENT_TEST[0], "what": what, "dtype": dtype, "max_abs": maxabs, "rel_l2": rel,
+                    "bound_rel_l2": bound_rel, "bound_max_abs": bound_maxabs})
+
+
 def assert_close(got, ref, dtype, what=""):
     maxabs, rel = errors(got, ref)
+    if dtype == "f32":
+        record(what, dtype, maxabs, rel, None, TOL_F32_MAXABS)
+    else:
+        record(what, dtype, maxabs, rel, TOL_BF16_REL_L2, TOL_BF16_MAXABS)
     if dtype == "f32":
         assert maxabs <= TOL_F32_MAXABS, f"{what}: max-abs {maxabs:.3e} > {TOL_F32_MAXABS}"
     else:
