@@ -495,6 +495,10 @@ def bench_ours(args):
     pro = bench_prologue(w, dev, flush, stream, reps, peaks)
     pro["value"] = job_throughput(w.B * w.L, ws_n, max_over_ranks(dist, pro["ms_per_call"]))
 
+    # the block prologue fused into the chunked forward, against the two calls
+    fused = bench_prologue_chunk(w, dev, flush, stream, reps, peaks)
+    fused["value"] = job_throughput(w.B * w.L, ws_n, max_over_ranks(dist, fused["ms_per_call"]))
+
     # the other chunked-forward workloads of the table (parity cases, timed here too)
     others = {}
     for key, name in (("small_f32", "prefill_b1_h2_l256_d64_f32"), ("varlen", "varlen_t32768_h16_d128_bf16"),
@@ -533,6 +537,7 @@ def bench_ours(args):
                                           "frac": m_ach / peaks["hbm_gbs"], "algorithmic_bytes": mbytes},
                              "timing": f"{wd.steps} tokens as {calls} calls in one CUDA graph, median of {reps}"},
             "prologue": pro,
+            "prologue_chunk_fwd": fused,
             "backward": bwd,
             **others,
             "gpu_launches": args.steps * launches_per_step,
@@ -622,6 +627,69 @@ def bench_prologue(w: inputs.Workload, dev, flush, stream, reps: int, peaks, K: 
                          "frac": ach / peaks["hbm_gbs"], "traffic": traffic_record("prologue"),
                          "algorithmic_bytes": nbytes},
             "timing": f"median of {max(reps, 5)} calls, L2 flushed before each"}
+
+
+def bench_prologue_chunk(w: inputs.Workload, dev, flush, stream, reps: int, peaks, K: int = PROLOGUE_K):
+    """gdn_prologue_chunk_fwd (the block prologue fused into the chunked forward) on the workload's shape,
+    against gdn_prologue followed by gdn_chunk_fwd on the same projections."""
+    import gated_delta_rule_12_gb300 as gdn
+    gen = torch.Generator().manual_seed(w.seed + 300)
+    rn = lambda *shape: torch.randn(shape, generator=gen, dtype=torch.float32)
+    B, T, H, dk, dv = w.B, w.L, w.H, w.dk, w.dv
+    x = [rn(B, T, H, dk).to(torch.bfloat16).to(dev), rn(B, T, H, dk).to(torch.bfloat16).to(dev),
+         rn(B, T, H, dv).to(torch.bfloat16).to(dev)]
+    wts = [(0.5 * rn(H, dk, K)).to(dev), (0.5 * rn(H, dk, K)).to(dev), (0.5 * rn(H, dv, K)).to(dev)]
+    ab = [rn(B, T, H).to(dev), rn(B, T, H).to(dev)]
+    par = [(0.5 * rn(H) - 1.0).to(dev), (0.5 * rn(H)).to(dev)]
+    s_in = torch.zeros((B, K - 1, H, 2 * dk + dv), dtype=torch.bfloat16, device=dev)
+    s_out = torch.empty_like(s_in)
+    s0 = torch.zeros((B, H, dv, dk), dtype=torch.float32, device=dev)
+    out = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device=dev)
+    sf = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev)
+    ws_f = torch.empty(int(gdn.load_library().gdn_prologue_chunk_fwd_workspace_size(B, T, H, dk, dv, 0, gdn.GDN_BF16)),
+                       dtype=torch.uint8, device=dev)
+    ws_s = torch.empty(gdn.chunk_fwd_workspace_size(B, T, H, dk, dv, 0, torch.bfloat16), dtype=torch.uint8, device=dev)
+    mid = (torch.empty_like(x[0]), torch.empty_like(x[1]), torch.empty_like(x[2]),
+           torch.empty((B, T, H), dtype=torch.float32, device=dev), torch.empty((B, T, H), dtype=torch.float32, device=dev))
+
+    def fused():
+        gdn.prologue_chunk_fwd(*x, *wts, *ab, *par, conv_state_in=s_in, conv_state_out=s_out, init_state=s0,
+                               scale=w.scale, out=out, final_state=sf, workspace=ws_f)
+
+    def separate():
+        q, k, v, g, beta = gdn.prologue(*x, *wts, *ab, *par, conv_state_in=s_in, conv_state_out=s_out, out=mid)
+        gdn.chunk_fwd(q, k, v, g, beta, init_state=s0, scale=w.scale, out=out, final_state=sf, workspace=ws_s)
+
+    def timed(fn):
+        for _ in range(3):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        t = []
+        for _ in range(max(reps, 5)):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            t.append(a.elapsed_time(b))
+        return statistics.median(t)
+
+    ms_f, ms_s = timed(fused), timed(separate)
+    th = B * T * H
+    # algorithmic bytes of the fused call: projections and gate projections in, out, the states once
+    nbytes = th * ((2 * dk + dv) * 2 + 8 + dv * 2) + 2 * B * (K - 1) * H * (2 * dk + dv) * 2 + 2 * B * H * dv * dk * 4
+    # the separate calls also write q, k, v, g, beta and read them back
+    extra = 2 * th * ((2 * dk + dv) * 2 + 8)
+    ach = nbytes / (ms_f * 1e-3) / 1e9
+    return {"workload": f"{PREFILL} from projections, conv width {K}", "unit": "tokens/s",
+            "value": B * T / (ms_f * 1e-3), "ms_per_call": ms_f, "separate_ms_per_call": ms_s,
+            "separate_value": B * T / (ms_s * 1e-3),
+            "algorithmic_bytes": nbytes, "bytes_not_moved_vs_separate": extra,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / peaks["hbm_gbs"], "algorithmic_bytes": nbytes},
+            "timing": f"median of {max(reps, 5)} calls each, L2 flushed before each"}
 
 
 # ---------------------------------------------------------------------------

@@ -12,6 +12,8 @@ Entry points (same names as the C ABI, without the ``gdn_`` prefix):
     decode_step(state, q, k, v, g, beta)  -> out            (state updated in place)
     decode_multi(state, q, k, v, g, beta) -> out [N,T,H,dv] (T tokens per call, state in place)
     prologue(xq, xk, xv, wq, wk, wv, a, b, A_log, dt_bias, ...) -> (q, k, v, g, beta)
+    prologue_chunk_fwd(xq, xk, xv, wq, wk, wv, a, b, A_log, dt_bias, ...) -> (out, final_state)
+                                          (prologue fused into the chunked forward)
     chunk_fwd_workspace_size(...)         -> bytes
     chunk_fwd_kernel_count(...)           -> kernels one chunk_fwd call launches
     chunk_bwd(q, k, v, g, beta, dout, ...) -> (dq, dk, dv, dg, dbeta, dinit_state)
@@ -36,7 +38,8 @@ CHUNK = 64
 
 EXPORTS = ["gdn_status_string", "gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd_kernel_count", "gdn_chunk_fwd",
            "gdn_chunk_bwd_workspace_size", "gdn_chunk_bwd", "gdn_decode_step", "gdn_decode_multi", "gdn_prologue",
-           "gdn_check_device_error", "gdn_chunk_fwd_noalloc"]
+           "gdn_check_device_error", "gdn_chunk_fwd_noalloc", "gdn_prologue_chunk_fwd_workspace_size",
+           "gdn_prologue_chunk_fwd"]
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -99,6 +102,11 @@ def load_library(path: str = LIB_PATH, build_if_missing: bool = False) -> ctypes
                                               _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _f32, _i32, _i32,
                                               _vp]
         lib.gdn_chunk_fwd_noalloc.restype = ctypes.c_int
+        lib.gdn_prologue_chunk_fwd_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_int]
+        lib.gdn_prologue_chunk_fwd_workspace_size.restype = _sz
+        lib.gdn_prologue_chunk_fwd.argtypes = [_vp] * 13 + [_vp, _i32, _vp, _vp] + [_i32] * 6 + \
+            [ctypes.c_int, _f32, _i32, _i32, _vp, _sz, _vp]
+        lib.gdn_prologue_chunk_fwd.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -328,6 +336,60 @@ def prologue(xq, xk, xv, wq, wk, wv, a, b, A_log, dt_bias, conv_state_in=None, c
     if rc != GDN_OK:
         raise GDNError(rc, "gdn_prologue")
     return q, k, v, g, beta
+
+
+def prologue_chunk_fwd(xq, xk, xv, wq, wk, wv, a, b, A_log, dt_bias, conv_state_in=None, conv_state_out=None,
+                       init_state=None, cu_seqlens=None, scale=None, use_qk_l2norm=True, out=None, final_state=None,
+                       output_final_state=True, workspace=None, chunk_size=CHUNK, stream=None):
+    """Block prologue and chunked forward in one call (``gdn_prologue_chunk_fwd``): the result of
+    ``prologue`` followed by ``chunk_fwd``, without q, k, v, g, beta ever being written out.
+
+    xq, xk [B,T,H,dk], xv [B,T,H,dv] bf16 (dk = 128, dv a multiple of 128); wq, wk [H,dk,K], wv [H,dv,K]
+    fp32; a, b [B,T,H] fp32; A_log, dt_bias [H] fp32; conv states [N,K-1,H,2dk+dv] bf16 or None;
+    init_state [N,H,dv,dk] fp32 or None; cu_seqlens int32 [N+1] or None.  Returns ``(out, final_state)``.
+    """
+    lib = load_library()
+    B, T, H, dk = xq.shape
+    dv = xv.shape[-1]
+    K = wq.shape[-1]
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else B
+    if scale is None:
+        scale = dk ** -0.5
+    if xq.dtype != torch.bfloat16 or xk.dtype != torch.bfloat16 or xv.dtype != torch.bfloat16:
+        raise TypeError("prologue_chunk_fwd: projections must be bfloat16")
+    for t in (wq, wk, wv, a, b, A_log, dt_bias, init_state, final_state):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError("filters, gate projections, gate parameters and states must be float32")
+    if wq.shape != (H, dk, K) or wk.shape != (H, dk, K) or wv.shape != (H, dv, K):
+        raise ValueError("prologue_chunk_fwd: filters must be [H, d, K]")
+    if a.shape != (B, T, H) or b.shape != (B, T, H) or A_log.shape != (H,) or dt_bias.shape != (H,):
+        raise ValueError("prologue_chunk_fwd: gate shapes")
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    for t in (conv_state_in, conv_state_out):
+        if t is not None and (t.dtype != torch.bfloat16 or tuple(t.shape) != (N, K - 1, H, 2 * dk + dv)):
+            raise ValueError("conv states must be bfloat16 [N, K-1, H, 2dk+dv]")
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device=xq.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, dv, dk), dtype=torch.float32, device=xq.device)
+    _need_cuda(xq, xk, xv, wq, wk, wv, a, b, A_log, dt_bias, conv_state_in, conv_state_out, init_state, cu_seqlens,
+               out, final_state)
+    num_seqs = N if cu_seqlens is not None else 0
+    need = int(lib.gdn_prologue_chunk_fwd_workspace_size(B, T, H, dk, dv, num_seqs, GDN_BF16))
+    if need == 0:
+        raise GDNError(2, "gdn_prologue_chunk_fwd (unsupported size)")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=xq.device)
+    rc = lib.gdn_prologue_chunk_fwd(_ptr(xq), _ptr(xk), _ptr(xv), _ptr(wq), _ptr(wk), _ptr(wv), _ptr(a), _ptr(b),
+                                    _ptr(A_log), _ptr(dt_bias), _ptr(conv_state_in), _ptr(conv_state_out),
+                                    _ptr(init_state), _ptr(cu_seqlens), num_seqs, _ptr(out), _ptr(final_state),
+                                    B, T, H, dk, dv, K, GDN_BF16, float(scale), int(bool(use_qk_l2norm)),
+                                    int(chunk_size), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream(stream))
+    if rc != GDN_OK:
+        raise GDNError(rc, "gdn_prologue_chunk_fwd")
+    return out, final_state
 
 
 def check_device_error(workspace, stream=None):

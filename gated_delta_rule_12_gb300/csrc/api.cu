@@ -261,6 +261,92 @@ gdn_status gdn_selftest_wait_timeout(void *workspace, uint32_t limit_us, void *s
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+size_t gdn_prologue_chunk_fwd_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv,
+                                             int32_t num_seqs, gdn_dtype dt)
+{
+    if (B < 1 || T < 0 || H < 1 || num_seqs < 0) return 0;
+    if (dt != GDN_BF16 || !chunk_tc_supported(1, dk, dv, 1)) return 0;
+    const bool varlen = num_seqs > 0;
+    if (varlen && B != 1) return 0;
+    const int64_t slots = (int64_t)B * T > 0 ? num_slots(B, T, varlen ? num_seqs : B, varlen) : 0;
+    return chunk_tc_workspace_bytes(slots, H, true);
+}
+
+gdn_status gdn_prologue_chunk_fwd(const void *xq, const void *xk, const void *xv, const float *wq,
+                                  const float *wk, const float *wv, const float *a, const float *b,
+                                  const float *A_log, const float *dt_bias, const void *conv_state_in,
+                                  void *conv_state_out, const float *init_state, const int32_t *cu_seqlens,
+                                  int32_t num_seqs, void *out, float *final_state, int32_t B, int32_t T,
+                                  int32_t H, int32_t dk, int32_t dv, int32_t K, gdn_dtype dt, float scale,
+                                  int32_t use_qk_l2norm, int32_t chunk_size, void *workspace,
+                                  size_t workspace_bytes, void *stream)
+{
+    if (B < 1 || T < 0 || H < 1 || dk < 1 || dv < 1) return GDN_ERR_INVALID_ARG;
+    if (dt != GDN_F32 && dt != GDN_BF16) return GDN_ERR_INVALID_ARG;
+    if (chunk_size != kChunk) return GDN_ERR_UNSUPPORTED;
+    if (dt != GDN_BF16 || !chunk_tc_supported(1, dk, dv, 1) || K < 1 || K > 4) return GDN_ERR_UNSUPPORTED;
+    const bool varlen = cu_seqlens != nullptr;
+    if (varlen && (B != 1 || num_seqs < 1)) return GDN_ERR_INVALID_ARG;
+    if (!varlen && num_seqs != 0 && num_seqs != B) return GDN_ERR_INVALID_ARG;
+    const int N = varlen ? num_seqs : B;
+    const int64_t tokens = (int64_t)B * T;
+    if (tokens >= ((int64_t)1 << 31)) return GDN_ERR_INVALID_ARG;
+    const bool have_tokens = tokens > 0;
+    if (have_tokens) {
+        const void *need[] = {xq, xk, xv, wq, wk, wv, a, b, A_log, dt_bias, out};
+        for (const void *p : need)
+            if (!p) return GDN_ERR_INVALID_ARG;
+    }
+    const void *al16[] = {xq, xk, xv, out, init_state, final_state, conv_state_in, conv_state_out};
+    for (const void *p : al16)
+        if (p && !aligned16(p)) return GDN_ERR_INVALID_ARG;
+    const void *al4[] = {wq, wk, wv, a, b, A_log, dt_bias, cu_seqlens};
+    for (const void *p : al4)
+        if (p && !aligned_to(p, 4)) return GDN_ERR_INVALID_ARG;
+    if (conv_state_in && conv_state_out && K > 1) {   // the two state buffers must not overlap
+        const size_t bytes = (size_t)N * (K - 1) * H * (2 * dk + dv) * 2;
+        const uintptr_t i0 = (uintptr_t)conv_state_in, o0 = (uintptr_t)conv_state_out;
+        if (i0 < o0 + bytes && o0 < i0 + bytes) return GDN_ERR_INVALID_ARG;
+    }
+    if (!workspace || ((uintptr_t)workspace & 255u) != 0) return GDN_ERR_WORKSPACE;
+    const size_t need = gdn_prologue_chunk_fwd_workspace_size(B, T, H, dk, dv, varlen ? num_seqs : 0, dt);
+    if (need == 0) return GDN_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return GDN_ERR_WORKSPACE;
+
+    PrologueArgs pa;
+    pa.xq = xq; pa.xk = xk; pa.xv = xv; pa.wq = wq; pa.wk = wk; pa.wv = wv;
+    pa.a = a; pa.b = b; pa.A_log = A_log; pa.dt_bias = dt_bias;
+    pa.state_in = K > 1 ? conv_state_in : nullptr;
+    pa.state_out = K > 1 ? conv_state_out : nullptr;
+    pa.cu = cu_seqlens;
+    pa.q = nullptr; pa.k = nullptr; pa.v = nullptr; pa.g = nullptr; pa.beta = nullptr;
+    pa.B = B; pa.T = T; pa.H = H; pa.dk = dk; pa.dv = dv; pa.N = N; pa.K = K;
+    pa.dt = 1;
+    ChunkArgs ca;
+    ca.q = nullptr; ca.k = nullptr; ca.v = nullptr; ca.g = nullptr; ca.beta = nullptr;
+    ca.init_state = init_state; ca.out = out; ca.final_state = final_state;
+    ca.gm.B = B; ca.gm.T = T; ca.gm.H = H; ca.gm.dk = dk; ca.gm.dv = dv; ca.gm.N = N;
+    ca.gm.cu = cu_seqlens;
+    ca.gm.nct = ceil_div(T, kChunk);
+    ca.slots = have_tokens ? num_slots(B, T, N, varlen) : 0;
+    ca.dt = 1;
+    ca.scale = scale;
+    ca.l2 = use_qk_l2norm ? 1 : 0;
+    ca.workspace = workspace;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e;
+    if (!have_tokens) {
+        // nothing to transform: the states pass through (the prologue kernel carries the
+        // convolution state of empty sequences; the CUDA-core path copies init to final)
+        e = pa.state_out ? launch_prologue(pa, st) : cudaSuccess;
+        if (e == cudaSuccess) e = launch_chunk_simt(ca, st);
+    } else {
+        ca.fuse = &pa;
+        e = launch_chunk_tc(ca, st);
+    }
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 gdn_status gdn_check_device_error(void *workspace, void *stream)
 {
     if (!workspace || ((uintptr_t)workspace & 255u) != 0) return GDN_ERR_INVALID_ARG;

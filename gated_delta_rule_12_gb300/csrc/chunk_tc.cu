@@ -62,6 +62,10 @@ constexpr uint32_t PB_AQT = 32768;     // Aqk^T [64 i][64 r] fp16             (M
 constexpr uint32_t PB_KT = 40960;      // K->   [d-block][64 r][64 d]  x 2    (MN-major B of c), fp16
 constexpr uint32_t PB_SC = 57344;      // fq[64], e^{b_C}, range flag, 2 x 0 (fp32)
 constexpr uint32_t kPrepBlock = 57856;
+// With the block prologue fused in, the chunk-local kernel also leaves the convolved Q tile
+// (both 64-wide d-blocks, in the TMA box layout) for the recurrence.
+constexpr uint32_t PB_QC = kPrepBlock;
+constexpr uint32_t kPrepBlockFused = kPrepBlock + 16384;
 constexpr uint32_t kWsHeader = 1024;   // device error word + padding
 
 // ---- ut_tc_kernel shared memory
@@ -86,6 +90,7 @@ static_assert(4 * (kSmemUt + 1024) <= 233472, "four UT CTAs per SM");
 //                       merged c product; afterwards the chunk's output staging tile
 //   the bf16 state (A of a2) and the bf16 V_new^T (A of c), and a ring of per-chunk factors.
 constexpr int kThreadsRc = 448;        // warp 0: loads, TMEM; warp 1: MMA; warps 2-9: state; 10-13: outputs
+                                       // (and, with the block prologue fused in, the V convolution)
 constexpr int kEarly = 2, kLate = 2, kScSlots = 4;
 constexpr uint32_t E_TP = 0, E_V = 16384, E_WQ = 32768, kEarlyBytes = 65536;
 constexpr uint32_t kLateBytes = 24576;
@@ -100,7 +105,8 @@ constexpr uint32_t R_BAR = R_SCR + kScSlots * kScStride;
 constexpr uint32_t R_MISC = R_BAR + 32 * 8;
 constexpr uint32_t kSmemRc = R_MISC + 64 + 1024;
 static_assert(kEarlyBytes % 1024 == 0 && kLateBytes % 1024 == 0 && kSmemRc <= 232448, "recurrence smem");
-constexpr uint32_t kEarlyTx = 16384 + 16384 + 32768;    // T' (hi, lo), V, W~ and Q
+constexpr uint32_t kEarlyTxA = 16384 + 16384;          // T' (hi, lo) and V
+constexpr uint32_t kEarlyTxB = 32768;                  // W~ and Q
 constexpr uint32_t kLateTx = 24576;                     // Aqk^T and K->
 
 // recurrence tensor-memory columns (512).  The two output accumulators alternate by
@@ -113,11 +119,14 @@ __device__ __forceinline__ uint32_t tm_d2a(int c) { return (c & 1) ? 448u : 64u;
 __device__ __forceinline__ uint32_t tm_d2b(int c) { return (c & 1) ? 320u : 128u; }
 __device__ __forceinline__ uint32_t tm_c(int c) { return (c & 1) ? 192u : 128u; }
 
-enum : int { RB_EF = 0, RB_EE = 2, RB_LF = 4, RB_LE = 6, RB_SCF = 8, RB_SCE = 12,   // rings
+// The early ring's two halves fill and drain separately: A (T', V) is read only by a1 and may be
+// refilled as soon as a1 completes; B ([W~ | Q]) is read by a2.
+enum : int { RB_EF = 0, RB_EE = 2, RB_LF = 4, RB_LE = 6, RB_SCF = 8, RB_SCE = 12,   // rings (EF/EE: half A)
              RB_D1 = 16, RB_X = 17, RB_S = 18, RB_SP = 19, RB_D2 = 20,
              RB_D2O = 21, RB_OFREE = 23,                                         // [2] by parity
-             RB_FIN = 25, RB_COUNT = 26 };
-enum : int { UB_QK = 0, UB_P1 = 1, UB_TRDY = 2, UB_P2 = 3, UB_FIN = 4 };
+             RB_FIN = 25, RB_VC = 26,                    // RB_VC [2]: V convolved (early slot)
+             RB_EFB = 28, RB_EEB = 30, RB_COUNT = 32 };  // early ring, half B
+enum : int { UB_QK = 0, UB_P1 = 1, UB_TRDY = 2, UB_P2 = 3, UB_FIN = 4, UB_CONV = 5, UB_COUNT = 6 };
 
 // Development-only phase timestamps (SM clock) of the first CTA; compiled out
 // of the library unless GDN_KERNEL_TRACE is defined.
@@ -383,16 +392,37 @@ __device__ __forceinline__ void solve_in_place(float *__restrict__ A, float *__r
 // ===========================================================================
 // chunk-local UT transform
 // ===========================================================================
+// The block prologue, when it is fused into the chunked forward ("Gated Delta Networks: Improving
+// Mamba2 with Delta Rule", §3.4 "Token mixing block", Fig. 1): q, k, v = SiLU(short causal
+// depthwise convolution of the projections), g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b).
+// The arithmetic is written exactly as in prologue.cu, so the fused call reproduces
+// gdn_prologue followed by gdn_chunk_fwd bit for bit.
+struct ConvParams {
+    const __nv_bfloat16 *xq, *xk, *xv;         // raw projections [rows, H, d] (halo rows are read here)
+    const float *wq, *wk, *wv;                 // filters [H, d, K]
+    const float *a, *b, *A_log, *dt_bias;      // gate projections [rows, H]; per-head parameters [H]
+    const __nv_bfloat16 *state_in;             // [N, K-1, H, 2 dk + dv] or null (zeros)
+    __nv_bfloat16 *state_out;                  // same layout, or null
+};
+
+__device__ __forceinline__ float conv_silu(float z) { return __fdividef(z, 1.f + __expf(-z)); }
+__device__ __forceinline__ float gate_softplus(float z) { return z > 20.f ? z : log1pf(expf(z)); }
+
 struct UtParams {
     const float *g, *beta;
     uint8_t *blocks;
+    size_t block_bytes;
     unsigned *err;
     Geometry gm;
     float scale;
     int l2;
     long long *trace;
+    ConvParams cv;      // used when the kernel is instantiated with a convolution width KC > 0
 };
 
+// KC = 0: q, k, g, beta are the operator's inputs.  KC = 1..4: they are made here from the raw
+// projections by the block prologue with a convolution of width KC.
+template <int KC>
 __global__ void __launch_bounds__(kThreadsUt, 4)
 ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk, const UtParams p)
 {
@@ -414,10 +444,10 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + U_MISC + 4);
     volatile int *range_flag = reinterpret_cast<volatile int *>(sm + U_MISC + 8);
     auto bar = [&](int i) -> uint32_t { return sb + U_BAR + 8u * (uint32_t)i; };
-    uint8_t *blk = p.blocks + ((size_t)slot * H + h) * kPrepBlock;
+    uint8_t *blk = p.blocks + ((size_t)slot * H + h) * p.block_bytes;
 
     if (tid == 0) {
-        for (int i = 0; i < 5; ++i) mbar_init(bar(i), 1);
+        for (int i = 0; i < UB_COUNT; ++i) mbar_init(bar(i), 1);
         *abort_flag = 0;
         *range_flag = 0;
         fence_mbar_init();
@@ -437,7 +467,10 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
             tma_load_3d(sb + U_QK + 8192, &tmq, 0, h, z, bar(UB_QK));
             tma_load_3d(sb + U_QK + 16384, &tmk, 64, h, z, bar(UB_QK));
             tma_load_3d(sb + U_QK + 24576, &tmq, 64, h, z, bar(UB_QK));
-            if (wait_bar(bar(UB_QK), 0, abort_flag, p.err)) {
+            bool tiles = wait_bar(bar(UB_QK), 0, abort_flag, p.err);
+            if (KC > 0 && tiles) tiles = wait_bar(bar(UB_CONV), 0, abort_flag, p.err);   // convolved in place
+            if (tiles) {
+                fence_after_sync();
                 const uint32_t id_p1 = idesc_bf16(128, 128, false, false);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {   // G = [K; Q] [K; Q]^T  (rows 0-63: K K^T | K Q^T)
@@ -479,7 +512,11 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 const int64_t t = (tok0c + r) * H + h;
                 float x = 0.f;
                 if (prow < 64) {
-                    x = (r < rows) ? p.g[t] * kLog2e : 0.f;
+                    if (KC > 0) {
+                        x = (r < rows) ? -expf(p.cv.A_log[h]) * gate_softplus(p.cv.a[t] + p.cv.dt_bias[h]) * kLog2e : 0.f;
+                    } else {
+                        x = (r < rows) ? p.g[t] * kLog2e : 0.f;
+                    }
 #pragma unroll
                     for (int o = 1; o < 32; o <<= 1) {
                         const float y = __shfl_up_sync(0xffffffffu, x, o);
@@ -487,11 +524,91 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                     }
                     if (lane == 31) sc[576 + (prow >> 5)] = x;
                 } else {
-                    bet[r] = (r < rows) ? p.beta[t] : 0.f;
+                    if (KC > 0) bet[r] = (r < rows) ? 1.f / (1.f + expf(-p.cv.b[t])) : 0.f;
+                    else bet[r] = (r < rows) ? p.beta[t] : 0.f;
                 }
                 group_sync(1, 128);
                 if (prow < 64) bsum[prow] = x + ((prow >= 32) ? sc[576] : 0.f);
                 group_sync(1, 128);
+            }
+            if constexpr (KC > 0) {
+                // (1b) block prologue on the raw Q and K tiles, in place: thread p takes the channel
+                //      pair 2(p % 64), 2(p % 64) + 1 of Q (p < 64) or K over the chunk's 64 rows, with
+                //      the KC - 1 inputs before each row in registers (the previous chunk's last rows,
+                //      or the carried convolution state before a sequence's first chunk)
+                bool okc = wait_bar(bar(UB_QK), 0, abort_flag, p.err);
+                if (okc) {
+                    const bool isq = prow < 64;
+                    const int dk = gm.dk, Cw = 2 * dk + gm.dv;
+                    const int c0 = 2 * (prow & 63);
+                    uint8_t *tile = sm + U_QK + (isq ? 8192 : 0) + (c0 >> 6) * 16384;
+                    const __nv_bfloat16 *xg = isq ? p.cv.xq : p.cv.xk;
+                    const float *wf = isq ? p.cv.wq : p.cv.wk;
+                    const int chan = (isq ? 0 : dk) + c0;   // channel in the [q | k | v] state axis
+                    float2 wt[KC];
+#pragma unroll
+                    for (int j = 0; j < KC; ++j)
+                        wt[j] = make_float2(wf[((int64_t)h * dk + c0) * KC + j], wf[((int64_t)h * dk + c0 + 1) * KC + j]);
+                    constexpr int KH = KC > 1 ? KC - 1 : 1;
+                    float2 hist[KH];   // hist[m]: the input KC-1-m rows before the current one
+#pragma unroll
+                    for (int m = 0; m < KC - 1; ++m) {
+                        if (c > 0)
+                            hist[m] = unpack_bf16(*reinterpret_cast<const uint32_t *>(
+                                xg + (tok0c - (KC - 1) + m) * H * dk + (int64_t)h * dk + c0));
+                        else if (p.cv.state_in)
+                            hist[m] = unpack_bf16(*reinterpret_cast<const uint32_t *>(
+                                p.cv.state_in + (((int64_t)n * (KC - 1) + m) * H + h) * Cw + chan));
+                        else
+                            hist[m] = make_float2(0.f, 0.f);
+                    }
+                    int64_t s0;
+                    int len;
+                    seq_span(gm, n, s0, len);
+                    const bool last = (int64_t)c * kChunk + rows == len;
+                    float2 snap[KH];   // the KC-1 inputs up to the chunk's last row (the carried state)
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        // the 32 raw rows first (their loads overlap), then filter and store in place
+                        uint32_t raw[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            raw[i] = *reinterpret_cast<const uint32_t *>(tile + sw128_offset(32 * half + i, c0 & 63));
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int tr = 32 * half + i;
+                            const float2 xt = unpack_bf16(raw[i]);
+                            float2 z = make_float2(wt[KC - 1].x * xt.x, wt[KC - 1].y * xt.y);
+#pragma unroll
+                            for (int j = 0; j < KC - 1; ++j) {
+                                z.x += wt[j].x * hist[j].x;
+                                z.y += wt[j].y * hist[j].y;
+                            }
+                            *reinterpret_cast<uint32_t *>(tile + sw128_offset(tr, c0 & 63)) =
+                                pack_bf16(conv_silu(z.x), conv_silu(z.y));
+#pragma unroll
+                            for (int m = 0; m + 1 < KC - 1; ++m) hist[m] = hist[m + 1];
+                            if (KC > 1) hist[KH - 1] = xt;
+                            if (tr == rows - 1)
+#pragma unroll
+                                for (int m = 0; m < KH; ++m) snap[m] = hist[m];
+                        }
+                    }
+                    if (last && p.cv.state_out)   // the sequence's last KC-1 inputs, oldest first
+#pragma unroll
+                        for (int m = 0; m < KC - 1; ++m)
+                            *reinterpret_cast<uint32_t *>(p.cv.state_out + (((int64_t)n * (KC - 1) + m) * H + h) * Cw + chan) =
+                                pack_bf16(snap[m].x, snap[m].y);
+                }
+                fence_proxy_async();
+                if (group_sync_or(2, 128, !okc || *abort_flag)) break;
+#pragma unroll
+                for (int k2 = 0; k2 < 8; ++k2) {   // the convolved Q tile (2 x 8 KB) for the recurrence
+                    const int u = prow + 128 * k2, q = u >> 9, o = (u & 511) * 16;
+                    *reinterpret_cast<uint4 *>(blk + PB_QC + q * 8192 + o) =
+                        *reinterpret_cast<const uint4 *>(sm + U_QK + 8192 + q * 16384 + o);
+                }
+                if (prow == 0) mbar_arrive(bar(UB_CONV));
             }
             // (2) inverse norms from the diagonal of the Gram product: thread p reads
             //     G_pp (= ||k_p||^2 or ||q_{p-64}||^2, fp32 sums of exact bf16 products)
@@ -776,13 +893,16 @@ ut_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
 struct RcParams {
     const float *init_state;
     const uint8_t *blocks;
+    size_t block_bytes;
     __nv_bfloat16 *out;
     float *final_state;
     unsigned *err;
     Geometry gm;
     long long *trace;
+    ConvParams cv;      // KC > 0: the raw V tile is convolved in place, Q comes convolved from the workspace
 };
 
+template <int KC>
 __global__ void __launch_bounds__(kThreadsRc, 1)
 recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmv, const RcParams p)
 {
@@ -818,29 +938,38 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
 
     if (warp == 0) {
         // ------------------------------------------------------------ loads
-        // lane 0: early ring (T', V, W~ | Q); lane 1: factor ring; lane 2: late ring (Aqk^T, K->)
-        if (lane < 3 && nch > 0) {
+        // lane 0: early ring half A (T', V); lane 3: half B (W~ | Q); lane 1: factor ring;
+        // lane 2: late ring (Aqk^T, K->)
+        if (lane < 4 && nch > 0) {
             if (lane == 0) { prefetch_tmap(&tmq); prefetch_tmap(&tmv); }
-            const int slots = lane == 0 ? kEarly : (lane == 1 ? kScSlots : kLate);
-            const int fbar = lane == 0 ? RB_EF : (lane == 1 ? RB_SCF : RB_LF);
-            const int ebar = lane == 0 ? RB_EE : (lane == 1 ? RB_SCE : RB_LE);
+            const int slots = (lane == 0 || lane == 3) ? kEarly : (lane == 1 ? kScSlots : kLate);
+            const int fbar = lane == 0 ? RB_EF : (lane == 1 ? RB_SCF : (lane == 2 ? RB_LF : RB_EFB));
+            const int ebar = lane == 0 ? RB_EE : (lane == 1 ? RB_SCE : (lane == 2 ? RB_LE : RB_EEB));
             int last = -1;
             for (int c = 0; c < nch; ++c) {
                 const int s = c % slots;
                 if (c >= slots && !wait_bar(bar(ebar + s), ((c / slots) - 1) & 1, abort_flag, p.err)) break;
                 const int z = (int)(tok0 + (int64_t)c * kChunk);
-                const uint8_t *blk = p.blocks + ((size_t)(slot0 + c) * H + h) * kPrepBlock;
+                const uint8_t *blk = p.blocks + ((size_t)(slot0 + c) * H + h) * p.block_bytes;
                 const uint32_t fb = bar(fbar + s);
                 if (lane == 0) {
                     const uint32_t base = sb + early(c);
-                    mbar_expect_tx(fb, kEarlyTx);
+                    mbar_expect_tx(fb, kEarlyTxA);
                     bulk_load(base + E_TP, blk + PB_TP, 16384, fb);                 // T'_hi, T'_lo
                     tma_load_3d(base + E_V, &tmv, j0, h, z, fb);
                     tma_load_3d(base + E_V + 8192, &tmv, j0 + 64, h, z, fb);
+                } else if (lane == 3) {
+                    const uint32_t base = sb + early(c);
+                    mbar_expect_tx(fb, kEarlyTxB);
                     bulk_load(base + E_WQ, blk + PB_W, 8192, fb);                 // W~ d 0-63   -> rows 0-63
-                    tma_load_3d(base + E_WQ + 8192, &tmq, 0, h, z, fb);           // Q  d 0-63   -> rows 64-127
                     bulk_load(base + E_WQ + 16384, blk + PB_W + 8192, 8192, fb);  // W~ d 64-127
-                    tma_load_3d(base + E_WQ + 24576, &tmq, 64, h, z, fb);         // Q  d 64-127
+                    if (KC > 0) {   // the convolved Q left by the chunk-local kernel
+                        bulk_load(base + E_WQ + 8192, blk + PB_QC, 8192, fb);
+                        bulk_load(base + E_WQ + 24576, blk + PB_QC + 8192, 8192, fb);
+                    } else {
+                        tma_load_3d(base + E_WQ + 8192, &tmq, 0, h, z, fb);       // Q  d 0-63   -> rows 64-127
+                        tma_load_3d(base + E_WQ + 24576, &tmq, 64, h, z, fb);     // Q  d 64-127
+                    }
                 } else if (lane == 1) {
                     mbar_expect_tx(fb, kScBytes);
                     bulk_load(sb + R_SCR + s * kScStride, blk + PB_SC, kScBytes, fb);
@@ -875,17 +1004,20 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             auto issue_a1 = [&](int c) -> bool {
                 const uint32_t eb = sb + early(c);
                 if (!wait_spin(bar(RB_EF + c % kEarly), (c / kEarly) & 1, abort_flag, p.err)) return false;
+                if (KC > 0 && !wait_spin(bar(RB_VC + c % kEarly), (c / kEarly) & 1, abort_flag, p.err)) return false;
                 fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)   // K-steps 0-3 against T'_hi, 4-7 against T'_lo
                     mma_ss(tb + tm_d1(c), smem_desc(eb + E_V + (ks & 3) * 2048, 8192, 1024),
                            smem_desc(eb + E_TP + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), id_a1, ks > 0);
+                commit(bar(RB_EE + c % kEarly));   // half A may be refilled once a1 has read it
                 return true;
             };
             auto issue_a2 = [&](int c) -> bool {
                 const uint32_t eb = sb + early(c);
                 if (!wait_spin(bar(RB_OFREE + (c & 1)), (c >> 1) & 1, abort_flag, p.err)) return false;
                 if (!wait_spin(bar(RB_S), c & 1, abort_flag, p.err)) return false;
+                if (!wait_spin(bar(RB_EFB + c % kEarly), (c / kEarly) & 1, abort_flag, p.err)) return false;
                 GDN_TR(p.trace, 1, c, 0);
                 fence_after_sync();
 #pragma unroll
@@ -893,7 +1025,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     mma_ss(tb + tm_d1(c), smem_desc(sb + R_SBF + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                            smem_desc(eb + E_WQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id_a2, 1);
                 commit(bar(RB_D1));
-                commit(bar(RB_EE + c % kEarly));
+                commit(bar(RB_EEB + c % kEarly));
                 GDN_TR(p.trace, 1, c, 4);
                 return true;
             };
@@ -1081,7 +1213,95 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             mbar_arrive(bar(RB_OFREE));
             mbar_arrive(bar(RB_OFREE + 1));
         }
-        for (int c = 0; c < nch; ++c) {
+        // With the block prologue fused in, these warps also turn each landed raw V tile into
+        // SiLU(short convolution) in place (bf16, exactly as the block prologue writes v), two
+        // chunks ahead of its a1 product.  Thread j takes the channel pair j0 + 2(j % 64),
+        // j0 + 2(j % 64) + 1 over rows 32(j / 64) .. 32(j / 64) + 31.
+        const int cpr = 2 * (j & 63), chalf = j >> 6;
+        const int Cw = 2 * gm.dk + dv, vchan = 2 * gm.dk + j0 + cpr;
+        constexpr int KH = KC > 1 ? KC - 1 : 1;
+        float2 wv[KC > 0 ? KC : 1];
+#pragma unroll
+        for (int jj = 0; jj < KC; ++jj)
+            wv[jj] = make_float2(p.cv.wv[((int64_t)h * dv + j0 + cpr) * KC + jj],
+                                 p.cv.wv[((int64_t)h * dv + j0 + cpr + 1) * KC + jj]);
+        // raw input of this thread's channel pair at token position pos of sequence n (the carried
+        // state before the sequence's first token)
+        auto raw_v = [&](int64_t pos) -> float2 {
+            if (pos >= tok0)
+                return unpack_bf16(*reinterpret_cast<const uint32_t *>(p.cv.xv + pos * H * dv + (int64_t)h * dv + j0 + cpr));
+            if (p.cv.state_in)
+                return unpack_bf16(*reinterpret_cast<const uint32_t *>(
+                    p.cv.state_in + (((int64_t)n * (KC - 1) + (KC - 1) + (pos - tok0)) * H + h) * Cw + vchan));
+            return make_float2(0.f, 0.f);
+        };
+        auto convert_v = [&](int cc) -> bool {
+          if constexpr (KC > 0) {
+            const int s = cc % kEarly;
+            bool okv = true;
+            if (leader) okv = wait_bar(bar(RB_EF + s), (cc / kEarly) & 1, abort_flag, p.err);
+            if (osync(!okv)) return false;
+            uint8_t *tile = sm + early(cc) + E_V + (cpr >> 6) * 8192;
+            float2 hist[KH];
+            uint32_t raw[32];
+#pragma unroll
+            for (int m = 0; m < KC - 1; ++m)   // the KC-1 inputs before the thread's first row
+                hist[m] = chalf ? unpack_bf16(*reinterpret_cast<const uint32_t *>(
+                                      tile + sw128_offset(32 - (KC - 1) + m, cpr & 63)))
+                                : raw_v(tok0 + (int64_t)cc * kChunk - (KC - 1) + m);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                raw[i] = *reinterpret_cast<const uint32_t *>(tile + sw128_offset(32 * chalf + i, cpr & 63));
+            if (osync(*abort_flag)) return false;   // every raw row is read before any is overwritten
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float2 xt = unpack_bf16(raw[i]);
+                float2 z = make_float2(wv[KC - 1].x * xt.x, wv[KC - 1].y * xt.y);
+#pragma unroll
+                for (int jj = 0; jj < KC - 1; ++jj) {
+                    z.x += wv[jj].x * hist[jj].x;
+                    z.y += wv[jj].y * hist[jj].y;
+                }
+                *reinterpret_cast<uint32_t *>(tile + sw128_offset(32 * chalf + i, cpr & 63)) =
+                    pack_bf16(conv_silu(z.x), conv_silu(z.y));
+#pragma unroll
+                for (int m = 0; m + 1 < KC - 1; ++m) hist[m] = hist[m + 1];
+                if (KC > 1) hist[KH - 1] = xt;
+            }
+            if (cc == nch - 1 && chalf == 0 && p.cv.state_out)   // the sequence's last KC-1 inputs
+#pragma unroll
+                for (int m = 0; m < KC - 1; ++m) {
+                    const float2 x = raw_v(tok0 + len - (KC - 1) + m);
+                    *reinterpret_cast<uint32_t *>(p.cv.state_out + (((int64_t)n * (KC - 1) + m) * H + h) * Cw + vchan) =
+                        pack_bf16(x.x, x.y);
+                }
+            fence_proxy_async();
+            if (osync(*abort_flag)) return false;
+            if (leader) mbar_arrive(bar(RB_VC + s));
+          }
+            return true;
+        };
+        bool nch_out_abort = false;
+        if constexpr (KC > 0) {
+            if (nch == 0 && p.cv.state_out) {
+                // an empty sequence carries its convolution state through unchanged (this CTA's v
+                // channels; the CTA of the first v slice also takes q and k)
+                const int64_t base = ((int64_t)n * (KC - 1) * H + h) * Cw;
+                for (int e = j; e < 64 + (j0 == 0 ? gm.dk : 0); e += 128) {   // channel pairs
+                    const int ch = e < 64 ? vchan - 2 * (j & 63) + 2 * e : 2 * (e - 64);
+#pragma unroll
+                    for (int m = 0; m < KC - 1; ++m) {
+                        const int64_t o = base + (int64_t)m * H * Cw + ch;
+                        *reinterpret_cast<uint32_t *>(p.cv.state_out + o) =
+                            p.cv.state_in ? *reinterpret_cast<const uint32_t *>(p.cv.state_in + o) : 0u;
+                    }
+                }
+            }
+            bool okc = true;
+            for (int cc = 0; cc < 2 && cc < nch && okc; ++cc) okc = convert_v(cc);
+            if (!okc) nch_out_abort = true;
+        }
+        for (int c = 0; c < nch && !nch_out_abort; ++c) {
             const float *fq = reinterpret_cast<const float *>(sm + R_SCR + (c % kScSlots) * kScStride);
             bool ok = true;
             if (leader) {
@@ -1126,6 +1346,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                 mbar_arrive(bar(RB_SCE + c % kScSlots));   // and the factor slot
             }
             if (leader) GDN_TR(p.trace, 0, c, 2);
+            if (KC > 0 && c + 2 < nch && !convert_v(c + 2)) break;
         }
     }
 
@@ -1209,17 +1430,35 @@ cudaError_t launch_wait_selftest(unsigned *err, uint64_t limit_ns, cudaStream_t 
     return cudaGetLastError();
 }
 
-size_t chunk_tc_workspace_bytes(int64_t slots, int H)
+size_t chunk_tc_workspace_bytes(int64_t slots, int H, bool fused)
 {
-    return kWsHeader + (size_t)slots * H * kPrepBlock;
+    return kWsHeader + (size_t)slots * H * (fused ? kPrepBlockFused : kPrepBlock);
 }
+
+namespace {
+
+template <int KC>
+cudaError_t launch_pair(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const UtParams &up,
+                        const RcParams &rp, const Geometry &gm, int64_t slots, cudaStream_t st)
+{
+    cudaError_t e = cudaFuncSetAttribute(ut_tc_kernel<KC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemUt);
+    if (e != cudaSuccess) return e;
+    ut_tc_kernel<KC><<<dim3((unsigned)slots, gm.H), kThreadsUt, kSmemUt, st>>>(tq, tk, up);
+    e = cudaFuncSetAttribute(recur_tc_kernel<KC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemRc);
+    if (e != cudaSuccess) return e;
+    recur_tc_kernel<KC><<<dim3(gm.N, gm.H, gm.dv / 128), kThreadsRc, kSmemRc, st>>>(tq, tv, rp);
+    return cudaGetLastError();
+}
+
+}  // namespace
 
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st)
 {
     const int64_t rows = (int64_t)a.gm.B * a.gm.T;
+    const PrologueArgs *f = a.fuse;
     CUtensorMap tq, tk, tv;
-    if (!make_tmap(&tq, a.q, a.gm.dk, a.gm.H, rows) || !make_tmap(&tk, a.k, a.gm.dk, a.gm.H, rows) ||
-        !make_tmap(&tv, a.v, a.gm.dv, a.gm.H, rows))
+    if (!make_tmap(&tq, f ? f->xq : a.q, a.gm.dk, a.gm.H, rows) || !make_tmap(&tk, f ? f->xk : a.k, a.gm.dk, a.gm.H, rows) ||
+        !make_tmap(&tv, f ? f->xv : a.v, a.gm.dv, a.gm.H, rows))
         return cudaErrorInvalidValue;
     long long *trace = nullptr;
 #ifdef GDN_KERNEL_TRACE
@@ -1227,21 +1466,33 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st)
 #endif
     uint8_t *blocks = reinterpret_cast<uint8_t *>(a.workspace) + kWsHeader;
     unsigned *err = reinterpret_cast<unsigned *>(a.workspace);
+    ConvParams cv{};
+    if (f) {
+        cv.xq = reinterpret_cast<const __nv_bfloat16 *>(f->xq);
+        cv.xk = reinterpret_cast<const __nv_bfloat16 *>(f->xk);
+        cv.xv = reinterpret_cast<const __nv_bfloat16 *>(f->xv);
+        cv.wq = f->wq; cv.wk = f->wk; cv.wv = f->wv;
+        cv.a = f->a; cv.b = f->b; cv.A_log = f->A_log; cv.dt_bias = f->dt_bias;
+        cv.state_in = reinterpret_cast<const __nv_bfloat16 *>(f->state_in);
+        cv.state_out = reinterpret_cast<__nv_bfloat16 *>(f->state_out);
+    }
+    const size_t block_bytes = f ? kPrepBlockFused : kPrepBlock;
 
     UtParams up;
-    up.g = a.g; up.beta = a.beta; up.blocks = blocks; up.err = err; up.gm = a.gm;
-    up.scale = a.scale; up.l2 = a.l2; up.trace = trace;
-    cudaError_t e = cudaFuncSetAttribute(ut_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemUt);
-    if (e != cudaSuccess) return e;
-    ut_tc_kernel<<<dim3((unsigned)a.slots, a.gm.H), kThreadsUt, kSmemUt, st>>>(tq, tk, up);
-
+    up.g = a.g; up.beta = a.beta; up.blocks = blocks; up.block_bytes = block_bytes; up.err = err; up.gm = a.gm;
+    up.scale = a.scale; up.l2 = a.l2; up.trace = trace; up.cv = cv;
     RcParams rp;
-    rp.init_state = a.init_state; rp.blocks = blocks; rp.out = reinterpret_cast<__nv_bfloat16 *>(a.out);
-    rp.final_state = a.final_state; rp.err = err; rp.gm = a.gm; rp.trace = trace;
-    e = cudaFuncSetAttribute(recur_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemRc);
-    if (e != cudaSuccess) return e;
-    recur_tc_kernel<<<dim3(a.gm.N, a.gm.H, a.gm.dv / 128), kThreadsRc, kSmemRc, st>>>(tq, tv, rp);
-    return cudaGetLastError();
+    rp.init_state = a.init_state; rp.blocks = blocks; rp.block_bytes = block_bytes;
+    rp.out = reinterpret_cast<__nv_bfloat16 *>(a.out);
+    rp.final_state = a.final_state; rp.err = err; rp.gm = a.gm; rp.trace = trace; rp.cv = cv;
+    switch (f ? f->K : 0) {
+        case 0: return launch_pair<0>(tq, tk, tv, up, rp, a.gm, a.slots, st);
+        case 1: return launch_pair<1>(tq, tk, tv, up, rp, a.gm, a.slots, st);
+        case 2: return launch_pair<2>(tq, tk, tv, up, rp, a.gm, a.slots, st);
+        case 3: return launch_pair<3>(tq, tk, tv, up, rp, a.gm, a.slots, st);
+        case 4: return launch_pair<4>(tq, tk, tv, up, rp, a.gm, a.slots, st);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace gdn

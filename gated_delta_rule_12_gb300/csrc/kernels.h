@@ -9,6 +9,8 @@
 
 namespace gdn {
 
+struct PrologueArgs;
+
 struct ChunkArgs {
     const void *q, *k, *v;
     const float *g, *beta, *init_state;
@@ -20,6 +22,7 @@ struct ChunkArgs {
     float scale;
     int l2;
     void *workspace;
+    const PrologueArgs *fuse = nullptr;   // non-null: q, k, v, g, beta are made from these projections
 };
 
 struct DecodeArgs {
@@ -63,7 +66,7 @@ cudaError_t launch_chunk_bwd(const BwdArgs &a, cudaStream_t st);
 size_t chunk_bwd_workspace_bytes(int64_t slots, int H, int dk, int dv);
 cudaError_t launch_prologue(const PrologueArgs &a, cudaStream_t st);
 bool chunk_tc_supported(int dt, int dk, int dv, int64_t tokens);
-size_t chunk_tc_workspace_bytes(int64_t slots, int H);
+size_t chunk_tc_workspace_bytes(int64_t slots, int H, bool fused = false);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
 // one CTA whose bounded wait on a never-completed mbarrier phase gives up after limit_ns

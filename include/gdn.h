@@ -265,6 +265,42 @@ gdn_status gdn_prologue(const void *xq, const void *xk, const void *xv,
                         gdn_dtype dt, void *stream);
 
 /*
+ * Block prologue and chunked forward in one call: the output and final state
+ * of gdn_chunk_fwd on the q, k, v, g, beta that gdn_prologue would make from
+ * these projections, without q, k, v, g or beta ever being written to memory.
+ * "Gated Delta Networks: Improving Mamba2 with Delta Rule", §3.4 "Token mixing
+ * block" and Fig. 1 (short convolution + SiLU, gate activations) feeding §3.3
+ * (the chunkwise form).  The short convolution and SiLU run on each chunk's
+ * q and k tiles inside the chunk-local kernel and on its v tile inside the
+ * recurrence; the gates are activated as they are read.  The result is bit
+ * for bit that of gdn_prologue followed by gdn_chunk_fwd (same roundings).
+ *   xq, xk, xv, wq, wk, wv, a, b, A_log, dt_bias, conv_state_in,
+ *   conv_state_out, K           as gdn_prologue (conv_state_out receives the
+ *                               K-1 most recent projection inputs of each
+ *                               sequence; NULL to skip).
+ *   init_state, cu_seqlens, num_seqs, out, final_state, B, T, H, scale,
+ *   use_qk_l2norm, chunk_size   as gdn_chunk_fwd.
+ *   dt            GDN_BF16 only; dk = 128, dv a multiple of 128 (the tensor-core
+ *                 path); other sizes return GDN_ERR_UNSUPPORTED.
+ *   workspace     at least gdn_prologue_chunk_fwd_workspace_size() bytes,
+ *                 256-byte aligned (as gdn_chunk_fwd's, plus the convolved q
+ *                 of each chunk, 16 KB per chunk and head).
+ * Errors: GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA.
+ */
+size_t gdn_prologue_chunk_fwd_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv,
+                                             int32_t num_seqs, gdn_dtype dt);
+
+gdn_status gdn_prologue_chunk_fwd(const void *xq, const void *xk, const void *xv,
+                                  const float *wq, const float *wk, const float *wv,
+                                  const float *a, const float *b, const float *A_log, const float *dt_bias,
+                                  const void *conv_state_in, void *conv_state_out,
+                                  const float *init_state, const int32_t *cu_seqlens, int32_t num_seqs,
+                                  void *out, float *final_state,
+                                  int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, int32_t K,
+                                  gdn_dtype dt, float scale, int32_t use_qk_l2norm, int32_t chunk_size,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * gdn_chunk_fwd_noalloc -- gdn_chunk_fwd for callers that cannot allocate.
  * The pages have no counterpart of this call: it exists for callers that may
  * not call cudaMalloc or any allocating routine where they run the operator
