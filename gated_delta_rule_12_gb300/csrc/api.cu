@@ -18,7 +18,13 @@ namespace {
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 bool aligned_to(const void *p, unsigned a) { return ((uintptr_t)p & (uintptr_t)(a - 1)) == 0; }
 
-bool chunk_dims_supported(int dk, int dv) { return (dk == 64 || dk == 128) && dv >= 32 && dv <= 256 && dv % 32 == 0; }
+bool chunk_dims_supported(int dk, int dv)
+{
+    return (dk == 64 || dk == 128 || dk == 256) && dv >= 32 && dv <= 256 && dv % 32 == 0;
+}
+
+// the backward kernels are built and tested for dk in {64, 128}
+bool bwd_dims_supported(int dk, int dv) { return (dk == 64 || dk == 128) && dv >= 32 && dv <= 256 && dv % 32 == 0; }
 
 }  // namespace
 
@@ -112,7 +118,7 @@ size_t gdn_chunk_bwd_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk,
 {
     if (B < 1 || T < 0 || H < 1 || num_seqs < 0) return 0;
     if (dt != GDN_F32 && dt != GDN_BF16) return 0;
-    if (!chunk_dims_supported(dk, dv)) return 0;
+    if (!bwd_dims_supported(dk, dv)) return 0;
     const bool varlen = num_seqs > 0;
     if (varlen && B != 1) return 0;
     return chunk_bwd_workspace_bytes(num_slots(B, T, varlen ? num_seqs : B, varlen), H, dk, dv);
@@ -129,7 +135,7 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, const void *v, const floa
     if (B < 1 || T < 0 || H < 1 || dk < 1 || dv < 1) return GDN_ERR_INVALID_ARG;
     if (dt != GDN_F32 && dt != GDN_BF16) return GDN_ERR_INVALID_ARG;
     if (chunk_size != kChunk) return GDN_ERR_UNSUPPORTED;
-    if (!chunk_dims_supported(dk, dv)) return GDN_ERR_UNSUPPORTED;
+    if (!bwd_dims_supported(dk, dv)) return GDN_ERR_UNSUPPORTED;
     const bool varlen = cu_seqlens != nullptr;
     if (varlen && (B != 1 || num_seqs < 1)) return GDN_ERR_INVALID_ARG;
     if (!varlen && num_seqs != 0 && num_seqs != B) return GDN_ERR_INVALID_ARG;

@@ -168,12 +168,17 @@ ut_simt_kernel(const T *__restrict__ k, const T *__restrict__ v, const float *__
 // ---------------------------------------------------------------------------
 constexpr int kRowsSimt = 32;
 
+// At DK = 256 the three 64 x DK tiles would not fit in shared memory together: W<- is then read
+// from the workspace directly (each value is a broadcast to the 32 threads of a warp).
+template <int DK>
+constexpr bool ws_in_smem() { return DK <= 128; }
+
 template <int DK>
 __host__ __device__ constexpr size_t recur_simt_smem_floats()
 {
     return (size_t)kChunk * DK           /* Qs  */
          + (size_t)kChunk * (DK + 1)     /* Ks  */
-         + (size_t)kChunk * DK           /* Ws  */
+         + (ws_in_smem<DK>() ? (size_t)kChunk * DK : 0)   /* Ws  */
          + (size_t)kChunk * kRowsSimt    /* Us  */
          + (size_t)kRowsSimt * (DK + 1)  /* Ss  */
          + (size_t)kChunk * kRowsSimt    /* Vn  */
@@ -196,7 +201,7 @@ recur_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
     float *Qs = smem;
     float *Ks = Qs + kChunk * DK;
     float *Ws = Ks + kChunk * (DK + 1);
-    float *Us = Ws + kChunk * DK;
+    float *Us = Ws + (ws_in_smem<DK>() ? kChunk * DK : 0);
     float *Ss = Us + kChunk * kRowsSimt;
     float *Vn = Ss + kRowsSimt * (DK + 1);
     float *Aqk = Vn + kChunk * kRowsSimt;
@@ -240,7 +245,7 @@ recur_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
             }
             Qs[r * DK + d] = xq;
             Ks[r * (DK + 1) + d] = xk;
-            Ws[r * DK + d] = Wg[base * DK + (size_t)r * DK + d];
+            if (ws_in_smem<DK>()) Ws[r * DK + d] = Wg[base * DK + (size_t)r * DK + d];
         }
         for (int e = tid; e < kChunk * kRowsSimt; e += blockDim.x) {
             const int r = e / kRowsSimt, j = e % kRowsSimt;
@@ -252,9 +257,10 @@ recur_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
         {
             const int j = tid & 31;
             for (int r = tid >> 5; r < kChunk; r += 8) {
+                const float *wr = ws_in_smem<DK>() ? Ws + r * DK : Wg + base * DK + (size_t)r * DK;
                 float acc = 0.f;
 #pragma unroll 8
-                for (int d = 0; d < DK; ++d) acc += Ws[r * DK + d] * Ss[j * (DK + 1) + d];
+                for (int d = 0; d < DK; ++d) acc += (ws_in_smem<DK>() ? wr[d] : __ldg(wr + d)) * Ss[j * (DK + 1) + d];
                 Vn[r * kRowsSimt + j] = Us[r * kRowsSimt + j] - acc;
             }
         }
@@ -337,9 +343,11 @@ cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t st)
 {
     if (a.dt == 0) {
         if (a.gm.dk == 64) return launch_simt_typed<float, 64>(a, st);
+        if (a.gm.dk == 256) return launch_simt_typed<float, 256>(a, st);
         return launch_simt_typed<float, 128>(a, st);
     }
     if (a.gm.dk == 64) return launch_simt_typed<__nv_bfloat16, 64>(a, st);
+    if (a.gm.dk == 256) return launch_simt_typed<__nv_bfloat16, 256>(a, st);
     return launch_simt_typed<__nv_bfloat16, 128>(a, st);
 }
 

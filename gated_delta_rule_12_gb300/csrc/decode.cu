@@ -164,6 +164,142 @@ decode_kernel(float *__restrict__ state, const T *__restrict__ q, const T *__res
     }
 }
 
+// Several tokens per call with the per-token work that does not depend on the state -- loading
+// and normalising k and q, k . q, alpha and beta -- done once per token for a run of GPW row
+// groups of one (sequence, head), instead of once per group.  Each group then runs exactly the
+// arithmetic of decode_kernel (same operations in the same order), so the results are bit for
+// bit those of NT single steps.  NT <= 4 tokens, DK <= 128 (the token vectors stay in registers).
+template <typename T, int DK, int NT, int GPW>
+__global__ void __launch_bounds__(256, 3)
+decode_multi_kernel(float *__restrict__ state, const T *__restrict__ q, const T *__restrict__ k,
+                    const T *__restrict__ v, const float *__restrict__ g, const float *__restrict__ beta,
+                    T *__restrict__ out, int NH, int H, int dv, float scale, int l2)
+{
+    constexpr int R = 8;           // rows of S per group
+    constexpr int VEC = DK / 32;   // entries of a row per lane
+    // the run's normalised keys and queries, each lane's own VEC entries (shared memory keeps them
+    // out of the registers that hold the state rows)
+    __shared__ __align__(16) float tkq[8][NT][2][DK];
+    __shared__ float tsc[8][NT][4];   // per token: k . q, alpha, beta
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int myrow = lane >> 2;
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int groups_per_head = dv / R;
+    const int runs_per_head = (groups_per_head + GPW - 1) / GPW;
+    const int64_t total = (int64_t)NH * runs_per_head;
+
+    for (int64_t run = warp0; run < total; run += nwarps) {
+        const int64_t nh = run / runs_per_head;
+        const int g0 = (int)(run % runs_per_head) * GPW;
+        const int64_t n = nh / H, h = nh % H;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const int64_t tok = (n * NT + t) * H + h;
+            float kv[VEC], qv[VEC];
+            float sk = 0.f, sq = 0.f;
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) {
+                kv[i] = to_f32(k[tok * DK + lane * VEC + i]);
+                qv[i] = to_f32(q[tok * DK + lane * VEC + i]);
+                sk += kv[i] * kv[i];
+                sq += qv[i] * qv[i];
+            }
+            const float alpha_t = expf(g[tok]);
+            const float beta_t = beta[tok];
+            float rk = 1.f, rq = scale;
+            if (l2) {
+                sk = warp_sum(sk);
+                sq = warp_sum(sq);
+                rk = 1.f / sqrtf(sk + kL2Eps);
+                rq = scale / sqrtf(sq + kL2Eps);
+            }
+            float kqt = 0.f;
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) {
+                kv[i] *= rk;
+                qv[i] *= rq;
+                kqt += kv[i] * qv[i];
+                tkq[wib][t][0][lane * VEC + i] = kv[i];
+                tkq[wib][t][1][lane * VEC + i] = qv[i];
+            }
+            kqt = warp_sum(kqt);
+            if (lane == 0) {
+                tsc[wib][t][0] = kqt;
+                tsc[wib][t][1] = alpha_t;
+                tsc[wib][t][2] = beta_t;
+            }
+        }
+        __syncwarp();
+#pragma unroll 1
+        for (int gi = g0; gi < g0 + GPW && gi < groups_per_head; ++gi) {
+            const int j0 = gi * R;
+            float *S = state + ((size_t)nh * dv + j0) * DK + lane * VEC;
+            float s[R][VEC];
+#pragma unroll
+            for (int r = 0; r < R; ++r) load_row<VEC>(S + (size_t)r * DK, s[r]);
+#pragma unroll 1
+            for (int t = 0; t < NT; ++t) {
+                const int64_t tok = (n * NT + t) * H + h;
+                const float vj = to_f32(v[tok * dv + j0 + myrow]);
+                const float kqt = tsc[wib][t][0], alpha_t = tsc[wib][t][1], beta_t = tsc[wib][t][2];
+                float kv[VEC], qv[VEC];
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) {
+                    kv[i] = tkq[wib][t][0][lane * VEC + i];
+                    qv[i] = tkq[wib][t][1][lane * VEC + i];
+                }
+                float pk[R], pq[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    pk[r] = 0.f;
+                    pq[r] = 0.f;
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) {
+                        pk[r] += s[r][i] * kv[i];
+                        pq[r] += s[r][i] * qv[i];
+                    }
+                }
+                const float pkm = warp_sum8_transposed(pk, lane);
+                const float pqm = warp_sum8_transposed(pq, lane);
+                const float em = beta_t * (vj - alpha_t * pkm);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float e = __shfl_sync(0xffffffffu, em, 4 * r);
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) s[r][i] = alpha_t * s[r][i] + e * kv[i];
+                }
+                if ((lane & 3) == 0) out[tok * dv + j0 + myrow] = from_f32<T>(alpha_t * pqm + em * kqt);
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) store_row<VEC>(S + (size_t)r * DK, s[r]);
+        }
+        __syncwarp();   // the buffer is rewritten by the next run's tokens
+    }
+}
+
+template <typename T, int DK, int NT>
+static cudaError_t launch_decode_multi_kernel(const DecodeArgs &a, cudaStream_t st)
+{
+    constexpr int GPW = 4;   // row groups per warp run (32 rows)
+    const int NH = a.N * a.H;
+    const int64_t runs = (int64_t)NH * ((a.dv / 8 + GPW - 1) / GPW);
+    int dev = 0, sms = 152;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_multi_kernel<T, DK, NT, GPW>, 256, 0);
+    if (per_sm < 1) per_sm = 1;
+    int64_t blocks = (runs + 7) / 8;
+    const int64_t cap = (int64_t)sms * per_sm;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    decode_multi_kernel<T, DK, NT, GPW><<<(unsigned)blocks, 256, 0, st>>>(
+        a.state, (const T *)a.q, (const T *)a.k, (const T *)a.v, a.g, a.beta, (T *)a.out, NH, a.H, a.dv,
+        a.scale, a.l2);
+    return cudaGetLastError();
+}
+
 template <typename T, int DK, bool MULTI>
 static cudaError_t launch_decode_kernel(const DecodeArgs &a, cudaStream_t st)
 {
@@ -188,6 +324,14 @@ static cudaError_t launch_decode_kernel(const DecodeArgs &a, cudaStream_t st)
 template <typename T, int DK>
 static cudaError_t launch_decode_typed(const DecodeArgs &a, cudaStream_t st)
 {
+    if constexpr (DK <= 128) {
+        switch (a.ntok) {
+            case 2: return launch_decode_multi_kernel<T, DK, 2>(a, st);
+            case 3: return launch_decode_multi_kernel<T, DK, 3>(a, st);
+            case 4: return launch_decode_multi_kernel<T, DK, 4>(a, st);
+            default: break;
+        }
+    }
     return a.ntok > 1 ? launch_decode_kernel<T, DK, true>(a, st) : launch_decode_kernel<T, DK, false>(a, st);
 }
 

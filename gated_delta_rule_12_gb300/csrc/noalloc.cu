@@ -86,7 +86,7 @@ extern "C" gdn_status gdn_chunk_fwd_noalloc(const void *q, const void *k, const 
     if (B < 1 || T < 0 || H < 1 || dk < 1 || dv < 1) return GDN_ERR_INVALID_ARG;
     if (dt != GDN_F32 && dt != GDN_BF16) return GDN_ERR_INVALID_ARG;
     if (chunk_size != kChunk) return GDN_ERR_UNSUPPORTED;
-    if (!((dk == 64 || dk == 128) && dv >= 32 && dv <= 256 && dv % 32 == 0)) return GDN_ERR_UNSUPPORTED;
+    if (!((dk == 64 || dk == 128 || dk == 256) && dv >= 32 && dv <= 256 && dv % 32 == 0)) return GDN_ERR_UNSUPPORTED;
     const bool varlen = cu_seqlens != nullptr;
     if (varlen && (B != 1 || num_seqs < 1)) return GDN_ERR_INVALID_ARG;
     if (!varlen && num_seqs != 0 && num_seqs != B) return GDN_ERR_INVALID_ARG;

@@ -102,8 +102,10 @@ int32_t gdn_chunk_fwd_kernel_count(int32_t B, int32_t T, int32_t H, int32_t dk, 
  *   out           [B, T, H, dv] dtype dt, written for every token.
  *   final_state   [N, H, dv, dk] fp32, or NULL to skip; may alias init_state.
  *   B, T, H       batch, tokens per row, heads (T >= 0, B, H >= 1).
- *   dk, dv        head dims: dk in {64, 128}; dv a multiple of 32 up to 256
- *                 (others return GDN_ERR_UNSUPPORTED).
+ *   dk, dv        head dims: dk in {64, 128, 256}; dv a multiple of 32 up to 256
+ *                 (others return GDN_ERR_UNSUPPORTED).  bf16 with dk = 128 and dv
+ *                 a multiple of 128 runs on the tensor cores, every other size on
+ *                 the CUDA cores.
  *   dt            GDN_F32 or GDN_BF16 (q, k, v and out); arithmetic is fp32.
  *   scale         multiplier of q (commonly 1/sqrt(dk)).
  *   chunk_size    must be 64.
@@ -154,7 +156,7 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
  *   workspace     at least gdn_chunk_bwd_workspace_size() bytes, 256-byte aligned
  *                 (fp32 intermediates, about 0.35 MB per chunk and head at
  *                 dk = dv = 128).
- * The kernels are fp32 on the CUDA cores.
+ * The kernels are fp32 on the CUDA cores; dk in {64, 128}, dv as gdn_chunk_fwd.
  * Errors: GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA.
  */
 size_t gdn_chunk_bwd_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv,

@@ -48,7 +48,7 @@ def test_headline_small_fp32_case_exact_config():
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 256), (128, 32)])
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 256), (128, 32), (256, 128), (256, 64)])
 def test_prefill_ragged_with_initial_state(dtype, dk, dv):
     d = inputs.make_prefill(B=2, L=200, H=3, dk=dk, dv=dv, dtype=dtype, seed=11, decay=0.3, init_state=True)
     out, sf, ro, rs = run_both(d, dk)
@@ -76,6 +76,32 @@ def test_varlen_boundaries(dtype):
     assert_close(sf, rs, dtype, "final_state")
     # a length-0 sequence keeps its initial state
     np.testing.assert_allclose(sf[4].cpu().numpy(), d["init_state"][4].numpy(), atol=0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_dk256_varlen_and_agreement_with_decode(dtype):
+    """dk = 256 on the chunked forward (CUDA-core path): varlen with empty and 1-token sequences against
+    the oracle, and the same tokens through the multi-token decode (which takes dk = 256 too) give the
+    same outputs and final states."""
+    lens = [1, 0, 70, 129]
+    d = inputs.make_prefill(B=1, L=sum(lens), H=2, dk=256, dv=64, dtype=dtype, seed=57, decay=0.3,
+                            init_state=True, num_seqs=len(lens), lengths=lens)
+    out, sf, ro, rs = run_both(d, 256)
+    assert_close(out, ro, dtype, "out")
+    assert_close(sf, rs, dtype, "final_state")
+    # equal-length batch through the decode path: 3 sequences of 20 tokens
+    e = inputs.make_prefill(B=3, L=20, H=2, dk=256, dv=64, dtype=dtype, seed=58, decay=0.3, init_state=True)
+    ee = cuda(e)
+    o_c, s_c = gdn.chunk_fwd(ee["q"], ee["k"], ee["v"], ee["g"], ee["beta"], init_state=ee["init_state"])
+    st = ee["init_state"].clone()
+    o_d = gdn.decode_multi(st, ee["q"], ee["k"], ee["v"], ee["g"], ee["beta"])
+    torch.cuda.synchronize()
+    ro2, rs2 = oracle.recurrent_fwd(e["q"], e["k"], e["v"], e["g"], e["beta"], init_state=e["init_state"],
+                                    scale=256 ** -0.5, use_qk_l2norm=True)
+    assert_close(o_c, ro2, dtype, "chunked out")
+    assert_close(o_d, ro2, dtype, "decode out")
+    assert_close(s_c, rs2, dtype, "chunked state")
+    assert_close(st, rs2, dtype, "decode state")
 
 
 def test_heavy_decay_no_overflow():
