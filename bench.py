@@ -453,6 +453,34 @@ def bench_ours(args):
     dbytes = decode_algorithmic_bytes(wd)
     d_ach = dbytes / (dms * 1e-3) / 1e9
 
+    # The same steps over two state sets in turn (two batches of the workload served alternately):
+    # a step never reads the state the step before it wrote, so none of it can still sit in the
+    # 129 MB L2 and every state byte of the roofline comes from DRAM.
+    state2 = [dd["state0"].clone(), dd["state0"].clone()]
+
+    def decode_alt():
+        for t in range(wd.steps):
+            gdn.decode_step(state2[t % 2], dd["q"][t], dd["k"][t], dd["v"][t], dd["g"][t], dd["beta"][t],
+                            scale=wd.scale, use_qk_l2norm=True, out=dout)
+
+    decode_alt()
+    torch.cuda.synchronize()
+    agraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(agraph):
+        decode_alt()
+    agraph.replay()
+    torch.cuda.synchronize()
+    a_ms = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        agraph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        a_ms.append(a.elapsed_time(b) / wd.steps)
+    dms_cold = max_over_ranks(dist, statistics.median(a_ms))
+    del state2, agraph
+
     # several tokens per call: the same 64 tokens as MULTI_T tokens x (64 / MULTI_T) calls,
     # the state read and written once per call
     tmaj = lambda x: x.transpose(0, 1).contiguous()          # [steps, N, ...] -> [N, steps, ...]
@@ -486,6 +514,32 @@ def bench_ours(args):
     mms = max_over_ranks(dist, statistics.median(m_ms))
     mbytes = decode_multi_algorithmic_bytes(wd, MULTI_T)
     m_ach = mbytes / (mms * 1e-3) / 1e9
+
+    # the same calls over two state sets in turn (see decode_alt)
+    mstate2 = [dd["state0"].clone(), dd["state0"].clone()]
+
+    def decode_multi_alt():
+        for c in range(calls):
+            x = msl[c]
+            gdn.decode_multi(mstate2[c % 2], x["q"], x["k"], x["v"], x["g"], x["beta"], scale=wd.scale, out=mout)
+
+    decode_multi_alt()
+    torch.cuda.synchronize()
+    magraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(magraph):
+        decode_multi_alt()
+    magraph.replay()
+    torch.cuda.synchronize()
+    ma_ms = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        magraph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ma_ms.append(a.elapsed_time(b) / calls)
+    mms_cold = max_over_ranks(dist, statistics.median(ma_ms))
+    del mstate2, magraph
 
     # backward of the chunked forward on the bench shape
     bwd = bench_backward(w, d, dev, flush, stream, reps, peaks)
@@ -529,13 +583,19 @@ def bench_ours(args):
                        "roofline": {"bound": "hbm", "achieved": d_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                     "frac": d_ach / peaks["hbm_gbs"], "traffic": traffic_record("decode"),
                                     "algorithmic_bytes": dbytes},
-                       "timing": f"{wd.steps} steps in one CUDA graph, median of {reps}"},
+                       "timing": f"{wd.steps} steps in one CUDA graph, median of {reps}",
+                       "l2_cold": {"ms_per_step": dms_cold, "frac": dbytes / (dms_cold * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                   "how": "the same steps over two state sets in turn, so no step reads a state "
+                                          "still in L2 from the step before"}},
             "decode_multi": {"workload": DECODE, "tokens_per_call": MULTI_T,
                              "value": job_throughput(wd.num_seqs * MULTI_T, ws_n, mms), "unit": "tokens/s",
                              "ms_per_call": mms,
                              "roofline": {"bound": "hbm", "achieved": m_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                           "frac": m_ach / peaks["hbm_gbs"], "algorithmic_bytes": mbytes},
-                             "timing": f"{wd.steps} tokens as {calls} calls in one CUDA graph, median of {reps}"},
+                             "timing": f"{wd.steps} tokens as {calls} calls in one CUDA graph, median of {reps}",
+                             "l2_cold": {"ms_per_call": mms_cold,
+                                         "frac": mbytes / (mms_cold * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                         "how": "the same calls over two state sets in turn"}},
             "prologue": pro,
             "prologue_chunk_fwd": fused,
             "backward": bwd,
