@@ -277,3 +277,43 @@ def test_fp16_operand_range_is_reported():
     ro, rs = oracle.recurrent_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=128 ** -0.5, use_qk_l2norm=True)
     assert_close(out, ro, "bf16", "out after the range error")
     assert_close(sf, rs, "bf16", "final_state after the range error")
+
+
+@pytest.mark.parametrize("dtype,dk", [("bf16", 128), ("f32", 64)])
+def test_degenerate_gates_and_vectors(dtype, dk):
+    """The degenerate cases of eq. 10 ("Gated Delta Networks", §3.1), on the tensor-core path (bf16,
+    dk = 128) and the CUDA-core path (fp32, dk = 64):
+      * beta = 0 everywhere: nothing is written, the state only decays, so
+        o_t = (prod_{s<=t} alpha_s) S_0 q^_t and the final state is (prod alpha) S_0 (closed form);
+      * g = 0 everywhere (alpha = 1): the plain delta rule over several chunks;
+      * zero keys and zero queries at some tokens: a zero key writes and erases nothing, a zero
+        query reads exactly 0."""
+    # beta = 0: the closed form, independently of the oracle
+    d = inputs.make_prefill(B=2, L=150, H=2, dk=dk, dv=dk, dtype=dtype, seed=81, decay=0.05, init_state=True)
+    d["beta"] = torch.zeros_like(d["beta"])
+    out, sf, ro, rs = run_both(d, dk)
+    assert_close(out, ro, dtype, "beta=0 out")
+    assert_close(sf, rs, dtype, "beta=0 final_state")
+    g = d["g"].double().numpy()                                    # [B, T, H]
+    q = d["q"].double().numpy()
+    qh = q / np.sqrt((q * q).sum(-1, keepdims=True) + 1e-6) * dk ** -0.5
+    S0 = d["init_state"].double().numpy()                          # [B, H, dv, dk]
+    decay = np.exp(np.cumsum(g, axis=1))                           # prod_{s<=t} alpha_s
+    closed = np.einsum("bth,bhvk,bthk->bthv", decay, S0, qh)
+    assert_close(out, closed, dtype, "beta=0 out vs closed form")
+    assert_close(sf, S0 * decay[:, -1][..., None, None], dtype, "beta=0 final_state vs closed form")
+    # alpha = 1
+    d = inputs.make_prefill(B=1, L=320, H=2, dk=dk, dv=dk, dtype=dtype, seed=82, init_state=True)
+    d["g"] = torch.zeros_like(d["g"])
+    out, sf, ro, rs = run_both(d, dk)
+    assert_close(out, ro, dtype, "g=0 out")
+    assert_close(sf, rs, dtype, "g=0 final_state")
+    # zero keys and queries
+    d = inputs.make_prefill(B=2, L=200, H=2, dk=dk, dv=dk, dtype=dtype, seed=83, decay=0.2, init_state=True)
+    zk, zq = [3, 64, 65, 127, 199], [0, 5, 63, 64, 130]
+    d["k"][:, zk] = 0
+    d["q"][:, zq] = 0
+    out, sf, ro, rs = run_both(d, dk)
+    assert_close(out, ro, dtype, "zero k/q out")
+    assert_close(sf, rs, dtype, "zero k/q final_state")
+    assert (out[:, zq].float() == 0).all(), "a zero query must read exactly 0"
