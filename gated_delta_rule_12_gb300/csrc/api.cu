@@ -24,7 +24,7 @@ bool chunk_dims_supported(int dk, int dv)
 }
 
 // the backward kernels are built and tested for dk in {64, 128}
-bool bwd_dims_supported(int dk, int dv) { return (dk == 64 || dk == 128) && dv >= 32 && dv <= 256 && dv % 32 == 0; }
+bool bwd_dims_supported(int dk, int dv) { return (dk == 64 || dk == 128 || dk == 256) && dv >= 32 && dv <= 256 && dv % 32 == 0; }
 
 }  // namespace
 

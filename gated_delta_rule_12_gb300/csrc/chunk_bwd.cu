@@ -440,7 +440,7 @@ bwd_fwd_scan_kernel(const BwdParams p)
                                      }, sA, sB);
         __syncthreads();
         const float gC = expf(b[63]);
-        block_gemm<2, 8, false, false>(kScanRows, dk, 64, [&](int i, int r) { return vn[r * dv + j0 + i]; },
+        block_gemm_cols<2, false, false>(kScanRows, dk, 64, [&](int i, int r) { return vn[r * dv + j0 + i]; },
                                        [&](int r, int d) { return kd[r * dk + d]; },
                                        [&](int i, int d, float x) {
                                            float &s_ = S[(int64_t)i * dk + d];
@@ -487,7 +487,7 @@ bwd_bwd_scan_kernel(const BwdParams p)
         __syncthreads();
         // dS <- gC dS' + dO^T Qd - dV_new^T W  (dO^T Qd comes from the prep kernel)
         const float gC = expf(b[63]);
-        block_gemm<2, 8, false, false>(kScanRows, dk, 64, [&](int i, int k) { return -dvn[k * dv + j0 + i]; },
+        block_gemm_cols<2, false, false>(kScanRows, dk, 64, [&](int i, int k) { return -dvn[k * dv + j0 + i]; },
                                        [&](int k, int d) { return W[k * dk + d]; },
                                        [&](int i, int d, float x) {
                                            float &s_ = dS[(int64_t)i * dk + d];

@@ -154,9 +154,10 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
  *   dg, dbeta     outputs [B, T, H] fp32.
  *   dinit_state   output [N, H, dv, dk] fp32, or NULL to skip.
  *   workspace     at least gdn_chunk_bwd_workspace_size() bytes, 256-byte aligned
- *                 (fp32 intermediates, about 0.35 MB per chunk and head at
+ *                 (fp32 intermediates, about 0.66 MB per chunk and head at
  *                 dk = dv = 128).
- * The kernels are fp32 on the CUDA cores; dk in {64, 128}, dv as gdn_chunk_fwd.
+ * The kernels are fp32 on the CUDA cores (products on the tensor cores as three
+ * tf32 passes, fp32-accurate); dk in {64, 128, 256}, dv as gdn_chunk_fwd.
  * Errors: GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA.
  */
 size_t gdn_chunk_bwd_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv,

@@ -83,7 +83,8 @@ def test_workspace_size_rules(lib):
     # dk = 256 (CUDA-core path): the fp32 layout, 256 B + 64 * (12 + 4 * (dk + dv)) B per chunk and head
     assert ws(1, 128, 2, 256, 128, 0, gdn.GDN_BF16) == 256 + 2 * 2 * 64 * (12 + 4 * (256 + 128))
     assert lib.gdn_chunk_fwd_kernel_count(1, 128, 2, 256, 128, 0, gdn.GDN_BF16) == 3
-    assert lib.gdn_chunk_bwd_workspace_size(1, 128, 2, 256, 128, 0, gdn.GDN_BF16) == 0   # the backward: dk <= 128
+    assert lib.gdn_chunk_bwd_workspace_size(1, 128, 2, 256, 128, 0, gdn.GDN_BF16) > 0    # the backward takes dk = 256 too
+    assert lib.gdn_chunk_bwd_workspace_size(1, 128, 2, 96, 128, 0, gdn.GDN_BF16) == 0
     # grows with the problem
     assert ws(1, 4096, 2, 64, 64, 0, 0) > ws(1, 2048, 2, 64, 64, 0, 0)
     assert ws(1, 0, 2, 64, 64, 0, 0) >= 256

@@ -74,7 +74,7 @@ def check_all(out, ref, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 256)])
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 256), (256, 64), (256, 256)])
 def test_bwd_ragged_with_states(dtype, dk, dv):
     d = inputs.make_prefill(B=2, L=150, H=2, dk=dk, dv=dv, dtype=dtype, seed=70, decay=0.3, init_state=True)
     dO, dS = cotangents(d, 71)
