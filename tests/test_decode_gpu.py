@@ -86,6 +86,38 @@ def test_decode_beta_up_to_two(dtype):
     assert_close(st, ref, dtype, "state")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_degenerate_cases(dtype):
+    """The step's degenerate cases ("Gated DeltaNet：先忘一点，再按误差更新记忆", "为什么再加一个遗忘门？"):
+    beta = 0 writes nothing (S <- alpha S and o = alpha S q, a closed form); alpha = 1 (g = 0) is the
+    plain delta rule; a zero key leaves S as alpha S; a zero query reads exactly 0."""
+    steps = 6
+    d = inputs.make_decode(N=3, H=2, dk=128, dv=128, steps=steps, dtype=dtype, seed=27)
+    d["beta"][0] = 0          # step 0: beta = 0 everywhere
+    d["g"][1] = 0             # step 1: alpha = 1
+    d["k"][2, 1] = 0          # step 2: sequence 1's keys are zero
+    d["q"][3, 2] = 0          # step 3: sequence 2's queries are zero
+    dd = cuda(d)
+    st = dd["state0"].clone()
+    ref = d["state0"].double().numpy()
+    for t in range(steps):
+        prev = st.double().cpu().numpy()
+        o = gdn.decode_step(st, dd["q"][t], dd["k"][t], dd["v"][t], dd["g"][t], dd["beta"][t], scale=128 ** -0.5)
+        ro, ref = oracle.decode_step(ref, d["q"][t], d["k"][t], d["v"][t], d["g"][t], d["beta"][t],
+                                     scale=128 ** -0.5, use_qk_l2norm=True)
+        torch.cuda.synchronize()
+        assert_close(o, ro, dtype, f"out step {t}")
+        assert_close(st, ref, dtype, f"state step {t}")
+        if t == 0:   # beta = 0: the closed form from the kernel's own previous state
+            a = np.exp(d["g"][0].double().numpy())[..., None, None]
+            q = d["q"][0].double().numpy()
+            qh = q / np.sqrt((q * q).sum(-1, keepdims=True) + 1e-6) * 128 ** -0.5
+            assert_close(st, a * prev, dtype, "beta=0 state vs alpha S")
+            assert_close(o, np.einsum("nhvk,nhk->nhv", a * prev, qh), dtype, "beta=0 out vs alpha S q")
+        if t == 3:
+            assert (o[2].float() == 0).all(), "a zero query must read exactly 0"
+
+
 # ---------------------------------------------------------------------------
 # several tokens per call ("Decode 递归": ordered composition of steps)
 # ---------------------------------------------------------------------------
