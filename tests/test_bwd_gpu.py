@@ -102,6 +102,20 @@ def test_bwd_varlen_beta_up_to_two(dtype):
     check_all(out, ref, dtype)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_bwd_beta_near_two_nearly_parallel_keys(dtype):
+    """The conditioning stress of the UT solve ("Gated Delta Networks", §2.2, beta in (0, 2)) for the
+    gradients: keys of each head nearly parallel and beta in (1.8, 2), so the strictly-lower system
+    entries approach 2 in magnitude and the chunk-local products nearly cancel; standard tolerances."""
+    d = inputs.make_prefill(B=1, L=320, H=2, dk=128, dv=128, dtype=dtype, seed=24, decay=0.02, beta_max=2.0)
+    k = d["k"].float()
+    d["k"] = (k[:, :1] + 0.05 * k).to(d["k"].dtype)
+    d["beta"] = (1.8 + 0.1 * d["beta"]).contiguous()
+    dO, dS = cotangents(d, 77)
+    out, ref = grads(d, dO, dS, 128)
+    check_all(out, ref, dtype)
+
+
 def test_bwd_without_l2norm_and_without_state_gradients():
     d = inputs.make_prefill(B=1, L=200, H=3, dk=64, dv=64, dtype="f32", seed=74, decay=0.2)
     d["q"] = d["q"] / d["q"].norm(dim=-1, keepdim=True)
