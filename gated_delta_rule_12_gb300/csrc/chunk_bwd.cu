@@ -246,6 +246,7 @@ struct BwdParams {
     void *dq, *dk, *dv;             // dtype dt
     float *dg, *dbeta, *dinit;
     float *ws;                      // per (slot, head) blocks of BwdLayout
+    int need_u;                     // U~ is only read by the CUDA-core forward scan
     Geometry gm;
     float scale;
     int l2;
@@ -381,11 +382,12 @@ bwd_prep_kernel(const BwdParams p)
     for (int e = tid; e < 64 * 64; e += kBT) blk[LY.t + e] = sT[(e >> 6) * 65 + (e & 63)];
     const float *Tm = sT;   // pitch 65 below
     // U = T diag(beta) V,  W = T diag(beta gam) K^
-    block_gemm_cols<4, true, false>(64, dv, 64, [&](int i, int k) { return Tm[i * 65 + k]; },
-                                    [&](int k, int j) {
-                                        return k < rows ? sbe[k] * ld<T>(p.v, ((tok0 + k) * H + h) * dv + j) : 0.f;
-                                    },
-                                    [&](int i, int j, float x) { blk[LY.u + i * dv + j] = x; }, sA, sB);
+    if (p.need_u)
+        block_gemm_cols<4, true, false>(64, dv, 64, [&](int i, int k) { return Tm[i * 65 + k]; },
+                                        [&](int k, int j) {
+                                            return k < rows ? sbe[k] * ld<T>(p.v, ((tok0 + k) * H + h) * dv + j) : 0.f;
+                                        },
+                                        [&](int i, int j, float x) { blk[LY.u + i * dv + j] = x; }, sA, sB);
     block_gemm_cols<4, true, false>(64, dk, 64, [&](int i, int k) { return Tm[i * 65 + k]; },
                                     [&](int k, int j) { return sbe[k] * sgam[k] * kh[k * dk + j]; },
                                     [&](int i, int j, float x) { blk[LY.w + i * dk + j] = x; }, sA, sB);
@@ -704,6 +706,8 @@ cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t st)
     p.init_state = a.init_state; p.dfinal = a.dfinal;
     p.dq = a.dq; p.dk = a.dk; p.dv = a.dv; p.dg = a.dg; p.dbeta = a.dbeta; p.dinit = a.dinit;
     p.ws = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(a.workspace) + 256);
+    const bool tc_scan = a.dt == 1 && chunk_tc_supported(1, a.gm.dk, a.gm.dv, (int64_t)a.gm.B * a.gm.T);
+    p.need_u = tc_scan ? 0 : 1;
     p.gm = a.gm; p.scale = a.scale; p.l2 = a.l2;
     const size_t stage = 2 * (size_t)kStage * sizeof(float);
     const size_t sm_prep = stage + sizeof(float) * (2 * 64 * 65 + 4 * 64);
@@ -720,7 +724,24 @@ cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t st)
         return e;
     if (a.slots > 0) bwd_prep_kernel<T><<<dim3((unsigned)a.slots, a.gm.H), kBT, sm_prep, st>>>(p);
     const dim3 sgrid(a.gm.N, a.gm.H, a.gm.dv / kScanRows);
-    bwd_fwd_scan_kernel<<<sgrid, kBT, sm_scan, st>>>(p);
+    if (tc_scan) {
+        // The forward scan on the tensor cores: the chunked forward itself, saving the state at every
+        // chunk start and V_new into their workspace fields.  Its chunk-local blocks (57.8 KB each) sit
+        // in the local kernel's scratch fields (dq^, dk^, dW: 96 KB at dk = 128), free until then.
+        const BwdLayout LY = bwd_layout(a.gm.dk, a.gm.dv);
+        ChunkArgs f;
+        f.q = a.q; f.k = a.k; f.v = a.v; f.g = a.g; f.beta = a.beta; f.init_state = a.init_state;
+        f.out = nullptr; f.final_state = nullptr; f.gm = a.gm; f.slots = a.slots; f.dt = 1;
+        f.scale = a.scale; f.l2 = a.l2; f.workspace = a.workspace;
+        f.blocks = p.ws + LY.dqh;
+        f.block_stride = (size_t)LY.total * sizeof(float);
+        f.save_s = p.ws + LY.s;
+        f.save_vn = p.ws + LY.vn;
+        f.save_stride = LY.total;
+        if ((e = launch_chunk_tc(f, st))) return e;
+    } else {
+        bwd_fwd_scan_kernel<<<sgrid, kBT, sm_scan, st>>>(p);
+    }
     bwd_bwd_scan_kernel<T><<<sgrid, kBT, sm_scan, st>>>(p);
     if (a.slots > 0) bwd_local_kernel<T><<<dim3((unsigned)a.slots, a.gm.H), kBT, sm_local, st>>>(p);
     return cudaGetLastError();

@@ -900,9 +900,15 @@ struct RcParams {
     Geometry gm;
     long long *trace;
     ConvParams cv;      // KC > 0: the raw V tile is convolved in place, Q comes convolved from the workspace
+    // For the backward pass: when save_s is set, the state at every chunk start (fp32 [dv][128]) and
+    // V_new (fp32 [64][dv]) go to per (slot, head) blocks save_stride floats apart; out may then be null.
+    float *save_s, *save_vn;
+    int64_t save_stride;
 };
 
-template <int KC>
+// SAVE (the backward's forward scan): the chunk-start states and V_new go to p.save_s and p.save_vn,
+// and the outputs are not written.
+template <int KC, bool SAVE = false>
 __global__ void __launch_bounds__(kThreadsRc, 1)
 recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmv, const RcParams p)
 {
@@ -1067,6 +1073,14 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             if (leader) ok = wait_spin(bar(b), parity, abort_flag, p.err);
             return !gsync(!ok);
         };
+        // the state at the start of chunk c: this thread's 64 entries of row j0 + j
+        auto save_state = [&](int c, const uint32_t (&sv)[64]) {
+            float *dst = p.save_s + ((slot0 + c) * H + h) * p.save_stride + (size_t)(j0 + j) * 128 + hf * 64;
+#pragma unroll
+            for (int e = 0; e < 64; e += 4)
+                *reinterpret_cast<float4 *>(dst + e) = make_float4(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1]),
+                                                                   __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]));
+        };
         // 64 fp32 state entries (this thread's half of row j) -> the bf16 A tile of a2
         auto put_sbf = [&](const uint32_t (&sv)[64]) {
             uint8_t *row = sm + R_SBF + hf * 16384;
@@ -1100,6 +1114,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     sv[e + 2] = __float_as_uint(v4.z); sv[e + 3] = __float_as_uint(v4.w);
                 }
                 put_sbf(sv);
+                if constexpr (SAVE) save_state(0, sv);
                 fence_proxy_async();
                 if (gsync(*abort_flag)) break;
                 if (leader) mbar_arrive(bar(RB_S));
@@ -1138,6 +1153,11 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                         *reinterpret_cast<uint4 *>(sm + R_X + sw128_offset(j, hf * 32 + ch * 8)) = w;
                     }
                     if (xmax > kF16Max) atomicExch(p.err, kDevErrRange);
+                    if constexpr (SAVE) {   // V_new[t][j0 + j] for this thread's 32 tokens (a warp stores 128 B a token)
+                        float *dst = p.save_vn + ((slot0 + c) * H + h) * p.save_stride + (size_t)(hf * 32) * dv + j0 + j;
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) dst[(size_t)t * dv] = __uint_as_float(a[t]);
+                    }
                 }
                 fence_proxy_async();
                 fence_before_sync();
@@ -1161,6 +1181,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
                     fence_proxy_async();
                     if (gsync(*abort_flag)) break;
                     if (leader) mbar_arrive(bar(RB_S));   // the bf16 state is ready: the next a2 may start
+                    if constexpr (SAVE) save_state(c + 1, sv);
                     if (leader) GDN_TR(p.trace, 2, c, 2);
 #pragma unroll
                     for (int e = 0; e < 64; ++e) sv[e] = __float_as_uint(e1 * __uint_as_float(sv[e]));
@@ -1336,7 +1357,7 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
 #pragma unroll
             for (int it = 0; it < 8; ++it) {
                 const int idx = it * 128 + j, r = idx >> 4, ch = idx & 15;
-                if (r < rows)
+                if (!SAVE && r < rows)
                     *reinterpret_cast<uint4 *>(obase + (size_t)r * H * dv + ch * 8) =
                         *reinterpret_cast<const uint4 *>(stg + r * 256 + ch * 16);
             }
@@ -1444,6 +1465,14 @@ cudaError_t launch_pair(const CUtensorMap &tq, const CUtensorMap &tk, const CUte
     cudaError_t e = cudaFuncSetAttribute(ut_tc_kernel<KC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemUt);
     if (e != cudaSuccess) return e;
     ut_tc_kernel<KC><<<dim3((unsigned)slots, gm.H), kThreadsUt, kSmemUt, st>>>(tq, tk, up);
+    if constexpr (KC == 0) {
+        if (rp.save_s) {
+            e = cudaFuncSetAttribute(recur_tc_kernel<0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemRc);
+            if (e != cudaSuccess) return e;
+            recur_tc_kernel<0, true><<<dim3(gm.N, gm.H, gm.dv / 128), kThreadsRc, kSmemRc, st>>>(tq, tv, rp);
+            return cudaGetLastError();
+        }
+    }
     e = cudaFuncSetAttribute(recur_tc_kernel<KC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemRc);
     if (e != cudaSuccess) return e;
     recur_tc_kernel<KC><<<dim3(gm.N, gm.H, gm.dv / 128), kThreadsRc, kSmemRc, st>>>(tq, tv, rp);
@@ -1464,7 +1493,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st)
 #ifdef GDN_KERNEL_TRACE
     trace = g_trace_buffer;
 #endif
-    uint8_t *blocks = reinterpret_cast<uint8_t *>(a.workspace) + kWsHeader;
+    uint8_t *blocks = a.blocks ? reinterpret_cast<uint8_t *>(a.blocks) : reinterpret_cast<uint8_t *>(a.workspace) + kWsHeader;
     unsigned *err = reinterpret_cast<unsigned *>(a.workspace);
     ConvParams cv{};
     if (f) {
@@ -1476,7 +1505,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st)
         cv.state_in = reinterpret_cast<const __nv_bfloat16 *>(f->state_in);
         cv.state_out = reinterpret_cast<__nv_bfloat16 *>(f->state_out);
     }
-    const size_t block_bytes = f ? kPrepBlockFused : kPrepBlock;
+    const size_t block_bytes = a.blocks ? a.block_stride : (f ? kPrepBlockFused : kPrepBlock);
 
     UtParams up;
     up.g = a.g; up.beta = a.beta; up.blocks = blocks; up.block_bytes = block_bytes; up.err = err; up.gm = a.gm;
@@ -1485,6 +1514,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st)
     rp.init_state = a.init_state; rp.blocks = blocks; rp.block_bytes = block_bytes;
     rp.out = reinterpret_cast<__nv_bfloat16 *>(a.out);
     rp.final_state = a.final_state; rp.err = err; rp.gm = a.gm; rp.trace = trace; rp.cv = cv;
+    rp.save_s = a.save_s; rp.save_vn = a.save_vn; rp.save_stride = a.save_stride;
     switch (f ? f->K : 0) {
         case 0: return launch_pair<0>(tq, tk, tv, up, rp, a.gm, a.slots, st);
         case 1: return launch_pair<1>(tq, tk, tv, up, rp, a.gm, a.slots, st);

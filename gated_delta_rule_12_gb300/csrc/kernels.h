@@ -23,6 +23,12 @@ struct ChunkArgs {
     int l2;
     void *workspace;
     const PrologueArgs *fuse = nullptr;   // non-null: q, k, v, g, beta are made from these projections
+    // Tensor-core path, for the backward pass: chunk-local blocks at blocks + (slot * H + h) * block_stride
+    // (instead of after the workspace header), and the chunk-start states and V_new saved (see RcParams).
+    void *blocks = nullptr;
+    size_t block_stride = 0;
+    float *save_s = nullptr, *save_vn = nullptr;
+    int64_t save_stride = 0;
 };
 
 struct DecodeArgs {

@@ -157,7 +157,10 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
  *                 (fp32 intermediates, about 0.66 MB per chunk and head at
  *                 dk = dv = 128).
  * The kernels are fp32 on the CUDA cores (products on the tensor cores as three
- * tf32 passes, fp32-accurate); dk in {64, 128, 256}, dv as gdn_chunk_fwd.
+ * tf32 passes, fp32-accurate); dk in {64, 128, 256}, dv as gdn_chunk_fwd.  For
+ * bf16 inputs with dk = 128 and dv a multiple of 128 the chunk-start states and
+ * V_new come from the tensor-core chunked forward (its precision, see
+ * gdn_chunk_fwd); everything else stays fp32.
  * Errors: GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA.
  */
 size_t gdn_chunk_bwd_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv,
