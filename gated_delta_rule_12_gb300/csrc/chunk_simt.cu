@@ -311,6 +311,207 @@ recur_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
 }
 
 // ---------------------------------------------------------------------------
+// K3, register-tiled (dk <= 128): the same recurrence with each thread computing
+// a small tile of every product from 16-B shared-memory loads along the
+// contraction (rows padded to DK + 4 floats, so the rows a warp reads start in
+// different banks): about one 16-B load per eight FMAs instead of two 4-B loads
+// per FMA in the kernel above, which is bound by shared-memory traffic.
+//   (a) V_new = U~ - W<- S^T            64 x 32, thread tile 4 r x 2 j
+//   (b) Aqk = (Q K^T) o Gamma           64 x 64 lower, thread tile 4 r x 4 i
+//   (c) O = e^b (Q S^T) + Aqk V_new     64 x 32, thread tile 4 r x 2 j
+//   (d) S <- e^{b_C} S + (ed o V_new)^T K->   32 x DK, thread tile 2 j x DK/16 d
+// ---------------------------------------------------------------------------
+template <int DK>
+__host__ __device__ constexpr size_t recur_tiled_smem_floats()
+{
+    return (size_t)kChunk * (DK + 4) * 3       /* Q, K, W rows            */
+         + (size_t)kRowsSimt * (DK + 4)        /* S rows                  */
+         + (size_t)kChunk * 36 * 3             /* U, V_new, ed o V_new    */
+         + (size_t)kChunk * 68                 /* Aqk rows                */
+         + 3 * kChunk;                         /* b, e^b, e^{b_C - b}     */
+}
+
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+
+template <typename T, int DK>
+__global__ void __launch_bounds__(256)
+recur_simt_tiled_kernel(const T *__restrict__ q, const T *__restrict__ k,
+                        const float *__restrict__ init_state, T *__restrict__ out,
+                        float *__restrict__ final_state, Geometry gm,
+                        const float *__restrict__ bcum, const float *__restrict__ rq,
+                        const float *__restrict__ rk, const float *__restrict__ Wg,
+                        const float *__restrict__ Ug, unsigned *__restrict__ err_word)
+{
+    static_assert(DK == 64 || DK == 128, "tiled path: dk 64 or 128");
+    constexpr int P = DK + 4, PV = 36, PA = 68, DT = DK / 16;   // pitches; d per thread in (d)
+    if (err_word && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0)
+        *err_word = kDevErrNone;
+    extern __shared__ float smem[];
+    float *Qs = smem, *Ks = Qs + kChunk * P, *Ws = Ks + kChunk * P, *Ss = Ws + kChunk * P;
+    float *Us = Ss + kRowsSimt * P, *Vn = Us + kChunk * PV, *Ve = Vn + kChunk * PV;
+    float *Aq = Ve + kChunk * PV, *bs = Aq + kChunk * PA, *eb = bs + kChunk, *ed = eb + kChunk;
+
+    const int n = blockIdx.x, h = blockIdx.y, j0 = blockIdx.z * kRowsSimt;
+    const int tid = threadIdx.x;
+    const int H = gm.H, dv = gm.dv;
+    int64_t tok0;
+    int len;
+    seq_span(gm, n, tok0, len);
+    const int64_t sbase = slot_base(gm, n);
+    const size_t st_off = ((size_t)n * H + h) * (size_t)dv * DK;
+    // thread tiles
+    const int tr = tid >> 4, tc = tid & 15;          // (a), (b), (c): rows 4 tr..; columns by tc
+    const int r0 = 4 * tr, ja = 2 * tc, ia = 4 * tc;
+    const int jd = 2 * (tid >> 4), dd = DT * (tid & 15);   // (d): rows jd, jd + 1 of S, columns dd..
+
+    for (int e = tid; e < kRowsSimt * DK; e += 256) {
+        const int j = e / DK, d = e % DK;
+        Ss[j * P + d] = init_state ? init_state[st_off + (size_t)(j0 + j) * DK + d] : 0.f;
+    }
+    const int nchunks = ceil_div(len, kChunk);
+    for (int c = 0; c < nchunks; ++c) {
+        const int64_t slot = sbase + c;
+        const size_t base = ((size_t)slot * H + h) * kChunk;
+        const int rows = min(kChunk, len - c * kChunk);
+        const int64_t t0 = tok0 + (int64_t)c * kChunk;
+        __syncthreads();   // the previous chunk is done with every buffer
+        if (tid < kChunk) {
+            const float b = bcum[base + tid];
+            bs[tid] = b;
+            eb[tid] = expf(b);
+        }
+        for (int e = tid; e < kChunk * DK; e += 256) {
+            const int r = e / DK, d = e % DK;
+            float xq = 0.f, xk = 0.f;
+            if (r < rows) {
+                const size_t gi = ((size_t)(t0 + r) * H + h) * DK + d;
+                xq = to_f32(q[gi]) * rq[base + r];
+                xk = to_f32(k[gi]) * rk[base + r];
+            }
+            Qs[r * P + d] = xq;
+            Ks[r * P + d] = xk;
+            Ws[r * P + d] = Wg[base * DK + (size_t)r * DK + d];
+        }
+        for (int e = tid; e < kChunk * kRowsSimt; e += 256) {
+            const int r = e / kRowsSimt, j = e % kRowsSimt;
+            Us[r * PV + j] = Ug[base * dv + (size_t)r * dv + j0 + j];
+        }
+        __syncthreads();
+        if (tid < kChunk) ed[tid] = expf(bs[kChunk - 1] - bs[tid]);
+        {   // (a) V_new and (b) Aqk
+            float va[4][2] = {}, qs[4][2] = {};
+#pragma unroll 4
+            for (int d = 0; d < DK; d += 4) {
+                const float4 s0 = ld4(Ss + ja * P + d), s1 = ld4(Ss + (ja + 1) * P + d);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float4 w = ld4(Ws + (r0 + u) * P + d), x = ld4(Qs + (r0 + u) * P + d);
+                    va[u][0] += w.x * s0.x + w.y * s0.y + w.z * s0.z + w.w * s0.w;
+                    va[u][1] += w.x * s1.x + w.y * s1.y + w.z * s1.z + w.w * s1.w;
+                    qs[u][0] += x.x * s0.x + x.y * s0.y + x.z * s0.z + x.w * s0.w;
+                    qs[u][1] += x.x * s1.x + x.y * s1.y + x.z * s1.z + x.w * s1.w;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                Vn[(r0 + u) * PV + ja] = Us[(r0 + u) * PV + ja] - va[u][0];
+                Vn[(r0 + u) * PV + ja + 1] = Us[(r0 + u) * PV + ja + 1] - va[u][1];
+            }
+            float ac[4][4] = {};
+            if (ia <= r0 + 3) {
+#pragma unroll 4
+                for (int d = 0; d < DK; d += 4) {
+                    float4 kk[4];
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) kk[v] = ld4(Ks + (ia + v) * P + d);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float4 x = ld4(Qs + (r0 + u) * P + d);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            ac[u][v] += x.x * kk[v].x + x.y * kk[v].y + x.z * kk[v].z + x.w * kk[v].w;
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int r = r0 + u, i = ia + v;
+                    Aq[r * PA + i] = (i <= r) ? ac[u][v] * expf(bs[r] - bs[i]) : 0.f;
+                }
+            __syncthreads();
+            // (c) O = e^b (Q S^T) + Aqk V_new
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                qs[u][0] *= eb[r0 + u];
+                qs[u][1] *= eb[r0 + u];
+            }
+            for (int i = 0; i <= r0; i += 4) {
+                const float2 v0 = *reinterpret_cast<const float2 *>(Vn + i * PV + ja);
+                const float2 v1 = *reinterpret_cast<const float2 *>(Vn + (i + 1) * PV + ja);
+                const float2 v2 = *reinterpret_cast<const float2 *>(Vn + (i + 2) * PV + ja);
+                const float2 v3 = *reinterpret_cast<const float2 *>(Vn + (i + 3) * PV + ja);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float4 a = ld4(Aq + (r0 + u) * PA + i);
+                    qs[u][0] += a.x * v0.x + a.y * v1.x + a.z * v2.x + a.w * v3.x;
+                    qs[u][1] += a.x * v0.y + a.y * v1.y + a.z * v2.y + a.w * v3.y;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int r = r0 + u;
+                if (r < rows) {
+                    T *o = out + ((size_t)(t0 + r) * H + h) * dv + j0 + ja;
+                    o[0] = from_f32<T>(qs[u][0]);
+                    o[1] = from_f32<T>(qs[u][1]);
+                }
+            }
+        }
+        // (d) S <- e^{b_C} S + (ed o V_new)^T K->, after every thread has read S for (a) and (c)
+        for (int e = tid; e < kChunk * kRowsSimt; e += 256) {
+            const int r = e / kRowsSimt, j = e % kRowsSimt;
+            Ve[r * PV + j] = ed[r] * Vn[r * PV + j];
+        }
+        __syncthreads();
+        {
+            const float gC = eb[kChunk - 1];
+            float sacc[2][DT];
+#pragma unroll
+            for (int v = 0; v < DT; ++v) {
+                sacc[0][v] = gC * Ss[jd * P + dd + v];
+                sacc[1][v] = gC * Ss[(jd + 1) * P + dd + v];
+            }
+#pragma unroll 4
+            for (int r = 0; r < kChunk; ++r) {
+                const float2 x = *reinterpret_cast<const float2 *>(Ve + r * PV + jd);
+#pragma unroll
+                for (int v4 = 0; v4 < DT; v4 += 4) {
+                    const float4 kk = ld4(Ks + r * P + dd + v4);
+                    sacc[0][v4] += x.x * kk.x; sacc[0][v4 + 1] += x.x * kk.y;
+                    sacc[0][v4 + 2] += x.x * kk.z; sacc[0][v4 + 3] += x.x * kk.w;
+                    sacc[1][v4] += x.y * kk.x; sacc[1][v4 + 1] += x.y * kk.y;
+                    sacc[1][v4 + 2] += x.y * kk.z; sacc[1][v4 + 3] += x.y * kk.w;
+                }
+            }
+#pragma unroll
+            for (int v = 0; v < DT; ++v) {
+                Ss[jd * P + dd + v] = sacc[0][v];
+                Ss[(jd + 1) * P + dd + v] = sacc[1][v];
+            }
+        }
+    }
+    __syncthreads();
+    if (final_state) {
+        for (int e = tid; e < kRowsSimt * DK; e += 256) {
+            const int j = e / DK, d = e % DK;
+            final_state[st_off + (size_t)(j0 + j) * DK + d] = Ss[j * P + d];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // launcher
 // ---------------------------------------------------------------------------
 template <typename T, int DK>
@@ -330,12 +531,20 @@ static cudaError_t launch_simt_typed(const ChunkArgs &a, cudaStream_t st)
         cudaFuncSetAttribute(ut_simt_kernel<T, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);
         ut_simt_kernel<T, DK><<<grid1, 256, sm2, st>>>(k, v, a.beta, a.gm, bcum, rk, W, U);
     }
-    const size_t sm3 = sizeof(float) * recur_simt_smem_floats<DK>();
-    cudaFuncSetAttribute(recur_simt_kernel<T, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3);
     dim3 grid3(a.gm.N, a.gm.H, a.gm.dv / kRowsSimt);
-    recur_simt_kernel<T, DK><<<grid3, 256, sm3, st>>>(q, k, a.init_state, (T *)a.out, a.final_state,
-                                                      a.gm, bcum, rq, rk, W, U,
-                                                      a.slots > 0 ? nullptr : err);
+    if constexpr (DK <= 128) {
+        const size_t sm3 = sizeof(float) * recur_tiled_smem_floats<DK>();
+        cudaFuncSetAttribute(recur_simt_tiled_kernel<T, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3);
+        recur_simt_tiled_kernel<T, DK><<<grid3, 256, sm3, st>>>(q, k, a.init_state, (T *)a.out, a.final_state,
+                                                                a.gm, bcum, rq, rk, W, U,
+                                                                a.slots > 0 ? nullptr : err);
+    } else {
+        const size_t sm3 = sizeof(float) * recur_simt_smem_floats<DK>();
+        cudaFuncSetAttribute(recur_simt_kernel<T, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3);
+        recur_simt_kernel<T, DK><<<grid3, 256, sm3, st>>>(q, k, a.init_state, (T *)a.out, a.final_state,
+                                                          a.gm, bcum, rq, rk, W, U,
+                                                          a.slots > 0 ? nullptr : err);
+    }
     return cudaGetLastError();
 }
 
