@@ -95,8 +95,9 @@ ut_simt_kernel(const T *__restrict__ k, const T *__restrict__ v, const float *__
                float *__restrict__ Wout, float *__restrict__ Uout)
 {
     extern __shared__ float smem[];
-    float *Ks = smem;                       // [64][DK+1]
-    float *A = Ks + kChunk * (DK + 1);      // [64][65]  strictly lower system matrix
+    constexpr int P = DK + 4;               // row pitch of K: 16-B rows for the tiled Gram product
+    float *Ks = smem;                       // [64][DK+4]
+    float *A = Ks + kChunk * P;             // [64][65]  strictly lower system matrix
     float *bs = A + kChunk * 65;            // [64]
     float *bt = bs + kChunk;                // [64]   beta (0 on padded rows)
 
@@ -117,19 +118,35 @@ ut_simt_kernel(const T *__restrict__ k, const T *__restrict__ v, const float *__
         const int r = e / DK, d = e % DK;
         float x = 0.f;
         if (r < rows) x = to_f32(k[((tok0 + r) * gm.H + h) * DK + d]) * rk[base + r];
-        Ks[r * (DK + 1) + d] = x;
+        Ks[r * P + d] = x;
     }
     __syncthreads();
-    for (int e = tid; e < kChunk * kChunk; e += blockDim.x) {
-        const int r = e / kChunk, i = e % kChunk;
-        float val = 0.f;
-        if (i < r) {
-            float acc = 0.f;
-#pragma unroll 8
-            for (int d = 0; d < DK; ++d) acc += Ks[r * (DK + 1) + d] * Ks[i * (DK + 1) + d];
-            val = bt[r] * expf(bs[r] - bs[i]) * acc;
+    {   // K K^T, a 4 x 4 tile of rows r0.., columns i0.. per thread, 16-B loads along d
+        const int r0 = 4 * (tid >> 4), i0 = 4 * (tid & 15);
+        float acc[4][4] = {};
+        if (i0 < r0 + 3) {
+#pragma unroll 4
+            for (int d = 0; d < DK; d += 4) {
+                float4 kr[4], ki[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    kr[u] = *reinterpret_cast<const float4 *>(Ks + (r0 + u) * P + d);
+                    ki[u] = *reinterpret_cast<const float4 *>(Ks + (i0 + u) * P + d);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        acc[u][v] += kr[u].x * ki[v].x + kr[u].y * ki[v].y + kr[u].z * ki[v].z + kr[u].w * ki[v].w;
+            }
         }
-        A[r * 65 + i] = val;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const int r = r0 + u, i = i0 + v;
+                A[r * 65 + i] = (i < r) ? bt[r] * expf(bs[r] - bs[i]) * acc[u][v] : 0.f;
+            }
     }
     __syncthreads();
 
@@ -139,19 +156,20 @@ ut_simt_kernel(const T *__restrict__ k, const T *__restrict__ v, const float *__
         float x[kChunk];
         if (col < DK) {
 #pragma unroll
-            for (int r = 0; r < kChunk; ++r) x[r] = bt[r] * expf(bs[r]) * Ks[r * (DK + 1) + col];
+            for (int r = 0; r < kChunk; ++r) x[r] = bt[r] * expf(bs[r]) * Ks[r * P + col];
         } else {
             const int j = col - DK;
 #pragma unroll
             for (int r = 0; r < kChunk; ++r)
                 x[r] = (r < rows) ? bt[r] * to_f32(v[((tok0 + r) * gm.H + h) * dv + j]) : 0.f;
         }
+        // forward substitution, column-oriented: once x_i is final it is taken out of every later
+        // row, so the updates of one step are independent (a chain of 63 steps, not of 2016 FMAs)
 #pragma unroll
-        for (int r = 1; r < kChunk; ++r) {
-            float acc = x[r];
+        for (int i = 0; i < kChunk - 1; ++i) {
+            const float xi = x[i];
 #pragma unroll
-            for (int i = 0; i < r; ++i) acc -= A[r * 65 + i] * x[i];
-            x[r] = acc;
+            for (int r = i + 1; r < kChunk; ++r) x[r] -= A[r * 65 + i] * xi;
         }
         if (col < DK) {
 #pragma unroll
@@ -527,7 +545,7 @@ static cudaError_t launch_simt_typed(const ChunkArgs &a, cudaStream_t st)
     if (a.slots > 0) {
         dim3 grid1((unsigned)a.slots, a.gm.H);
         prologue_kernel<T><<<grid1, 256, 0, st>>>(q, k, a.g, a.gm, a.scale, a.l2, bcum, rq, rk, err);
-        const size_t sm2 = sizeof(float) * ((size_t)kChunk * (DK + 1) + kChunk * 65 + 2 * kChunk);
+        const size_t sm2 = sizeof(float) * ((size_t)kChunk * (DK + 4) + kChunk * 65 + 2 * kChunk);
         cudaFuncSetAttribute(ut_simt_kernel<T, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);
         ut_simt_kernel<T, DK><<<grid1, 256, sm2, st>>>(k, v, a.beta, a.gm, bcum, rk, W, U);
     }
