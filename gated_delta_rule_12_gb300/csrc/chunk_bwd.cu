@@ -26,6 +26,7 @@
 // (block_gemm) on the tensor cores with fp32 accuracy (three tf32 products per pair).
 #include "common.cuh"
 #include "kernels.h"
+#include "umma.cuh"
 
 namespace gdn {
 namespace {
@@ -247,6 +248,7 @@ struct BwdParams {
     float *dg, *dbeta, *dinit;
     float *ws;                      // per (slot, head) blocks of BwdLayout
     int need_u;                     // U~ is only read by the CUDA-core forward scan
+    unsigned *err;                  // device error word (the workspace's first word)
     Geometry gm;
     float scale;
     int l2;
@@ -698,6 +700,634 @@ bwd_local_kernel(const BwdParams p)
     }
 }
 
+// ===========================================================================
+// bwd_local_tc_kernel: the products of bwd_local_kernel on the tcgen05 tensor
+// cores, for bf16 inputs with dk = dv = 128.  Every operand is staged once into
+// shared memory as 128-B-swizzled bf16 tiles -- an fp32 intermediate x as the pair
+// hi = bf16(x), lo = bf16(x - hi) (about 16 significand bits), a bf16 input as it
+// is -- and serves every product that reads it, as a K-major or an MN-major
+// operand.  One thread issues hi*hi + hi*lo + lo*hi (two products when one side is
+// an exact bf16 input) into fp32 accumulators in tensor memory; the epilogues and
+// the elementwise steps are those of bwd_local_kernel.  The MMAs are M = 128 with
+// the chunk's 64 rows in lanes 0-63 (the rows behind a 64-row tile only feed lanes
+// 64-127, which are never read); warps 0, 1 (columns 0-63 of a row) and 4, 5
+// (columns 64-127) read them back.
+// ===========================================================================
+namespace lt {
+using umma::smem_desc;
+using umma::idesc_bf16;
+using umma::mma_ss;
+using umma::sw128_offset;
+
+// shared memory, bytes from the 1024-aligned base.  Tiles are [64-column block][rows][128 B].
+constexpr uint32_t DO = 0;                   // dO [64 r][128 j] bf16; then dT (hi, lo); then M (hi, lo)
+constexpr uint32_t VNH = 16384, VNL = 32768; // V_new [64 r][128 j] hi, lo; then K^ [64 i][128 d] hi, lo
+constexpr uint32_t DVH = 49152, DVL = 65536; // dV_new [64 r][128 j] hi, lo; then dA' (hi, lo) at DVH
+constexpr uint32_t BH = 81920, BL = 114688;  // S, then dS' [128 j][128 d] hi, lo; then dW hi, lo (BH, BH + 16K),
+                                             // V [64 j][128 c] bf16 (BL), X (hi, lo) (BL + 16K); then Q^ (BH, BH + 16K)
+constexpr uint32_t TT = 147456;              // T [64 r][64 i] hi, lo (8 KB each)
+constexpr uint32_t FA = 163840, FB = 180224; // fp32 [64][64]: dA, then dA o Gamma;  dT, then dL, then M
+constexpr uint32_t VEC = 196608;             // per-row vectors, 16 x 64 floats
+constexpr uint32_t MISC = VEC + 16 * 64 * 4; // mbarrier, tensor-memory base, abort flag
+constexpr uint32_t kSmem = MISC + 64 + 1024;
+static_assert(kSmem <= 232448, "local kernel shared memory");
+constexpr uint64_t kWaitNs = 1000000000ull;
+
+__device__ __forceinline__ void split_pair(float x, float y, uint32_t &hi, uint32_t &lo)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+// 8 consecutive floats of row r, columns 8 c8 .. 8 c8 + 7, into the hi and lo tiles of R rows
+__device__ __forceinline__ void put8(uint8_t *hi, uint8_t *lo, int R, int r, int c8, const float (&v)[8])
+{
+    uint4 h, l;
+    split_pair(v[0], v[1], h.x, l.x);
+    split_pair(v[2], v[3], h.y, l.y);
+    split_pair(v[4], v[5], h.z, l.z);
+    split_pair(v[6], v[7], h.w, l.w);
+    const uint32_t o = (uint32_t)(c8 >> 3) * (uint32_t)R * 128u + sw128_offset((uint32_t)r, (uint32_t)(c8 & 7) * 8u);
+    *reinterpret_cast<uint4 *>(hi + o) = h;
+    *reinterpret_cast<uint4 *>(lo + o) = l;
+}
+
+// fp32 [R][C] (row stride ld floats, 16-B aligned rows) -> hi, lo tiles; rows >= valid are zero.
+// Each thread takes R C / (8 kBT) chunks of 8 columns and issues all their loads before the first
+// conversion, so the staging waits on one memory latency, not one per chunk.
+template <int R, int C>
+__device__ __forceinline__ void stage_f32(uint8_t *hi, uint8_t *lo, const float *src, int ld, int valid)
+{
+    constexpr int per_row = C / 8, NI = R * per_row / kBT;
+    static_assert(NI * kBT == R * per_row, "whole chunks per thread");
+    float4 a[NI], b[NI];
+#pragma unroll
+    for (int u = 0; u < NI; ++u) {
+        const int id = threadIdx.x + u * kBT, r = id / per_row, c8 = id % per_row;
+        if (r < valid) {
+            a[u] = *reinterpret_cast<const float4 *>(src + (int64_t)r * ld + 8 * c8);
+            b[u] = *reinterpret_cast<const float4 *>(src + (int64_t)r * ld + 8 * c8 + 4);
+        } else {
+            a[u] = b[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < NI; ++u) {
+        const int id = threadIdx.x + u * kBT, r = id / per_row, c8 = id % per_row;
+        const float v[8] = {a[u].x, a[u].y, a[u].z, a[u].w, b[u].x, b[u].y, b[u].z, b[u].w};
+        put8(hi, lo, R, r, c8, v);
+    }
+}
+
+// stage_f32 over tiles that hold another matrix of the same shape, returning this thread's part of
+// sum(new * old), the old entries read back as hi + lo (about 16 significand bits) before they are
+// overwritten
+template <int R, int C>
+__device__ __forceinline__ float stage_f32_dot_old(uint8_t *hi, uint8_t *lo, const float *src, int ld)
+{
+    constexpr int per_row = C / 8, NI = R * per_row / kBT;
+    static_assert(NI * kBT == R * per_row, "whole chunks per thread");
+    float4 a[NI], b[NI];
+#pragma unroll
+    for (int u = 0; u < NI; ++u) {
+        const int id = threadIdx.x + u * kBT, r = id / per_row, c8 = id % per_row;
+        a[u] = *reinterpret_cast<const float4 *>(src + (int64_t)r * ld + 8 * c8);
+        b[u] = *reinterpret_cast<const float4 *>(src + (int64_t)r * ld + 8 * c8 + 4);
+    }
+    float dot = 0.f;
+#pragma unroll
+    for (int u = 0; u < NI; ++u) {
+        const int id = threadIdx.x + u * kBT, r = id / per_row, c8 = id % per_row;
+        const float v[8] = {a[u].x, a[u].y, a[u].z, a[u].w, b[u].x, b[u].y, b[u].z, b[u].w};
+        const uint32_t o = (uint32_t)(c8 >> 3) * (uint32_t)R * 128u + sw128_offset((uint32_t)r, (uint32_t)(c8 & 7) * 8u);
+        const uint4 oh = *reinterpret_cast<const uint4 *>(hi + o), ol = *reinterpret_cast<const uint4 *>(lo + o);
+        const uint32_t hw[4] = {oh.x, oh.y, oh.z, oh.w}, lw[4] = {ol.x, ol.y, ol.z, ol.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 h2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&hw[e]));
+            const float2 l2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&lw[e]));
+            dot += v[2 * e] * (h2.x + l2.x) + v[2 * e + 1] * (h2.y + l2.y);
+        }
+        put8(hi, lo, R, r, c8, v);
+    }
+    return dot;
+}
+
+// bf16 [R][C] (row stride ld elements) -> one tile; rows >= valid are zero (loads batched as above)
+template <int R, int C>
+__device__ __forceinline__ void stage_bf16(uint8_t *dst, const __nv_bfloat16 *src, int64_t ld, int valid)
+{
+    constexpr int per_row = C / 8, NI = R * per_row / kBT;
+    static_assert(NI * kBT == R * per_row, "whole chunks per thread");
+    uint4 w[NI];
+#pragma unroll
+    for (int u = 0; u < NI; ++u) {
+        const int id = threadIdx.x + u * kBT, r = id / per_row, c8 = id % per_row;
+        w[u] = r < valid ? *reinterpret_cast<const uint4 *>(src + r * ld + 8 * c8) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < NI; ++u) {
+        const int id = threadIdx.x + u * kBT, r = id / per_row, c8 = id % per_row;
+        const uint32_t o = (uint32_t)(c8 >> 3) * (uint32_t)R * 128u + sw128_offset((uint32_t)r, (uint32_t)(c8 & 7) * 8u);
+        *reinterpret_cast<uint4 *>(dst + o) = w[u];
+    }
+}
+
+// K-step ks (16 elements of K) of a tile of R rows read as a K-major operand (K along the columns)
+__device__ __forceinline__ uint64_t kmaj(uint32_t base, int R, int ks)
+{
+    return smem_desc(base + (uint32_t)(ks >> 2) * (uint32_t)R * 128u + (uint32_t)(ks & 3) * 32u, 16, 1024);
+}
+// K-step ks of a tile of R rows read as an MN-major operand (K along the rows)
+__device__ __forceinline__ uint64_t mnmaj(uint32_t base, int R, int ks)
+{
+    return smem_desc(base + (uint32_t)ks * 2048u, (uint32_t)R * 128u, 1024);
+}
+}  // namespace lt
+
+template <typename T>
+__global__ void __launch_bounds__(kBT, 1)
+bwd_local_tc_kernel(const BwdParams p)
+{
+    using namespace lt;
+    extern __shared__ uint8_t smraw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sb0 = umma::smem_u32(sm);
+    const Geometry gm = p.gm;
+    constexpr int DK = 128, DV = 128;
+    const int H = gm.H, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t slot = blockIdx.x;
+    int n, c, rows;
+    int64_t tok0;
+    if (!chunk_of(gm, slot, n, c, tok0, rows)) return;
+    const BwdLayout LY = bwd_layout(DK, DV);
+    float *blk = p.ws + (slot * H + h) * LY.total;
+    const float *qh = blk + LY.qh, *kh = blk + LY.kh, *Tm = blk + LY.t, *S = blk + LY.s, *Vn = blk + LY.vn,
+                *dVn = blk + LY.dvn, *dSn = blk + LY.dsn;
+    float *dQ = blk + LY.dqh, *dK = blk + LY.dkh;
+    float *sDA = reinterpret_cast<float *>(sm + FA), *sDT = reinterpret_cast<float *>(sm + FB), *sDL = sDT;
+    float *vec = reinterpret_cast<float *>(sm + VEC);
+    float *sb = vec, *sbe = vec + 64, *sgam = vec + 128, *sfk = vec + 192, *sdgam = vec + 256, *sdkdf = vec + 320,
+          *sdbeta = vec + 384, *st = vec + 448, *sgrow = vec + 512, *sgcol = vec + 576, *sred = vec + 640;   // sred [256]
+    const uint32_t bar = sb0 + MISC, cbar = sb0 + MISC + 16;   // MMA commits; bulk copies
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + MISC + 8);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + MISC + 12);
+    const __nv_bfloat16 *dO = reinterpret_cast<const __nv_bfloat16 *>(p.dout) + (tok0 * H + h) * DV;
+    const __nv_bfloat16 *Vraw = reinterpret_cast<const __nv_bfloat16 *>(p.v) + (tok0 * H + h) * DV;
+    const int64_t tstride = (int64_t)H * DV;   // elements between tokens of dO and v
+
+    if (tid == 0) {
+        umma::mbar_init(bar, 1);
+        umma::mbar_init(cbar, 1);
+        *abort_flag = 0;
+        umma::fence_mbar_init();
+    }
+    if (warp == 0) umma::tmem_alloc(tmem_holder, 512);
+    if (tid < 64) {
+        sb[tid] = blk[LY.b + tid];
+        sbe[tid] = tid < rows ? p.beta[(tok0 + tid) * H + h] : 0.f;
+        sgam[tid] = expf(sb[tid]);
+        sdgam[tid] = 0.f;
+        sdkdf[tid] = 0.f;
+        sdbeta[tid] = 0.f;
+        sgcol[tid] = 0.f;
+    }
+    // phase 1 operands
+    stage_bf16<64, DV>(sm + DO, dO, tstride, rows);
+    stage_f32<64, DV>(sm + VNH, sm + VNL, Vn, DV, 64);
+    stage_f32<64, DV>(sm + DVH, sm + DVL, dVn, DV, 64);
+    stage_f32<DV, DK>(sm + BH, sm + BL, S, DK, DV);
+    umma::fence_proxy_async();
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tm = *tmem_holder;
+    if (tid < 64) sfk[tid] = expf(sb[63] - sb[tid]);   // gC / gam
+    const float gC = expf(sb[63]);
+    uint32_t phase = 0;
+    // bounded wait for the MMAs committed so far; the verdict is the same for every thread
+    auto wait_all = [&]() -> bool {
+        bool ok = umma::mbar_wait(bar, phase, kWaitNs);
+        if (!ok) {
+            *abort_flag = 1;
+            atomicExch(p.err, kDevErrTimeout);
+        }
+        phase ^= 1u;
+        const bool bad = __syncthreads_or(!ok || *abort_flag);
+        umma::fence_after_sync();
+        return !bad;
+    };
+    uint32_t cphase = 0;
+    auto wait_copies = [&]() -> bool {
+        bool ok2 = umma::mbar_wait(cbar, cphase, kWaitNs);
+        if (!ok2) {
+            *abort_flag = 1;
+            atomicExch(p.err, kDevErrTimeout);
+        }
+        cphase ^= 1u;
+        return !__syncthreads_or(!ok2 || *abort_flag);
+    };
+    // one product: nks K-steps, A and B descriptors for (step, lo) via functors; a_exact/b_exact skip lo terms
+    auto mma = [&](uint32_t dcol, int N, bool a_mn, bool b_mn, int nks, auto ad, auto bd, bool a_exact, bool b_exact) {
+        const uint32_t id = idesc_bf16(128, N, a_mn, b_mn);
+        for (int ks = 0; ks < nks; ++ks) {
+            const uint64_t ah = ad(ks, 0), bh = bd(ks, 0);
+            mma_ss(tm + dcol, ah, bh, id, ks > 0 ? 1u : 0u);
+            if (!b_exact) mma_ss(tm + dcol, ah, bd(ks, 1), id, 1u);
+            if (!a_exact) mma_ss(tm + dcol, ad(ks, 1), bh, id, 1u);
+        }
+    };
+    // tensor-memory row of the calling warp (warps 0, 1, 4, 5): 16 x n16 columns from col
+    const int q4 = warp & 3, half = warp >> 2, row = 32 * q4 + lane;
+    const bool reader = q4 < 2;
+    auto ld_row = [&](uint32_t col, uint32_t (&u)[64], int n16) {
+        const uint32_t a = tm + ((uint32_t)(32 * q4) << 16) + col;
+        for (int i = 0; i < n16; ++i) umma::tmem_ld16(a + 16 * i, *reinterpret_cast<uint32_t(*)[16]>(u + 16 * i));
+        umma::tmem_wait_ld();
+    };
+    auto f = [](uint32_t u) { return __uint_as_float(u); };
+    const uint32_t C1a = 0, C1b = 128, C3 = 256, C4 = 384;
+
+    // ---- phase 1: dQd = dO S, dW' = dV_new S, dA = dO V_new^T; then dKd = V_new dS'
+    if (tid == 0) {
+        mma(C1a, 128, false, true, 8, [&](int ks, int) { return kmaj(sb0 + DO, 64, ks); },
+            [&](int ks, int lo) { return mnmaj(sb0 + (lo ? BL : BH), 128, ks); }, true, false);
+        mma(C1b, 128, false, true, 8, [&](int ks, int lo) { return kmaj(sb0 + (lo ? DVL : DVH), 64, ks); },
+            [&](int ks, int lo) { return mnmaj(sb0 + (lo ? BL : BH), 128, ks); }, false, false);
+        mma(C4, 64, false, false, 8, [&](int ks, int) { return kmaj(sb0 + DO, 64, ks); },
+            [&](int ks, int lo) { return kmaj(sb0 + (lo ? VNL : VNH), 64, ks); }, true, false);
+        umma::commit(bar);
+    }
+    bool ok = wait_all();
+    if (ok) {
+        // dS' over S; dgC = <dS', S> on the way (S read back from its tiles)
+        sred[tid] = stage_f32_dot_old<DV, DK>(sm + BH, sm + BL, dSn, DK);
+        umma::fence_proxy_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
+        if (tid == 0) {
+            mma(C3, 128, false, true, 8, [&](int ks, int lo) { return kmaj(sb0 + (lo ? VNL : VNH), 64, ks); },
+                [&](int ks, int lo) { return mnmaj(sb0 + (lo ? BL : BH), 128, ks); }, false, false);
+            umma::commit(bar);
+        }
+        // while it runs: dQ = gam dQd (dgam += Q^ . dQd) and dA, from columns this warp's half owns
+        if (reader) {
+            uint32_t u[64];
+            ld_row(C1a + 64 * half, u, 4);
+            float acc = 0.f;
+            const float g = sgam[row];
+#pragma unroll
+            for (int e = 0; e < 64; e += 4) {
+                const int d = 64 * half + e;
+                const float4 qv = *reinterpret_cast<const float4 *>(qh + row * DK + d);
+                acc += qv.x * f(u[e]) + qv.y * f(u[e + 1]) + qv.z * f(u[e + 2]) + qv.w * f(u[e + 3]);
+                *reinterpret_cast<float4 *>(dQ + row * DK + d) =
+                    make_float4(g * f(u[e]), g * f(u[e + 1]), g * f(u[e + 2]), g * f(u[e + 3]));
+            }
+            atomicAdd(&sdgam[row], acc);
+            ld_row(C4 + 32 * half, u, 2);
+            for (int e = 0; e < 32; ++e) {
+                const int i = 32 * half + e;
+                sDA[row * 64 + i] = i <= row ? f(u[e]) : 0.f;
+            }
+        }
+        ok = wait_all();
+    }
+    if (ok) {
+        // dK = fk dKd (dkdf += K^ . dKd); dW = -dW' into its tiles over dS'
+        if (reader) {
+            uint32_t u[64];
+            ld_row(C3 + 64 * half, u, 4);
+            float acc = 0.f;
+            const float fk = sfk[row];
+#pragma unroll
+            for (int e = 0; e < 64; e += 4) {
+                const int d = 64 * half + e;
+                const float4 kv = *reinterpret_cast<const float4 *>(kh + row * DK + d);
+                acc += kv.x * f(u[e]) + kv.y * f(u[e + 1]) + kv.z * f(u[e + 2]) + kv.w * f(u[e + 3]);
+                *reinterpret_cast<float4 *>(dK + row * DK + d) =
+                    make_float4(fk * f(u[e]), fk * f(u[e + 1]), fk * f(u[e + 2]), fk * f(u[e + 3]));
+            }
+            atomicAdd(&sdkdf[row], acc);
+            ld_row(C1b + 64 * half, u, 4);
+            for (int c8 = 0; c8 < 8; ++c8) {
+                float v[8];
+                for (int e = 0; e < 8; ++e) v[e] = -f(u[8 * c8 + e]);
+                put8(sm + BH, sm + BH + 16384, 64, row, 8 * half + c8, v);
+            }
+        }
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    if (*abort_flag) goto done;
+    // phase 2 operands: T, K^ (over V_new) and V (bf16, over dS' lo)
+    stage_f32<64, 64>(sm + TT, sm + TT + 8192, Tm, 64, 64);
+    stage_f32<64, DK>(sm + VNH, sm + VNL, kh, DK, 64);
+    stage_bf16<64, DV>(sm + BL, Vraw, tstride, rows);
+    umma::fence_proxy_async();
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    {
+        // ---- phase 2: T^T dV_new, T^T dW, dV_new V^T, dW K^^T
+        const uint32_t C5a = 0, C5b = 128, C6a = 256, C6b = 320;
+        if (tid == 0) {
+            mma(C5a, 128, true, true, 4, [&](int ks, int lo) { return mnmaj(sb0 + TT + (lo ? 8192u : 0u), 64, ks); },
+                [&](int ks, int lo) { return mnmaj(sb0 + (lo ? DVL : DVH), 64, ks); }, false, false);
+            mma(C5b, 128, true, true, 4, [&](int ks, int lo) { return mnmaj(sb0 + TT + (lo ? 8192u : 0u), 64, ks); },
+                [&](int ks, int lo) { return mnmaj(sb0 + BH + (lo ? 16384u : 0u), 64, ks); }, false, false);
+            mma(C6a, 64, false, false, 8, [&](int ks, int lo) { return kmaj(sb0 + (lo ? DVL : DVH), 64, ks); },
+                [&](int ks, int) { return kmaj(sb0 + BL, 64, ks); }, false, true);
+            mma(C6b, 64, false, false, 8, [&](int ks, int lo) { return kmaj(sb0 + BH + (lo ? 16384u : 0u), 64, ks); },
+                [&](int ks, int lo) { return kmaj(sb0 + (lo ? VNL : VNH), 64, ks); }, false, false);
+            umma::commit(bar);
+        }
+        if (!wait_all()) goto done;
+        if (reader) {
+            const int i = row;
+            uint32_t u[64];
+            // dv = beta T^T dV_new,  dbeta += (T^T dV_new) . V
+            ld_row(C5a + 64 * half, u, 4);
+            float db = 0.f;
+            {   // dv row i into a bf16 [64][136] staging tile over dV_new (copied out coalesced below; the
+                // 8-element pad spreads the rows a warp writes over the banks)
+                __nv_bfloat16 *dvs = reinterpret_cast<__nv_bfloat16 *>(sm + DVH) + i * (DV + 8) + 64 * half;
+#pragma unroll
+                for (int e = 0; e < 64; e += 2) {
+                    const int j = 64 * half + e;
+                    *reinterpret_cast<__nv_bfloat162 *>(dvs + e) =
+                        __floats2bfloat162_rn(sbe[i] * f(u[e]), sbe[i] * f(u[e + 1]));
+                    const __nv_bfloat162 vb = *reinterpret_cast<const __nv_bfloat162 *>(
+                        sm + BL + (uint32_t)(j >> 6) * 8192u + sw128_offset((uint32_t)i, (uint32_t)(j & 63)));
+                    const float2 v2 = __bfloat1622float2(vb);
+                    db += f(u[e]) * v2.x + f(u[e + 1]) * v2.y;
+                }
+            }
+            // dK += beta gam T^T dW,  dbeta += gam (T^T dW) . K^,  dgam += beta (T^T dW) . K^
+            ld_row(C5b + 64 * half, u, 4);
+            float tk = 0.f;
+            const float bg = sbe[i] * sgam[i];
+#pragma unroll
+            for (int e = 0; e < 64; e += 4) {
+                const int d = 64 * half + e;
+                const float4 kv = *reinterpret_cast<const float4 *>(kh + i * DK + d);
+                float4 dk4 = *reinterpret_cast<float4 *>(dK + i * DK + d);
+                dk4.x += bg * f(u[e]); dk4.y += bg * f(u[e + 1]); dk4.z += bg * f(u[e + 2]); dk4.w += bg * f(u[e + 3]);
+                *reinterpret_cast<float4 *>(dK + i * DK + d) = dk4;
+                tk += f(u[e]) * kv.x + f(u[e + 1]) * kv.y + f(u[e + 2]) * kv.z + f(u[e + 3]) * kv.w;
+            }
+            atomicAdd(&sdbeta[i], db + sgam[i] * tk);
+            atomicAdd(&sdgam[i], sbe[i] * tk);
+            // dT = dV_new (diag(beta) V)^T + dW (diag(beta gam) K^)^T, columns j of this warp's half
+            uint32_t w[64];
+            ld_row(C6a + 32 * half, u, 2);
+            ld_row(C6b + 32 * half, w, 2);
+            for (int e = 0; e < 32; ++e) {
+                const int j = 32 * half + e;
+                sDT[i * 64 + j] = sbe[j] * f(u[e]) + sbe[j] * sgam[j] * f(w[e]);
+            }
+        }
+        umma::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {   // K^K^T, Q^K^T for the 64 x 64 pass: bulk copies into the dead dW tiles
+            umma::mbar_expect_tx(cbar, 32768);
+            umma::bulk_load(sb0 + BH, blk + LY.kk, 16384, cbar);
+            umma::bulk_load(sb0 + BH + 16384, blk + LY.qk, 16384, cbar);
+        }
+        {   // dv: the staged rows out in 16-B pieces, a warp covering two rows
+            const __nv_bfloat16 *dvs = reinterpret_cast<const __nv_bfloat16 *>(sm + DVH);
+            T *dvo = reinterpret_cast<T *>(p.dv) + (tok0 * H + h) * DV;
+#pragma unroll
+            for (int u4 = 0; u4 < 4; ++u4) {
+                const int id = tid + u4 * kBT, r = id >> 4, c8 = id & 15;
+                if (r < rows)
+                    *reinterpret_cast<uint4 *>(dvo + (int64_t)r * H * DV + 8 * c8) =
+                        *reinterpret_cast<const uint4 *>(dvs + r * (DV + 8) + 8 * c8);
+            }
+        }
+        __syncthreads();
+        // ---- phase 3: X = T^T dT, then dL = strictLower(-X T^T)
+        stage_f32<64, 64>(sm + DO, sm + DO + 8192, sDT, 64, 64);
+        umma::fence_proxy_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
+        const uint32_t C7 = 0, C8 = 64;
+        if (tid == 0) {
+            mma(C7, 64, true, true, 4, [&](int ks, int lo) { return mnmaj(sb0 + TT + (lo ? 8192u : 0u), 64, ks); },
+                [&](int ks, int lo) { return mnmaj(sb0 + DO + (lo ? 8192u : 0u), 64, ks); }, false, false);
+            umma::commit(bar);
+        }
+        if (!wait_all()) goto done;
+        if (reader) {   // X row i, this warp's 32 columns -> X tiles (K-major [i][r])
+            uint32_t u[64];
+            ld_row(C7 + 32 * half, u, 2);
+            for (int c8 = 0; c8 < 4; ++c8) {
+                float v[8];
+                for (int e = 0; e < 8; ++e) v[e] = f(u[8 * c8 + e]);
+                put8(sm + BL + 16384, sm + BL + 16384 + 8192, 64, row, 4 * half + c8, v);
+            }
+        }
+        umma::fence_proxy_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
+        if (tid == 0) {
+            mma(C8, 64, false, false, 4, [&](int ks, int lo) { return kmaj(sb0 + BL + 16384 + (lo ? 8192u : 0u), 64, ks); },
+                [&](int ks, int lo) { return kmaj(sb0 + TT + (lo ? 8192u : 0u), 64, ks); }, false, false);
+            umma::commit(bar);
+        }
+        if (!wait_all()) goto done;
+        if (reader) {
+            uint32_t u[64];
+            ld_row(C8 + 32 * half, u, 2);
+            for (int e = 0; e < 32; ++e) {
+                const int j = 32 * half + e;
+                sDL[row * 64 + j] = j < row ? -f(u[e]) : 0.f;
+            }
+        }
+        __syncthreads();
+        // ---- the 64 x 64 pass (as bwd_local_kernel): GG's row and column sums, dbeta, dA o Gamma, M
+        {
+            if (!wait_copies()) goto done;
+            const float *KK = reinterpret_cast<const float *>(sm + BH), *QK = reinterpret_cast<const float *>(sm + BH + 16384);
+            float gcol[2] = {0.f, 0.f};
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr) {
+                const int r = warp * 8 + rr;
+                float db = 0.f, grow = 0.f;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int i = lane + 32 * h2, e = r * 64 + i;
+                    const float G = i <= r ? expf(sb[r] - sb[i]) : 0.f, dl = sDL[e], da = sDA[e], kk = KK[e];
+                    const float gg = G * (dl * sbe[r] * kk + da * QK[e]);
+                    grow += gg;
+                    gcol[h2] += gg;
+                    if (i < r) db += dl * G * kk;
+                    sDA[e] = da * G;
+                    sDL[e] = dl * sbe[r] * G;
+                }
+                db = warp_sum(db);
+                grow = warp_sum(grow);
+                if (lane == 0) {
+                    sdbeta[r] += db;
+                    sgrow[r] = grow;
+                }
+            }
+            atomicAdd(&sgcol[lane], gcol[0]);
+            atomicAdd(&sgcol[lane + 32], gcol[1]);
+        }
+        __syncthreads();
+        // ---- phase 4: dQ += (dA o Gamma) K^;  dK += (dA o Gamma)^T Q^ + M K^ + M^T K^
+        stage_f32<64, 64>(sm + DVH, sm + DVH + 8192, sDA, 64, 64);   // dA o Gamma [r][i]
+        stage_f32<64, 64>(sm + DO, sm + DO + 8192, sDL, 64, 64);     // M [i][j]
+        stage_f32<64, DK>(sm + BH, sm + BH + 16384, qh, DK, 64);     // Q^ over dW
+        umma::fence_proxy_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
+        const uint32_t C9 = 0, C10 = 128;
+        if (tid == 0) {
+            // K^ [i][d] as MN-major B (K = i), at VNH / VNL
+            auto khB = [&](int ks, int lo) { return mnmaj(sb0 + (lo ? VNL : VNH), 64, ks); };
+            mma(C9, 128, false, true, 4, [&](int ks, int lo) { return kmaj(sb0 + DVH + (lo ? 8192u : 0u), 64, ks); },
+                khB, false, false);
+            const uint32_t id = idesc_bf16(128, 128, true, true), idk = idesc_bf16(128, 128, false, true);
+            for (int ks = 0; ks < 4; ++ks) {   // (dA o Gamma)^T Q^: A MN-major from the [r][i] tile, K = r
+                const uint64_t ah = mnmaj(sb0 + DVH, 64, ks), al = mnmaj(sb0 + DVH + 8192, 64, ks);
+                const uint64_t bh = mnmaj(sb0 + BH, 64, ks), bl = mnmaj(sb0 + BH + 16384, 64, ks);
+                mma_ss(tm + C10, ah, bh, id, ks > 0 ? 1u : 0u);
+                mma_ss(tm + C10, ah, bl, id, 1u);
+                mma_ss(tm + C10, al, bh, id, 1u);
+            }
+            for (int ks = 0; ks < 4; ++ks) {   // M K^: A K-major [i][j], K = j
+                const uint64_t ah = kmaj(sb0 + DO, 64, ks), al = kmaj(sb0 + DO + 8192, 64, ks);
+                const uint64_t bh = khB(ks, 0), bl = khB(ks, 1);
+                mma_ss(tm + C10, ah, bh, idk, 1u);
+                mma_ss(tm + C10, ah, bl, idk, 1u);
+                mma_ss(tm + C10, al, bh, idk, 1u);
+            }
+            for (int ks = 0; ks < 4; ++ks) {   // M^T K^: A MN-major from the [j][i] tile, K = j
+                const uint64_t ah = mnmaj(sb0 + DO, 64, ks), al = mnmaj(sb0 + DO + 8192, 64, ks);
+                const uint64_t bh = khB(ks, 0), bl = khB(ks, 1);
+                mma_ss(tm + C10, ah, bh, id, 1u);
+                mma_ss(tm + C10, ah, bl, id, 1u);
+                mma_ss(tm + C10, al, bh, id, 1u);
+            }
+            umma::commit(bar);
+        }
+        if (!wait_all()) goto done;
+        if (warp == 0) {   // q and k rows of the chunk for the normalisation: bulk copies over T and the dA staging
+            if (lane == 0) umma::mbar_expect_tx(cbar, (uint32_t)(2 * rows * DK * 2));
+            __syncwarp();
+            for (int r = lane; r < rows; r += 32) {
+                const int64_t th = (tok0 + r) * H + h;
+                umma::bulk_load(sb0 + TT + (uint32_t)r * 256u, reinterpret_cast<const T *>(p.q) + th * DK, 256, cbar);
+                umma::bulk_load(sb0 + FA + (uint32_t)r * 256u, reinterpret_cast<const T *>(p.k) + th * DK, 256, cbar);
+            }
+        }
+        // the finished dQ and dK rows, fp32 [64][132] each (33 KB: VNH .. DVH + 1 KB and BH .. BL + 1 KB; a
+        // 4-float pad so the rows a warp reads start in different banks), over tiles no product reads any more
+        float *fQ = reinterpret_cast<float *>(sm + VNH), *fK = reinterpret_cast<float *>(sm + BH);
+        constexpr int PF = DK + 4;
+        if (reader) {
+            uint32_t u[64];
+            ld_row(C9 + 64 * half, u, 4);
+#pragma unroll
+            for (int e = 0; e < 64; e += 4) {
+                const int d = 64 * half + e;
+                float4 a = *reinterpret_cast<float4 *>(dQ + row * DK + d);
+                a.x += f(u[e]); a.y += f(u[e + 1]); a.z += f(u[e + 2]); a.w += f(u[e + 3]);
+                *reinterpret_cast<float4 *>(fQ + row * PF + d) = a;
+            }
+            ld_row(C10 + 64 * half, u, 4);
+#pragma unroll
+            for (int e = 0; e < 64; e += 4) {
+                const int d = 64 * half + e;
+                float4 a = *reinterpret_cast<float4 *>(dK + row * DK + d);
+                a.x += f(u[e]); a.y += f(u[e + 1]); a.z += f(u[e + 2]); a.w += f(u[e + 3]);
+                *reinterpret_cast<float4 *>(fK + row * PF + d) = a;
+            }
+        }
+        __syncthreads();
+        for (int off = kBT / 2; off > 0; off >>= 1) {
+            if (tid < off) sred[tid] += sred[tid + off];
+            __syncthreads();
+        }
+        const float dgC = sred[0];
+        if (tid < 64) {
+            const int r = tid;
+            const float t = sdkdf[r] * sfk[r];
+            st[r] = t;
+            sb[r] = sgrow[r] - sgcol[r] + sdgam[r] * sgam[r] - t;   // sb is no longer needed as b
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float tsum = 0.f;
+            for (int r = 0; r < 64; ++r) tsum += st[r];
+            sb[63] += tsum + dgC * gC;
+            float acc = 0.f;
+            for (int r = 63; r >= 0; --r) { acc += sb[r]; sb[r] = acc; }
+        }
+        __syncthreads();
+        if (tid < rows) {
+            const int64_t th = (tok0 + tid) * H + h;
+            p.dg[th] = sb[tid];
+            p.dbeta[th] = sdbeta[tid];
+        }
+        // dq, dk through the normalisations (and scale on q): one warp per row, the q and k rows of
+        // all the warp's rows loaded first
+        if (!wait_copies()) goto done;
+        {
+            const T *sq_rows = reinterpret_cast<const T *>(sm + TT), *sk_rows = reinterpret_cast<const T *>(sm + FA);
+            float qv[8][4], kv[8][4];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int r = min(warp + 8 * m, 63);
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const int d = lane + 32 * x;
+                    qv[m][x] = to_f32(sq_rows[r * DK + d]);
+                    kv[m][x] = to_f32(sk_rows[r * DK + d]);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int r = warp + 8 * m;
+                if (r >= rows) continue;
+                const int64_t th = (tok0 + r) * H + h;
+                float sq = 0.f, sk = 0.f, qd = 0.f, kd = 0.f;
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const int d = lane + 32 * x;
+                    sq += qv[m][x] * qv[m][x]; sk += kv[m][x] * kv[m][x];
+                    qd += qv[m][x] * fQ[r * PF + d]; kd += kv[m][x] * fK[r * PF + d];
+                }
+                sq = warp_sum(sq); sk = warp_sum(sk); qd = warp_sum(qd); kd = warp_sum(kd);
+                const float rq = p.l2 ? rsqrtf(sq + kL2Eps) : 1.f, rk = p.l2 ? rsqrtf(sk + kL2Eps) : 1.f;
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const int d = lane + 32 * x;
+                    const float gq = p.l2 ? p.scale * (rq * fQ[r * PF + d] - rq * rq * rq * qd * qv[m][x])
+                                          : p.scale * fQ[r * PF + d];
+                    const float gk = p.l2 ? rk * fK[r * PF + d] - rk * rk * rk * kd * kv[m][x] : fK[r * PF + d];
+                    reinterpret_cast<T *>(p.dq)[th * DK + d] = from_f32<T>(gq);
+                    reinterpret_cast<T *>(p.dk)[th * DK + d] = from_f32<T>(gk);
+                }
+            }
+        }
+    }
+done:
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    if (warp == 0) umma::tmem_dealloc(tm, 512);
+}
+
 template <typename T>
 cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t st)
 {
@@ -706,6 +1336,7 @@ cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t st)
     p.init_state = a.init_state; p.dfinal = a.dfinal;
     p.dq = a.dq; p.dk = a.dk; p.dv = a.dv; p.dg = a.dg; p.dbeta = a.dbeta; p.dinit = a.dinit;
     p.ws = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(a.workspace) + 256);
+    p.err = reinterpret_cast<unsigned *>(a.workspace);
     const bool tc_scan = a.dt == 1 && chunk_tc_supported(1, a.gm.dk, a.gm.dv, (int64_t)a.gm.B * a.gm.T);
     p.need_u = tc_scan ? 0 : 1;
     p.gm = a.gm; p.scale = a.scale; p.l2 = a.l2;
@@ -743,7 +1374,16 @@ cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t st)
         bwd_fwd_scan_kernel<<<sgrid, kBT, sm_scan, st>>>(p);
     }
     bwd_bwd_scan_kernel<T><<<sgrid, kBT, sm_scan, st>>>(p);
-    if (a.slots > 0) bwd_local_kernel<T><<<dim3((unsigned)a.slots, a.gm.H), kBT, sm_local, st>>>(p);
+    if (a.slots > 0) {
+        if (a.dt == 1 && a.gm.dk == 128 && a.gm.dv == 128) {
+            if ((e = cudaFuncSetAttribute(bwd_local_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)lt::kSmem)))
+                return e;
+            bwd_local_tc_kernel<T><<<dim3((unsigned)a.slots, a.gm.H), kBT, lt::kSmem, st>>>(p);
+        } else {
+            bwd_local_kernel<T><<<dim3((unsigned)a.slots, a.gm.H), kBT, sm_local, st>>>(p);
+        }
+    }
     return cudaGetLastError();
 }
 
