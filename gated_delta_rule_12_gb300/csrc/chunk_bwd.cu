@@ -1328,6 +1328,233 @@ done:
     if (warp == 0) umma::tmem_dealloc(tm, 512);
 }
 
+// ---------------------------------------------------------------------------
+// bwd_scan_tc_kernel: the reverse scan on the tensor cores, for bf16 inputs with dk = 128 and dv a
+// multiple of 128.  One CTA per (sequence, head, 128 state rows), chunks in reverse:
+//   save dS' (the gradient of the state after the chunk);
+//   dV_new^T = dS' Kd^T + (A^T dO)^T            (saved as dV_new);
+//   dS = gC dS' + dO^T Qd - dV_new^T W.
+// dS stays in registers, one state row per thread and half of its columns (the rows and columns a
+// warp reads from tensor memory).  Each product reads dS', Kd, -dV_new^T and W from shared memory
+// as bf16 (high, low) pairs and sums high.high + high.low + low.high in the fp32 accumulator.  The
+// next chunk's Kd and W are loaded into registers while a product runs and staged once the product
+// that reads their tiles has finished.
+// ---------------------------------------------------------------------------
+namespace rs {
+constexpr uint32_t SAH = 0, SAL = 32768;        // dS' [128 j][128 d] high, low
+constexpr uint32_t KDH = 65536, KDL = 81920;    // Kd [64 r][128 d]
+constexpr uint32_t WH = 98304, WL = 114688;     // W [64 r][128 d]
+constexpr uint32_t VAH = 131072, VAL = 147456;  // -dV_new^T [128 j][64 r]
+constexpr uint32_t MISC = 163840;               // mbarrier, tensor-memory base, abort flag
+constexpr uint32_t kSmem = MISC + 64 + 1024;
+constexpr int kRows = 128;                      // state rows per CTA
+
+// an fp32 [64][128] block held in registers between its load and its staging (as stage_f32)
+struct Block64 {
+    float4 a[4], b[4];
+};
+__device__ __forceinline__ void block_load(Block64 &t, const float *src)
+{
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int id = threadIdx.x + u * kBT, r = id >> 4, c8 = id & 15;
+        t.a[u] = *reinterpret_cast<const float4 *>(src + r * 128 + 8 * c8);
+        t.b[u] = *reinterpret_cast<const float4 *>(src + r * 128 + 8 * c8 + 4);
+    }
+}
+__device__ __forceinline__ void block_put(uint8_t *hi, uint8_t *lo, const Block64 &t)
+{
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int id = threadIdx.x + u * kBT, r = id >> 4, c8 = id & 15;
+        const float v[8] = {t.a[u].x, t.a[u].y, t.a[u].z, t.a[u].w, t.b[u].x, t.b[u].y, t.b[u].z, t.b[u].w};
+        lt::put8(hi, lo, 64, r, c8, v);
+    }
+}
+}  // namespace rs
+
+template <typename T>
+__global__ void __launch_bounds__(kBT, 1)
+bwd_scan_tc_kernel(const BwdParams p)
+{
+    using namespace rs;
+    extern __shared__ uint8_t smraw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sb0 = umma::smem_u32(sm);
+    const Geometry gm = p.gm;
+    constexpr int DK = 128;
+    const int H = gm.H, dv = gm.dv, n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5,
+              lane = tid & 31;
+    const int j0 = blockIdx.z * kRows;
+    const int q4 = warp & 3, half = warp >> 2, j = 32 * q4 + lane;   // this thread's state row and column half
+    const BwdLayout LY = bwd_layout(DK, dv);
+    int64_t tok0;
+    int len;
+    seq_span(gm, n, tok0, len);
+    const int nch = ceil_div(len, kChunk);
+    const int64_t slot0 = slot_base(gm, n);
+    const int64_t soff = (((int64_t)n * H + h) * dv + j0 + j) * DK + 64 * half;   // in a [N][H][dv][dk] state
+
+    float dS[64];
+#pragma unroll
+    for (int e = 0; e < 64; e += 4) {
+        const float4 x = p.dfinal ? *reinterpret_cast<const float4 *>(p.dfinal + soff + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        dS[e] = x.x; dS[e + 1] = x.y; dS[e + 2] = x.z; dS[e + 3] = x.w;
+    }
+    if (nch == 0) {   // an empty sequence: the state gradient passes through
+        if (p.dinit)
+#pragma unroll
+            for (int e = 0; e < 64; e += 4)
+                *reinterpret_cast<float4 *>(p.dinit + soff + e) = make_float4(dS[e], dS[e + 1], dS[e + 2], dS[e + 3]);
+        return;
+    }
+    const uint32_t bar = sb0 + MISC;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + MISC + 8);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + MISC + 12);
+    if (tid == 0) {
+        umma::mbar_init(bar, 1);
+        *abort_flag = 0;
+        umma::fence_mbar_init();
+    }
+    if (warp == 0) umma::tmem_alloc(tmem_holder, 256);
+    {   // the last chunk's Kd and W
+        const float *blk = p.ws + ((slot0 + nch - 1) * H + h) * LY.total;
+        Block64 t;
+        block_load(t, blk + LY.kd);
+        block_put(sm + KDH, sm + KDL, t);
+        block_load(t, blk + LY.w);
+        block_put(sm + WH, sm + WL, t);
+    }
+    umma::fence_proxy_async();
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tm = *tmem_holder;
+    const uint32_t D1 = 0, D2 = 128;   // dV_new^T [128 j][64 r];  dO^T Qd - dV_new^T W [128 j][128 d]
+    const uint32_t trow = tm + ((uint32_t)(32 * q4) << 16);
+    uint32_t phase = 0;
+    auto wait_mma = [&]() -> bool {   // bounded; the verdict is the same for every thread
+        const bool ok = umma::mbar_wait(bar, phase, lt::kWaitNs);
+        if (!ok) {
+            *abort_flag = 1;
+            atomicExch(p.err, kDevErrTimeout);
+        }
+        phase ^= 1u;
+        const bool bad = __syncthreads_or(!ok || *abort_flag);
+        umma::fence_after_sync();
+        return !bad;
+    };
+    auto mma3 = [&](uint32_t dcol, int N, bool b_mn, int nks, auto ad, auto bd) {
+        const uint32_t id = umma::idesc_bf16(128, N, false, b_mn);
+        for (int ks = 0; ks < nks; ++ks) {
+            const uint64_t ah = ad(ks, 0), bh = bd(ks, 0);
+            umma::mma_ss(tm + dcol, ah, bh, id, ks > 0 ? 1u : 0u);
+            umma::mma_ss(tm + dcol, ah, bd(ks, 1), id, 1u);
+            umma::mma_ss(tm + dcol, ad(ks, 1), bh, id, 1u);
+        }
+    };
+    auto f = [](uint32_t u) { return __uint_as_float(u); };
+
+    bool ok = true;
+    for (int c = nch - 1; c >= 0 && ok; --c) {
+        float *blk = p.ws + ((slot0 + c) * H + h) * LY.total;
+        const float *nblk = p.ws + ((slot0 + (c > 0 ? c - 1 : 0)) * H + h) * LY.total;
+        {   // dS' saved for the local kernel and staged for the first product
+            float *dsn = blk + LY.dsn + (int64_t)(j0 + j) * DK + 64 * half;
+#pragma unroll
+            for (int e = 0; e < 64; e += 4)
+                *reinterpret_cast<float4 *>(dsn + e) = make_float4(dS[e], dS[e + 1], dS[e + 2], dS[e + 3]);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float v[8] = {dS[8 * q], dS[8 * q + 1], dS[8 * q + 2], dS[8 * q + 3],
+                                    dS[8 * q + 4], dS[8 * q + 5], dS[8 * q + 6], dS[8 * q + 7]};
+                lt::put8(sm + SAH, sm + SAL, kRows, j, 8 * half + q, v);
+            }
+        }
+        umma::fence_proxy_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
+        if (tid == 0) {   // dS' Kd^T: A [128 j][128 d] K-major, B [64 r][128 d] K-major
+            mma3(D1, 64, false, 8, [&](int ks, int lo) { return lt::kmaj(sb0 + (lo ? SAL : SAH), kRows, ks); },
+                 [&](int ks, int lo) { return lt::kmaj(sb0 + (lo ? KDL : KDH), 64, ks); });
+            umma::commit(bar);
+        }
+        // while it runs: this thread's 32 entries of A^T dO, and the next chunk's Kd
+        float ado[32];
+        {
+            const float *a0 = blk + LY.ado + j0 + j + (int64_t)(32 * half) * dv;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ado[e] = a0[(int64_t)e * dv];
+        }
+        Block64 nxt;
+        if (c > 0) block_load(nxt, nblk + LY.kd);
+        if (!(ok = wait_mma())) break;
+        {   // dV_new^T = dS' Kd^T + (A^T dO)^T: saved as dV_new [r][j], staged negated as A [128 j][64 r]
+            uint32_t u[32];
+            umma::tmem_ld16(trow + D1 + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(u));
+            umma::tmem_ld16(trow + D1 + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16));
+            umma::tmem_wait_ld();
+            float *dvn = blk + LY.dvn + j0 + j + (int64_t)(32 * half) * dv;
+            float x[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                x[e] = f(u[e]) + ado[e];
+                dvn[(int64_t)e * dv] = x[e];
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float v[8] = {-x[8 * q], -x[8 * q + 1], -x[8 * q + 2], -x[8 * q + 3],
+                                    -x[8 * q + 4], -x[8 * q + 5], -x[8 * q + 6], -x[8 * q + 7]};
+                lt::put8(sm + VAH, sm + VAL, kRows, j, 4 * half + q, v);
+            }
+        }
+        if (c > 0) block_put(sm + KDH, sm + KDL, nxt);   // the first product is done with Kd
+        umma::fence_proxy_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
+        if (tid == 0) {   // -dV_new^T W: A [128 j][64 r] K-major, B [64 r][128 d] MN-major
+            mma3(D2, 128, true, 4, [&](int ks, int lo) { return lt::kmaj(sb0 + (lo ? VAL : VAH), kRows, ks); },
+                 [&](int ks, int lo) { return lt::mnmaj(sb0 + (lo ? WL : WH), 64, ks); });
+            umma::commit(bar);
+        }
+        // while it runs: this thread's part of dO^T Qd, the chunk's decay and the next chunk's W
+        float4 dq[16];
+        {
+            const float *d0 = blk + LY.doq + (int64_t)(j0 + j) * DK + 64 * half;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) dq[e] = *reinterpret_cast<const float4 *>(d0 + 4 * e);
+        }
+        const float gC = expf(blk[LY.b + 63]);
+        if (c > 0) block_load(nxt, nblk + LY.w);
+        if (!(ok = wait_mma())) break;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {   // dS = gC dS' + dO^T Qd - dV_new^T W
+            uint32_t u[16];
+            umma::tmem_ld16(trow + D2 + 64 * half + 16 * i, u);
+            umma::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+                const float4 a = dq[(16 * i + e) >> 2];
+                dS[16 * i + e] = gC * dS[16 * i + e] + a.x + f(u[e]);
+                dS[16 * i + e + 1] = gC * dS[16 * i + e + 1] + a.y + f(u[e + 1]);
+                dS[16 * i + e + 2] = gC * dS[16 * i + e + 2] + a.z + f(u[e + 2]);
+                dS[16 * i + e + 3] = gC * dS[16 * i + e + 3] + a.w + f(u[e + 3]);
+            }
+        }
+        if (c > 0) block_put(sm + WH, sm + WL, nxt);   // the second product is done with W
+    }
+    if (ok && p.dinit)
+#pragma unroll
+        for (int e = 0; e < 64; e += 4)
+            *reinterpret_cast<float4 *>(p.dinit + soff + e) = make_float4(dS[e], dS[e + 1], dS[e + 2], dS[e + 3]);
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    if (warp == 0) umma::tmem_dealloc(tm, 256);
+}
+
 template <typename T>
 cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t st)
 {
@@ -1373,7 +1600,14 @@ cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t st)
     } else {
         bwd_fwd_scan_kernel<<<sgrid, kBT, sm_scan, st>>>(p);
     }
-    bwd_bwd_scan_kernel<T><<<sgrid, kBT, sm_scan, st>>>(p);
+    if (tc_scan) {
+        if ((e = cudaFuncSetAttribute(bwd_scan_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)rs::kSmem)))
+            return e;
+        bwd_scan_tc_kernel<T><<<dim3(a.gm.N, a.gm.H, a.gm.dv / rs::kRows), kBT, rs::kSmem, st>>>(p);
+    } else {
+        bwd_bwd_scan_kernel<T><<<sgrid, kBT, sm_scan, st>>>(p);
+    }
     if (a.slots > 0) {
         if (a.dt == 1 && a.gm.dk == 128 && a.gm.dv == 128) {
             if ((e = cudaFuncSetAttribute(bwd_local_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
