@@ -248,6 +248,8 @@ struct BwdParams {
     float *dg, *dbeta, *dinit;
     float *ws;                      // per (slot, head) blocks of BwdLayout
     int need_u;                     // U~ is only read by the CUDA-core forward scan
+    int tc_scan;                    // reverse scan on the tensor cores (bf16, dk = dv = 128): dO^T Qd is
+                                    // stored transposed, [dk][dv], and dS' as bf16 (high, low) tiles
     unsigned *err;                  // device error word (the workspace's first word)
     Geometry gm;
     float scale;
@@ -402,7 +404,10 @@ bwd_prep_kernel(const BwdParams p)
     for (int j0 = 0; j0 < dv; j0 += 64)
         block_gemm_cols<4, false, false>(min(64, dv - j0), dk, 64, [&](int i, int r) { return dOf(r, j0 + i); },
                                          [&](int r, int d) { return qd[r * dk + d]; },
-                                         [&](int i, int d, float x) { blk[LY.doq + (int64_t)(j0 + i) * dk + d] = x; },
+                                         [&](int i, int d, float x) {
+                                             if (p.tc_scan) blk[LY.doq + (int64_t)d * dv + j0 + i] = x;
+                                             else blk[LY.doq + (int64_t)(j0 + i) * dk + d] = x;
+                                         },
                                          sA, sB);
 }
 
@@ -782,36 +787,39 @@ __device__ __forceinline__ void stage_f32(uint8_t *hi, uint8_t *lo, const float 
     }
 }
 
-// stage_f32 over tiles that hold another matrix of the same shape, returning this thread's part of
-// sum(new * old), the old entries read back as hi + lo (about 16 significand bits) before they are
-// overwritten
-template <int R, int C>
-__device__ __forceinline__ float stage_f32_dot_old(uint8_t *hi, uint8_t *lo, const float *src, int ld)
+// bf16 (high, low) tile pairs of BYTES bytes each, stored high then low at src in the layout of the
+// tiles at hi and lo, copied over those tiles; returns this thread's part of sum(new * old), each
+// entry read as high + low (about 16 significand bits).  Consecutive threads take consecutive 16-B
+// pieces, so the global loads coalesce and the shared-memory accesses are conflict-free.
+template <int BYTES>
+__device__ __forceinline__ float copy_pairs_dot_old(uint8_t *hi, uint8_t *lo, const uint8_t *src)
 {
-    constexpr int per_row = C / 8, NI = R * per_row / kBT;
-    static_assert(NI * kBT == R * per_row, "whole chunks per thread");
-    float4 a[NI], b[NI];
+    constexpr int NI = BYTES / 16 / kBT;
+    static_assert(NI * 16 * kBT == BYTES, "whole pieces per thread");
+    uint4 nh[NI], nl[NI];
 #pragma unroll
     for (int u = 0; u < NI; ++u) {
-        const int id = threadIdx.x + u * kBT, r = id / per_row, c8 = id % per_row;
-        a[u] = *reinterpret_cast<const float4 *>(src + (int64_t)r * ld + 8 * c8);
-        b[u] = *reinterpret_cast<const float4 *>(src + (int64_t)r * ld + 8 * c8 + 4);
+        const uint32_t o = (threadIdx.x + u * kBT) * 16u;
+        nh[u] = *reinterpret_cast<const uint4 *>(src + o);
+        nl[u] = *reinterpret_cast<const uint4 *>(src + BYTES + o);
     }
     float dot = 0.f;
 #pragma unroll
     for (int u = 0; u < NI; ++u) {
-        const int id = threadIdx.x + u * kBT, r = id / per_row, c8 = id % per_row;
-        const float v[8] = {a[u].x, a[u].y, a[u].z, a[u].w, b[u].x, b[u].y, b[u].z, b[u].w};
-        const uint32_t o = (uint32_t)(c8 >> 3) * (uint32_t)R * 128u + sw128_offset((uint32_t)r, (uint32_t)(c8 & 7) * 8u);
+        const uint32_t o = (threadIdx.x + u * kBT) * 16u;
         const uint4 oh = *reinterpret_cast<const uint4 *>(hi + o), ol = *reinterpret_cast<const uint4 *>(lo + o);
-        const uint32_t hw[4] = {oh.x, oh.y, oh.z, oh.w}, lw[4] = {ol.x, ol.y, ol.z, ol.w};
+        const uint32_t ohw[4] = {oh.x, oh.y, oh.z, oh.w}, olw[4] = {ol.x, ol.y, ol.z, ol.w};
+        const uint32_t nhw[4] = {nh[u].x, nh[u].y, nh[u].z, nh[u].w}, nlw[4] = {nl[u].x, nl[u].y, nl[u].z, nl[u].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float2 h2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&hw[e]));
-            const float2 l2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&lw[e]));
-            dot += v[2 * e] * (h2.x + l2.x) + v[2 * e + 1] * (h2.y + l2.y);
+            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ohw[e]));
+            const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&olw[e]));
+            const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&nhw[e]));
+            const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&nlw[e]));
+            dot += (x.x + y.x) * (a.x + b.x) + (x.y + y.y) * (a.y + b.y);
         }
-        put8(hi, lo, R, r, c8, v);
+        *reinterpret_cast<uint4 *>(hi + o) = nh[u];
+        *reinterpret_cast<uint4 *>(lo + o) = nl[u];
     }
     return dot;
 }
@@ -963,8 +971,8 @@ bwd_local_tc_kernel(const BwdParams p)
     }
     bool ok = wait_all();
     if (ok) {
-        // dS' over S; dgC = <dS', S> on the way (S read back from its tiles)
-        sred[tid] = stage_f32_dot_old<DV, DK>(sm + BH, sm + BL, dSn, DK);
+        // dS' (saved by the reverse scan as bf16 high and low tiles) over S; dgC = <dS', S> on the way
+        sred[tid] = copy_pairs_dot_old<DV * DK * 2>(sm + BH, sm + BL, reinterpret_cast<const uint8_t *>(dSn));
         umma::fence_proxy_async();
         umma::fence_before_sync();
         __syncthreads();
@@ -1338,7 +1346,9 @@ done:
 // warp reads from tensor memory).  Each product reads dS', Kd, -dV_new^T and W from shared memory
 // as bf16 (high, low) pairs and sums high.high + high.low + low.high in the fp32 accumulator.  The
 // next chunk's Kd and W are loaded into registers while a product runs and staged once the product
-// that reads their tiles has finished.
+// that reads their tiles has finished.  dS' is saved by two bulk copies of its staged tiles (the
+// local kernel reads it back in that form), and dO^T Qd is read in its transposed layout, so every
+// global access of the chain is coalesced.
 // ---------------------------------------------------------------------------
 namespace rs {
 constexpr uint32_t SAH = 0, SAL = 32768;        // dS' [128 j][128 d] high, low
@@ -1385,7 +1395,7 @@ bwd_scan_tc_kernel(const BwdParams p)
     constexpr int DK = 128;
     const int H = gm.H, dv = gm.dv, n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5,
               lane = tid & 31;
-    const int j0 = blockIdx.z * kRows;
+    const int j0 = 0;   // dv = 128: one CTA per (sequence, head)
     const int q4 = warp & 3, half = warp >> 2, j = 32 * q4 + lane;   // this thread's state row and column half
     const BwdLayout LY = bwd_layout(DK, dv);
     int64_t tok0;
@@ -1459,11 +1469,7 @@ bwd_scan_tc_kernel(const BwdParams p)
     for (int c = nch - 1; c >= 0 && ok; --c) {
         float *blk = p.ws + ((slot0 + c) * H + h) * LY.total;
         const float *nblk = p.ws + ((slot0 + (c > 0 ? c - 1 : 0)) * H + h) * LY.total;
-        {   // dS' saved for the local kernel and staged for the first product
-            float *dsn = blk + LY.dsn + (int64_t)(j0 + j) * DK + 64 * half;
-#pragma unroll
-            for (int e = 0; e < 64; e += 4)
-                *reinterpret_cast<float4 *>(dsn + e) = make_float4(dS[e], dS[e + 1], dS[e + 2], dS[e + 3]);
+        {   // dS' staged for the first product (and saved from there)
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const float v[8] = {dS[8 * q], dS[8 * q + 1], dS[8 * q + 2], dS[8 * q + 3],
@@ -1479,6 +1485,11 @@ bwd_scan_tc_kernel(const BwdParams p)
             mma3(D1, 64, false, 8, [&](int ks, int lo) { return lt::kmaj(sb0 + (lo ? SAL : SAH), kRows, ks); },
                  [&](int ks, int lo) { return lt::kmaj(sb0 + (lo ? KDL : KDH), 64, ks); });
             umma::commit(bar);
+            // dS' for the local kernel: its high and low tiles as they are, 32 KB each
+            uint8_t *dsn = reinterpret_cast<uint8_t *>(blk + LY.dsn);
+            umma::bulk_store(dsn, sb0 + SAH, 32768);
+            umma::bulk_store(dsn + 32768, sb0 + SAL, 32768);
+            umma::bulk_commit();
         }
         // while it runs: this thread's 32 entries of A^T dO, and the next chunk's Kd
         float ado[32];
@@ -1519,29 +1530,25 @@ bwd_scan_tc_kernel(const BwdParams p)
                  [&](int ks, int lo) { return lt::mnmaj(sb0 + (lo ? WL : WH), 64, ks); });
             umma::commit(bar);
         }
-        // while it runs: this thread's part of dO^T Qd, the chunk's decay and the next chunk's W
-        float4 dq[16];
+        // while it runs: this thread's part of dO^T Qd (stored [d][j]), the chunk's decay and the next W
+        float dq[64];
         {
-            const float *d0 = blk + LY.doq + (int64_t)(j0 + j) * DK + 64 * half;
+            const float *d0 = blk + LY.doq + (int64_t)(64 * half) * dv + j0 + j;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) dq[e] = *reinterpret_cast<const float4 *>(d0 + 4 * e);
+            for (int e = 0; e < 64; ++e) dq[e] = d0[(int64_t)e * dv];
         }
         const float gC = expf(blk[LY.b + 63]);
         if (c > 0) block_load(nxt, nblk + LY.w);
+        if (tid == 0) umma::bulk_wait_read();   // dS' tiles read out before the next chunk restages them
         if (!(ok = wait_mma())) break;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {   // dS = gC dS' + dO^T Qd - dV_new^T W
-            uint32_t u[16];
-            umma::tmem_ld16(trow + D2 + 64 * half + 16 * i, u);
+        for (int i = 0; i < 2; ++i) {   // dS = gC dS' + dO^T Qd - dV_new^T W
+            uint32_t u[32];
+            umma::tmem_ld16(trow + D2 + 64 * half + 32 * i, *reinterpret_cast<uint32_t(*)[16]>(u));
+            umma::tmem_ld16(trow + D2 + 64 * half + 32 * i + 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16));
             umma::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; e += 4) {
-                const float4 a = dq[(16 * i + e) >> 2];
-                dS[16 * i + e] = gC * dS[16 * i + e] + a.x + f(u[e]);
-                dS[16 * i + e + 1] = gC * dS[16 * i + e + 1] + a.y + f(u[e + 1]);
-                dS[16 * i + e + 2] = gC * dS[16 * i + e + 2] + a.z + f(u[e + 2]);
-                dS[16 * i + e + 3] = gC * dS[16 * i + e + 3] + a.w + f(u[e + 3]);
-            }
+            for (int e = 0; e < 32; ++e) dS[32 * i + e] = gC * dS[32 * i + e] + dq[32 * i + e] + f(u[e]);
         }
         if (c > 0) block_put(sm + WH, sm + WL, nxt);   // the second product is done with W
     }
@@ -1549,6 +1556,7 @@ bwd_scan_tc_kernel(const BwdParams p)
 #pragma unroll
         for (int e = 0; e < 64; e += 4)
             *reinterpret_cast<float4 *>(p.dinit + soff + e) = make_float4(dS[e], dS[e + 1], dS[e + 2], dS[e + 3]);
+    if (tid == 0) umma::bulk_wait_all();
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
@@ -1565,7 +1573,9 @@ cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t st)
     p.ws = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(a.workspace) + 256);
     p.err = reinterpret_cast<unsigned *>(a.workspace);
     const bool tc_scan = a.dt == 1 && chunk_tc_supported(1, a.gm.dk, a.gm.dv, (int64_t)a.gm.B * a.gm.T);
+    const bool tc_local = a.dt == 1 && a.gm.dk == 128 && a.gm.dv == 128;   // implies tc_scan
     p.need_u = tc_scan ? 0 : 1;
+    p.tc_scan = tc_local ? 1 : 0;
     p.gm = a.gm; p.scale = a.scale; p.l2 = a.l2;
     const size_t stage = 2 * (size_t)kStage * sizeof(float);
     const size_t sm_prep = stage + sizeof(float) * (2 * 64 * 65 + 4 * 64);
@@ -1600,16 +1610,16 @@ cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t st)
     } else {
         bwd_fwd_scan_kernel<<<sgrid, kBT, sm_scan, st>>>(p);
     }
-    if (tc_scan) {
+    if (tc_local) {
         if ((e = cudaFuncSetAttribute(bwd_scan_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)rs::kSmem)))
             return e;
-        bwd_scan_tc_kernel<T><<<dim3(a.gm.N, a.gm.H, a.gm.dv / rs::kRows), kBT, rs::kSmem, st>>>(p);
+        bwd_scan_tc_kernel<T><<<dim3(a.gm.N, a.gm.H), kBT, rs::kSmem, st>>>(p);
     } else {
         bwd_bwd_scan_kernel<T><<<sgrid, kBT, sm_scan, st>>>(p);
     }
     if (a.slots > 0) {
-        if (a.dt == 1 && a.gm.dk == 128 && a.gm.dv == 128) {
+        if (tc_local) {
             if ((e = cudaFuncSetAttribute(bwd_local_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)lt::kSmem)))
                 return e;

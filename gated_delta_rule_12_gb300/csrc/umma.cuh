@@ -233,6 +233,19 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
                  :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
+// Plain bulk copy shared -> global, in the issuing thread's bulk async-group.  Both addresses
+// 16-B aligned, size a multiple of 16.  Commit with bulk_commit(); bulk_wait_read() returns once
+// the thread's committed copies have read their shared-memory source, bulk_wait_all() once their
+// writes are done.  Both waits end by themselves: they depend on no other thread or agent.
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(dst), "r"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");
