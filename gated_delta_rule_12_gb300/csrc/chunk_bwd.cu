@@ -764,7 +764,7 @@ __device__ __forceinline__ void put8(uint8_t *hi, uint8_t *lo, int R, int r, int
 // Each thread takes R C / (8 kBT) chunks of 8 columns and issues all their loads before the first
 // conversion, so the staging waits on one memory latency, not one per chunk.
 template <int R, int C>
-__device__ __forceinline__ void stage_f32(uint8_t *hi, uint8_t *lo, const float *src, int ld, int valid)
+__device__ __noinline__ void stage_f32(uint8_t *hi, uint8_t *lo, const float *src, int ld, int valid)
 {
     constexpr int per_row = C / 8, NI = R * per_row / kBT;
     static_assert(NI * kBT == R * per_row, "whole chunks per thread");
@@ -792,7 +792,7 @@ __device__ __forceinline__ void stage_f32(uint8_t *hi, uint8_t *lo, const float 
 // entry read as high + low (about 16 significand bits).  Consecutive threads take consecutive 16-B
 // pieces, so the global loads coalesce and the shared-memory accesses are conflict-free.
 template <int BYTES>
-__device__ __forceinline__ float copy_pairs_dot_old(uint8_t *hi, uint8_t *lo, const uint8_t *src)
+__device__ __noinline__ float copy_pairs_dot_old(uint8_t *hi, uint8_t *lo, const uint8_t *src)
 {
     constexpr int NI = BYTES / 16 / kBT;
     static_assert(NI * 16 * kBT == BYTES, "whole pieces per thread");
@@ -826,7 +826,7 @@ __device__ __forceinline__ float copy_pairs_dot_old(uint8_t *hi, uint8_t *lo, co
 
 // bf16 [R][C] (row stride ld elements) -> one tile; rows >= valid are zero (loads batched as above)
 template <int R, int C>
-__device__ __forceinline__ void stage_bf16(uint8_t *dst, const __nv_bfloat16 *src, int64_t ld, int valid)
+__device__ __noinline__ void stage_bf16(uint8_t *dst, const __nv_bfloat16 *src, int64_t ld, int valid)
 {
     constexpr int per_row = C / 8, NI = R * per_row / kBT;
     static_assert(NI * kBT == R * per_row, "whole chunks per thread");
@@ -941,6 +941,7 @@ bwd_local_tc_kernel(const BwdParams p)
     // one product: nks K-steps, A and B descriptors for (step, lo) via functors; a_exact/b_exact skip lo terms
     auto mma = [&](uint32_t dcol, int N, bool a_mn, bool b_mn, int nks, auto ad, auto bd, bool a_exact, bool b_exact) {
         const uint32_t id = idesc_bf16(128, N, a_mn, b_mn);
+#pragma unroll 1
         for (int ks = 0; ks < nks; ++ks) {
             const uint64_t ah = ad(ks, 0), bh = bd(ks, 0);
             mma_ss(tm + dcol, ah, bh, id, ks > 0 ? 1u : 0u);
@@ -948,15 +949,24 @@ bwd_local_tc_kernel(const BwdParams p)
             if (!a_exact) mma_ss(tm + dcol, ad(ks, 1), bh, id, 1u);
         }
     };
-    // tensor-memory row of the calling warp (warps 0, 1, 4, 5): 16 x n16 columns from col
+    // the calling warp's tensor-memory lanes (rows 0-63 are read by warps 0, 1, 4 and 5), its column half
     const int q4 = warp & 3, half = warp >> 2, row = 32 * q4 + lane;
     const bool reader = q4 < 2;
-    auto ld_row = [&](uint32_t col, uint32_t (&u)[64], int n16) {
-        const uint32_t a = tm + ((uint32_t)(32 * q4) << 16) + col;
-        for (int i = 0; i < n16; ++i) umma::tmem_ld16(a + 16 * i, *reinterpret_cast<uint32_t(*)[16]>(u + 16 * i));
-        umma::tmem_wait_ld();
-    };
     auto f = [](uint32_t u) { return __uint_as_float(u); };
+    // the calling warp's tensor-memory row, n32 groups of 32 columns from col, fn(u, first column of the
+    // group) per group.  The group loop stays rolled: this kernel runs each phase once per CTA, and
+    // straight-line epilogues were bound by instruction fetch.
+    auto row_groups = [&](uint32_t col, int n32, auto fn) {
+        const uint32_t a = tm + ((uint32_t)(32 * q4) << 16) + col;
+#pragma unroll 1
+        for (int g = 0; g < n32; ++g) {
+            uint32_t u[32];
+            umma::tmem_ld16(a + 32 * g, *reinterpret_cast<uint32_t(*)[16]>(u));
+            umma::tmem_ld16(a + 32 * g + 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16));
+            umma::tmem_wait_ld();
+            fn(u, 32 * g);
+        }
+    };
     const uint32_t C1a = 0, C1b = 128, C3 = 256, C4 = 384;
 
     // ---- phase 1: dQd = dO S, dW' = dV_new S, dA = dO V_new^T; then dKd = V_new dS'
@@ -984,49 +994,54 @@ bwd_local_tc_kernel(const BwdParams p)
         }
         // while it runs: dQ = gam dQd (dgam += Q^ . dQd) and dA, from columns this warp's half owns
         if (reader) {
-            uint32_t u[64];
-            ld_row(C1a + 64 * half, u, 4);
             float acc = 0.f;
             const float g = sgam[row];
+            row_groups(C1a + 64 * half, 2, [&](const uint32_t (&u)[32], int b) {
 #pragma unroll
-            for (int e = 0; e < 64; e += 4) {
-                const int d = 64 * half + e;
-                const float4 qv = *reinterpret_cast<const float4 *>(qh + row * DK + d);
-                acc += qv.x * f(u[e]) + qv.y * f(u[e + 1]) + qv.z * f(u[e + 2]) + qv.w * f(u[e + 3]);
-                *reinterpret_cast<float4 *>(dQ + row * DK + d) =
-                    make_float4(g * f(u[e]), g * f(u[e + 1]), g * f(u[e + 2]), g * f(u[e + 3]));
-            }
+                for (int e = 0; e < 32; e += 4) {
+                    const int d = 64 * half + b + e;
+                    const float4 qv = *reinterpret_cast<const float4 *>(qh + row * DK + d);
+                    acc += qv.x * f(u[e]) + qv.y * f(u[e + 1]) + qv.z * f(u[e + 2]) + qv.w * f(u[e + 3]);
+                    *reinterpret_cast<float4 *>(dQ + row * DK + d) =
+                        make_float4(g * f(u[e]), g * f(u[e + 1]), g * f(u[e + 2]), g * f(u[e + 3]));
+                }
+            });
             atomicAdd(&sdgam[row], acc);
-            ld_row(C4 + 32 * half, u, 2);
-            for (int e = 0; e < 32; ++e) {
-                const int i = 32 * half + e;
-                sDA[row * 64 + i] = i <= row ? f(u[e]) : 0.f;
-            }
+            row_groups(C4 + 32 * half, 1, [&](const uint32_t (&u)[32], int) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int i = 32 * half + e;
+                    sDA[row * 64 + i] = i <= row ? f(u[e]) : 0.f;
+                }
+            });
         }
         ok = wait_all();
     }
     if (ok) {
         // dK = fk dKd (dkdf += K^ . dKd); dW = -dW' into its tiles over dS'
         if (reader) {
-            uint32_t u[64];
-            ld_row(C3 + 64 * half, u, 4);
             float acc = 0.f;
             const float fk = sfk[row];
+            row_groups(C3 + 64 * half, 2, [&](const uint32_t (&u)[32], int b) {
 #pragma unroll
-            for (int e = 0; e < 64; e += 4) {
-                const int d = 64 * half + e;
-                const float4 kv = *reinterpret_cast<const float4 *>(kh + row * DK + d);
-                acc += kv.x * f(u[e]) + kv.y * f(u[e + 1]) + kv.z * f(u[e + 2]) + kv.w * f(u[e + 3]);
-                *reinterpret_cast<float4 *>(dK + row * DK + d) =
-                    make_float4(fk * f(u[e]), fk * f(u[e + 1]), fk * f(u[e + 2]), fk * f(u[e + 3]));
-            }
+                for (int e = 0; e < 32; e += 4) {
+                    const int d = 64 * half + b + e;
+                    const float4 kv = *reinterpret_cast<const float4 *>(kh + row * DK + d);
+                    acc += kv.x * f(u[e]) + kv.y * f(u[e + 1]) + kv.z * f(u[e + 2]) + kv.w * f(u[e + 3]);
+                    *reinterpret_cast<float4 *>(dK + row * DK + d) =
+                        make_float4(fk * f(u[e]), fk * f(u[e + 1]), fk * f(u[e + 2]), fk * f(u[e + 3]));
+                }
+            });
             atomicAdd(&sdkdf[row], acc);
-            ld_row(C1b + 64 * half, u, 4);
-            for (int c8 = 0; c8 < 8; ++c8) {
-                float v[8];
-                for (int e = 0; e < 8; ++e) v[e] = -f(u[8 * c8 + e]);
-                put8(sm + BH, sm + BH + 16384, 64, row, 8 * half + c8, v);
-            }
+            row_groups(C1b + 64 * half, 2, [&](const uint32_t (&u)[32], int b) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = -f(u[8 * q + e]);
+                    put8(sm + BH, sm + BH + 16384, 64, row, 8 * half + b / 8 + q, v);
+                }
+            });
         }
     }
     umma::fence_before_sync();
@@ -1057,46 +1072,52 @@ bwd_local_tc_kernel(const BwdParams p)
         if (!wait_all()) goto done;
         if (reader) {
             const int i = row;
-            uint32_t u[64];
-            // dv = beta T^T dV_new,  dbeta += (T^T dV_new) . V
-            ld_row(C5a + 64 * half, u, 4);
+            // dv = beta T^T dV_new,  dbeta += (T^T dV_new) . V: dv row i into a bf16 [64][136] staging tile
+            // over dV_new (copied out coalesced below; the 8-element pad spreads a warp's rows over the banks)
             float db = 0.f;
-            {   // dv row i into a bf16 [64][136] staging tile over dV_new (copied out coalesced below; the
-                // 8-element pad spreads the rows a warp writes over the banks)
-                __nv_bfloat16 *dvs = reinterpret_cast<__nv_bfloat16 *>(sm + DVH) + i * (DV + 8) + 64 * half;
+            __nv_bfloat16 *dvs = reinterpret_cast<__nv_bfloat16 *>(sm + DVH) + i * (DV + 8) + 64 * half;
+            row_groups(C5a + 64 * half, 2, [&](const uint32_t (&u)[32], int b) {
 #pragma unroll
-                for (int e = 0; e < 64; e += 2) {
-                    const int j = 64 * half + e;
-                    *reinterpret_cast<__nv_bfloat162 *>(dvs + e) =
+                for (int e = 0; e < 32; e += 2) {
+                    const int j = 64 * half + b + e;
+                    *reinterpret_cast<__nv_bfloat162 *>(dvs + b + e) =
                         __floats2bfloat162_rn(sbe[i] * f(u[e]), sbe[i] * f(u[e + 1]));
                     const __nv_bfloat162 vb = *reinterpret_cast<const __nv_bfloat162 *>(
                         sm + BL + (uint32_t)(j >> 6) * 8192u + sw128_offset((uint32_t)i, (uint32_t)(j & 63)));
                     const float2 v2 = __bfloat1622float2(vb);
                     db += f(u[e]) * v2.x + f(u[e + 1]) * v2.y;
                 }
-            }
+            });
             // dK += beta gam T^T dW,  dbeta += gam (T^T dW) . K^,  dgam += beta (T^T dW) . K^
-            ld_row(C5b + 64 * half, u, 4);
             float tk = 0.f;
             const float bg = sbe[i] * sgam[i];
+            row_groups(C5b + 64 * half, 2, [&](const uint32_t (&u)[32], int b) {
 #pragma unroll
-            for (int e = 0; e < 64; e += 4) {
-                const int d = 64 * half + e;
-                const float4 kv = *reinterpret_cast<const float4 *>(kh + i * DK + d);
-                float4 dk4 = *reinterpret_cast<float4 *>(dK + i * DK + d);
-                dk4.x += bg * f(u[e]); dk4.y += bg * f(u[e + 1]); dk4.z += bg * f(u[e + 2]); dk4.w += bg * f(u[e + 3]);
-                *reinterpret_cast<float4 *>(dK + i * DK + d) = dk4;
-                tk += f(u[e]) * kv.x + f(u[e + 1]) * kv.y + f(u[e + 2]) * kv.z + f(u[e + 3]) * kv.w;
-            }
+                for (int e = 0; e < 32; e += 4) {
+                    const int d = 64 * half + b + e;
+                    const float4 kv = *reinterpret_cast<const float4 *>(kh + i * DK + d);
+                    float4 dk4 = *reinterpret_cast<float4 *>(dK + i * DK + d);
+                    dk4.x += bg * f(u[e]); dk4.y += bg * f(u[e + 1]); dk4.z += bg * f(u[e + 2]); dk4.w += bg * f(u[e + 3]);
+                    *reinterpret_cast<float4 *>(dK + i * DK + d) = dk4;
+                    tk += f(u[e]) * kv.x + f(u[e + 1]) * kv.y + f(u[e + 2]) * kv.z + f(u[e + 3]) * kv.w;
+                }
+            });
             atomicAdd(&sdbeta[i], db + sgam[i] * tk);
             atomicAdd(&sdgam[i], sbe[i] * tk);
             // dT = dV_new (diag(beta) V)^T + dW (diag(beta gam) K^)^T, columns j of this warp's half
-            uint32_t w[64];
-            ld_row(C6a + 32 * half, u, 2);
-            ld_row(C6b + 32 * half, w, 2);
-            for (int e = 0; e < 32; ++e) {
-                const int j = 32 * half + e;
-                sDT[i * 64 + j] = sbe[j] * f(u[e]) + sbe[j] * sgam[j] * f(w[e]);
+            {
+                uint32_t u[32], w[32];
+                const uint32_t a = tm + ((uint32_t)(32 * q4) << 16);
+                umma::tmem_ld16(a + C6a + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(u));
+                umma::tmem_ld16(a + C6a + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16));
+                umma::tmem_ld16(a + C6b + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(w));
+                umma::tmem_ld16(a + C6b + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(w + 16));
+                umma::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int j = 32 * half + e;
+                    sDT[i * 64 + j] = sbe[j] * f(u[e]) + sbe[j] * sgam[j] * f(w[e]);
+                }
             }
         }
         umma::fence_before_sync();
@@ -1131,15 +1152,16 @@ bwd_local_tc_kernel(const BwdParams p)
             umma::commit(bar);
         }
         if (!wait_all()) goto done;
-        if (reader) {   // X row i, this warp's 32 columns -> X tiles (K-major [i][r])
-            uint32_t u[64];
-            ld_row(C7 + 32 * half, u, 2);
-            for (int c8 = 0; c8 < 4; ++c8) {
-                float v[8];
-                for (int e = 0; e < 8; ++e) v[e] = f(u[8 * c8 + e]);
-                put8(sm + BL + 16384, sm + BL + 16384 + 8192, 64, row, 4 * half + c8, v);
-            }
-        }
+        if (reader)   // X row i, this warp's 32 columns -> X tiles (K-major [i][r])
+            row_groups(C7 + 32 * half, 1, [&](const uint32_t (&u)[32], int) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = f(u[8 * q + e]);
+                    put8(sm + BL + 16384, sm + BL + 16384 + 8192, 64, row, 4 * half + q, v);
+                }
+            });
         umma::fence_proxy_async();
         umma::fence_before_sync();
         __syncthreads();
@@ -1150,21 +1172,21 @@ bwd_local_tc_kernel(const BwdParams p)
             umma::commit(bar);
         }
         if (!wait_all()) goto done;
-        if (reader) {
-            uint32_t u[64];
-            ld_row(C8 + 32 * half, u, 2);
-            for (int e = 0; e < 32; ++e) {
-                const int j = 32 * half + e;
-                sDL[row * 64 + j] = j < row ? -f(u[e]) : 0.f;
-            }
-        }
+        if (reader)
+            row_groups(C8 + 32 * half, 1, [&](const uint32_t (&u)[32], int) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int j = 32 * half + e;
+                    sDL[row * 64 + j] = j < row ? -f(u[e]) : 0.f;
+                }
+            });
         __syncthreads();
         // ---- the 64 x 64 pass (as bwd_local_kernel): GG's row and column sums, dbeta, dA o Gamma, M
         {
             if (!wait_copies()) goto done;
             const float *KK = reinterpret_cast<const float *>(sm + BH), *QK = reinterpret_cast<const float *>(sm + BH + 16384);
             float gcol[2] = {0.f, 0.f};
-#pragma unroll
+#pragma unroll 1
             for (int rr = 0; rr < 8; ++rr) {
                 const int r = warp * 8 + rr;
                 float db = 0.f, grow = 0.f;
@@ -1243,22 +1265,25 @@ bwd_local_tc_kernel(const BwdParams p)
         float *fQ = reinterpret_cast<float *>(sm + VNH), *fK = reinterpret_cast<float *>(sm + BH);
         constexpr int PF = DK + 4;
         if (reader) {
-            uint32_t u[64];
-            ld_row(C9 + 64 * half, u, 4);
+            // columns [64 half, 64 half + 64) of C9 (dQ), then the same columns of C10 (dK): one rolled loop
+            const uint32_t a0 = tm + ((uint32_t)(32 * q4) << 16);
+#pragma unroll 1
+            for (int g = 0; g < 4; ++g) {
+                const bool kpart = g >= 2;
+                const int d0 = 64 * half + 32 * (g & 1);
+                uint32_t u[32];
+                const uint32_t col = (kpart ? C10 : C9) + (uint32_t)d0;
+                umma::tmem_ld16(a0 + col, *reinterpret_cast<uint32_t(*)[16]>(u));
+                umma::tmem_ld16(a0 + col + 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16));
+                umma::tmem_wait_ld();
+                const float *src = (kpart ? dK : dQ) + row * DK + d0;
+                float *dst = (kpart ? fK : fQ) + row * PF + d0;
 #pragma unroll
-            for (int e = 0; e < 64; e += 4) {
-                const int d = 64 * half + e;
-                float4 a = *reinterpret_cast<float4 *>(dQ + row * DK + d);
-                a.x += f(u[e]); a.y += f(u[e + 1]); a.z += f(u[e + 2]); a.w += f(u[e + 3]);
-                *reinterpret_cast<float4 *>(fQ + row * PF + d) = a;
-            }
-            ld_row(C10 + 64 * half, u, 4);
-#pragma unroll
-            for (int e = 0; e < 64; e += 4) {
-                const int d = 64 * half + e;
-                float4 a = *reinterpret_cast<float4 *>(dK + row * DK + d);
-                a.x += f(u[e]); a.y += f(u[e + 1]); a.z += f(u[e + 2]); a.w += f(u[e + 3]);
-                *reinterpret_cast<float4 *>(fK + row * PF + d) = a;
+                for (int e = 0; e < 32; e += 4) {
+                    float4 a = *reinterpret_cast<const float4 *>(src + e);
+                    a.x += f(u[e]); a.y += f(u[e + 1]); a.z += f(u[e + 2]); a.w += f(u[e + 3]);
+                    *reinterpret_cast<float4 *>(dst + e) = a;
+                }
             }
         }
         __syncthreads();
@@ -1287,42 +1312,32 @@ bwd_local_tc_kernel(const BwdParams p)
             p.dg[th] = sb[tid];
             p.dbeta[th] = sdbeta[tid];
         }
-        // dq, dk through the normalisations (and scale on q): one warp per row, the q and k rows of
-        // all the warp's rows loaded first
+        // dq, dk through the normalisations (and scale on q): one warp per row, the row loop rolled
         if (!wait_copies()) goto done;
         {
             const T *sq_rows = reinterpret_cast<const T *>(sm + TT), *sk_rows = reinterpret_cast<const T *>(sm + FA);
-            float qv[8][4], kv[8][4];
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const int r = min(warp + 8 * m, 63);
-#pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    const int d = lane + 32 * x;
-                    qv[m][x] = to_f32(sq_rows[r * DK + d]);
-                    kv[m][x] = to_f32(sk_rows[r * DK + d]);
-                }
-            }
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const int r = warp + 8 * m;
-                if (r >= rows) continue;
+#pragma unroll 1
+            for (int r = warp; r < rows; r += 8) {
                 const int64_t th = (tok0 + r) * H + h;
+                float qv[4], kv[4], fq[4], fk[4];
                 float sq = 0.f, sk = 0.f, qd = 0.f, kd = 0.f;
 #pragma unroll
                 for (int x = 0; x < 4; ++x) {
                     const int d = lane + 32 * x;
-                    sq += qv[m][x] * qv[m][x]; sk += kv[m][x] * kv[m][x];
-                    qd += qv[m][x] * fQ[r * PF + d]; kd += kv[m][x] * fK[r * PF + d];
+                    qv[x] = to_f32(sq_rows[r * DK + d]);
+                    kv[x] = to_f32(sk_rows[r * DK + d]);
+                    fq[x] = fQ[r * PF + d];
+                    fk[x] = fK[r * PF + d];
+                    sq += qv[x] * qv[x]; sk += kv[x] * kv[x];
+                    qd += qv[x] * fq[x]; kd += kv[x] * fk[x];
                 }
                 sq = warp_sum(sq); sk = warp_sum(sk); qd = warp_sum(qd); kd = warp_sum(kd);
                 const float rq = p.l2 ? rsqrtf(sq + kL2Eps) : 1.f, rk = p.l2 ? rsqrtf(sk + kL2Eps) : 1.f;
 #pragma unroll
                 for (int x = 0; x < 4; ++x) {
                     const int d = lane + 32 * x;
-                    const float gq = p.l2 ? p.scale * (rq * fQ[r * PF + d] - rq * rq * rq * qd * qv[m][x])
-                                          : p.scale * fQ[r * PF + d];
-                    const float gk = p.l2 ? rk * fK[r * PF + d] - rk * rk * rk * kd * kv[m][x] : fK[r * PF + d];
+                    const float gq = p.l2 ? p.scale * (rq * fq[x] - rq * rq * rq * qd * qv[x]) : p.scale * fq[x];
+                    const float gk = p.l2 ? rk * fk[x] - rk * rk * rk * kd * kv[x] : fk[x];
                     reinterpret_cast<T *>(p.dq)[th * DK + d] = from_f32<T>(gq);
                     reinterpret_cast<T *>(p.dk)[th * DK + d] = from_f32<T>(gk);
                 }
