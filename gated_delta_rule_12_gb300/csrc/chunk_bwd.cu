@@ -875,7 +875,9 @@ bwd_local_tc_kernel(const BwdParams p)
     float *blk = p.ws + (slot * H + h) * LY.total;
     const float *qh = blk + LY.qh, *kh = blk + LY.kh, *Tm = blk + LY.t, *S = blk + LY.s, *Vn = blk + LY.vn,
                 *dVn = blk + LY.dvn, *dSn = blk + LY.dsn;
-    float *dQ = blk + LY.dqh, *dK = blk + LY.dkh;
+    // dQ^ and dK^ accumulate in the scratch fields transposed, [d][r]: a warp's 32 rows of one column
+    // are then one 128-B line
+    float *dQt = blk + LY.dqh, *dKt = blk + LY.dkh;
     float *sDA = reinterpret_cast<float *>(sm + FA), *sDT = reinterpret_cast<float *>(sm + FB), *sDL = sDT;
     float *vec = reinterpret_cast<float *>(sm + VEC);
     float *sb = vec, *sbe = vec + 64, *sgam = vec + 128, *sfk = vec + 192, *sdgam = vec + 256, *sdkdf = vec + 320,
@@ -1002,8 +1004,8 @@ bwd_local_tc_kernel(const BwdParams p)
                     const int d = 64 * half + b + e;
                     const float4 qv = *reinterpret_cast<const float4 *>(qh + row * DK + d);
                     acc += qv.x * f(u[e]) + qv.y * f(u[e + 1]) + qv.z * f(u[e + 2]) + qv.w * f(u[e + 3]);
-                    *reinterpret_cast<float4 *>(dQ + row * DK + d) =
-                        make_float4(g * f(u[e]), g * f(u[e + 1]), g * f(u[e + 2]), g * f(u[e + 3]));
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) dQt[(d + x) * 64 + row] = g * f(u[e + x]);
                 }
             });
             atomicAdd(&sdgam[row], acc);
@@ -1028,8 +1030,8 @@ bwd_local_tc_kernel(const BwdParams p)
                     const int d = 64 * half + b + e;
                     const float4 kv = *reinterpret_cast<const float4 *>(kh + row * DK + d);
                     acc += kv.x * f(u[e]) + kv.y * f(u[e + 1]) + kv.z * f(u[e + 2]) + kv.w * f(u[e + 3]);
-                    *reinterpret_cast<float4 *>(dK + row * DK + d) =
-                        make_float4(fk * f(u[e]), fk * f(u[e + 1]), fk * f(u[e + 2]), fk * f(u[e + 3]));
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) dKt[(d + x) * 64 + row] = fk * f(u[e + x]);
                 }
             });
             atomicAdd(&sdkdf[row], acc);
@@ -1093,13 +1095,21 @@ bwd_local_tc_kernel(const BwdParams p)
             const float bg = sbe[i] * sgam[i];
             row_groups(C5b + 64 * half, 2, [&](const uint32_t (&u)[32], int b) {
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
+                for (int e = 0; e < 32; e += 8) {
                     const int d = 64 * half + b + e;
-                    const float4 kv = *reinterpret_cast<const float4 *>(kh + i * DK + d);
-                    float4 dk4 = *reinterpret_cast<float4 *>(dK + i * DK + d);
-                    dk4.x += bg * f(u[e]); dk4.y += bg * f(u[e + 1]); dk4.z += bg * f(u[e + 2]); dk4.w += bg * f(u[e + 3]);
-                    *reinterpret_cast<float4 *>(dK + i * DK + d) = dk4;
-                    tk += f(u[e]) * kv.x + f(u[e + 1]) * kv.y + f(u[e + 2]) * kv.z + f(u[e + 3]) * kv.w;
+                    // K^ row i, columns d .. d + 7, from its staged tiles as high + low
+                    const uint32_t o = (uint32_t)(d >> 6) * 8192u + sw128_offset((uint32_t)i, (uint32_t)(d & 63));
+                    const uint4 kh4 = *reinterpret_cast<const uint4 *>(sm + VNH + o);
+                    const uint4 kl4 = *reinterpret_cast<const uint4 *>(sm + VNL + o);
+                    const uint32_t hw[4] = {kh4.x, kh4.y, kh4.z, kh4.w}, lw[4] = {kl4.x, kl4.y, kl4.z, kl4.w};
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&hw[x]));
+                        const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&lw[x]));
+                        tk += f(u[e + 2 * x]) * (a.x + c.x) + f(u[e + 2 * x + 1]) * (a.y + c.y);
+                    }
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) dKt[(d + x) * 64 + i] += bg * f(u[e + x]);
                 }
             });
             atomicAdd(&sdbeta[i], db + sgam[i] * tk);
@@ -1276,12 +1286,15 @@ bwd_local_tc_kernel(const BwdParams p)
                 umma::tmem_ld16(a0 + col, *reinterpret_cast<uint32_t(*)[16]>(u));
                 umma::tmem_ld16(a0 + col + 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16));
                 umma::tmem_wait_ld();
-                const float *src = (kpart ? dK : dQ) + row * DK + d0;
+                const float *src = (kpart ? dKt : dQt) + d0 * 64 + row;
                 float *dst = (kpart ? fK : fQ) + row * PF + d0;
 #pragma unroll
                 for (int e = 0; e < 32; e += 4) {
-                    float4 a = *reinterpret_cast<const float4 *>(src + e);
-                    a.x += f(u[e]); a.y += f(u[e + 1]); a.z += f(u[e + 2]); a.w += f(u[e + 3]);
+                    float4 a;
+                    a.x = src[e * 64] + f(u[e]);
+                    a.y = src[(e + 1) * 64] + f(u[e + 1]);
+                    a.z = src[(e + 2) * 64] + f(u[e + 2]);
+                    a.w = src[(e + 3) * 64] + f(u[e + 3]);
                     *reinterpret_cast<float4 *>(dst + e) = a;
                 }
             }
