@@ -250,6 +250,8 @@ struct BwdParams {
     int need_u;                     // U~ is only read by the CUDA-core forward scan
     int tc_scan;                    // reverse scan on the tensor cores (bf16, dk = dv = 128): dO^T Qd is
                                     // stored transposed, [dk][dv], and dS' as bf16 (high, low) tiles
+    int s_t;                        // the chunk-start states are stored transposed, [dk][dv] (they come
+                                    // from the tensor-core forward scan)
     unsigned *err;                  // device error word (the workspace's first word)
     Geometry gm;
     float scale;
@@ -556,7 +558,7 @@ bwd_local_kernel(const BwdParams p)
 
     // dQd = dO S  ->  dQ = gam dQd,  dgam += Q^ . dQd
     block_gemm_cols<4, true, false, 1>(64, dk, dv, [&](int r, int j) { return dOf(r, j); },
-                                       [&](int j, int d) { return S[(int64_t)j * dk + d]; },
+                                       [&](int j, int d) { return p.s_t ? S[(int64_t)d * dv + j] : S[(int64_t)j * dk + d]; },
                                        [&](int r, int d, float x) {
                                            dQ[r * dk + d] = sgam[r] * x;
                                            return make_float2(qh[r * dk + d] * x, 0.f);
@@ -570,7 +572,7 @@ bwd_local_kernel(const BwdParams p)
                                        }, sA, sB, sdkdf);
     // dW = -dV_new S
     block_gemm_cols<4, true, false>(64, dk, dv, [&](int r, int j) { return dVn[r * dv + j]; },
-                                    [&](int j, int d) { return S[(int64_t)j * dk + d]; },
+                                    [&](int j, int d) { return p.s_t ? S[(int64_t)d * dv + j] : S[(int64_t)j * dk + d]; },
                                     [&](int r, int d, float x) { dW[r * dk + d] = -x; }, sA, sB);
     // dA = tril(dO V_new^T) (diagonal included)
     block_gemm<4, 4, true, true>(64, 64, dv, [&](int r, int j) { return dOf(r, j); },
@@ -652,7 +654,8 @@ bwd_local_kernel(const BwdParams p)
                                     [&](int i, int d, float x) { dK[i * dk + d] += x; }, sA, sB);
     // dgC = <dS', S>
     float part = 0.f;
-    for (int64_t e = tid; e < (int64_t)dv * dk; e += kBT) part += dSn[e] * S[e];
+    for (int64_t e = tid; e < (int64_t)dv * dk; e += kBT)   // e = j dk + d
+        part += dSn[e] * (p.s_t ? S[(e % dk) * dv + e / dk] : S[e]);
     sred[tid] = part;
     __syncthreads();
     for (int off = kBT / 2; off > 0; off >>= 1) {
@@ -728,7 +731,7 @@ using umma::sw128_offset;
 constexpr uint32_t DO = 0;                   // dO [64 r][128 j] bf16; then dT (hi, lo); then M (hi, lo)
 constexpr uint32_t VNH = 16384, VNL = 32768; // V_new [64 r][128 j] hi, lo; then K^ [64 i][128 d] hi, lo
 constexpr uint32_t DVH = 49152, DVL = 65536; // dV_new [64 r][128 j] hi, lo; then dA' (hi, lo) at DVH
-constexpr uint32_t BH = 81920, BL = 114688;  // S, then dS' [128 j][128 d] hi, lo; then dW hi, lo (BH, BH + 16K),
+constexpr uint32_t BH = 81920, BL = 114688;  // S^T, then dS'^T [128 d][128 j] hi, lo; then dW hi, lo (BH, BH + 16K),
                                              // V [64 j][128 c] bf16 (BL), X (hi, lo) (BL + 16K); then Q^ (BH, BH + 16K)
 constexpr uint32_t TT = 147456;              // T [64 r][64 i] hi, lo (8 KB each)
 constexpr uint32_t FA = 163840, FB = 180224; // fp32 [64][64]: dA, then dA o Gamma;  dT, then dL, then M
@@ -909,7 +912,7 @@ bwd_local_tc_kernel(const BwdParams p)
     stage_bf16<64, DV>(sm + DO, dO, tstride, rows);
     stage_f32<64, DV>(sm + VNH, sm + VNL, Vn, DV, 64);
     stage_f32<64, DV>(sm + DVH, sm + DVL, dVn, DV, 64);
-    stage_f32<DV, DK>(sm + BH, sm + BL, S, DK, DV);
+    stage_f32<DK, DV>(sm + BH, sm + BL, S, DV, DK);   // S^T [d][j]
     umma::fence_proxy_async();
     umma::fence_before_sync();
     __syncthreads();
@@ -972,11 +975,13 @@ bwd_local_tc_kernel(const BwdParams p)
     const uint32_t C1a = 0, C1b = 128, C3 = 256, C4 = 384;
 
     // ---- phase 1: dQd = dO S, dW' = dV_new S, dA = dO V_new^T; then dKd = V_new dS'
+    // (S and dS' are staged transposed, [d][j], as the forward scan and the reverse scan store them:
+    // B operands with K = j along the rows' 128 B)
     if (tid == 0) {
-        mma(C1a, 128, false, true, 8, [&](int ks, int) { return kmaj(sb0 + DO, 64, ks); },
-            [&](int ks, int lo) { return mnmaj(sb0 + (lo ? BL : BH), 128, ks); }, true, false);
-        mma(C1b, 128, false, true, 8, [&](int ks, int lo) { return kmaj(sb0 + (lo ? DVL : DVH), 64, ks); },
-            [&](int ks, int lo) { return mnmaj(sb0 + (lo ? BL : BH), 128, ks); }, false, false);
+        mma(C1a, 128, false, false, 8, [&](int ks, int) { return kmaj(sb0 + DO, 64, ks); },
+            [&](int ks, int lo) { return kmaj(sb0 + (lo ? BL : BH), 128, ks); }, true, false);
+        mma(C1b, 128, false, false, 8, [&](int ks, int lo) { return kmaj(sb0 + (lo ? DVL : DVH), 64, ks); },
+            [&](int ks, int lo) { return kmaj(sb0 + (lo ? BL : BH), 128, ks); }, false, false);
         mma(C4, 64, false, false, 8, [&](int ks, int) { return kmaj(sb0 + DO, 64, ks); },
             [&](int ks, int lo) { return kmaj(sb0 + (lo ? VNL : VNH), 64, ks); }, true, false);
         umma::commit(bar);
@@ -990,8 +995,8 @@ bwd_local_tc_kernel(const BwdParams p)
         __syncthreads();
         umma::fence_after_sync();
         if (tid == 0) {
-            mma(C3, 128, false, true, 8, [&](int ks, int lo) { return kmaj(sb0 + (lo ? VNL : VNH), 64, ks); },
-                [&](int ks, int lo) { return mnmaj(sb0 + (lo ? BL : BH), 128, ks); }, false, false);
+            mma(C3, 128, false, false, 8, [&](int ks, int lo) { return kmaj(sb0 + (lo ? VNL : VNH), 64, ks); },
+                [&](int ks, int lo) { return kmaj(sb0 + (lo ? BL : BH), 128, ks); }, false, false);
             umma::commit(bar);
         }
         // while it runs: dQ = gam dQd (dgam += Q^ . dQd) and dA, from columns this warp's half owns
@@ -1379,7 +1384,7 @@ done:
 // global access of the chain is coalesced.
 // ---------------------------------------------------------------------------
 namespace rs {
-constexpr uint32_t SAH = 0, SAL = 32768;        // dS' [128 j][128 d] high, low
+constexpr uint32_t SAH = 0, SAL = 32768;        // dS'^T [128 d][128 j] high, low (A, MN-major)
 constexpr uint32_t KDH = 65536, KDL = 81920;    // Kd [64 r][128 d]
 constexpr uint32_t WH = 98304, WL = 114688;     // W [64 r][128 d]
 constexpr uint32_t VAH = 131072, VAL = 147456;  // -dV_new^T [128 j][64 r]
@@ -1482,8 +1487,8 @@ bwd_scan_tc_kernel(const BwdParams p)
         umma::fence_after_sync();
         return !bad;
     };
-    auto mma3 = [&](uint32_t dcol, int N, bool b_mn, int nks, auto ad, auto bd) {
-        const uint32_t id = umma::idesc_bf16(128, N, false, b_mn);
+    auto mma3 = [&](uint32_t dcol, int N, bool a_mn, bool b_mn, int nks, auto ad, auto bd) {
+        const uint32_t id = umma::idesc_bf16(128, N, a_mn, b_mn);
         for (int ks = 0; ks < nks; ++ks) {
             const uint64_t ah = ad(ks, 0), bh = bd(ks, 0);
             umma::mma_ss(tm + dcol, ah, bh, id, ks > 0 ? 1u : 0u);
@@ -1497,23 +1502,27 @@ bwd_scan_tc_kernel(const BwdParams p)
     for (int c = nch - 1; c >= 0 && ok; --c) {
         float *blk = p.ws + ((slot0 + c) * H + h) * LY.total;
         const float *nblk = p.ws + ((slot0 + (c > 0 ? c - 1 : 0)) * H + h) * LY.total;
-        {   // dS' staged for the first product (and saved from there)
+        {   // dS' staged transposed for the first product (and saved from there): column j of rows d;
+            // a warp's 32 lanes write 64 contiguous bytes of one row
+            const uint32_t cb = (uint32_t)(j >> 6) * 16384u;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float v[8] = {dS[8 * q], dS[8 * q + 1], dS[8 * q + 2], dS[8 * q + 3],
-                                    dS[8 * q + 4], dS[8 * q + 5], dS[8 * q + 6], dS[8 * q + 7]};
-                lt::put8(sm + SAH, sm + SAL, kRows, j, 8 * half + q, v);
+            for (int e = 0; e < 64; ++e) {
+                const __nv_bfloat16 hb = __float2bfloat16_rn(dS[e]);
+                const __nv_bfloat16 lb = __float2bfloat16_rn(dS[e] - __bfloat162float(hb));
+                const uint32_t o = cb + umma::sw128_offset((uint32_t)(64 * half + e), (uint32_t)(j & 63));
+                *reinterpret_cast<__nv_bfloat16 *>(sm + SAH + o) = hb;
+                *reinterpret_cast<__nv_bfloat16 *>(sm + SAL + o) = lb;
             }
         }
         umma::fence_proxy_async();
         umma::fence_before_sync();
         __syncthreads();
         umma::fence_after_sync();
-        if (tid == 0) {   // dS' Kd^T: A [128 j][128 d] K-major, B [64 r][128 d] K-major
-            mma3(D1, 64, false, 8, [&](int ks, int lo) { return lt::kmaj(sb0 + (lo ? SAL : SAH), kRows, ks); },
+        if (tid == 0) {   // dS' Kd^T: A from the [128 d][128 j] tiles (MN-major), B [64 r][128 d] K-major
+            mma3(D1, 64, true, false, 8, [&](int ks, int lo) { return lt::mnmaj(sb0 + (lo ? SAL : SAH), kRows, ks); },
                  [&](int ks, int lo) { return lt::kmaj(sb0 + (lo ? KDL : KDH), 64, ks); });
             umma::commit(bar);
-            // dS' for the local kernel: its high and low tiles as they are, 32 KB each
+            // dS' for the local kernel: its high and low tiles as they are ([d][j]), 32 KB each
             uint8_t *dsn = reinterpret_cast<uint8_t *>(blk + LY.dsn);
             umma::bulk_store(dsn, sb0 + SAH, 32768);
             umma::bulk_store(dsn + 32768, sb0 + SAL, 32768);
@@ -1554,7 +1563,7 @@ bwd_scan_tc_kernel(const BwdParams p)
         __syncthreads();
         umma::fence_after_sync();
         if (tid == 0) {   // -dV_new^T W: A [128 j][64 r] K-major, B [64 r][128 d] MN-major
-            mma3(D2, 128, true, 4, [&](int ks, int lo) { return lt::kmaj(sb0 + (lo ? VAL : VAH), kRows, ks); },
+            mma3(D2, 128, false, true, 4, [&](int ks, int lo) { return lt::kmaj(sb0 + (lo ? VAL : VAH), kRows, ks); },
                  [&](int ks, int lo) { return lt::mnmaj(sb0 + (lo ? WL : WH), 64, ks); });
             umma::commit(bar);
         }
@@ -1604,6 +1613,7 @@ cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t st)
     const bool tc_local = a.dt == 1 && a.gm.dk == 128 && a.gm.dv == 128;   // implies tc_scan
     p.need_u = tc_scan ? 0 : 1;
     p.tc_scan = tc_local ? 1 : 0;
+    p.s_t = tc_scan ? 1 : 0;
     p.gm = a.gm; p.scale = a.scale; p.l2 = a.l2;
     const size_t stage = 2 * (size_t)kStage * sizeof(float);
     const size_t sm_prep = stage + sizeof(float) * (2 * 64 * 65 + 4 * 64);

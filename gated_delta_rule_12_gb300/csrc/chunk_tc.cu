@@ -900,8 +900,9 @@ struct RcParams {
     Geometry gm;
     long long *trace;
     ConvParams cv;      // KC > 0: the raw V tile is convolved in place, Q comes convolved from the workspace
-    // For the backward pass: when save_s is set, the state at every chunk start (fp32 [dv][128]) and
-    // V_new (fp32 [64][dv]) go to per (slot, head) blocks save_stride floats apart; out may then be null.
+    // For the backward pass: when save_s is set, the state at every chunk start (fp32, transposed:
+    // [128][dv], S^T) and V_new (fp32 [64][dv]) go to per (slot, head) blocks save_stride floats
+    // apart; out may then be null.
     float *save_s, *save_vn;
     int64_t save_stride;
 };
@@ -1073,13 +1074,12 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
             if (leader) ok = wait_spin(bar(b), parity, abort_flag, p.err);
             return !gsync(!ok);
         };
-        // the state at the start of chunk c: this thread's 64 entries of row j0 + j
+        // the state at the start of chunk c: this thread's 64 entries of row j0 + j, stored transposed
+        // (column d of the state at d dv), so that a warp's 32 rows of one column are one 128-B line
         auto save_state = [&](int c, const uint32_t (&sv)[64]) {
-            float *dst = p.save_s + ((slot0 + c) * H + h) * p.save_stride + (size_t)(j0 + j) * 128 + hf * 64;
+            float *dst = p.save_s + ((slot0 + c) * H + h) * p.save_stride + (size_t)(hf * 64) * dv + j0 + j;
 #pragma unroll
-            for (int e = 0; e < 64; e += 4)
-                *reinterpret_cast<float4 *>(dst + e) = make_float4(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1]),
-                                                                   __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]));
+            for (int e = 0; e < 64; ++e) dst[(size_t)e * dv] = __uint_as_float(sv[e]);
         };
         // 64 fp32 state entries (this thread's half of row j) -> the bf16 A tile of a2
         auto put_sbf = [&](const uint32_t (&sv)[64]) {
