@@ -1377,9 +1377,9 @@ done:
 //   dS = gC dS' + dO^T Qd - dV_new^T W.
 // dS stays in registers, one state row per thread and half of its columns (the rows and columns a
 // warp reads from tensor memory).  Each product reads dS', Kd, -dV_new^T and W from shared memory
-// as bf16 (high, low) pairs and sums high.high + high.low + low.high in the fp32 accumulator.  The
-// next chunk's Kd and W are loaded into registers while a product runs and staged once the product
-// that reads their tiles has finished.  dS' is saved by two bulk copies of its staged tiles (the
+// as bf16 (high, low) pairs and sums high.high + high.low + low.high in the fp32 accumulator.  Kd and
+// W arrive as ready tile pairs (written so by bwd_prep_tc_kernel): the next chunk's copy is issued as
+// soon as the product that reads the tiles has finished.  dS' is saved by two bulk copies of its staged tiles (the
 // local kernel reads it back in that form), and dO^T Qd is read in its transposed layout, so every
 // global access of the chain is coalesced.
 // ---------------------------------------------------------------------------
@@ -1388,32 +1388,10 @@ constexpr uint32_t SAH = 0, SAL = 32768;        // dS'^T [128 d][128 j] high, lo
 constexpr uint32_t KDH = 65536, KDL = 81920;    // Kd [64 r][128 d]
 constexpr uint32_t WH = 98304, WL = 114688;     // W [64 r][128 d]
 constexpr uint32_t VAH = 131072, VAL = 147456;  // -dV_new^T [128 j][64 r]
-constexpr uint32_t MISC = 163840;               // mbarrier, tensor-memory base, abort flag
+constexpr uint32_t MISC = 163840;               // mbarriers (MMA, Kd copy, W copy), tensor-memory base, abort flag
 constexpr uint32_t kSmem = MISC + 64 + 1024;
 constexpr int kRows = 128;                      // state rows per CTA
 
-// an fp32 [64][128] block held in registers between its load and its staging (as stage_f32)
-struct Block64 {
-    float4 a[4], b[4];
-};
-__device__ __forceinline__ void block_load(Block64 &t, const float *src)
-{
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int id = threadIdx.x + u * kBT, r = id >> 4, c8 = id & 15;
-        t.a[u] = *reinterpret_cast<const float4 *>(src + r * 128 + 8 * c8);
-        t.b[u] = *reinterpret_cast<const float4 *>(src + r * 128 + 8 * c8 + 4);
-    }
-}
-__device__ __forceinline__ void block_put(uint8_t *hi, uint8_t *lo, const Block64 &t)
-{
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int id = threadIdx.x + u * kBT, r = id >> 4, c8 = id & 15;
-        const float v[8] = {t.a[u].x, t.a[u].y, t.a[u].z, t.a[u].w, t.b[u].x, t.b[u].y, t.b[u].z, t.b[u].w};
-        lt::put8(hi, lo, 64, r, c8, v);
-    }
-}
 }  // namespace rs
 
 template <typename T>
@@ -1451,28 +1429,34 @@ bwd_scan_tc_kernel(const BwdParams p)
                 *reinterpret_cast<float4 *>(p.dinit + soff + e) = make_float4(dS[e], dS[e + 1], dS[e + 2], dS[e + 3]);
         return;
     }
-    const uint32_t bar = sb0 + MISC;
+    const uint32_t bar = sb0 + MISC, kbar = sb0 + MISC + 16, wbar = sb0 + MISC + 24;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + MISC + 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + MISC + 12);
+    // the Kd and W tile pairs of one chunk: 32 KB each, contiguous in the workspace and here
+    auto copy_kd = [&](int cc) {
+        umma::mbar_expect_tx(kbar, 32768);
+        umma::bulk_load(sb0 + KDH, p.ws + ((slot0 + cc) * H + h) * LY.total + LY.kd, 32768, kbar);
+    };
+    auto copy_w = [&](int cc) {
+        umma::mbar_expect_tx(wbar, 32768);
+        umma::bulk_load(sb0 + WH, p.ws + ((slot0 + cc) * H + h) * LY.total + LY.w, 32768, wbar);
+    };
     if (tid == 0) {
         umma::mbar_init(bar, 1);
+        umma::mbar_init(kbar, 1);
+        umma::mbar_init(wbar, 1);
         *abort_flag = 0;
         umma::fence_mbar_init();
+        copy_kd(nch - 1);
+        copy_w(nch - 1);
     }
     if (warp == 0) umma::tmem_alloc(tmem_holder, 256);
-    {   // the last chunk's Kd and W
-        const float *blk = p.ws + ((slot0 + nch - 1) * H + h) * LY.total;
-        Block64 t;
-        block_load(t, blk + LY.kd);
-        block_put(sm + KDH, sm + KDL, t);
-        block_load(t, blk + LY.w);
-        block_put(sm + WH, sm + WL, t);
-    }
-    umma::fence_proxy_async();
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tm = *tmem_holder;
+    uint32_t kph = 0, wph = 0;
+    bool kpend = true, wpend = true;   // copies in flight
     const uint32_t D1 = 0, D2 = 128;   // dV_new^T [128 j][64 r];  dO^T Qd - dV_new^T W [128 j][128 d]
     const uint32_t trow = tm + ((uint32_t)(32 * q4) << 16);
     uint32_t phase = 0;
@@ -1497,11 +1481,21 @@ bwd_scan_tc_kernel(const BwdParams p)
         }
     };
     auto f = [](uint32_t u) { return __uint_as_float(u); };
+    // bounded wait for a tile copy by every thread; false (for all of them) after a timeout
+    auto wait_copy = [&](uint32_t b, uint32_t &ph, bool &pend) -> bool {
+        const bool ok1 = umma::mbar_wait(b, ph, lt::kWaitNs);
+        if (!ok1) {
+            *abort_flag = 1;
+            atomicExch(p.err, kDevErrTimeout);
+        }
+        ph ^= 1u;
+        pend = false;
+        return ok1;
+    };
 
     bool ok = true;
     for (int c = nch - 1; c >= 0 && ok; --c) {
         float *blk = p.ws + ((slot0 + c) * H + h) * LY.total;
-        const float *nblk = p.ws + ((slot0 + (c > 0 ? c - 1 : 0)) * H + h) * LY.total;
         {   // dS' staged transposed for the first product (and saved from there): column j of rows d;
             // a warp's 32 lanes write 64 contiguous bytes of one row
             const uint32_t cb = (uint32_t)(j >> 6) * 16384u;
@@ -1514,9 +1508,10 @@ bwd_scan_tc_kernel(const BwdParams p)
                 *reinterpret_cast<__nv_bfloat16 *>(sm + SAL + o) = lb;
             }
         }
+        wait_copy(kbar, kph, kpend);   // this chunk's Kd
         umma::fence_proxy_async();
         umma::fence_before_sync();
-        __syncthreads();
+        if (__syncthreads_or(*abort_flag)) { ok = false; break; }
         umma::fence_after_sync();
         if (tid == 0) {   // dS' Kd^T: A from the [128 d][128 j] tiles (MN-major), B [64 r][128 d] K-major
             mma3(D1, 64, true, false, 8, [&](int ks, int lo) { return lt::mnmaj(sb0 + (lo ? SAL : SAH), kRows, ks); },
@@ -1528,16 +1523,18 @@ bwd_scan_tc_kernel(const BwdParams p)
             umma::bulk_store(dsn + 32768, sb0 + SAL, 32768);
             umma::bulk_commit();
         }
-        // while it runs: this thread's 32 entries of A^T dO, and the next chunk's Kd
+        // while it runs: this thread's 32 entries of A^T dO
         float ado[32];
         {
             const float *a0 = blk + LY.ado + j0 + j + (int64_t)(32 * half) * dv;
 #pragma unroll
             for (int e = 0; e < 32; ++e) ado[e] = a0[(int64_t)e * dv];
         }
-        Block64 nxt;
-        if (c > 0) block_load(nxt, nblk + LY.kd);
         if (!(ok = wait_mma())) break;
+        if (tid == 0 && c > 0) {   // the first product is done with Kd: the next chunk's comes in
+            copy_kd(c - 1);
+            kpend = true;
+        }
         {   // dV_new^T = dS' Kd^T + (A^T dO)^T: saved as dV_new [r][j], staged negated as A [128 j][64 r]
             uint32_t u[32];
             umma::tmem_ld16(trow + D1 + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(u));
@@ -1557,17 +1554,17 @@ bwd_scan_tc_kernel(const BwdParams p)
                 lt::put8(sm + VAH, sm + VAL, kRows, j, 4 * half + q, v);
             }
         }
-        if (c > 0) block_put(sm + KDH, sm + KDL, nxt);   // the first product is done with Kd
+        wait_copy(wbar, wph, wpend);   // this chunk's W
         umma::fence_proxy_async();
         umma::fence_before_sync();
-        __syncthreads();
+        if (__syncthreads_or(*abort_flag)) { ok = false; break; }
         umma::fence_after_sync();
         if (tid == 0) {   // -dV_new^T W: A [128 j][64 r] K-major, B [64 r][128 d] MN-major
             mma3(D2, 128, false, true, 4, [&](int ks, int lo) { return lt::kmaj(sb0 + (lo ? VAL : VAH), kRows, ks); },
                  [&](int ks, int lo) { return lt::mnmaj(sb0 + (lo ? WL : WH), 64, ks); });
             umma::commit(bar);
         }
-        // while it runs: this thread's part of dO^T Qd (stored [d][j]), the chunk's decay and the next W
+        // while it runs: this thread's part of dO^T Qd (stored [d][j]) and the chunk's decay
         float dq[64];
         {
             const float *d0 = blk + LY.doq + (int64_t)(64 * half) * dv + j0 + j;
@@ -1575,9 +1572,12 @@ bwd_scan_tc_kernel(const BwdParams p)
             for (int e = 0; e < 64; ++e) dq[e] = d0[(int64_t)e * dv];
         }
         const float gC = expf(blk[LY.b + 63]);
-        if (c > 0) block_load(nxt, nblk + LY.w);
         if (tid == 0) umma::bulk_wait_read();   // dS' tiles read out before the next chunk restages them
         if (!(ok = wait_mma())) break;
+        if (tid == 0 && c > 0) {   // the second product is done with W: the next chunk's comes in
+            copy_w(c - 1);
+            wpend = true;
+        }
 #pragma unroll
         for (int i = 0; i < 2; ++i) {   // dS = gC dS' + dO^T Qd - dV_new^T W
             uint32_t u[32];
@@ -1587,13 +1587,404 @@ bwd_scan_tc_kernel(const BwdParams p)
 #pragma unroll
             for (int e = 0; e < 32; ++e) dS[32 * i + e] = gC * dS[32 * i + e] + dq[32 * i + e] + f(u[e]);
         }
-        if (c > 0) block_put(sm + WH, sm + WL, nxt);   // the second product is done with W
     }
     if (ok && p.dinit)
 #pragma unroll
         for (int e = 0; e < 64; e += 4)
             *reinterpret_cast<float4 *>(p.dinit + soff + e) = make_float4(dS[e], dS[e + 1], dS[e + 2], dS[e + 3]);
-    if (tid == 0) umma::bulk_wait_all();
+    if (tid == 0) {   // copies still in flight after an abort: bounded waits before the CTA leaves
+        if (kpend) umma::mbar_wait(kbar, kph, lt::kWaitNs);
+        if (wpend) umma::mbar_wait(wbar, wph, lt::kWaitNs);
+        umma::bulk_wait_all();
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    if (warp == 0) umma::tmem_dealloc(tm, 256);
+}
+
+// ---------------------------------------------------------------------------
+// bwd_prep_tc_kernel: the prep step on the tensor cores, for bf16 inputs with dk = dv = 128.  One CTA
+// per (slot, head), two per SM.  The products, each accumulated in fp32 in tensor memory:
+//   G = [K; Q] K^T on the raw bf16 rows: exact products, one MMA per K-step; the norms and the
+//     scale are applied afterwards, giving K^K^T and Q^K^T;
+//   W = (T diag(beta gam / |k|)) K, with that left factor as a bf16 (high, low) pair;
+//   A^T dO, with A = (Q^K^T) o Gamma as a pair;
+//   dO^T Qd = (diag(gam scale / |q|) dO)^T Q, with the scaled dO as a pair.
+// T = (I + L)^{-1} by the block rule on the CUDA cores, as in bwd_prep_kernel (L kept transposed).
+// Kd and W are written as bf16 (high, low) tile pairs, [2 column blocks][64 rows][128 B] each, the
+// layout the tensor-core reverse scan copies straight into its operand tiles.
+// ---------------------------------------------------------------------------
+namespace pp {
+// Products with M = 128 whose A has 64 rows read 64 more rows past the tile (their results are not
+// read back); the map keeps every such over-read inside this CTA's tiles.
+constexpr uint32_t KQ = 0;                    // [K; Q]: [2 column blocks][128 rows][128 B] bf16
+constexpr uint32_t DOT = 32768;               // dO [2][64 rows][128 B] bf16
+constexpr uint32_t LT = 49152;                // L^T fp32 [64][64]; then A (high, low) [64 q][64 k]
+constexpr uint32_t TD = 65536;                // merge scratch; then T diag(beta gam / |k|) (high, low) [64 i][64 r]
+constexpr uint32_t ST = 81920;                // T fp32 [64][65]
+constexpr uint32_t SD = 65536;                // diag(gam scale / |q|) dO (high, low) [2][64 r][128 B], over TD and T
+constexpr uint32_t VEC = 98560;               // per-row vectors, 8 x 64 floats
+constexpr uint32_t MISC = VEC + 8 * 64 * 4;   // mbarrier, tensor-memory base, abort flag
+constexpr uint32_t kSmem = MISC + 64 + 1024;
+static_assert(TD + 16384 <= ST && ST + 64 * 65 * 4 <= VEC && SD + 32768 <= VEC, "prep tile map");
+static_assert(TD + 8192 + 16384 <= ST + 64 * 65 * 4, "rows 64-127 of the low TD tile lie inside T");
+static_assert(LT + 8192 + 16384 <= TD + 16384, "the second M block of the low A tile lies inside TD");
+
+__device__ __forceinline__ void unpack8(const uint4 &w, float (&v)[8])
+{
+    const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x[e]));
+        v[2 * e] = f2.x;
+        v[2 * e + 1] = f2.y;
+    }
+}
+__device__ __forceinline__ void split8(const float (&v)[8], uint4 &hi, uint4 &lo)
+{
+    lt::split_pair(v[0], v[1], hi.x, lo.x);
+    lt::split_pair(v[2], v[3], hi.y, lo.y);
+    lt::split_pair(v[4], v[5], hi.z, lo.z);
+    lt::split_pair(v[6], v[7], hi.w, lo.w);
+}
+}  // namespace pp
+
+__global__ void __launch_bounds__(kBT, 2)
+bwd_prep_tc_kernel(const BwdParams p)
+{
+    using namespace pp;
+    using umma::sw128_offset;
+    extern __shared__ uint8_t smraw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sb0 = umma::smem_u32(sm);
+    const Geometry gm = p.gm;
+    constexpr int DK = 128;
+    const int H = gm.H, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t slot = blockIdx.x;
+    int n, c, rows;
+    int64_t tok0;
+    if (!chunk_of(gm, slot, n, c, tok0, rows)) return;
+    const BwdLayout LY = bwd_layout(DK, DK);
+    float *blk = p.ws + (slot * H + h) * LY.total;
+    float *vec = reinterpret_cast<float *>(sm + VEC);
+    float *sb = vec, *sbe = vec + 64, *sgam = vec + 128, *sfk = vec + 192, *snk = vec + 256, *snq = vec + 320,
+          *scoef = vec + 384;
+    float *sLT = reinterpret_cast<float *>(sm + LT), *sT = reinterpret_cast<float *>(sm + ST);
+    const uint32_t bar = sb0 + MISC;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + MISC + 8);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + MISC + 12);
+    const int64_t tstride = (int64_t)H * DK;   // elements between tokens of q, k and dO
+    const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(p.q) + (tok0 * H + h) * DK;
+    const __nv_bfloat16 *kg = reinterpret_cast<const __nv_bfloat16 *>(p.k) + (tok0 * H + h) * DK;
+    const __nv_bfloat16 *dog = reinterpret_cast<const __nv_bfloat16 *>(p.dout) + (tok0 * H + h) * DK;
+
+    if (tid == 0) {
+        umma::mbar_init(bar, 1);
+        *abort_flag = 0;
+        umma::fence_mbar_init();
+    }
+    if (warp == 0) umma::tmem_alloc(tmem_holder, 256);
+    // gates: chunk-local cumulative log-gate (padding rows: g = 0, beta = 0), a warp scan per half
+    if (tid < 64) {
+        const int64_t th = (tok0 + tid) * H + h;
+        float x = tid < rows ? p.g[th] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        sb[tid] = x;
+        sbe[tid] = tid < rows ? p.beta[th] : 0.f;
+    }
+    {   // K, Q and dO rows into their tiles (rows past the sequence are zero): 12 16-B pieces a thread
+        uint4 w[12];
+#pragma unroll
+        for (int u = 0; u < 12; ++u) {
+            const int id = tid + u * kBT, m = id >> 10, r = (id >> 4) & 63, c8 = id & 15;
+            const __nv_bfloat16 *src = m == 0 ? kg : (m == 1 ? qg : dog);
+            w[u] = r < rows ? *reinterpret_cast<const uint4 *>(src + r * tstride + 8 * c8) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 12; ++u) {
+            const int id = tid + u * kBT, m = id >> 10, r = (id >> 4) & 63, c8 = id & 15;
+            const uint32_t o = m < 2 ? (uint32_t)(c8 >> 3) * 16384u + sw128_offset((uint32_t)(64 * m + r), (uint32_t)(c8 & 7) * 8u)
+                                     : DOT + (uint32_t)(c8 >> 3) * 8192u + sw128_offset((uint32_t)r, (uint32_t)(c8 & 7) * 8u);
+            *reinterpret_cast<uint4 *>(sm + o) = w[u];
+        }
+    }
+    umma::fence_proxy_async();
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tm = *tmem_holder;
+    uint32_t phase = 0;
+    auto wait_mma = [&]() -> bool {   // bounded; the verdict is the same for every thread
+        const bool ok = umma::mbar_wait(bar, phase, lt::kWaitNs);
+        if (!ok) {
+            *abort_flag = 1;
+            atomicExch(p.err, kDevErrTimeout);
+        }
+        phase ^= 1u;
+        const bool bad = __syncthreads_or(!ok || *abort_flag);
+        umma::fence_after_sync();
+        return !bad;
+    };
+    // nks K-steps into dcol; the low half of A joins unless a_exact, of B unless b_exact
+    auto mma = [&](uint32_t dcol, int N, bool a_mn, bool b_mn, int nks, auto ad, auto bd, bool a_exact, bool b_exact) {
+        const uint32_t id = umma::idesc_bf16(128, N, a_mn, b_mn);
+#pragma unroll 1
+        for (int ks = 0; ks < nks; ++ks) {
+            const uint64_t ah = ad(ks, 0), bh = bd(ks, 0);
+            umma::mma_ss(tm + dcol, ah, bh, id, ks > 0 ? 1u : 0u);
+            if (!b_exact) umma::mma_ss(tm + dcol, ah, bd(ks, 1), id, 1u);
+            if (!a_exact) umma::mma_ss(tm + dcol, ad(ks, 1), bh, id, 1u);
+        }
+    };
+    auto f = [](uint32_t u) { return __uint_as_float(u); };
+    const int q4 = warp & 3, hh = warp >> 2, R = 32 * q4 + lane;   // tensor-memory lane (row) and column half
+    const uint32_t trow = tm + ((uint32_t)(32 * q4) << 16);
+    const uint32_t DG = 0, DW = 0, DA = 128, DQ = 0;   // columns: G; then W and A^T dO; then dO^T Qd
+    auto ld32 = [&](uint32_t col, uint32_t (&u)[32]) {
+        umma::tmem_ld16(trow + col, *reinterpret_cast<uint32_t(*)[16]>(u));
+        umma::tmem_ld16(trow + col + 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16));
+        umma::tmem_wait_ld();
+    };
+
+    if (tid == 0) {   // G = [K; Q] K^T: A all 128 rows of [K; Q], B its first 64 (both K-major)
+        mma(DG, 64, false, false, 8, [&](int ks, int) { return lt::kmaj(sb0 + KQ, 128, ks); },
+            [&](int ks, int) { return lt::kmaj(sb0 + KQ, 128, ks); }, true, true);
+        umma::commit(bar);
+    }
+    if (tid >= 32 && tid < 64) sb[tid] += sb[31];
+    {   // norms: four threads a row, each a quarter of its columns, from the staged tiles
+        const int r = tid >> 2, qq = tid & 3;
+        float sk = 0.f, sq = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            const int c8 = 4 * qq + cc;
+            const uint32_t o = (uint32_t)(c8 >> 3) * 16384u + sw128_offset((uint32_t)r, (uint32_t)(c8 & 7) * 8u);
+            float kv[8], qv[8];
+            unpack8(*reinterpret_cast<const uint4 *>(sm + o), kv);
+            unpack8(*reinterpret_cast<const uint4 *>(sm + o + 8192u), qv);   // row 64 + r
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                sk += kv[e] * kv[e];
+                sq += qv[e] * qv[e];
+            }
+        }
+        sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+        sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+        if (qq == 0) {
+            snk[r] = p.l2 ? rsqrtf(sk + kL2Eps) : 1.f;
+            snq[r] = (p.l2 ? rsqrtf(sq + kL2Eps) : 1.f) * p.scale;
+        }
+    }
+    __syncthreads();
+    if (tid < 64) {
+        sgam[tid] = expf(sb[tid]);
+        sfk[tid] = expf(sb[63] - sb[tid]);
+        scoef[tid] = sbe[tid] * sgam[tid] * snk[tid];
+        blk[LY.b + tid] = sb[tid];
+    }
+    __syncthreads();
+    if (!wait_mma()) goto done;
+    {   // K^K^T (rows 0-63) and Q^K^T (rows 64-127), this thread's 32 columns
+        uint32_t u[32];
+        ld32(DG + 32 * hh, u);
+        if (R < 64) {
+            const int i = R;
+            const float ni = snk[i], bi = sbe[i], gi = sb[i];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int j = 32 * hh + e;
+                const float x = f(u[e]) * ni * snk[j];
+                blk[LY.kk + j * 64 + i] = x;   // symmetric: row j, column i is this row's entry j (coalesced)
+                sLT[j * 64 + i] = j < i ? bi * expf(gi - sb[j]) * x : 0.f;
+            }
+        } else {
+            const int q = R - 64;
+            const float nq = snq[q];
+            float *dst = blk + LY.qk + q * 64 + 32 * hh;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+                const int j = 32 * hh + e;
+                *reinterpret_cast<float4 *>(dst + e) =
+                    make_float4(f(u[e]) * nq * snk[j], f(u[e + 1]) * nq * snk[j + 1], f(u[e + 2]) * nq * snk[j + 2],
+                                f(u[e + 3]) * nq * snk[j + 3]);
+            }
+        }
+    }
+    __syncthreads();
+    // T = (I + L)^{-1} by the block rule (as bwd_prep_kernel), L read from its transpose
+    for (int e = tid; e < 64 * 64; e += kBT) {
+        const int r = e >> 6, cc = e & 63;
+        if ((cc >> 4) > (r >> 4)) sT[r * 65 + cc] = 0.f;
+    }
+    if (tid < 64) {
+        const int b0 = 16 * (tid >> 4), cc = tid & 15;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float acc = r == cc ? 1.f : 0.f;
+#pragma unroll
+            for (int i = 0; i < r; ++i) acc -= sLT[(b0 + i) * 64 + b0 + r] * x[i];
+            x[r] = acc;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) sT[(b0 + r) * 65 + b0 + cc] = x[r];
+    }
+    __syncthreads();
+    {
+        auto merge = [&](int nn, int a0, int b0, float *X, int e0, int estep) {
+            for (int e = e0; e < nn * nn; e += estep) {
+                const int r = e / nn, cc = e % nn;
+                float acc = 0.f;
+                for (int i = cc; i < nn; ++i) acc += sLT[(a0 + i) * 64 + b0 + r] * sT[(a0 + i) * 65 + a0 + cc];
+                X[e] = acc;
+            }
+            __syncthreads();
+            for (int e = e0; e < nn * nn; e += estep) {
+                const int r = e / nn, cc = e % nn;
+                float acc = 0.f;
+                for (int i = 0; i <= r; ++i) acc += sT[(b0 + r) * 65 + b0 + i] * X[i * nn + cc];
+                sT[(b0 + r) * 65 + a0 + cc] = -acc;
+            }
+            __syncthreads();
+        };
+        float *X = reinterpret_cast<float *>(sm + TD);
+        merge(16, 32 * (tid >> 7), 32 * (tid >> 7) + 16, X + 256 * (tid >> 7), tid & 127, 128);   // 16 -> 32, two at once
+        merge(32, 0, 32, X, tid, kBT);                                                            // 32 -> 64
+    }
+    for (int e = tid; e < 64 * 64; e += kBT) blk[LY.t + e] = sT[(e >> 6) * 65 + (e & 63)];
+    // T diag(beta gam / |k|) as a pair (A of the W product, K-major [i][r])
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int id = tid + u * kBT, i = id >> 3, c8 = id & 7;
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = sT[i * 65 + 8 * c8 + e] * scoef[8 * c8 + e];
+        lt::put8(sm + TD, sm + TD + 8192, 64, i, c8, v);
+    }
+    if (q4 >= 2) {   // A = (Q^K^T) o Gamma (lower, diagonal included) as a pair, [q][k], over L^T
+        const int q = R - 64;
+        uint32_t u[32];
+        ld32(DG + 32 * hh, u);
+        const float nq = snq[q], gq = sb[q];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int j = 32 * hh + 8 * cc + e;
+                v[e] = j <= q ? expf(gq - sb[j]) * f(u[8 * cc + e]) * nq * snk[j] : 0.f;
+            }
+            lt::put8(sm + LT, sm + LT + 8192, 64, q, 4 * hh + cc, v);
+        }
+    }
+    umma::fence_proxy_async();
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    if (tid == 0) {
+        // W = TD K: A [64 i][64 r] K-major (rows 64-127 of the product are not read), B = K [r][d] MN-major
+        mma(DW, 128, false, true, 4, [&](int ks, int lo) { return lt::kmaj(sb0 + TD + (lo ? 8192u : 0u), 64, ks); },
+            [&](int ks, int) { return lt::mnmaj(sb0 + KQ, 128, ks); }, false, true);
+        // A^T dO: A MN-major from the [q][k] tile (M = k), B = dO [q][j] MN-major
+        mma(DA, 128, true, true, 4, [&](int ks, int lo) { return lt::mnmaj(sb0 + LT + (lo ? 8192u : 0u), 64, ks); },
+            [&](int ks, int) { return lt::mnmaj(sb0 + DOT, 64, ks); }, false, true);
+        umma::commit(bar);
+    }
+    // while they run: q^, k^ (fp32) and Kd = diag(gC / gam / |k|) K as a pair of tiles, from the staged rows
+#pragma unroll 1
+    for (int u = 0; u < 4; ++u) {
+        const int id = tid + u * kBT, r = id >> 4, c8 = id & 15;
+        const uint32_t o = (uint32_t)(c8 >> 3) * 16384u + sw128_offset((uint32_t)r, (uint32_t)(c8 & 7) * 8u);
+        float kv[8], qv[8];
+        unpack8(*reinterpret_cast<const uint4 *>(sm + o), kv);
+        unpack8(*reinterpret_cast<const uint4 *>(sm + o + 8192u), qv);
+        const float rk = snk[r], rq = snq[r], fk = sfk[r] * rk;
+        float *qo = blk + LY.qh + r * DK + 8 * c8, *ko = blk + LY.kh + r * DK + 8 * c8;
+        *reinterpret_cast<float4 *>(qo) = make_float4(qv[0] * rq, qv[1] * rq, qv[2] * rq, qv[3] * rq);
+        *reinterpret_cast<float4 *>(qo + 4) = make_float4(qv[4] * rq, qv[5] * rq, qv[6] * rq, qv[7] * rq);
+        *reinterpret_cast<float4 *>(ko) = make_float4(kv[0] * rk, kv[1] * rk, kv[2] * rk, kv[3] * rk);
+        *reinterpret_cast<float4 *>(ko + 4) = make_float4(kv[4] * rk, kv[5] * rk, kv[6] * rk, kv[7] * rk);
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = fk * kv[e];
+        uint4 hi, lo;
+        split8(v, hi, lo);
+        uint8_t *kt = reinterpret_cast<uint8_t *>(blk + LY.kd) + (c8 >> 3) * 8192 + sw128_offset((uint32_t)r, (uint32_t)(c8 & 7) * 8u);
+        *reinterpret_cast<uint4 *>(kt) = hi;
+        *reinterpret_cast<uint4 *>(kt + 16384) = lo;
+    }
+    if (!wait_mma()) goto done;
+    if (q4 < 2) {   // rows 0-63: W as a pair of tiles [r][d], and A^T dO [k][j] (fp32)
+        const int i = R;
+        uint8_t *wt = reinterpret_cast<uint8_t *>(blk + LY.w);
+#pragma unroll 1
+        for (int g = 0; g < 2; ++g) {
+            const int d0 = 64 * hh + 32 * g;
+            uint32_t u[32];
+            ld32(DW + d0, u);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = f(u[8 * cc + e]);
+                uint4 hi, lo;
+                split8(v, hi, lo);
+                const int d = d0 + 8 * cc;
+                uint8_t *dst = wt + (d >> 6) * 8192 + sw128_offset((uint32_t)i, (uint32_t)(d & 63));
+                *reinterpret_cast<uint4 *>(dst) = hi;
+                *reinterpret_cast<uint4 *>(dst + 16384) = lo;
+            }
+            ld32(DA + d0, u);
+            float *ado = blk + LY.ado + i * DK + d0;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<float4 *>(ado + e) = make_float4(f(u[e]), f(u[e + 1]), f(u[e + 2]), f(u[e + 3]));
+        }
+    }
+    // diag(gam scale / |q|) dO as a pair [r][j] (A of dO^T Qd), over T and TD (their products are done)
+#pragma unroll 1
+    for (int u = 0; u < 4; ++u) {
+        const int id = tid + u * kBT, r = id >> 4, c8 = id & 15;
+        const uint32_t o = (uint32_t)(c8 >> 3) * 8192u + sw128_offset((uint32_t)r, (uint32_t)(c8 & 7) * 8u);
+        float v[8];
+        unpack8(*reinterpret_cast<const uint4 *>(sm + DOT + o), v);
+        const float sr = sgam[r] * snq[r];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] *= sr;
+        uint4 hi, lo;
+        split8(v, hi, lo);
+        *reinterpret_cast<uint4 *>(sm + SD + o) = hi;
+        *reinterpret_cast<uint4 *>(sm + SD + 16384 + o) = lo;
+    }
+    umma::fence_proxy_async();
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    if (tid == 0) {   // dO^T Qd: A MN-major from the scaled dO [r][j] (M = j), B = Q [r][d] MN-major
+        mma(DQ, 128, true, true, 4, [&](int ks, int lo) { return lt::mnmaj(sb0 + SD + (lo ? 16384u : 0u), 64, ks); },
+            [&](int ks, int) { return lt::mnmaj(sb0 + KQ + 8192, 128, ks); }, false, true);
+        umma::commit(bar);
+    }
+    if (!wait_mma()) goto done;
+    {   // dO^T Qd, all 128 rows j, stored transposed ([d][j]: a warp's rows of one column are one line)
+        float *dq = blk + LY.doq;
+#pragma unroll 1
+        for (int g = 0; g < 2; ++g) {
+            const int d0 = 64 * hh + 32 * g;
+            uint32_t u[32];
+            ld32(DQ + d0, u);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) dq[(d0 + e) * 128 + R] = f(u[e]);
+        }
+    }
+done:
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
@@ -1628,7 +2019,15 @@ cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t st)
         return e;
     if ((e = cudaFuncSetAttribute(bwd_local_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_local)))
         return e;
-    if (a.slots > 0) bwd_prep_kernel<T><<<dim3((unsigned)a.slots, a.gm.H), kBT, sm_prep, st>>>(p);
+    if (a.slots > 0) {
+        if (tc_local) {
+            if ((e = cudaFuncSetAttribute(bwd_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pp::kSmem)))
+                return e;
+            bwd_prep_tc_kernel<<<dim3((unsigned)a.slots, a.gm.H), kBT, pp::kSmem, st>>>(p);
+        } else {
+            bwd_prep_kernel<T><<<dim3((unsigned)a.slots, a.gm.H), kBT, sm_prep, st>>>(p);
+        }
+    }
     const dim3 sgrid(a.gm.N, a.gm.H, a.gm.dv / kScanRows);
     if (tc_scan) {
         // The forward scan on the tensor cores: the chunked forward itself, saving the state at every
