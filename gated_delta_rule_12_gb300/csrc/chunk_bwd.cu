@@ -1227,9 +1227,17 @@ bwd_local_tc_kernel(const BwdParams p)
             atomicAdd(&sgcol[lane + 32], gcol[1]);
         }
         __syncthreads();
-        // ---- phase 4: dQ += (dA o Gamma) K^;  dK += (dA o Gamma)^T Q^ + M K^ + M^T K^
-        stage_f32<64, 64>(sm + DVH, sm + DVH + 8192, sDA, 64, 64);   // dA o Gamma [r][i]
-        stage_f32<64, 64>(sm + DO, sm + DO + 8192, sDL, 64, 64);     // M [i][j]
+        // ---- phase 4: [dQ-part; dK-part] = [dA o Gamma; M + M^T] K^ (one product, all 128 rows), then
+        // dK-part += (dA o Gamma)^T Q^.  The stacked A tile sits at DVH (high) and DVL (low).
+        stage_f32<64, 64>(sm + DVH, sm + DVL, sDA, 64, 64);   // rows 0-63: dA o Gamma [r][i]
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {   // rows 64-127: M + M^T (M is symmetric in its use: d(K^K^T) = M)
+            const int id = tid + u * kBT, r = id >> 3, c8 = id & 7;
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = sDL[r * 64 + 8 * c8 + e] + sDL[(8 * c8 + e) * 64 + r];
+            put8(sm + DVH + 8192, sm + DVL + 8192, 64, r, c8, v);
+        }
         stage_f32<64, DK>(sm + BH, sm + BH + 16384, qh, DK, 64);     // Q^ over dW
         umma::fence_proxy_async();
         umma::fence_before_sync();
@@ -1238,31 +1246,11 @@ bwd_local_tc_kernel(const BwdParams p)
         const uint32_t C9 = 0, C10 = 128;
         if (tid == 0) {
             // K^ [i][d] as MN-major B (K = i), at VNH / VNL
-            auto khB = [&](int ks, int lo) { return mnmaj(sb0 + (lo ? VNL : VNH), 64, ks); };
-            mma(C9, 128, false, true, 4, [&](int ks, int lo) { return kmaj(sb0 + DVH + (lo ? 8192u : 0u), 64, ks); },
-                khB, false, false);
-            const uint32_t id = idesc_bf16(128, 128, true, true), idk = idesc_bf16(128, 128, false, true);
-            for (int ks = 0; ks < 4; ++ks) {   // (dA o Gamma)^T Q^: A MN-major from the [r][i] tile, K = r
-                const uint64_t ah = mnmaj(sb0 + DVH, 64, ks), al = mnmaj(sb0 + DVH + 8192, 64, ks);
-                const uint64_t bh = mnmaj(sb0 + BH, 64, ks), bl = mnmaj(sb0 + BH + 16384, 64, ks);
-                mma_ss(tm + C10, ah, bh, id, ks > 0 ? 1u : 0u);
-                mma_ss(tm + C10, ah, bl, id, 1u);
-                mma_ss(tm + C10, al, bh, id, 1u);
-            }
-            for (int ks = 0; ks < 4; ++ks) {   // M K^: A K-major [i][j], K = j
-                const uint64_t ah = kmaj(sb0 + DO, 64, ks), al = kmaj(sb0 + DO + 8192, 64, ks);
-                const uint64_t bh = khB(ks, 0), bl = khB(ks, 1);
-                mma_ss(tm + C10, ah, bh, idk, 1u);
-                mma_ss(tm + C10, ah, bl, idk, 1u);
-                mma_ss(tm + C10, al, bh, idk, 1u);
-            }
-            for (int ks = 0; ks < 4; ++ks) {   // M^T K^: A MN-major from the [j][i] tile, K = j
-                const uint64_t ah = mnmaj(sb0 + DO, 64, ks), al = mnmaj(sb0 + DO + 8192, 64, ks);
-                const uint64_t bh = khB(ks, 0), bl = khB(ks, 1);
-                mma_ss(tm + C10, ah, bh, id, 1u);
-                mma_ss(tm + C10, ah, bl, id, 1u);
-                mma_ss(tm + C10, al, bh, id, 1u);
-            }
+            mma(C9, 128, false, true, 4, [&](int ks, int lo) { return kmaj(sb0 + (lo ? DVL : DVH), 128, ks); },
+                [&](int ks, int lo) { return mnmaj(sb0 + (lo ? VNL : VNH), 64, ks); }, false, false);
+            // (dA o Gamma)^T Q^: A MN-major from rows 0-63 of the stacked tile (M = i, K = r)
+            mma(C10, 128, true, true, 4, [&](int ks, int lo) { return mnmaj(sb0 + (lo ? DVL : DVH), 64, ks); },
+                [&](int ks, int lo) { return mnmaj(sb0 + BH + (lo ? 16384u : 0u), 64, ks); }, false, false);
             umma::commit(bar);
         }
         if (!wait_all()) goto done;
@@ -1279,9 +1267,25 @@ bwd_local_tc_kernel(const BwdParams p)
         // 4-float pad so the rows a warp reads start in different banks), over tiles no product reads any more
         float *fQ = reinterpret_cast<float *>(sm + VNH), *fK = reinterpret_cast<float *>(sm + BH);
         constexpr int PF = DK + 4;
+        const uint32_t a0 = tm + ((uint32_t)(32 * q4) << 16);
+        if (!reader) {   // rows 64-127 of C9 (the (M + M^T) K^ part of dK) into fK first
+            const int r = row - 64;
+#pragma unroll 1
+            for (int g = 0; g < 2; ++g) {
+                const int d0 = 64 * half + 32 * g;
+                uint32_t u[32];
+                umma::tmem_ld16(a0 + C9 + d0, *reinterpret_cast<uint32_t(*)[16]>(u));
+                umma::tmem_ld16(a0 + C9 + d0 + 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16));
+                umma::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4 *>(fK + r * PF + d0 + e) = make_float4(f(u[e]), f(u[e + 1]), f(u[e + 2]), f(u[e + 3]));
+            }
+        }
+        __syncthreads();
         if (reader) {
-            // columns [64 half, 64 half + 64) of C9 (dQ), then the same columns of C10 (dK): one rolled loop
-            const uint32_t a0 = tm + ((uint32_t)(32 * q4) << 16);
+            // columns [64 half, 64 half + 64) of C9 (dQ), then the same columns of C10 (dK, added to the
+            // part already in fK): one rolled loop
 #pragma unroll 1
             for (int g = 0; g < 4; ++g) {
                 const bool kpart = g >= 2;
@@ -1295,11 +1299,11 @@ bwd_local_tc_kernel(const BwdParams p)
                 float *dst = (kpart ? fK : fQ) + row * PF + d0;
 #pragma unroll
                 for (int e = 0; e < 32; e += 4) {
-                    float4 a;
-                    a.x = src[e * 64] + f(u[e]);
-                    a.y = src[(e + 1) * 64] + f(u[e + 1]);
-                    a.z = src[(e + 2) * 64] + f(u[e + 2]);
-                    a.w = src[(e + 3) * 64] + f(u[e + 3]);
+                    float4 a = kpart ? *reinterpret_cast<const float4 *>(dst + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    a.x += src[e * 64] + f(u[e]);
+                    a.y += src[(e + 1) * 64] + f(u[e + 1]);
+                    a.z += src[(e + 2) * 64] + f(u[e + 2]);
+                    a.w += src[(e + 3) * 64] + f(u[e + 3]);
                     *reinterpret_cast<float4 *>(dst + e) = a;
                 }
             }
