@@ -141,3 +141,25 @@ def test_bwd_full_size_sampled_heads():
                                    dfinal=dS[n:n + 1, h:h + 1], scale=w.scale, use_qk_l2norm=True)
         got = [t[n:n + 1, :, h:h + 1] for t in out[:5]] + [out[5][n:n + 1, h:h + 1]]
         check_all(got, ref, "bf16")
+
+
+@pytest.mark.parametrize("L", [1, 17, 65])
+def test_bwd_tensor_core_path_short_sequences(L):
+    """bf16 with dk = dv = 128 runs the tensor-core prep, reverse scan and local kernels: one-token
+    chunks, a ragged single chunk and a ragged second chunk, with initial and final state gradients."""
+    d = inputs.make_prefill(B=3, L=L, H=2, dk=128, dv=128, dtype="bf16", seed=77, decay=0.3, init_state=True)
+    dO, dS = cotangents(d, 78)
+    out, ref = grads(d, dO, dS, 128)
+    check_all(out, ref, "bf16")
+
+
+def test_bwd_tensor_core_path_without_l2norm_and_without_state_gradients():
+    """The tensor-core kernels without the L2 normalisation (pre-normalised inputs), no final-state
+    cotangent and no initial-state gradient requested."""
+    d = inputs.make_prefill(B=2, L=130, H=2, dk=128, dv=128, dtype="f32", seed=79, decay=0.2)
+    d["q"] = (d["q"] / d["q"].norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    d["k"] = (d["k"] / d["k"].norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    d["v"] = d["v"].to(torch.bfloat16)
+    dO, _ = cotangents(d, 80, with_state=False)
+    out, ref = grads(d, dO, None, 128, l2=False, want_dinit=False)
+    check_all(out, ref, "bf16")
