@@ -790,29 +790,38 @@ __device__ __noinline__ void stage_f32(uint8_t *hi, uint8_t *lo, const float *sr
     }
 }
 
-// bf16 (high, low) tile pairs of BYTES bytes each, stored high then low at src in the layout of the
-// tiles at hi and lo, copied over those tiles; returns this thread's part of sum(new * old), each
-// entry read as high + low (about 16 significand bits).  Consecutive threads take consecutive 16-B
-// pieces, so the global loads coalesce and the shared-memory accesses are conflict-free.
+// bf16 (high, low) tile pairs of BYTES bytes each, stored high then low in the layout of the tiles at
+// hi and lo: pairs_load issues this thread's 16-B pieces (consecutive threads take consecutive pieces,
+// so the loads coalesce) and pairs_store_dot later writes them over the tiles, returning this thread's
+// part of sum(new * old), each entry read as high + low (about 16 significand bits).  Split so that the
+// loads can be in flight while the products that still read the old tiles finish.
 template <int BYTES>
-__device__ __noinline__ float copy_pairs_dot_old(uint8_t *hi, uint8_t *lo, const uint8_t *src)
-{
-    constexpr int NI = BYTES / 16 / kBT;
+struct PairPieces {
+    static constexpr int NI = BYTES / 16 / kBT;
     static_assert(NI * 16 * kBT == BYTES, "whole pieces per thread");
     uint4 nh[NI], nl[NI];
+};
+template <int BYTES>
+__device__ __forceinline__ void pairs_load(PairPieces<BYTES> &pp, const uint8_t *src)
+{
 #pragma unroll
-    for (int u = 0; u < NI; ++u) {
+    for (int u = 0; u < PairPieces<BYTES>::NI; ++u) {
         const uint32_t o = (threadIdx.x + u * kBT) * 16u;
-        nh[u] = *reinterpret_cast<const uint4 *>(src + o);
-        nl[u] = *reinterpret_cast<const uint4 *>(src + BYTES + o);
+        pp.nh[u] = *reinterpret_cast<const uint4 *>(src + o);
+        pp.nl[u] = *reinterpret_cast<const uint4 *>(src + BYTES + o);
     }
+}
+template <int BYTES>
+__device__ __forceinline__ float pairs_store_dot(uint8_t *hi, uint8_t *lo, const PairPieces<BYTES> &pp)
+{
     float dot = 0.f;
 #pragma unroll
-    for (int u = 0; u < NI; ++u) {
+    for (int u = 0; u < PairPieces<BYTES>::NI; ++u) {
         const uint32_t o = (threadIdx.x + u * kBT) * 16u;
         const uint4 oh = *reinterpret_cast<const uint4 *>(hi + o), ol = *reinterpret_cast<const uint4 *>(lo + o);
         const uint32_t ohw[4] = {oh.x, oh.y, oh.z, oh.w}, olw[4] = {ol.x, ol.y, ol.z, ol.w};
-        const uint32_t nhw[4] = {nh[u].x, nh[u].y, nh[u].z, nh[u].w}, nlw[4] = {nl[u].x, nl[u].y, nl[u].z, nl[u].w};
+        const uint32_t nhw[4] = {pp.nh[u].x, pp.nh[u].y, pp.nh[u].z, pp.nh[u].w};
+        const uint32_t nlw[4] = {pp.nl[u].x, pp.nl[u].y, pp.nl[u].z, pp.nl[u].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ohw[e]));
@@ -821,8 +830,8 @@ __device__ __noinline__ float copy_pairs_dot_old(uint8_t *hi, uint8_t *lo, const
             const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&nlw[e]));
             dot += (x.x + y.x) * (a.x + b.x) + (x.y + y.y) * (a.y + b.y);
         }
-        *reinterpret_cast<uint4 *>(hi + o) = nh[u];
-        *reinterpret_cast<uint4 *>(lo + o) = nl[u];
+        *reinterpret_cast<uint4 *>(hi + o) = pp.nh[u];
+        *reinterpret_cast<uint4 *>(lo + o) = pp.nl[u];
     }
     return dot;
 }
@@ -986,10 +995,13 @@ bwd_local_tc_kernel(const BwdParams p)
             [&](int ks, int lo) { return kmaj(sb0 + (lo ? VNL : VNH), 64, ks); }, true, false);
         umma::commit(bar);
     }
+    // dS' (saved by the reverse scan as bf16 high and low tiles): loads in flight while the products run
+    PairPieces<DV * DK * 2> dsp;
+    pairs_load(dsp, reinterpret_cast<const uint8_t *>(dSn));
     bool ok = wait_all();
     if (ok) {
-        // dS' (saved by the reverse scan as bf16 high and low tiles) over S; dgC = <dS', S> on the way
-        sred[tid] = copy_pairs_dot_old<DV * DK * 2>(sm + BH, sm + BL, reinterpret_cast<const uint8_t *>(dSn));
+        // dS' over S; dgC = <dS', S> on the way
+        sred[tid] = pairs_store_dot(sm + BH, sm + BL, dsp);
         umma::fence_proxy_async();
         umma::fence_before_sync();
         __syncthreads();
