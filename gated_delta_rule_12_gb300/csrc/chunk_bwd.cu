@@ -856,6 +856,65 @@ __device__ __noinline__ void stage_bf16(uint8_t *dst, const __nv_bfloat16 *src, 
     }
 }
 
+// An fp32 [R][C] block (row stride ld, rows >= valid zero) or a bf16 [R][C] block held in registers
+// between its loads and its staging into tiles (the layouts of stage_f32 and stage_bf16), so that the
+// loads can be in flight while earlier work finishes.
+template <int R, int C>
+struct F32Block {
+    static constexpr int per_row = C / 8, NI = R * per_row / kBT;
+    static_assert(NI * kBT == R * per_row, "whole chunks per thread");
+    float4 a[NI], b[NI];
+};
+template <int R, int C>
+__device__ __forceinline__ void f32_load(F32Block<R, C> &t, const float *src, int ld, int valid)
+{
+#pragma unroll
+    for (int u = 0; u < F32Block<R, C>::NI; ++u) {
+        const int id = threadIdx.x + u * kBT, r = id / F32Block<R, C>::per_row, c8 = id % F32Block<R, C>::per_row;
+        if (r < valid) {
+            t.a[u] = *reinterpret_cast<const float4 *>(src + (int64_t)r * ld + 8 * c8);
+            t.b[u] = *reinterpret_cast<const float4 *>(src + (int64_t)r * ld + 8 * c8 + 4);
+        } else {
+            t.a[u] = t.b[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+}
+template <int R, int C>
+__device__ __forceinline__ void f32_put(uint8_t *hi, uint8_t *lo, const F32Block<R, C> &t)
+{
+#pragma unroll
+    for (int u = 0; u < F32Block<R, C>::NI; ++u) {
+        const int id = threadIdx.x + u * kBT, r = id / F32Block<R, C>::per_row, c8 = id % F32Block<R, C>::per_row;
+        const float v[8] = {t.a[u].x, t.a[u].y, t.a[u].z, t.a[u].w, t.b[u].x, t.b[u].y, t.b[u].z, t.b[u].w};
+        put8(hi, lo, R, r, c8, v);
+    }
+}
+template <int R, int C>
+struct Bf16Block {
+    static constexpr int per_row = C / 8, NI = R * per_row / kBT;
+    static_assert(NI * kBT == R * per_row, "whole chunks per thread");
+    uint4 w[NI];
+};
+template <int R, int C>
+__device__ __forceinline__ void bf16_load(Bf16Block<R, C> &t, const __nv_bfloat16 *src, int64_t ld, int valid)
+{
+#pragma unroll
+    for (int u = 0; u < Bf16Block<R, C>::NI; ++u) {
+        const int id = threadIdx.x + u * kBT, r = id / Bf16Block<R, C>::per_row, c8 = id % Bf16Block<R, C>::per_row;
+        t.w[u] = r < valid ? *reinterpret_cast<const uint4 *>(src + r * ld + 8 * c8) : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+template <int R, int C>
+__device__ __forceinline__ void bf16_put(uint8_t *dst, const Bf16Block<R, C> &t)
+{
+#pragma unroll
+    for (int u = 0; u < Bf16Block<R, C>::NI; ++u) {
+        const int id = threadIdx.x + u * kBT, r = id / Bf16Block<R, C>::per_row, c8 = id % Bf16Block<R, C>::per_row;
+        const uint32_t o = (uint32_t)(c8 >> 3) * (uint32_t)R * 128u + sw128_offset((uint32_t)r, (uint32_t)(c8 & 7) * 8u);
+        *reinterpret_cast<uint4 *>(dst + o) = t.w[u];
+    }
+}
+
 // K-step ks (16 elements of K) of a tile of R rows read as a K-major operand (K along the columns)
 __device__ __forceinline__ uint64_t kmaj(uint32_t base, int R, int ks)
 {
@@ -997,6 +1056,9 @@ bwd_local_tc_kernel(const BwdParams p)
     }
     // dS' (saved by the reverse scan as bf16 high and low tiles): loads in flight while the products run
     PairPieces<DV * DK * 2> dsp;
+    F32Block<64, 64> nT;     // the phase-2 operands T, K^ and V, loaded during the next product
+    F32Block<64, DK> nK;
+    Bf16Block<64, DV> nV;
     pairs_load(dsp, reinterpret_cast<const uint8_t *>(dSn));
     bool ok = wait_all();
     if (ok) {
@@ -1034,6 +1096,9 @@ bwd_local_tc_kernel(const BwdParams p)
                 }
             });
         }
+        f32_load(nT, Tm, 64, 64);
+        f32_load(nK, kh, DK, 64);
+        bf16_load(nV, Vraw, tstride, rows);
         ok = wait_all();
     }
     if (ok) {
@@ -1066,10 +1131,10 @@ bwd_local_tc_kernel(const BwdParams p)
     umma::fence_before_sync();
     __syncthreads();
     if (*abort_flag) goto done;
-    // phase 2 operands: T, K^ (over V_new) and V (bf16, over dS' lo)
-    stage_f32<64, 64>(sm + TT, sm + TT + 8192, Tm, 64, 64);
-    stage_f32<64, DK>(sm + VNH, sm + VNL, kh, DK, 64);
-    stage_bf16<64, DV>(sm + BL, Vraw, tstride, rows);
+    // phase 2 operands (loaded above): T, K^ (over V_new) and V (bf16, over dS' lo)
+    f32_put(sm + TT, sm + TT + 8192, nT);
+    f32_put(sm + VNH, sm + VNL, nK);
+    bf16_put(sm + BL, nV);
     umma::fence_proxy_async();
     umma::fence_before_sync();
     __syncthreads();
