@@ -1274,6 +1274,8 @@ bwd_local_tc_kernel(const BwdParams p)
             });
         __syncthreads();
         // ---- the 64 x 64 pass (as bwd_local_kernel): GG's row and column sums, dbeta, dA o Gamma, M
+        F32Block<64, DK> nQ;   // Q^ for phase 4, loaded during the pass
+        f32_load(nQ, qh, DK, 64);
         {
             if (!wait_copies()) goto done;
             const float *KK = reinterpret_cast<const float *>(sm + BH), *QK = reinterpret_cast<const float *>(sm + BH + 16384);
@@ -1315,7 +1317,7 @@ bwd_local_tc_kernel(const BwdParams p)
             for (int e = 0; e < 8; ++e) v[e] = sDL[r * 64 + 8 * c8 + e] + sDL[(8 * c8 + e) * 64 + r];
             put8(sm + DVH + 8192, sm + DVL + 8192, 64, r, c8, v);
         }
-        stage_f32<64, DK>(sm + BH, sm + BH + 16384, qh, DK, 64);     // Q^ over dW
+        f32_put(sm + BH, sm + BH + 16384, nQ);                       // Q^ over K^K^T and Q^K^T
         umma::fence_proxy_async();
         umma::fence_before_sync();
         __syncthreads();
@@ -1330,7 +1332,6 @@ bwd_local_tc_kernel(const BwdParams p)
                 [&](int ks, int lo) { return mnmaj(sb0 + BH + (lo ? 16384u : 0u), 64, ks); }, false, false);
             umma::commit(bar);
         }
-        if (!wait_all()) goto done;
         if (warp == 0) {   // q and k rows of the chunk for the normalisation: bulk copies over T and the dA staging
             if (lane == 0) umma::mbar_expect_tx(cbar, (uint32_t)(2 * rows * DK * 2));
             __syncwarp();
@@ -1340,6 +1341,12 @@ bwd_local_tc_kernel(const BwdParams p)
                 umma::bulk_load(sb0 + FA + (uint32_t)r * 256u, reinterpret_cast<const T *>(p.k) + th * DK, 256, cbar);
             }
         }
+        float pq[64];   // this reader's dQ^ scratch entries, loaded while the products run
+        if (reader) {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) pq[e] = dQt[(64 * half + e) * 64 + row];
+        }
+        if (!wait_all()) goto done;
         // the finished dQ and dK rows, fp32 [64][132] each (33 KB: VNH .. DVH + 1 KB and BH .. BL + 1 KB; a
         // 4-float pad so the rows a warp reads start in different banks), over tiles no product reads any more
         float *fQ = reinterpret_cast<float *>(sm + VNH), *fK = reinterpret_cast<float *>(sm + BH);
@@ -1361,22 +1368,34 @@ bwd_local_tc_kernel(const BwdParams p)
         }
         __syncthreads();
         if (reader) {
-            // columns [64 half, 64 half + 64) of C9 (dQ), then the same columns of C10 (dK, added to the
-            // part already in fK): one rolled loop
-#pragma unroll 1
-            for (int g = 0; g < 4; ++g) {
-                const bool kpart = g >= 2;
-                const int d0 = 64 * half + 32 * (g & 1);
+            // columns [64 half, 64 half + 64) of C9 (dQ, with the prefetched scratch), then the same
+            // columns of C10 (dK, added to the part already in fK)
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                const int d0 = 64 * half + 32 * g;
                 uint32_t u[32];
-                const uint32_t col = (kpart ? C10 : C9) + (uint32_t)d0;
-                umma::tmem_ld16(a0 + col, *reinterpret_cast<uint32_t(*)[16]>(u));
-                umma::tmem_ld16(a0 + col + 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16));
+                umma::tmem_ld16(a0 + C9 + d0, *reinterpret_cast<uint32_t(*)[16]>(u));
+                umma::tmem_ld16(a0 + C9 + d0 + 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16));
                 umma::tmem_wait_ld();
-                const float *src = (kpart ? dKt : dQt) + d0 * 64 + row;
-                float *dst = (kpart ? fK : fQ) + row * PF + d0;
+                float *dst = fQ + row * PF + d0;
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4 *>(dst + e) =
+                        make_float4(pq[32 * g + e] + f(u[e]), pq[32 * g + e + 1] + f(u[e + 1]),
+                                    pq[32 * g + e + 2] + f(u[e + 2]), pq[32 * g + e + 3] + f(u[e + 3]));
+            }
+#pragma unroll 1
+            for (int g = 0; g < 2; ++g) {
+                const int d0 = 64 * half + 32 * g;
+                uint32_t u[32];
+                umma::tmem_ld16(a0 + C10 + d0, *reinterpret_cast<uint32_t(*)[16]>(u));
+                umma::tmem_ld16(a0 + C10 + d0 + 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16));
+                umma::tmem_wait_ld();
+                const float *src = dKt + d0 * 64 + row;
+                float *dst = fK + row * PF + d0;
 #pragma unroll
                 for (int e = 0; e < 32; e += 4) {
-                    float4 a = kpart ? *reinterpret_cast<const float4 *>(dst + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    float4 a = *reinterpret_cast<const float4 *>(dst + e);
                     a.x += src[e * 64] + f(u[e]);
                     a.y += src[(e + 1) * 64] + f(u[e + 1]);
                     a.z += src[(e + 2) * 64] + f(u[e + 2]);
