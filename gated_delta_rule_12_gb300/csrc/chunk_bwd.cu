@@ -1102,18 +1102,32 @@ bwd_local_tc_kernel(const BwdParams p)
         ok = wait_all();
     }
     if (ok) {
-        // dK = fk dKd (dkdf += K^ . dKd); dW = -dW' into its tiles over dS'
+        // phase 2 operands (loaded above): T, K^ (over V_new, which the V_new dS' product has read) and V
+        // (bf16, over dS' lo)
+        f32_put(sm + TT, sm + TT + 8192, nT);
+        f32_put(sm + VNH, sm + VNL, nK);
+        bf16_put(sm + BL, nV);
+        __syncthreads();
+        // dK = fk dKd (dkdf += K^ . dKd, K^ read from its tiles); dW = -dW' into its tiles over dS'
         if (reader) {
             float acc = 0.f;
             const float fk = sfk[row];
             row_groups(C3 + 64 * half, 2, [&](const uint32_t (&u)[32], int b) {
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
+                for (int e = 0; e < 32; e += 8) {
                     const int d = 64 * half + b + e;
-                    const float4 kv = *reinterpret_cast<const float4 *>(kh + row * DK + d);
-                    acc += kv.x * f(u[e]) + kv.y * f(u[e + 1]) + kv.z * f(u[e + 2]) + kv.w * f(u[e + 3]);
+                    const uint32_t o = (uint32_t)(d >> 6) * 8192u + sw128_offset((uint32_t)row, (uint32_t)(d & 63));
+                    const uint4 kh4 = *reinterpret_cast<const uint4 *>(sm + VNH + o);
+                    const uint4 kl4 = *reinterpret_cast<const uint4 *>(sm + VNL + o);
+                    const uint32_t hw[4] = {kh4.x, kh4.y, kh4.z, kh4.w}, lw[4] = {kl4.x, kl4.y, kl4.z, kl4.w};
 #pragma unroll
-                    for (int x = 0; x < 4; ++x) dKt[(d + x) * 64 + row] = fk * f(u[e + x]);
+                    for (int x = 0; x < 4; ++x) {
+                        const float2 ka = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&hw[x]));
+                        const float2 kc = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&lw[x]));
+                        acc += (ka.x + kc.x) * f(u[e + 2 * x]) + (ka.y + kc.y) * f(u[e + 2 * x + 1]);
+                    }
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) dKt[(d + x) * 64 + row] = fk * f(u[e + x]);
                 }
             });
             atomicAdd(&sdkdf[row], acc);
@@ -1128,17 +1142,11 @@ bwd_local_tc_kernel(const BwdParams p)
             });
         }
     }
-    umma::fence_before_sync();
-    __syncthreads();
-    if (*abort_flag) goto done;
-    // phase 2 operands (loaded above): T, K^ (over V_new) and V (bf16, over dS' lo)
-    f32_put(sm + TT, sm + TT + 8192, nT);
-    f32_put(sm + VNH, sm + VNL, nK);
-    bf16_put(sm + BL, nV);
     umma::fence_proxy_async();
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
+    if (*abort_flag) goto done;
     {
         // ---- phase 2: T^T dV_new, T^T dW, dV_new V^T, dW K^^T
         const uint32_t C5a = 0, C5b = 128, C6a = 256, C6b = 320;
