@@ -1056,10 +1056,15 @@ bwd_local_tc_kernel(const BwdParams p)
     }
     // dS' (saved by the reverse scan as bf16 high and low tiles): loads in flight while the products run
     PairPieces<DV * DK * 2> dsp;
+    float4 qpre[16];         // a reader's 64 entries of its q^ row, for the dQd epilogue
     F32Block<64, 64> nT;     // the phase-2 operands T, K^ and V, loaded during the next product
     F32Block<64, DK> nK;
     Bf16Block<64, DV> nV;
     pairs_load(dsp, reinterpret_cast<const uint8_t *>(dSn));
+    if (reader) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) qpre[e] = *reinterpret_cast<const float4 *>(qh + row * DK + 64 * half + 4 * e);
+    }
     bool ok = wait_all();
     if (ok) {
         // dS' over S; dgC = <dS', S> on the way
@@ -1077,16 +1082,22 @@ bwd_local_tc_kernel(const BwdParams p)
         if (reader) {
             float acc = 0.f;
             const float g = sgam[row];
-            row_groups(C1a + 64 * half, 2, [&](const uint32_t (&u)[32], int b) {
+            const uint32_t a1 = tm + ((uint32_t)(32 * q4) << 16) + C1a + 64 * half;
+#pragma unroll
+            for (int gg = 0; gg < 2; ++gg) {   // unrolled: the prefetched q^ entries stay in registers
+                uint32_t u[32];
+                umma::tmem_ld16(a1 + 32 * gg, *reinterpret_cast<uint32_t(*)[16]>(u));
+                umma::tmem_ld16(a1 + 32 * gg + 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16));
+                umma::tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 32; e += 4) {
-                    const int d = 64 * half + b + e;
-                    const float4 qv = *reinterpret_cast<const float4 *>(qh + row * DK + d);
+                    const int d = 64 * half + 32 * gg + e;
+                    const float4 qv = qpre[(32 * gg + e) >> 2];
                     acc += qv.x * f(u[e]) + qv.y * f(u[e + 1]) + qv.z * f(u[e + 2]) + qv.w * f(u[e + 3]);
 #pragma unroll
                     for (int x = 0; x < 4; ++x) dQt[(d + x) * 64 + row] = g * f(u[e + x]);
                 }
-            });
+            }
             atomicAdd(&sdgam[row], acc);
             row_groups(C4 + 32 * half, 1, [&](const uint32_t (&u)[32], int) {
 #pragma unroll
