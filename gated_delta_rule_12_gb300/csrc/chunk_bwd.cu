@@ -1262,6 +1262,8 @@ bwd_local_tc_kernel(const BwdParams p)
                 [&](int ks, int lo) { return mnmaj(sb0 + DO + (lo ? 8192u : 0u), 64, ks); }, false, false);
             umma::commit(bar);
         }
+        F32Block<64, DK> nQ;   // Q^ for phase 4, loaded while phase 3 runs
+        f32_load(nQ, qh, DK, 64);
         if (!wait_all()) goto done;
         if (reader)   // X row i, this warp's 32 columns -> X tiles (K-major [i][r])
             row_groups(C7 + 32 * half, 1, [&](const uint32_t (&u)[32], int) {
@@ -1293,8 +1295,6 @@ bwd_local_tc_kernel(const BwdParams p)
             });
         __syncthreads();
         // ---- the 64 x 64 pass (as bwd_local_kernel): GG's row and column sums, dbeta, dA o Gamma, M
-        F32Block<64, DK> nQ;   // Q^ for phase 4, loaded during the pass
-        f32_load(nQ, qh, DK, 64);
         {
             if (!wait_copies()) goto done;
             const float *KK = reinterpret_cast<const float *>(sm + BH), *QK = reinterpret_cast<const float *>(sm + BH + 16384);
