@@ -156,11 +156,16 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
  *   workspace     at least gdn_chunk_bwd_workspace_size() bytes, 256-byte aligned
  *                 (fp32 intermediates, about 0.66 MB per chunk and head at
  *                 dk = dv = 128).
- * The kernels are fp32 on the CUDA cores (products on the tensor cores as three
- * tf32 passes, fp32-accurate); dk in {64, 128, 256}, dv as gdn_chunk_fwd.  For
- * bf16 inputs with dk = 128 and dv a multiple of 128 the chunk-start states and
- * V_new come from the tensor-core chunked forward (its precision, see
- * gdn_chunk_fwd); everything else stays fp32.
+ * dk in {64, 128, 256}, dv as gdn_chunk_fwd.  fp32 inputs and other head sizes run
+ * fp32 kernels on the CUDA cores (products on the tensor cores as three tf32 passes,
+ * fp32-accurate).  For bf16 inputs with dk = 128 and dv a multiple of 128 the
+ * chunk-start states and V_new come from the tensor-core chunked forward (its
+ * precision, see gdn_chunk_fwd); with dk = dv = 128 every step runs on the tcgen05
+ * tensor cores, fp32 intermediates entering each product as a bf16 (high, low) pair
+ * (high.high + high.low + low.high in an fp32 accumulator, which keeps about 16
+ * significand bits) and the raw bf16 inputs as exact operands.  Five launches then:
+ * prep, the chunk-local and saving-recurrence pair of the forward scan, the reverse
+ * scan and the local step.
  * Errors: GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA.
  */
 size_t gdn_chunk_bwd_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv,
