@@ -989,7 +989,7 @@ bwd_local_tc_kernel(const BwdParams p)
     if (tid < 64) sfk[tid] = expf(sb[63] - sb[tid]);   // gC / gam
     const float gC = expf(sb[63]);
     uint32_t phase = 0;
-    // bounded wait for the MMAs committed so far; the verdict is the same for every thread
+    // bounded wait for the MMAs committed so far; the outcome is the same for every thread
     auto wait_all = [&]() -> bool {
         bool ok = umma::mbar_wait(bar, phase, kWaitNs);
         if (!ok) {
@@ -1579,7 +1579,7 @@ bwd_scan_tc_kernel(const BwdParams p)
     const uint32_t D1 = 0, D2 = 128;   // dV_new^T [128 j][64 r];  dO^T Qd - dV_new^T W [128 j][128 d]
     const uint32_t trow = tm + ((uint32_t)(32 * q4) << 16);
     uint32_t phase = 0;
-    auto wait_mma = [&]() -> bool {   // bounded; the verdict is the same for every thread
+    auto wait_mma = [&]() -> bool {   // bounded; the outcome is the same for every thread
         const bool ok = umma::mbar_wait(bar, phase, lt::kWaitNs);
         if (!ok) {
             *abort_flag = 1;
@@ -1838,7 +1838,7 @@ bwd_prep_tc_kernel(const BwdParams p)
     umma::fence_after_sync();
     const uint32_t tm = *tmem_holder;
     uint32_t phase = 0;
-    auto wait_mma = [&]() -> bool {   // bounded; the verdict is the same for every thread
+    auto wait_mma = [&]() -> bool {   // bounded; the outcome is the same for every thread
         const bool ok = umma::mbar_wait(bar, phase, lt::kWaitNs);
         if (!ok) {
             *abort_flag = 1;
