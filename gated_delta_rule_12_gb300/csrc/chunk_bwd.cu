@@ -1502,6 +1502,11 @@ done:
 // local kernel reads it back in that form), and dO^T Qd is read in its transposed layout, so every
 // global access of the chain is coalesced.
 // ---------------------------------------------------------------------------
+// This grid may run beside the saving forward scan launched before it (programmatic dependent
+// launch): it reads nothing that scan writes, and waits for that grid to complete (and its writes
+// to be visible) before it exits, so that the kernels after it see both.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 namespace rs {
 constexpr uint32_t SAH = 0, SAL = 32768;        // dS'^T [128 d][128 j] high, low (A, MN-major)
 constexpr uint32_t KDH = 65536, KDL = 81920;    // Kd [64 r][128 d]
@@ -1546,6 +1551,7 @@ bwd_scan_tc_kernel(const BwdParams p)
 #pragma unroll
             for (int e = 0; e < 64; e += 4)
                 *reinterpret_cast<float4 *>(p.dinit + soff + e) = make_float4(dS[e], dS[e + 1], dS[e + 2], dS[e + 3]);
+        grid_dep_wait();
         return;
     }
     const uint32_t bar = sb0 + MISC, kbar = sb0 + MISC + 16, wbar = sb0 + MISC + 24;
@@ -1720,6 +1726,7 @@ bwd_scan_tc_kernel(const BwdParams p)
     __syncthreads();
     umma::fence_after_sync();
     if (warp == 0) umma::tmem_dealloc(tm, 256);
+    grid_dep_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -2170,7 +2177,18 @@ cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t st)
         if ((e = cudaFuncSetAttribute(bwd_scan_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)rs::kSmem)))
             return e;
-        bwd_scan_tc_kernel<T><<<dim3(a.gm.N, a.gm.H), kBT, rs::kSmem, st>>>(p);
+        // beside the saving forward scan: it may start once that grid's CTAs are all resident
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(a.gm.N, a.gm.H);
+        cfg.blockDim = dim3(kBT);
+        cfg.dynamicSmemBytes = rs::kSmem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&cfg, bwd_scan_tc_kernel<T>, p))) return e;
     } else {
         bwd_bwd_scan_kernel<T><<<sgrid, kBT, sm_scan, st>>>(p);
     }

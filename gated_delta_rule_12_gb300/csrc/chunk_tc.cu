@@ -918,6 +918,11 @@ recur_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
     const uint32_t sb = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = blockIdx.x, h = blockIdx.y, j0 = blockIdx.z * 128;
+    // The backward's reverse scan does not read what this saving instance writes: it may start on
+    // the free SMs once every CTA of this grid is resident (programmatic dependent launch; without
+    // a programmatic dependent this is a no-op).
+    if constexpr (SAVE)
+        if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const Geometry gm = p.gm;
     const int H = gm.H, dv = gm.dv;
     int64_t tok0;
