@@ -248,8 +248,6 @@ struct BwdParams {
     float *dg, *dbeta, *dinit;
     float *ws;                      // per (slot, head) blocks of BwdLayout
     int need_u;                     // U~ is only read by the CUDA-core forward scan
-    int tc_scan;                    // reverse scan on the tensor cores (bf16, dk = dv = 128): dO^T Qd is
-                                    // stored transposed, [dk][dv], and dS' as bf16 (high, low) tiles
     int s_t;                        // the chunk-start states are stored transposed, [dk][dv] (they come
                                     // from the tensor-core forward scan)
     unsigned *err;                  // device error word (the workspace's first word)
@@ -406,10 +404,7 @@ bwd_prep_kernel(const BwdParams p)
     for (int j0 = 0; j0 < dv; j0 += 64)
         block_gemm_cols<4, false, false>(min(64, dv - j0), dk, 64, [&](int i, int r) { return dOf(r, j0 + i); },
                                          [&](int r, int d) { return qd[r * dk + d]; },
-                                         [&](int i, int d, float x) {
-                                             if (p.tc_scan) blk[LY.doq + (int64_t)d * dv + j0 + i] = x;
-                                             else blk[LY.doq + (int64_t)(j0 + i) * dk + d] = x;
-                                         },
+                                         [&](int i, int d, float x) { blk[LY.doq + (int64_t)(j0 + i) * dk + d] = x; },
                                          sA, sB);
 }
 
@@ -2127,9 +2122,10 @@ cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t st)
     p.ws = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(a.workspace) + 256);
     p.err = reinterpret_cast<unsigned *>(a.workspace);
     const bool tc_scan = a.dt == 1 && chunk_tc_supported(1, a.gm.dk, a.gm.dv, (int64_t)a.gm.B * a.gm.T);
-    const bool tc_local = a.dt == 1 && a.gm.dk == 128 && a.gm.dv == 128;   // implies tc_scan
+    // bf16 with dk = dv = 128: the tensor-core prep, reverse scan and local kernels, which store dO^T Qd
+    // transposed ([dk][dv]) and dS', Kd and W as bf16 (high, low) tiles (implies tc_scan)
+    const bool tc_local = a.dt == 1 && a.gm.dk == 128 && a.gm.dv == 128;
     p.need_u = tc_scan ? 0 : 1;
-    p.tc_scan = tc_local ? 1 : 0;
     p.s_t = tc_scan ? 1 : 0;
     p.gm = a.gm; p.scale = a.scale; p.l2 = a.l2;
     const size_t stage = 2 * (size_t)kStage * sizeof(float);
