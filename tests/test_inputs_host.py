@@ -1,7 +1,9 @@
 """Host-side checks of the seeded input recipe (no GPU): the workload table against the stated
-configurations, and the generators' shapes, ranges, structure and determinism."""
+configurations, and the generators' shapes, ranges, structure and determinism; and the profiling
+driver's refusal to run without a GPU."""
 import math
 
+import pytest
 import torch
 
 from gated_delta_rule_12_gb300 import inputs
@@ -65,3 +67,20 @@ def test_beta_up_to_two_and_decode_generator():
     d = inputs.make_decode(N=4, H=2, dk=16, dv=8, steps=3, dtype="bf16", seed=3)
     assert d["q"].shape == (3, 4, 2, 16) and d["v"].shape == (3, 4, 2, 8) and d["g"].shape == (3, 4, 2)
     assert d["state0"].shape == (4, 2, 8, 16) and d["state0"].dtype == torch.float32
+
+
+def test_profile_case_refuses_to_run_without_a_gpu(monkeypatch):
+    """The profiling driver runs entry points on a GPU only; without one it stops with a message
+    instead of falling back to anything on the host."""
+    import torch
+    from gated_delta_rule_12_gb300 import profile_case
+    monkeypatch.setattr(torch.cuda, "is_available", lambda: False)
+    with pytest.raises(SystemExit) as e:
+        profile_case.main(["--op", "bwd", "--B", "1", "--L", "64"])
+    assert "CUDA device" in str(e.value)
+
+
+def test_profile_case_rejects_unknown_ops():
+    from gated_delta_rule_12_gb300 import profile_case
+    with pytest.raises(SystemExit):
+        profile_case.main(["--op", "prefill"])
