@@ -15,6 +15,7 @@ import torch
 import gated_delta_rule_12_gb300 as gdn
 import oracle
 from gated_delta_rule_12_gb300 import inputs
+import gpu_helpers
 from gpu_helpers import cuda, errors
 
 pytestmark = pytest.mark.gpu
@@ -37,6 +38,8 @@ def check(got, ref, dtype, what):
     maxabs, rel = errors(got, ref)
     rl, ma = TOL[dtype]
     scale = max(float(np.abs(ref).max()), 1e-30)
+    # logged with the max-abs bound in absolute terms (it is relative to the largest reference entry)
+    gpu_helpers.record(what, dtype, maxabs, rel, rl, ma * scale)
     assert rel <= rl and maxabs <= ma * scale, f"{what}: rel-L2 {rel:.3e}, max-abs {maxabs:.3e} (ref max {scale:.3e})"
 
 
