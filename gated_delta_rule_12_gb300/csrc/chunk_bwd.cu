@@ -1,4 +1,4 @@
-// chunk_bwd.cu -- backward pass of the chunked gated delta rule (fp32 throughout).
+// chunk_bwd.cu -- backward pass of the chunked gated delta rule.
 //
 // "Gated Delta Networks: Improving Mamba2 with Delta Rule", §3.3 (the chunkwise
 // form; the training forward whose gradients these are).  Per chunk, with
@@ -15,15 +15,19 @@
 // and, in parallel over chunks, the local gradients through A, Qd, Kd, U, W, T, L,
 // Gamma and the gates (see bwd_local_kernel), then through the normalisations.
 //
-// Four kernels:
+// Four fp32 kernels (fp32 inputs, other head sizes):
 //   bwd_prep_kernel      per chunk: q^, k^, b, T, U, W, A, Qd, Kd, the unmasked K^K^T and
 //                        Q^K^T, and the reverse scan's state-independent A^T dO and dO^T Qd
 //   bwd_fwd_scan_kernel  per (sequence, head, 32 state rows): the state at every chunk start
 //                        and V_new
 //   bwd_bwd_scan_kernel  the same units in reverse: dS' per chunk, dV_new, dS_0
 //   bwd_local_kernel     per chunk: dq, dk, dv, dg, dbeta
-// Every intermediate is fp32.  The matrix products go through one block-level GEMM
-// (block_gemm) on the tensor cores with fp32 accuracy (three tf32 products per pair).
+// Their intermediates are fp32 and their products go through one block-level GEMM (block_gemm)
+// on the tensor cores with fp32 accuracy (three tf32 products per pair).  For bf16 inputs with
+// dk = 128 and dv a multiple of 128 the forward scan is the tensor-core chunked forward (its
+// saving instance); with dk = dv = 128 the other three steps run on the tcgen05 tensor cores
+// too (bwd_prep_tc_kernel, bwd_scan_tc_kernel beside the forward scan, bwd_local_tc_kernel),
+// each fp32 intermediate entering a product as a bf16 (high, low) pair.
 #include "common.cuh"
 #include "kernels.h"
 #include "umma.cuh"
